@@ -1,0 +1,46 @@
+"""Plant plausible mistakes in a copy of the oracle (CPU only) and check that the pins catch
+each one. Every mutant is compiled from a modified copy of moe_oracle.c into a temporary
+directory; the pin suite then runs against it in a child process and must fail."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
+
+MUTANTS = {
+    "nibble_order_swapped": ("return (c % 2 == 0) ? (byte & 0x0F) : (byte >> 4);",
+                             "return (c % 2 == 0) ? (byte >> 4) : (byte & 0x0F);"),
+    "bias_term_dropped": ("* (double)code_at(q, cols, bits, r, c) + bi;", "* (double)code_at(q, cols, bits, r, c);"),
+    "scale_group_index_off": ("size_t gi = (size_t)r * ng + c / group;", "size_t gi = (size_t)r * ng + (c / group + 1) % ng;"),
+    "silu_sign_flipped": ("h[r] = g / (1.0 + exp(-g)) * v;", "h[r] = g / (1.0 + exp(g)) * v;"),
+    "gate_up_swapped": ("h[r] = g / (1.0 + exp(-g)) * v;", "h[r] = v / (1.0 + exp(-v)) * g;"),
+    "down_transposed": ("acc += Wd[(size_t)o * I + r] * h[r];", "acc += Wd[((size_t)r * H + o) % ((size_t)H * I)] * h[r];"),
+    "tie_break_higher_index": ("if (best < 0 || v > bestv) {", "if (best < 0 || v >= bestv) {"),
+    "renorm_missing": ("w[j] = renorm ? p / (sel / all) : p;", "w[j] = p;"),
+    "shared_gate_constant": ("return 1.0 / (1.0 + exp(-z));", "return 1.0;"),
+    "router_bias_dropped": ("acc += (double)bias[e];", "acc += 0.0;"),
+    "shared_term_dropped": ("y[o] += gs * ye[o];", "y[o] += 0.0 * ye[o];"),
+    "rmsnorm_eps_inside_wrong": ("double r = sqrt(ss / H + eps);", "double r = sqrt(ss + eps);"),
+    "bf16_round_truncates": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))", "if (0)"),
+    "section_order_swapped": ("sz[0] = q_bytes(I, H, bits);          /* gate.q */",
+                              "sz[0] = q_bytes(I, H, bits) + 16;     /* gate.q */"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    import oracle
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, name
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(old, new))
+    lib = oracle.compile_c(str(src), str(tmp_path / "libmutant.so"))
+    env = dict(os.environ, MOE_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
