@@ -1,0 +1,348 @@
+"""Benchmark: batch-1 MoE decode throughput on B300 through libmoe.
+
+Default workload: the 80B-shaped (hidden 2048, 512 experts, top-10, inter 512, shared 512,
+int4 group 64) 48-layer pre-norm residual stack with every expert blob resident in the HBM pool at
+a fixed stride. One step = one decode token through all 48 layers = one cooperative kernel launch
+(router, top-k, routed + shared experts, combine, residual for every layer). Each step streams
+~1.04 GB of weights, far above the 126 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an independent replica on its
+own GPU (the layer has no exchange step at batch 1); value = tokens of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CONFIGS = {
+    # name: (shape factory, layers, description)
+    "stack80": ("S80", 48, 4, "80B-shaped 48-layer resident MoE stack, batch-1 decode, int4"),
+    "stack35": ("S35", 40, 4, "35B-shaped 40-layer resident MoE stack, batch-1 decode, int4"),
+    "stack35_int8": ("S35", 40, 8, "35B-shaped 40-layer resident MoE stack, batch-1 decode, int8"),
+}
+METRIC = "MoE decode tokens/s (1 B300) and expert-byte HBM GB/s vs ~8 TB/s roofline"
+SEED = 0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+def _shape(name, bits):
+    from int4_routed_expert_05_b300 import synth
+    return getattr(synth, name).with_bits(bits)
+
+
+def _bytes_per_layer(sh):
+    """Algorithmic bytes of one layer for one token: routed + shared expert blobs, router, gate."""
+    from int4_routed_expert_05_b300 import moe
+    from int4_routed_expert_05_b300.resident import moe_shape
+    ms = moe_shape(sh)
+    blob = moe.expert_bytes(ms)
+    blob_s = moe.expert_bytes(ms, shared=True)
+    expert = sh.top_k * blob + blob_s
+    router = sh.n_experts * sh.hidden * 2 + sh.hidden * 2
+    return expert, router
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(ws, v):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(sh, n_layers_sample, n_layers_model, seed=SEED, budget_s=20.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of the same workload:
+    n_layers_sample layers of the stack for as many tokens as fit the budget (at least one).
+    Returns tokens/s of the full n_layers_model stack (time scaled by the layer ratio)."""
+    import oracle
+    from int4_routed_expert_05_b300 import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_ref import OracleLayers
+    O = OracleLayers(oracle, sh, seed, n_layers_sample)
+    for l in range(n_layers_sample):       # blobs of the layers are packed outside the timed region
+        O.dense(l)
+    t_total, tokens = 0.0, 0
+    while tokens == 0 or t_total < budget_s:
+        x = synth.activation_f32(sh, seed, 10_000 + tokens)[0].astype(np.float64)
+        for l in range(n_layers_sample):
+            u = oracle.rmsnorm_bf16(x)
+            # the selected experts' blobs are written outside the timed region
+            lg, _ = oracle.router_logits(O.dense(l)[0], u)
+            for e in oracle.topk(lg, sh.top_k, sh.renorm)[0]:
+                O.blob(l, int(e))
+            t0 = time.perf_counter()
+            r = O.layer(l, u)
+            t_total += time.perf_counter() - t0
+            x = x + r["y"]
+        tokens += 1
+        if tokens >= 8:
+            break
+    per_token_full = t_total / tokens * (n_layers_model / n_layers_sample)
+    return 1.0 / per_token_full, {"layers": n_layers_sample, "tokens": tokens, "seconds": t_total}
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores (single thread), on this arm's workload.
+    A step is a bounded sample: one full oracle layer for one token when K + W of them fit in
+    about two and a half minutes, else one expert FFN of a layer (the oracle's dominant cost), with
+    tokens/s of the whole stack derived from the sampled time."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    from int4_routed_expert_05_b300 import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_ref import OracleLayers
+    name, L, bits, desc = CONFIGS[args.config]
+    sh = _shape(name, bits)
+    O = OracleLayers(oracle, sh, SEED, 1)
+    Wr, w_sg, shared = O.dense(0)
+    x = synth.activation_f32(sh, SEED, 0)[0].astype(np.float64)
+    u = oracle.rmsnorm_bf16(x)
+    t0 = time.perf_counter()
+    r = O.layer(0, u)
+    t_layer = time.perf_counter() - t0
+    per_layer = (args.warmup + args.steps) * t_layer <= 150.0
+    blob = O.blob(0, int(r["idx"][0]))
+    if per_layer:  # every blob written before timing
+        for e in range(sh.n_experts):
+            O.blob(0, e)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        if per_layer:
+            O.layer(0, oracle.rmsnorm_bf16(x + i * 1e-3))
+        else:
+            oracle.expert_ffn(sh, blob, u)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times[args.warmup:]) if args.steps else times[-1]
+    if per_layer:
+        v = 1.0 / (t * L)
+        sample = f"one oracle layer (router, top-{sh.top_k}, {sh.top_k + 1} expert FFNs, combine) per step, x{L} layers"
+    else:
+        t0 = time.perf_counter()
+        oracle.router_logits(Wr, u)
+        t_router = time.perf_counter() - t0
+        v = 1.0 / (L * ((sh.top_k + 1) * t + t_router))
+        sample = f"one expert FFN per step, scaled by {sh.top_k + 1} experts and {L} layers plus the router"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.config, "description": desc, "batch": 1, "layers": L},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from int4_routed_expert_05_b300 import _build, synth
+    _build.build()
+    from int4_routed_expert_05_b300 import moe
+    from int4_routed_expert_05_b300.resident import Resident
+
+    name, L, bits, desc = CONFIGS[args.config]
+    sh = _shape(name, bits)
+    flags = moe.RENORM | moe.PRENORM | moe.RESIDUAL
+    R = Resident(sh, L, SEED, flags=flags, verbose=(rank == 0))
+    H = sh.hidden
+    n_in = args.warmup + args.steps
+    xs = torch.from_numpy(np.stack([synth.activation_f32(sh, SEED, s)[0] for s in range(min(n_in, 64))])).cuda()
+    out = torch.empty(H, dtype=torch.float32, device="cuda")
+    idx = torch.empty((L, sh.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((L, sh.top_k), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        R.pool.stack_forward(0, L, xs[i % xs.shape[0]], out, None, idx, w, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if R.pool.device_status() != moe.OK:
+        raise RuntimeError("device status after warm-up is not MOE_OK")
+
+    clocks = ClockSampler(local)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    ms = _max_over_ranks(ws, ms)
+    status = R.pool.device_status()
+    if status != moe.OK:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # end to end through the C ABI with host buffers: pinned x in, residual out, every step
+    h_x = torch.empty((xs.shape[0], H), dtype=torch.float32, pin_memory=True)
+    h_x.copy_(xs.cpu())
+    h_out = torch.empty(H, dtype=torch.float32, pin_memory=True)
+    d_x = torch.empty(H, dtype=torch.float32, device="cuda")
+    n_e2e = max(1, min(args.steps, 2000))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        d_x.copy_(h_x[i % h_x.shape[0]], non_blocking=True)
+        R.pool.stack_forward(0, L, d_x, out, None, None, None, stream)
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = _max_over_ranks(ws, e2e_s)
+
+    if rank != 0:
+        return
+    expert_b, router_b = _bytes_per_layer(sh)
+    per_launch_expert = expert_b * L
+    per_launch_all = (expert_b + router_b) * L
+    ms_step = ms / args.steps
+    tok_s = ws * args.steps / (ms / 1e3)
+    peak, peak_kind = _peaks()
+    achieved = per_launch_expert / (ms_step / 1e3) / 1e9
+    cpu_v, cpu_info = (None, None)
+    if ws == 1 and not args.no_cpu_baseline:
+        cpu_v, cpu_info = cpu_oracle_sample(sh, args.ref_layers, L, budget_s=args.ref_budget)
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        t = json.load(open(tp)).get(args.config)
+        traffic = t.get("bytes_per_launch") if t else None
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4" if bits == 4 else "int8",
+        "data": "synthetic (seeded generator, random-init weights of the stated shapes)",
+        "config": {"workload": args.config, "description": desc, "batch": 1, "layers": L,
+                   "hidden": sh.hidden, "experts": sh.n_experts, "top_k": sh.top_k, "inter": sh.inter,
+                   "shared_inter": sh.shared_inter, "bits": bits, "group": sh.group,
+                   "l2": "inputs larger than L2 (%.2f GB of weights per step vs 126 MB L2)" % (per_launch_all / 1e9),
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "layer_latency_us": ms_step * 1e3 / L,
+        "expert_gbs": achieved,
+        "all_weight_gbs": per_launch_all / (ms_step / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "moe_decode_kernel", "bytes_per_launch": per_launch_expert},
+        "cpu_baseline": None if cpu_v is None else {
+            "value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{cpu_info['tokens']} token(s) through {cpu_info['layers']} of {L} layers in "
+                      f"{cpu_info['seconds']:.1f} s, time scaled to the full stack"},
+        "e2e": {"value": ws * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * H, "d2h_bytes_per_step": 4 * H,
+                "steps": n_e2e},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="stack80", choices=sorted(CONFIGS))
+    ap.add_argument("--ref-layers", type=int, default=2)
+    ap.add_argument("--ref-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+/*
+ * moe.h -- C ABI of libmoe: the routed-expert Mixture-of-Experts FFN for batch-1 decode on
+ * B300 (sm_103a), with a fixed-stride pool of int4/int8 group-quantised expert blobs.
+ *
+ * Per token and layer the library computes
+ *     logits = Wr u (+ bias);  idx, w = top-k(logits) with renormalised softmax weights
+ *     y      = sum_j w_j * Wd_j (silu(Wg_j u) * (Wu_j u))  +  sigmoid(w_sg . u) * S(u)
+ * where expert j's gate/up/down matrices sit in one blob at  arena + slot * stride  and S is the
+ * always-on shared expert in the same blob format.
+ *
+ * Sources (web pages about the Swiftlet runtime; no code is printed on them):
+ *  [qpack]  paotong.dev commentary on Swiftlet (paotong.dev/a/b3a48bd74abb1ebf): routed experts
+ *           are repacked into one fixed-stride blob each and fetched with one read at
+ *           blobBase + expertIndex * expertStride; a bounded pool caches hot experts with LFU
+ *           plus recency eviction (reported hit rate 43-70%).
+ *  [route]  cheshm.ai, "Swiftlet fits an 80B-level Qwen giant into Mac", paragraph on scheduling:
+ *           each layer routes a token to 10 of 512 (80B) or 8 of 256 (35B) experts; router and
+ *           shared experts stay resident; popular experts are cached in a bounded pool with LFU
+ *           and recency.
+ *  [quant]  same item, closing paragraph: MLX-style int4/int8 group quantisation, byte-addressed
+ *           kernels with 64-bit offsets, high-sparsity MoE with shared experts.
+ *  [renorm] alphalab.site, "Swiftlet 實測資料解讀", section on the 35B correctness fix: top-k
+ *           routing weights are renormalised (norm_topk_prob = true).
+ *  [size]   same page, section on SSD reads: with no cache hits the 80B model requests at most
+ *           480 experts (about 810 MiB) per token, i.e. 1,769,472 bytes per expert.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named d_* are device pointers owned by the caller (for instance PyTorch tensors);
+ *    pointers named h_* are host pointers owned by the caller. The library never frees them.
+ *  - Streams are cudaStream_t values passed as void*; NULL is the legacy default stream.
+ *  - Work is enqueued on the given stream and the call returns without waiting for it, unless
+ *    the entry point says otherwise. No entry point allocates device memory after
+ *    moe_pool_create.
+ *  - Errors are returned as moe_status codes; moe_last_error() gives a message (per thread).
+ *    Nothing throws across the ABI, exits, or traps on the device. Problems found by a kernel
+ *    (an expert that is not resident, a grid barrier that timed out) are written to a device
+ *    status word that moe_device_status() reads.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_E_INVALID = 1,       /* bad argument (null pointer, out-of-range index, misalignment) */
+    MOE_E_SHAPE = 2,         /* shape outside what the kernels support */
+    MOE_E_NOT_RESIDENT = 3,  /* a selected expert has no slot in the pool */
+    MOE_E_POOL_FULL = 4,     /* every slot is pinned by the step in flight */
+    MOE_E_CUDA = 5,          /* a CUDA runtime call failed (message in moe_last_error) */
+    MOE_E_TIMEOUT = 6,       /* a device-side wait ran past its limit */
+    MOE_E_NOMEM = 7          /* workspace or arena too small */
+} moe_status;
+
+/* flags of moe_shape.flags */
+#define MOE_RENORM   1  /* renormalise the top-k weights ([renorm]); off: full-softmax weights */
+#define MOE_PRENORM  2  /* stack layer: u = bf16(x / sqrt(mean(x^2) + 1e-6)) from an fp32 residual */
+#define MOE_RESIDUAL 4  /* stack layer: output x + y instead of y */
+
+/* One MoE FFN layer. hidden H, n_experts E, top_k k, inter I (routed expert), shared_inter Is,
+ * bits 4 or 8, group 64. Supported: H % 256 == 0, I % 64 == 0, Is % 64 == 0, 1 <= k <= 16,
+ * k <= E <= 512, group == 64. */
+typedef struct {
+    int32_t hidden, n_experts, top_k, inter, shared_inter, bits, group, flags;
+} moe_shape;
+
+/* ----------------------------------------------------------------------------------------- */
+/* Blob format ([qpack], [quant], [size])                                                     */
+/* ----------------------------------------------------------------------------------------- */
+/*
+ * One expert = one contiguous blob, sections in this order with no gaps:
+ *   gate.q | up.q | down.q | gate.s | gate.b | up.s | up.b | down.s | down.b
+ * gate, up: [I][H] (out x in); down: [H][I]. Codes row-major, packed along the input dimension:
+ * int4 element c of a row is in byte c/2 of the row, low nibble for even c, high nibble for odd c;
+ * int8 codes take one byte. Scale s and bias b: bf16, row-major [out][in/64]; the weight is
+ * w = s * q + b with q the unsigned code. Blobs sit stride bytes apart, stride = blob bytes
+ * rounded up to 4096. For hidden 2048, inter 512, int4 both are 1,769,472 bytes ([size]).
+ */
+
+/* Bytes of one blob (shared = 1: the shared expert, whose inter is shape->shared_inter). */
+size_t moe_expert_bytes(const moe_shape* shape, int shared);
+/* Distance between consecutive blobs in a pool or host store. */
+size_t moe_expert_stride(const moe_shape* shape, int shared);
+
+/* Write one blob into h_blob (moe_expert_stride bytes, host; the padding is zeroed).
+ * h_codes[m]: uint8 [out][in] codes of matrix m (0 gate, 1 up, 2 down), each < 2^bits;
+ * h_scale[m], h_bias[m]: bf16 bit patterns [out][in/64]. Host-only, synchronous. */
+moe_status moe_pack_expert(const moe_shape* shape, int shared, const uint8_t* const h_codes[3],
+                           const uint16_t* const h_scale[3], const uint16_t* const h_bias[3],
+                           void* h_blob);
+
+/* ----------------------------------------------------------------------------------------- */
+/* Expert pool ([qpack], [route])                                                             */
+/* ----------------------------------------------------------------------------------------- */
+/*
+ * A pool is host metadata over a caller-owned device arena of n_slots blobs at a fixed stride,
+ * plus a caller-owned device workspace (size from moe_workspace_bytes) that holds the
+ * (layer, expert) -> slot table, the per-layer weight pointers and the kernels' scratch.
+ * It serves both modes:
+ *  - resident: every expert of every layer is placed once (moe_pool_place) and the fused kernels
+ *    look slots up on the device, with no host round trip inside a step;
+ *  - bounded: fewer slots than experts; per layer the caller routes (moe_route), looks up the
+ *    selected experts (moe_pool_lookup), fills misses from a pinned host store
+ *    (moe_pool_load_slot), runs moe_experts with the returned slots, then moe_pool_release.
+ */
+typedef struct moe_pool moe_pool;
+
+/* One layer's resident dense weights (device pointers, caller-owned, 16-byte aligned). */
+typedef struct {
+    const void* router;        /* bf16 [E][H] */
+    const void* shared_blob;   /* one blob of the shared expert (moe_expert_stride(shape, 1)) */
+    const void* shared_gate;   /* bf16 [H], the shared expert's gate vector w_sg */
+    const float* logit_bias;   /* fp32 [E] added to the router logits, or NULL. Not part of the
+                                  method: a hook for synthetic routing-popularity workloads. */
+} moe_layer_weights;
+
+/* Device workspace bytes for a pool over n_layers layers of this shape. */
+size_t moe_workspace_bytes(const moe_shape* shape, int32_t n_layers);
+
+/* Create a pool. d_arena: n_slots * moe_expert_stride(shape, 0) bytes (4096-aligned);
+ * d_workspace: moe_workspace_bytes bytes (256-aligned). Both stay owned by the caller and must
+ * outlive the pool. Initialises the workspace on the current device (synchronous). */
+moe_status moe_pool_create(const moe_shape* shape, int32_t n_layers, int32_t n_slots,
+                           void* d_arena, size_t arena_bytes, void* d_workspace,
+                           size_t workspace_bytes, moe_pool** out);
+void moe_pool_destroy(moe_pool* pool);
+
+/* Device address of a slot (arena + slot * stride), NULL if out of range. */
+void* moe_pool_slot_ptr(const moe_pool* pool, int32_t slot);
+
+/* Register layer `layer`'s dense weights (pointers are copied; takes effect at moe_pool_sync). */
+moe_status moe_pool_set_layer(moe_pool* pool, int32_t layer, const moe_layer_weights* w);
+
+/* Resident mode: declare that `slot` holds expert (layer, expert) (the caller wrote the blob).
+ * A slot holds at most one expert; placing over an occupied slot evicts its previous expert. */
+moe_status moe_pool_place(moe_pool* pool, int32_t layer, int32_t expert, int32_t slot);
+
+/* Upload the slot table and layer weights to the workspace (enqueued on `stream`; the host
+ * copies are staged before return). Call after set_layer/place and before forward calls. */
+moe_status moe_pool_sync(moe_pool* pool, void* stream);
+
+/* Bounded mode: look up n experts of `layer`. h_slots_out[i] = slot, or -1 on a miss.
+ * Every call advances the pool's tick by one. A hit counts one more use of the slot and stamps
+ * it with the tick; every expert passed (hit or later loaded) is pinned until moe_pool_release. */
+moe_status moe_pool_lookup(moe_pool* pool, int32_t layer, const int32_t* h_experts, int32_t n,
+                           int32_t* h_slots_out);
+
+/* Bounded mode: place expert (layer, expert) in a slot and copy its blob from pinned host memory
+ * h_blob (moe_expert_stride bytes) with cudaMemcpyAsync on copy_stream. The slot is the lowest
+ * free one, else the unpinned slot with the smallest (use count, last tick, slot index): LFU with
+ * recency as the tie-break. The copy waits (on copy_stream) for the last kernel that read the
+ * evicted slot. The new entry has use count 1 and the current tick, and is pinned.
+ * MOE_E_POOL_FULL if every slot is pinned. Returns the slot in *slot_out. */
+moe_status moe_pool_load_slot(moe_pool* pool, int32_t layer, int32_t expert, const void* h_blob,
+                              void* copy_stream, int32_t* slot_out);
+
+/* Make `compute_stream` wait for the copies issued by moe_pool_load_slot since the last call. */
+moe_status moe_pool_wait_loads(moe_pool* pool, void* compute_stream);
+
+/* Record the end of the work enqueued so far on compute_stream as the last use of every pinned
+ * slot, then unpin them all. */
+moe_status moe_pool_release(moe_pool* pool, void* compute_stream);
+
+/* Counters since creation: lookups that hit, lookups that missed, bytes copied by load_slot. */
+moe_status moe_pool_stats(const moe_pool* pool, int64_t* hits, int64_t* misses, int64_t* bytes_loaded);
+
+/* ----------------------------------------------------------------------------------------- */
+/* Forward passes                                                                             */
+/* ----------------------------------------------------------------------------------------- */
+
+/* One layer for n_tokens tokens taken one after another ([route], [quant], [renorm]).
+ * d_x: bf16 [T][H] layer input u (or fp32 [T][H] residual x when the shape has MOE_PRENORM).
+ * d_y: fp32 [T][H] layer output (y, or x + y with MOE_RESIDUAL).
+ * d_topk_idx (int32 [T][k]) and d_topk_w (fp32 [T][k]): selected experts in rank order (largest
+ * logit first, equal fp32 logits to the lower index) and their weights; either may be NULL.
+ * Every selected expert must be placed (resident mode); one that is not sets the device status
+ * MOE_E_NOT_RESIDENT and contributes nothing. One cooperative kernel launch. */
+moe_status moe_layer_forward(moe_pool* pool, int32_t layer, const void* d_x, int32_t n_tokens,
+                             float* d_y, int32_t* d_topk_idx, float* d_topk_w, void* stream);
+
+/* Layers [layer0, layer0 + n_layers) applied in order to one token, as a pre-norm residual
+ * stack: x <- x + MoE_l(bf16(rmsnorm(x))) (the shape needs MOE_PRENORM | MOE_RESIDUAL).
+ * d_x: fp32 [H] input residual; d_x_out: fp32 [H] final residual. d_trace (fp32
+ * [n_layers + 1][H], or NULL) receives each layer's input and the final residual.
+ * d_topk_idx / d_topk_w: [n_layers][k] or NULL. One cooperative kernel launch for all layers. */
+moe_status moe_stack_forward(moe_pool* pool, int32_t layer0, int32_t n_layers, const float* d_x,
+                             float* d_x_out, float* d_trace, int32_t* d_topk_idx, float* d_topk_w,
+                             void* stream);
+
+/* Bounded mode, first half of a layer: router and top-k only. d_x as for moe_layer_forward
+ * (one token); writes d_topk_idx [k] and d_topk_w [k]. */
+moe_status moe_route(moe_pool* pool, int32_t layer, const void* d_x, int32_t* d_topk_idx,
+                     float* d_topk_w, void* stream);
+
+/* Bounded mode, second half: experts and combine for one token given the selection.
+ * d_topk_w: fp32 [k] weights from moe_route; h_slots: host int32 [k], the pool slot of each
+ * selected expert in rank order (copied into the launch, so the array may be reused at once). */
+moe_status moe_experts(moe_pool* pool, int32_t layer, const void* d_x, const float* d_topk_w,
+                       const int32_t* h_slots, float* d_y, void* stream);
+
+/* Reference path: the same layer for one token with plain kernels (one thread per logit, one
+ * thread per selection, one thread per output row, fp32 sums in index order). Used to cross-check
+ * the fused kernel. Same arguments as moe_layer_forward with n_tokens = 1. */
+moe_status moe_layer_forward_scalar(moe_pool* pool, int32_t layer, const void* d_x, float* d_y,
+                                    int32_t* d_topk_idx, float* d_topk_w, void* stream);
+
+/* ----------------------------------------------------------------------------------------- */
+/* Status                                                                                      */
+/* ----------------------------------------------------------------------------------------- */
+
+/* Wait for `stream`, read and clear the pool's device status word into *h_status (a moe_status
+ * value, MOE_OK if no kernel reported a problem). After MOE_E_TIMEOUT the grid-barrier counter is
+ * reset too. Synchronous. */
+moe_status moe_device_status(moe_pool* pool, void* stream, int32_t* h_status);
+
+/* Limit, in nanoseconds, of every device-side wait of this pool's kernels (default 2 s). A wait
+ * that runs past it sets MOE_E_TIMEOUT in the device status and the kernel returns. */
+moe_status moe_pool_set_timeout(moe_pool* pool, uint64_t timeout_ns);
+
+/* Number of thread blocks the cooperative kernels of this pool launch (one per SM). */
+int32_t moe_pool_grid(const moe_pool* pool);
+
+/* Message of the last error on the calling thread ("" if none). */
+const char* moe_last_error(void);
+
+/* ----------------------------------------------------------------------------------------- */
+/* Inspection and test hooks                                                                  */
+/* ----------------------------------------------------------------------------------------- */
+
+/* Slot currently holding (layer, expert), -1 if none (host metadata; no device access). */
+moe_status moe_pool_slot_of(const moe_pool* pool, int32_t layer, int32_t expert, int32_t* slot);
+
+/* Replace the device copy of moe_pool_load_slot by a host callback fn(user, slot, h_blob, bytes)
+ * (fn = NULL restores the copy). A nonzero return makes load_slot fail with MOE_E_CUDA and leave
+ * the pool unchanged. Lets the slot policy and its failure handling run without a GPU on a
+ * host-only pool (moe_pool_create with d_workspace = NULL). */
+moe_status moe_pool_set_copy_hook(moe_pool* pool, int (*fn)(void* user, int32_t slot, const void* h_blob, size_t bytes),
+                                  void* user);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,664 @@
+// api.cu -- the C ABI declared in include/moe.h: argument checks, the expert pool, launches.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "layout.h"
+#include "policy.h"
+
+namespace moe {
+__global__ void moe_decode_kernel(const __grid_constant__ StepParams P);
+__host__ __device__ uint32_t decode_smem_bytes(const StepParams& P);
+__global__ void scalar_router(const StepParams P);
+__global__ void scalar_topk(const StepParams P, int32_t* sel);
+__global__ void scalar_gateup(const StepParams P, const int32_t* sel);
+__global__ void scalar_down(const StepParams P, const int32_t* sel);
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_err;
+
+moe_status fail(moe_status st, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+#define CUDA_TRY(call)                                                                         \
+    do {                                                                                       \
+        cudaError_t e_ = (call);                                                               \
+        if (e_ != cudaSuccess)                                                                 \
+            return fail(MOE_E_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));           \
+    } while (0)
+
+size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct WsLayout {
+    size_t bar, status, table, layers, logits, hbuf, xbuf, sel, total;
+};
+
+WsLayout ws_layout(const moe_shape& s, int L)
+{
+    WsLayout w{};
+    size_t o = 0;
+    w.bar = o;
+    o += 256;
+    w.status = o;
+    o += 256;
+    w.table = o;
+    o = up256(o + sizeof(int32_t) * (size_t)L * s.n_experts);
+    w.layers = o;
+    o = up256(o + sizeof(LayerDesc) * (size_t)L);
+    w.logits = o;
+    o = up256(o + sizeof(float) * (size_t)s.n_experts);
+    const int Imax = s.inter > s.shared_inter ? s.inter : s.shared_inter;
+    w.hbuf = o;
+    o = up256(o + sizeof(float) * (size_t)(s.top_k + 1) * Imax);
+    w.xbuf = o;
+    o = up256(o + sizeof(float) * (size_t)s.hidden);
+    w.sel = o;
+    o = up256(o + sizeof(int32_t) * 3 * kMaxK);
+    w.total = o;
+    return w;
+}
+
+moe_status check_shape(const moe_shape* s)
+{
+    if (!s)
+        return fail(MOE_E_INVALID, "shape is NULL");
+    if (s->group != 64)
+        return fail(MOE_E_SHAPE, "group must be 64 (got %d)", s->group);
+    if (s->bits != 4 && s->bits != 8)
+        return fail(MOE_E_SHAPE, "bits must be 4 or 8 (got %d)", s->bits);
+    if (s->hidden <= 0 || s->hidden % 256 != 0 || s->hidden > 8192)
+        return fail(MOE_E_SHAPE, "hidden must be a positive multiple of 256, at most 8192 (got %d)", s->hidden);
+    if (s->inter <= 0 || s->inter % 64 != 0 || s->shared_inter <= 0 || s->shared_inter % 64 != 0)
+        return fail(MOE_E_SHAPE, "inter and shared_inter must be positive multiples of 64");
+    if (s->inter > 4096 || s->shared_inter > 4096)
+        return fail(MOE_E_SHAPE, "inter and shared_inter must be at most 4096");
+    if (s->top_k < 1 || s->top_k > kMaxK)
+        return fail(MOE_E_SHAPE, "top_k must be in [1, %d] (got %d)", kMaxK, s->top_k);
+    if (s->n_experts < s->top_k || s->n_experts > kMaxE)
+        return fail(MOE_E_SHAPE, "n_experts must be in [top_k, %d] (got %d)", kMaxE, s->n_experts);
+    if (s->flags & ~(MOE_RENORM | MOE_PRENORM | MOE_RESIDUAL))
+        return fail(MOE_E_SHAPE, "unknown flag bits 0x%x", s->flags);
+    return MOE_OK;
+}
+
+}  // namespace
+
+struct moe_pool {
+    moe_shape shape{};
+    int L = 0, S = 0;
+    uint8_t* arena = nullptr;
+    size_t arena_bytes = 0;
+    uint8_t* ws = nullptr;
+    size_t ws_bytes = 0;
+    WsLayout wl{};
+    BlobGeo geo{}, geo_s{};
+    std::vector<LayerDesc> layers;
+    SlotPolicy policy;
+    int64_t hits = 0, misses = 0, bytes_loaded = 0;
+    int device = -1, grid = 0;
+    uint32_t smem = 0;
+    uint64_t timeout_ns = 2000000000ull;
+    // bounded mode: events
+    std::vector<cudaEvent_t> ring;   // last-use events, reused round robin
+    size_t ring_next = 0;
+    std::vector<cudaEvent_t> slot_last_use;  // per slot, nullptr if never read
+    cudaEvent_t loads_done = nullptr;
+    cudaStream_t last_copy_stream = nullptr;
+    bool loads_pending = false;
+    // test hook replacing the device copy of load_slot
+    int (*copy_hook)(void*, int32_t, const void*, size_t) = nullptr;
+    void* copy_user = nullptr;
+};
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err.c_str(); }
+
+size_t moe_expert_bytes(const moe_shape* s, int shared)
+{
+    if (!s)
+        return 0;
+    return blob_geo(s->hidden, shared ? s->shared_inter : s->inter, s->bits, s->group).bytes;
+}
+
+size_t moe_expert_stride(const moe_shape* s, int shared)
+{
+    if (!s)
+        return 0;
+    return blob_geo(s->hidden, shared ? s->shared_inter : s->inter, s->bits, s->group).stride;
+}
+
+moe_status moe_pack_expert(const moe_shape* s, int shared, const uint8_t* const codes[3],
+                           const uint16_t* const scale[3], const uint16_t* const bias[3], void* h_blob)
+{
+    moe_status st = check_shape(s);
+    if (st != MOE_OK)
+        return st;
+    if (!codes || !scale || !bias || !h_blob)
+        return fail(MOE_E_INVALID, "NULL argument to moe_pack_expert");
+    const BlobGeo g = blob_geo(s->hidden, shared ? s->shared_inter : s->inter, s->bits, s->group);
+    uint8_t* out = static_cast<uint8_t*>(h_blob);
+    memset(out, 0, g.stride);
+    for (int m = 0; m < 3; ++m) {
+        if (!codes[m] || !scale[m] || !bias[m])
+            return fail(MOE_E_INVALID, "NULL array for matrix %d", m);
+        const int rows = g.rows[m], cols = g.cols[m];
+        const uint8_t* q = codes[m];
+        uint8_t* dst = out + g.q_off[m];
+        const int maxq = (1 << s->bits) - 1;
+        for (size_t i = 0; i < (size_t)rows * cols; ++i)
+            if (q[i] > maxq)
+                return fail(MOE_E_INVALID, "code %d out of range in matrix %d", (int)q[i], m);
+        if (s->bits == 8) {
+            memcpy(dst, q, (size_t)rows * cols);
+        } else {
+            // two codes per byte: the even-indexed one in the low nibble
+            const size_t nbytes = (size_t)rows * cols / 2;
+            for (size_t b = 0; b < nbytes; ++b)
+                dst[b] = (uint8_t)(q[2 * b] | (q[2 * b + 1] << 4));
+        }
+        const size_t n = (size_t)rows * g.groups[m];
+        for (size_t i = 0; i < n; ++i) {
+            out[g.s_off[m] + 2 * i] = (uint8_t)(scale[m][i] & 0xFF);
+            out[g.s_off[m] + 2 * i + 1] = (uint8_t)(scale[m][i] >> 8);
+            out[g.b_off[m] + 2 * i] = (uint8_t)(bias[m][i] & 0xFF);
+            out[g.b_off[m] + 2 * i + 1] = (uint8_t)(bias[m][i] >> 8);
+        }
+    }
+    return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_shape* s, int32_t n_layers)
+{
+    if (!s || n_layers <= 0)
+        return 0;
+    return ws_layout(*s, n_layers).total;
+}
+
+moe_status moe_pool_create(const moe_shape* s, int32_t n_layers, int32_t n_slots, void* d_arena,
+                           size_t arena_bytes, void* d_workspace, size_t workspace_bytes, moe_pool** out)
+{
+    moe_status st = check_shape(s);
+    if (st != MOE_OK)
+        return st;
+    if (!out)
+        return fail(MOE_E_INVALID, "out is NULL");
+    *out = nullptr;
+    if (n_layers <= 0 || n_slots <= 0)
+        return fail(MOE_E_INVALID, "n_layers and n_slots must be positive");
+    const BlobGeo geo = blob_geo(s->hidden, s->inter, s->bits, s->group);
+    if (d_workspace) {
+        if (!d_arena)
+            return fail(MOE_E_INVALID, "d_arena is NULL");
+        if (reinterpret_cast<uintptr_t>(d_arena) % 256 || reinterpret_cast<uintptr_t>(d_workspace) % 256)
+            return fail(MOE_E_INVALID, "arena and workspace must be 256-byte aligned");
+        if (arena_bytes < (size_t)n_slots * geo.stride)
+            return fail(MOE_E_NOMEM, "arena holds %zu bytes, %d slots need %zu", arena_bytes, n_slots,
+                        (size_t)n_slots * geo.stride);
+        if (workspace_bytes < ws_layout(*s, n_layers).total)
+            return fail(MOE_E_NOMEM, "workspace holds %zu bytes, needs %zu", workspace_bytes,
+                        ws_layout(*s, n_layers).total);
+    }
+    moe_pool* p = new moe_pool();
+    p->shape = *s;
+    p->L = n_layers;
+    p->S = n_slots;
+    p->arena = static_cast<uint8_t*>(d_arena);
+    p->arena_bytes = arena_bytes;
+    p->ws = static_cast<uint8_t*>(d_workspace);
+    p->ws_bytes = workspace_bytes;
+    p->wl = ws_layout(*s, n_layers);
+    p->geo = geo;
+    p->geo_s = blob_geo(s->hidden, s->shared_inter, s->bits, s->group);
+    p->layers.assign(n_layers, LayerDesc{nullptr, nullptr, nullptr, nullptr});
+    p->policy = SlotPolicy(n_layers, s->n_experts, n_slots);
+    p->slot_last_use.assign(n_slots, nullptr);
+    if (!d_workspace) {  // host-only pool: slot policy without a device
+        *out = p;
+        return MOE_OK;
+    }
+    auto cleanup = [&](moe_status r) {
+        delete p;
+        return r;
+    };
+    if (cudaGetDevice(&p->device) != cudaSuccess)
+        return cleanup(fail(MOE_E_CUDA, "no CUDA device"));
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess)
+        return cleanup(fail(MOE_E_CUDA, "cudaDeviceGetAttribute failed"));
+    StepParams probe{};
+    probe.H = s->hidden;
+    probe.E = s->n_experts;
+    probe.k = s->top_k;
+    probe.I = s->inter;
+    probe.Is = s->shared_inter;
+    probe.bits = s->bits;
+    probe.group = s->group;
+    p->smem = decode_smem_bytes(probe);
+    cudaError_t e = cudaFuncSetAttribute(moe_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem);
+    if (e != cudaSuccess)
+        return cleanup(fail(MOE_E_CUDA, "cudaFuncSetAttribute(%u bytes): %s", p->smem, cudaGetErrorString(e)));
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_decode_kernel, kThreads, p->smem);
+    if (e != cudaSuccess || per_sm < 1)
+        return cleanup(fail(MOE_E_CUDA, "decode kernel cannot be resident (%d per SM): %s", per_sm,
+                            cudaGetErrorString(e)));
+    p->grid = sms;  // one block per SM
+    if (cudaMemset(p->ws, 0, p->wl.total) != cudaSuccess ||
+        cudaMemset(p->ws + p->wl.table, 0xFF, sizeof(int32_t) * (size_t)n_layers * s->n_experts) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+        return cleanup(fail(MOE_E_CUDA, "workspace initialisation failed"));
+    *out = p;
+    return MOE_OK;
+}
+
+void moe_pool_destroy(moe_pool* p)
+{
+    if (!p)
+        return;
+    for (cudaEvent_t ev : p->ring)
+        cudaEventDestroy(ev);
+    if (p->loads_done)
+        cudaEventDestroy(p->loads_done);
+    delete p;
+}
+
+void* moe_pool_slot_ptr(const moe_pool* p, int32_t slot)
+{
+    if (!p || !p->arena || slot < 0 || slot >= p->S)
+        return nullptr;
+    return p->arena + (size_t)slot * p->geo.stride;
+}
+
+int32_t moe_pool_grid(const moe_pool* p) { return p ? p->grid : 0; }
+
+moe_status moe_pool_set_timeout(moe_pool* p, uint64_t timeout_ns)
+{
+    if (!p || timeout_ns == 0)
+        return fail(MOE_E_INVALID, "bad pool or zero timeout");
+    p->timeout_ns = timeout_ns;
+    return MOE_OK;
+}
+
+moe_status moe_pool_set_layer(moe_pool* p, int32_t layer, const moe_layer_weights* w)
+{
+    if (!p || !w)
+        return fail(MOE_E_INVALID, "NULL pool or weights");
+    if (layer < 0 || layer >= p->L)
+        return fail(MOE_E_INVALID, "layer %d out of range [0, %d)", layer, p->L);
+    if (!w->router || !w->shared_blob || !w->shared_gate)
+        return fail(MOE_E_INVALID, "router, shared_blob and shared_gate are required");
+    if (reinterpret_cast<uintptr_t>(w->router) % 16 || reinterpret_cast<uintptr_t>(w->shared_blob) % 16 ||
+        reinterpret_cast<uintptr_t>(w->shared_gate) % 16)
+        return fail(MOE_E_INVALID, "layer weights must be 16-byte aligned");
+    p->layers[layer] = LayerDesc{static_cast<const uint16_t*>(w->router), static_cast<const uint8_t*>(w->shared_blob),
+                                 static_cast<const uint16_t*>(w->shared_gate), w->logit_bias};
+    return MOE_OK;
+}
+
+moe_status moe_pool_place(moe_pool* p, int32_t layer, int32_t expert, int32_t slot)
+{
+    if (!p)
+        return fail(MOE_E_INVALID, "NULL pool");
+    if (layer < 0 || layer >= p->L || expert < 0 || expert >= p->shape.n_experts || slot < 0 || slot >= p->S)
+        return fail(MOE_E_INVALID, "place(%d, %d, %d) out of range", layer, expert, slot);
+    p->policy.place(layer, expert, slot);
+    return MOE_OK;
+}
+
+moe_status moe_pool_sync(moe_pool* p, void* stream)
+{
+    if (!p || !p->ws)
+        return fail(MOE_E_INVALID, "pool has no device workspace");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const auto& t = p->policy.table();
+    CUDA_TRY(cudaMemcpyAsync(p->ws + p->wl.table, t.data(), sizeof(int32_t) * t.size(), cudaMemcpyHostToDevice, st));
+    CUDA_TRY(cudaMemcpyAsync(p->ws + p->wl.layers, p->layers.data(), sizeof(LayerDesc) * p->layers.size(),
+                             cudaMemcpyHostToDevice, st));
+    return MOE_OK;
+}
+
+moe_status moe_pool_lookup(moe_pool* p, int32_t layer, const int32_t* experts, int32_t n, int32_t* slots_out)
+{
+    if (!p || !experts || !slots_out || n < 0)
+        return fail(MOE_E_INVALID, "bad lookup arguments");
+    if (layer < 0 || layer >= p->L)
+        return fail(MOE_E_INVALID, "layer %d out of range", layer);
+    for (int i = 0; i < n; ++i)
+        if (experts[i] < 0 || experts[i] >= p->shape.n_experts)
+            return fail(MOE_E_INVALID, "expert %d out of range", experts[i]);
+    p->policy.lookup(layer, experts, n, slots_out, &p->hits, &p->misses);
+    return MOE_OK;
+}
+
+moe_status moe_pool_load_slot(moe_pool* p, int32_t layer, int32_t expert, const void* h_blob, void* copy_stream,
+                              int32_t* slot_out)
+{
+    if (!p || !h_blob || !slot_out)
+        return fail(MOE_E_INVALID, "bad load_slot arguments");
+    if (layer < 0 || layer >= p->L || expert < 0 || expert >= p->shape.n_experts)
+        return fail(MOE_E_INVALID, "load_slot(%d, %d) out of range", layer, expert);
+    const int have = p->policy.slot_of(layer, expert);
+    if (have >= 0) {  // already resident: nothing to copy
+        int64_t h = 0, m = 0;
+        int32_t s;
+        p->policy.lookup(layer, &expert, 1, &s, &h, &m);
+        *slot_out = have;
+        return MOE_OK;
+    }
+    int victim = -1;
+    const int s = p->policy.choose(&victim);
+    if (s < 0)
+        return fail(MOE_E_POOL_FULL, "every one of the %d slots is pinned", p->S);
+    const size_t bytes = p->geo.stride;
+    if (p->copy_hook) {
+        if (p->copy_hook(p->copy_user, s, h_blob, bytes) != 0)
+            return fail(MOE_E_CUDA, "copy into slot %d failed (copy hook)", s);
+    } else {
+        if (!p->arena)
+            return fail(MOE_E_INVALID, "host-only pool cannot copy");
+        cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+        if (p->slot_last_use[s])
+            CUDA_TRY(cudaStreamWaitEvent(cs, p->slot_last_use[s], 0));
+        CUDA_TRY(cudaMemcpyAsync(p->arena + (size_t)s * bytes, h_blob, bytes, cudaMemcpyHostToDevice, cs));
+        p->last_copy_stream = cs;
+        p->loads_pending = true;
+    }
+    p->policy.install(layer, expert, s);
+    p->bytes_loaded += (int64_t)bytes;
+    *slot_out = s;
+    return MOE_OK;
+}
+
+moe_status moe_pool_wait_loads(moe_pool* p, void* compute_stream)
+{
+    if (!p)
+        return fail(MOE_E_INVALID, "NULL pool");
+    if (!p->loads_pending)
+        return MOE_OK;
+    if (!p->loads_done)
+        CUDA_TRY(cudaEventCreateWithFlags(&p->loads_done, cudaEventDisableTiming));
+    CUDA_TRY(cudaEventRecord(p->loads_done, p->last_copy_stream));
+    CUDA_TRY(cudaStreamWaitEvent(static_cast<cudaStream_t>(compute_stream), p->loads_done, 0));
+    p->loads_pending = false;
+    return MOE_OK;
+}
+
+moe_status moe_pool_release(moe_pool* p, void* compute_stream)
+{
+    if (!p)
+        return fail(MOE_E_INVALID, "NULL pool");
+    if (p->arena && !p->copy_hook && !p->policy.pinned_list().empty()) {
+        const size_t kRing = 256;
+        if (p->ring.size() < kRing) {
+            cudaEvent_t ev;
+            CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+            p->ring.push_back(ev);
+        }
+        cudaEvent_t ev = p->ring[p->ring_next % p->ring.size()];
+        ++p->ring_next;
+        // A ring event recorded again later only makes a wait on it later (still safe).
+        CUDA_TRY(cudaEventRecord(ev, static_cast<cudaStream_t>(compute_stream)));
+        for (int s : p->policy.pinned_list())
+            p->slot_last_use[s] = ev;
+    }
+    p->policy.release();
+    return MOE_OK;
+}
+
+moe_status moe_pool_stats(const moe_pool* p, int64_t* hits, int64_t* misses, int64_t* bytes_loaded)
+{
+    if (!p)
+        return fail(MOE_E_INVALID, "NULL pool");
+    if (hits)
+        *hits = p->hits;
+    if (misses)
+        *misses = p->misses;
+    if (bytes_loaded)
+        *bytes_loaded = p->bytes_loaded;
+    return MOE_OK;
+}
+
+// test hook (declared in moe_test.h): replace the device copy of load_slot by a host callback
+moe_status moe_pool_set_copy_hook(moe_pool* p, int (*fn)(void*, int32_t, const void*, size_t), void* user)
+{
+    if (!p)
+        return fail(MOE_E_INVALID, "NULL pool");
+    p->copy_hook = fn;
+    p->copy_user = user;
+    return MOE_OK;
+}
+
+moe_status moe_pool_slot_of(const moe_pool* p, int32_t layer, int32_t expert, int32_t* slot)
+{
+    if (!p || !slot || layer < 0 || layer >= p->L || expert < 0 || expert >= p->shape.n_experts)
+        return fail(MOE_E_INVALID, "bad slot_of arguments");
+    *slot = p->policy.slot_of(layer, expert);
+    return MOE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+StepParams base_params(const moe_pool* p)
+{
+    StepParams P{};
+    const moe_shape& s = p->shape;
+    P.H = s.hidden;
+    P.E = s.n_experts;
+    P.k = s.top_k;
+    P.I = s.inter;
+    P.Is = s.shared_inter;
+    P.bits = s.bits;
+    P.group = s.group;
+    P.flags = s.flags;
+    P.geo = p->geo;
+    P.geo_s = p->geo_s;
+    P.arena = p->arena;
+    P.stride = p->geo.stride;
+    P.table = reinterpret_cast<const int32_t*>(p->ws + p->wl.table);
+    P.layers = reinterpret_cast<const LayerDesc*>(p->ws + p->wl.layers);
+    P.logits = reinterpret_cast<float*>(p->ws + p->wl.logits);
+    P.hbuf = reinterpret_cast<float*>(p->ws + p->wl.hbuf);
+    P.xbuf = reinterpret_cast<float*>(p->ws + p->wl.xbuf);
+    P.bar = reinterpret_cast<unsigned long long*>(p->ws + p->wl.bar);
+    P.status = reinterpret_cast<int*>(p->ws + p->wl.status);
+    P.timeout_ns = p->timeout_ns;
+    for (int j = 0; j < kMaxK; ++j)
+        P.slots[j] = -1;
+    return P;
+}
+
+moe_status check_layers(const moe_pool* p, int layer0, int n)
+{
+    if (!p || !p->ws)
+        return fail(MOE_E_INVALID, "pool has no device workspace");
+    if (layer0 < 0 || n <= 0 || layer0 + n > p->L)
+        return fail(MOE_E_INVALID, "layers [%d, %d) out of range [0, %d)", layer0, layer0 + n, p->L);
+    for (int l = layer0; l < layer0 + n; ++l)
+        if (!p->layers[l].router)
+            return fail(MOE_E_INVALID, "layer %d has no weights (moe_pool_set_layer)", l);
+    return MOE_OK;
+}
+
+moe_status launch(const moe_pool* p, const StepParams& P, cudaStream_t st)
+{
+    int dev = -1;
+    CUDA_TRY(cudaGetDevice(&dev));
+    if (dev != p->device)
+        return fail(MOE_E_INVALID, "current device %d differs from the pool's device %d", dev, p->device);
+    void* args[] = {const_cast<StepParams*>(&P)};
+    CUDA_TRY(cudaLaunchCooperativeKernel((const void*)moe_decode_kernel, dim3(p->grid), dim3(kThreads), args,
+                                         p->smem, st));
+    return MOE_OK;
+}
+
+moe_status check_ptr(const void* ptr, size_t align, const char* what)
+{
+    if (!ptr)
+        return fail(MOE_E_INVALID, "%s is NULL", what);
+    if (reinterpret_cast<uintptr_t>(ptr) % align)
+        return fail(MOE_E_INVALID, "%s must be %zu-byte aligned", what, align);
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_layer_forward(moe_pool* p, int32_t layer, const void* d_x, int32_t n_tokens, float* d_y,
+                             int32_t* d_topk_idx, float* d_topk_w, void* stream)
+{
+    moe_status st = check_layers(p, layer, 1);
+    if (st != MOE_OK)
+        return st;
+    if (n_tokens <= 0)
+        return fail(MOE_E_INVALID, "n_tokens must be positive");
+    if ((st = check_ptr(d_x, 16, "d_x")) != MOE_OK || (st = check_ptr(d_y, 16, "d_y")) != MOE_OK)
+        return st;
+    StepParams P = base_params(p);
+    P.mode = kModeFull;
+    P.layer0 = layer;
+    P.n_layers = 1;
+    P.n_tokens = n_tokens;
+    P.x_in = d_x;
+    P.y_out = d_y;
+    P.topk_idx = d_topk_idx;
+    P.topk_w = d_topk_w;
+    return launch(p, P, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_stack_forward(moe_pool* p, int32_t layer0, int32_t n_layers, const float* d_x, float* d_x_out,
+                             float* d_trace, int32_t* d_topk_idx, float* d_topk_w, void* stream)
+{
+    moe_status st = check_layers(p, layer0, n_layers);
+    if (st != MOE_OK)
+        return st;
+    if ((p->shape.flags & (MOE_PRENORM | MOE_RESIDUAL)) != (MOE_PRENORM | MOE_RESIDUAL))
+        return fail(MOE_E_SHAPE, "a stack needs MOE_PRENORM | MOE_RESIDUAL in the shape flags");
+    if ((st = check_ptr(d_x, 16, "d_x")) != MOE_OK || (st = check_ptr(d_x_out, 16, "d_x_out")) != MOE_OK)
+        return st;
+    StepParams P = base_params(p);
+    P.mode = kModeFull;
+    P.layer0 = layer0;
+    P.n_layers = n_layers;
+    P.n_tokens = 1;
+    P.x_in = d_x;
+    P.y_out = d_x_out;
+    P.trace = d_trace;
+    P.topk_idx = d_topk_idx;
+    P.topk_w = d_topk_w;
+    return launch(p, P, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_route(moe_pool* p, int32_t layer, const void* d_x, int32_t* d_topk_idx, float* d_topk_w, void* stream)
+{
+    moe_status st = check_layers(p, layer, 1);
+    if (st != MOE_OK)
+        return st;
+    if ((st = check_ptr(d_x, 16, "d_x")) != MOE_OK || (st = check_ptr(d_topk_idx, 4, "d_topk_idx")) != MOE_OK ||
+        (st = check_ptr(d_topk_w, 4, "d_topk_w")) != MOE_OK)
+        return st;
+    StepParams P = base_params(p);
+    P.mode = kModeRoute;
+    P.layer0 = layer;
+    P.n_layers = 1;
+    P.n_tokens = 1;
+    P.x_in = d_x;
+    P.topk_idx = d_topk_idx;
+    P.topk_w = d_topk_w;
+    return launch(p, P, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_experts(moe_pool* p, int32_t layer, const void* d_x, const float* d_topk_w, const int32_t* h_slots,
+                       float* d_y, void* stream)
+{
+    moe_status st = check_layers(p, layer, 1);
+    if (st != MOE_OK)
+        return st;
+    if ((st = check_ptr(d_x, 16, "d_x")) != MOE_OK || (st = check_ptr(d_y, 16, "d_y")) != MOE_OK ||
+        (st = check_ptr(d_topk_w, 4, "d_topk_w")) != MOE_OK || (st = check_ptr(h_slots, 4, "h_slots")) != MOE_OK)
+        return st;
+    StepParams P = base_params(p);
+    for (int j = 0; j < p->shape.top_k; ++j) {
+        if (h_slots[j] < 0 || h_slots[j] >= p->S)
+            return fail(MOE_E_INVALID, "slot %d of rank %d out of range [0, %d)", h_slots[j], j, p->S);
+        P.slots[j] = h_slots[j];
+    }
+    P.mode = kModeExperts;
+    P.layer0 = layer;
+    P.n_layers = 1;
+    P.n_tokens = 1;
+    P.x_in = d_x;
+    P.y_out = d_y;
+    P.topk_w = const_cast<float*>(d_topk_w);
+    return launch(p, P, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_forward_scalar(moe_pool* p, int32_t layer, const void* d_x, float* d_y, int32_t* d_topk_idx,
+                                    float* d_topk_w, void* stream)
+{
+    moe_status st = check_layers(p, layer, 1);
+    if (st != MOE_OK)
+        return st;
+    if (p->shape.flags & (MOE_PRENORM | MOE_RESIDUAL))
+        return fail(MOE_E_SHAPE, "the scalar reference path takes a bf16 layer input (no pre-norm, no residual)");
+    if ((st = check_ptr(d_x, 16, "d_x")) != MOE_OK || (st = check_ptr(d_y, 16, "d_y")) != MOE_OK)
+        return st;
+    StepParams P = base_params(p);
+    P.mode = kModeFull;
+    P.layer0 = layer;
+    P.n_layers = 1;
+    P.n_tokens = 1;
+    P.x_in = d_x;
+    P.y_out = d_y;
+    P.topk_idx = d_topk_idx;
+    P.topk_w = d_topk_w;
+    int32_t* sel = reinterpret_cast<int32_t*>(p->ws + p->wl.sel);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int Imax = P.I > P.Is ? P.I : P.Is;
+    scalar_router<<<(P.E + 127) / 128, 128, 0, cs>>>(P);
+    scalar_topk<<<1, 32, 0, cs>>>(P, sel);
+    scalar_gateup<<<((P.k + 1) * Imax + 127) / 128, 128, 0, cs>>>(P, sel);
+    scalar_down<<<(P.H + 127) / 128, 128, 0, cs>>>(P, sel);
+    CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+moe_status moe_device_status(moe_pool* p, void* stream, int32_t* h_status)
+{
+    if (!p || !p->ws || !h_status)
+        return fail(MOE_E_INVALID, "bad device_status arguments");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaStreamSynchronize(cs));
+    int32_t v = 0;
+    CUDA_TRY(cudaMemcpy(&v, p->ws + p->wl.status, sizeof v, cudaMemcpyDeviceToHost));
+    if (v != 0) {
+        CUDA_TRY(cudaMemset(p->ws + p->wl.status, 0, sizeof(int32_t)));
+        if (v == MOE_E_TIMEOUT)
+            CUDA_TRY(cudaMemset(p->ws + p->wl.bar, 0, sizeof(unsigned long long)));
+        CUDA_TRY(cudaDeviceSynchronize());
+    }
+    *h_status = v;
+    return MOE_OK;
+}
+
+}  // extern "C"

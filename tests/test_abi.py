@@ -1,0 +1,143 @@
+"""The C ABI without a GPU: exported symbols, blob sizes and bytes against the oracle's own
+writer, argument checks, and the bounded pool's slot policy against a brute-force simulator."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from int4_routed_expert_05_b300 import moe, synth
+from int4_routed_expert_05_b300.resident import moe_shape
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int4_routed_expert_05_b300 import _build
+    _build.build()
+    return moe.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moe.ENTRY_POINTS)
+
+
+@pytest.mark.parametrize("sh", [synth.TINY, synth.TINY.with_bits(8), synth.S80, synth.S35.with_bits(8)])
+def test_blob_sizes_match_oracle(lib, orc, sh):
+    ms = moe_shape(sh)
+    assert moe.expert_bytes(ms) == orc.blob_bytes(sh)
+    assert moe.expert_stride(ms) == orc.blob_stride(sh)
+    assert moe.expert_stride(ms, shared=True) == orc.blob_stride(sh, shared=True)
+
+
+@pytest.mark.parametrize("sh", [synth.TINY, synth.TINY.with_bits(8), synth.S80])
+def test_pack_matches_oracle_writer(lib, orc, sh):
+    """The library's packer and the oracle's own writer produce the same bytes."""
+    for e, shared in ((3, False), (synth.SHARED_EXPERT, True)):
+        t = synth.expert_tensors(sh, 9, 1, e)
+        a = moe.pack_expert(moe_shape(sh), t, shared=shared)
+        b = orc.pack(sh, t, shared=shared)
+        assert np.array_equal(a, b)
+
+
+def test_shape_and_argument_errors(lib):
+    bad = moe.make_shape(300, 16, 2, 64, 64)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.pack_expert(bad, synth.expert_tensors(synth.TINY, 0, 0, 0))
+    assert ei.value.status == moe.E_SHAPE
+    t = synth.expert_tensors(synth.TINY, 0, 0, 0)
+    t["gate_q"] = t["gate_q"].copy()
+    t["gate_q"][0, 0] = 16
+    with pytest.raises(moe.MoeError) as ei:
+        moe.pack_expert(moe_shape(synth.TINY), t)
+    assert ei.value.status == moe.E_INVALID
+    for args in [(17, 16, 2, 64, 64), (256, 16, 17, 64, 64), (256, 513, 2, 64, 64), (256, 16, 2, 96, 64)]:
+        with pytest.raises(moe.MoeError):
+            moe.Pool(moe.make_shape(*args), 1, 4)
+    assert moe.workspace_bytes(moe_shape(synth.S80), 48) > 0
+
+
+def _host_pool(n_slots, layers=4, experts=16):
+    sh = moe.make_shape(256, experts, 2, 64, 64)
+    return moe.Pool(sh, layers, n_slots)
+
+
+def test_policy_matches_bruteforce_simulator(lib):
+    from oracle.pool_sim import PoolSim
+    rng = np.random.default_rng(0)
+    for n_slots, trace_kind in [(6, "uniform"), (12, "zipf"), (3, "zipf")]:
+        pool = _host_pool(n_slots)
+        pool.set_copy_hook(lambda slot, blob, n: 0)
+        sim = PoolSim(n_slots)
+        blob = np.zeros(16, np.uint8)
+        for step in range(300):
+            layer = int(rng.integers(0, 4))
+            if trace_kind == "uniform":
+                ex = rng.choice(16, size=2, replace=False)
+            else:
+                p = 1.0 / np.arange(1, 17) ** 1.1
+                ex = rng.choice(16, size=2, replace=False, p=p / p.sum())
+            got = list(pool.lookup(layer, ex))
+            want = sim.lookup(layer, ex)
+            assert got == want, (step, got, want)
+            for e, s in zip(ex, got):
+                if s < 0:
+                    ws = sim.load(layer, int(e))
+                    if ws is None:
+                        with pytest.raises(moe.MoeError) as ei:
+                            pool.load_slot(layer, int(e), blob)
+                        assert ei.value.status == moe.E_POOL_FULL
+                    else:
+                        assert pool.load_slot(layer, int(e), blob) == ws
+            for l in range(4):
+                for e in range(16):
+                    k = sim.slot_of((l, e))
+                    assert pool.slot_of(l, e) == k
+            pool.release()
+            sim.release()
+        hits, misses, nbytes = pool.stats()
+        assert hits + misses == 600
+
+
+def test_pool_full_when_everything_pinned(lib):
+    pool = _host_pool(2)
+    pool.set_copy_hook(lambda slot, blob, n: 0)
+    blob = np.zeros(16, np.uint8)
+    pool.lookup(0, [1, 2, 3])
+    assert pool.load_slot(0, 1, blob) == 0
+    assert pool.load_slot(0, 2, blob) == 1
+    with pytest.raises(moe.MoeError) as ei:
+        pool.load_slot(0, 3, blob)
+    assert ei.value.status == moe.E_POOL_FULL
+    pool.release()
+    assert pool.load_slot(0, 3, blob) in (0, 1)
+
+
+def test_injected_copy_failure_leaves_pool_unchanged(lib):
+    pool = _host_pool(4)
+    blob = np.zeros(16, np.uint8)
+    calls = []
+    pool.set_copy_hook(lambda slot, b, n: calls.append(slot) or 0)
+    pool.lookup(1, [5])
+    s = pool.load_slot(1, 5, blob)
+    pool.release()
+    before = [[pool.slot_of(l, e) for e in range(16)] for l in range(4)]
+    pool.set_copy_hook(lambda slot, b, n: 1)
+    pool.lookup(2, [7])
+    with pytest.raises(moe.MoeError) as ei:
+        pool.load_slot(2, 7, blob)
+    assert ei.value.status == moe.E_CUDA
+    after = [[pool.slot_of(l, e) for e in range(16)] for l in range(4)]
+    assert before == after and pool.slot_of(1, 5) == s and calls == [s]
