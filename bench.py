@@ -226,6 +226,8 @@ def run_ours(args):
     from int4_routed_expert_05_b300.resident import Resident
 
     name, L, bits, desc = CONFIGS[args.config]
+    if args.layers:
+        L, desc = args.layers, desc + f" (first {args.layers} layers only)"
     sh = _shape(name, bits)
     flags = moe.RENORM | moe.PRENORM | moe.RESIDUAL
     R = Resident(sh, L, SEED, flags=flags, verbose=(rank == 0))
@@ -337,6 +339,8 @@ def main():
     ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers of the stack (small cases for profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
