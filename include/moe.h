@@ -210,6 +210,40 @@ moe_status moe_layer_forward_scalar(moe_pool* pool, int32_t layer, const void* d
                                     int32_t* d_topk_idx, float* d_topk_w, void* stream);
 
 /* ----------------------------------------------------------------------------------------- */
+/* Forward pass that allocates nothing                                                         */
+/* ----------------------------------------------------------------------------------------- */
+/*
+ * The pages have no counterpart of this entry point; it exists for callers that may not allocate
+ * device memory at all: a plugin running inside a host application that owns every device
+ * allocation, or a latency-critical loop that must never call cudaMalloc (which can synchronise
+ * the device). Such a caller cannot provide the workspace that moe_pool_create needs.
+ *
+ * moe_layer_forward_static computes the same layer as moe_layer_forward (same kernel, same
+ * arguments d_x, n_tokens, d_y, d_topk_idx, d_topk_w, same results) without a pool. Its scratch
+ * (barrier counter, status word, expert table, layer descriptor, logits, intermediate
+ * activations) is a file-scope device array of MOE_STATIC_SCRATCH_BYTES that every GPU which
+ * loads the library keeps until the process exits. It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *  - d_experts: the n_experts routed blobs in the fixed-stride container layout, expert e at
+ *    d_experts + e * moe_expert_stride(shape, 0) (256-byte aligned); w: the layer's resident
+ *    weights as for moe_pool_set_layer. All caller-owned, device memory.
+ *  - d_status: NULL, or a device int32 that receives the layer's device status (MOE_OK, or
+ *    MOE_E_TIMEOUT if a device-side wait ran past 2 s); it is reset to MOE_OK by the call.
+ *  - A shape whose scratch does not fit returns MOE_E_NOMEM (message in moe_last_error); other
+ *    argument errors return MOE_E_INVALID or MOE_E_SHAPE before anything is enqueued.
+ *  - The first call on a device does a one-time set-up with that device current (the scratch
+ *    array's device address via cudaGetSymbolAddress, the SM count). Make that first call before
+ *    any stream capture.
+ *  - Every call on a device shares the one scratch array, which keeps the previous call's
+ *    contents; each call resets the parts that must start at zero. Calls that overlap on the GPU
+ *    (issued on different streams without ordering) race on the array and give wrong results.
+ * Enqueues two kernels on `stream` and returns. */
+#define MOE_STATIC_SCRATCH_BYTES (128 * 1024)
+moe_status moe_layer_forward_static(const moe_shape* shape, const void* d_experts, const moe_layer_weights* w,
+                                    const void* d_x, int32_t n_tokens, float* d_y, int32_t* d_topk_idx,
+                                    float* d_topk_w, int32_t* d_status, void* stream);
+
+/* ----------------------------------------------------------------------------------------- */
 /* Status                                                                                      */
 /* ----------------------------------------------------------------------------------------- */
 

@@ -100,6 +100,11 @@ moe_status check_shape(const moe_shape* s)
 
 }  // namespace
 
+namespace moe {
+// Message for moe_last_error() from entry points defined in other files of the library.
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace moe
+
 struct moe_pool {
     moe_shape shape{};
     int L = 0, S = 0;

@@ -1,0 +1,240 @@
+// noalloc.cu -- moe_layer_forward_static: one MoE layer whose scratch lives in a file-scope device
+// array, for callers that must not allocate device memory (see include/moe.h).
+//
+// The fused decode kernel needs scratch beyond its inputs and outputs: a grid-barrier counter, a
+// status word, the expert -> blob table, the layer descriptor, the router logits, the
+// intermediate activations h of every selected expert and a residual row. moe_layer_forward takes
+// that scratch from a caller-allocated workspace. This entry point takes it from
+// g_static_scratch instead, a fixed-size array that every device loading the library holds until
+// the process exits. The experts are read where the fixed-stride container puts them: expert e at
+// d_experts + e * stride.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "layout.h"
+
+namespace moe {
+__global__ void moe_decode_kernel(const __grid_constant__ StepParams P);
+__host__ __device__ uint32_t decode_smem_bytes(const StepParams& P);
+void set_last_error(const char* msg);
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = 128 * 1024;  // MOE_STATIC_SCRATCH_BYTES in moe.h
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kStaticTimeoutNs = 2000000000ull;
+
+static_assert(kStaticScratchBytes == MOE_STATIC_SCRATCH_BYTES, "moe.h states the scratch size");
+
+}  // namespace
+
+// Shared by every call on a device. In host code this name is only a stand-in for the symbol:
+// the device address comes from cudaGetSymbolAddress in device_setup().
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+struct StaticLayout {
+    size_t bar, status, table, layer, logits, hbuf, xbuf, total;
+};
+
+size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+StaticLayout static_layout(const moe_shape& s)
+{
+    StaticLayout l{};
+    const int Imax = s.inter > s.shared_inter ? s.inter : s.shared_inter;
+    size_t o = 0;
+    l.bar = o;
+    o += 256;
+    l.status = o;
+    o += 256;
+    l.table = o;
+    o = round256(o + sizeof(int32_t) * (size_t)s.n_experts);
+    l.layer = o;
+    o = round256(o + sizeof(LayerDesc));
+    l.logits = o;
+    o = round256(o + sizeof(float) * (size_t)s.n_experts);
+    l.hbuf = o;
+    o = round256(o + sizeof(float) * (size_t)(s.top_k + 1) * Imax);
+    l.xbuf = o;
+    o = round256(o + sizeof(float) * (size_t)s.hidden);
+    l.total = o;
+    return l;
+}
+
+moe_status fail_static(moe_status st, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    set_last_error(buf);
+    return st;
+}
+
+struct DeviceSetup {
+    bool ready;
+    uint8_t* scratch;  // device address of g_static_scratch on this device
+    int sms;
+};
+
+std::mutex g_setup_mu;
+DeviceSetup g_setup[kMaxDevices];
+
+// Once per device, with that device current: the device address of the scratch array and the
+// SM count (the cooperative grid).
+moe_status device_setup(int dev, DeviceSetup* out)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail_static(MOE_E_INVALID, "device %d outside the %d devices this entry point serves", dev,
+                           kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    DeviceSetup& d = g_setup[dev];
+    if (!d.ready) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess)
+            return fail_static(MOE_E_CUDA, "cudaGetSymbolAddress(g_static_scratch) failed: %s", cudaGetErrorString(e));
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess || sms <= 0)
+            return fail_static(MOE_E_CUDA, "cudaDeviceGetAttribute(SM count) failed: %s", cudaGetErrorString(e));
+        d.scratch = static_cast<uint8_t*>(ptr);
+        d.sms = sms;
+        d.ready = true;
+    }
+    *out = d;
+    return MOE_OK;
+}
+
+// Resets what must start at zero (barrier counter, status words) and writes the identity
+// expert table and the layer descriptor into the scratch array.
+__global__ void static_prepare(uint8_t* scratch, StaticLayout sl, int n_experts, LayerDesc desc, int* status_out)
+{
+    if (threadIdx.x == 0) {
+        *reinterpret_cast<unsigned long long*>(scratch + sl.bar) = 0ull;
+        *reinterpret_cast<int*>(scratch + sl.status) = 0;
+        *reinterpret_cast<LayerDesc*>(scratch + sl.layer) = desc;
+        if (status_out)
+            *status_out = 0;
+    }
+    int32_t* table = reinterpret_cast<int32_t*>(scratch + sl.table);
+    for (int e = threadIdx.x; e < n_experts; e += blockDim.x)
+        table[e] = e;
+}
+
+moe_status check_static_shape(const moe_shape* s)
+{
+    if (!s)
+        return fail_static(MOE_E_INVALID, "shape is NULL");
+    if (s->group != 64 || (s->bits != 4 && s->bits != 8))
+        return fail_static(MOE_E_SHAPE, "group must be 64 and bits 4 or 8");
+    if (s->hidden <= 0 || s->hidden % 256 != 0 || s->hidden > 8192)
+        return fail_static(MOE_E_SHAPE, "hidden must be a positive multiple of 256, at most 8192 (got %d)", s->hidden);
+    if (s->inter <= 0 || s->inter % 64 != 0 || s->shared_inter <= 0 || s->shared_inter % 64 != 0 ||
+        s->inter > 4096 || s->shared_inter > 4096)
+        return fail_static(MOE_E_SHAPE, "inter and shared_inter must be positive multiples of 64, at most 4096");
+    if (s->top_k < 1 || s->top_k > kMaxK || s->n_experts < s->top_k || s->n_experts > kMaxE)
+        return fail_static(MOE_E_SHAPE, "need 1 <= top_k <= %d and top_k <= n_experts <= %d", kMaxK, kMaxE);
+    if (s->flags & ~(MOE_RENORM | MOE_PRENORM | MOE_RESIDUAL))
+        return fail_static(MOE_E_SHAPE, "unknown flag bits 0x%x", s->flags);
+    return MOE_OK;
+}
+
+bool misaligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; }
+
+}  // namespace
+
+extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const void* d_experts,
+                                               const moe_layer_weights* w, const void* d_x, int32_t n_tokens,
+                                               float* d_y, int32_t* d_topk_idx, float* d_topk_w,
+                                               int32_t* d_status, void* stream)
+{
+    moe_status st = check_static_shape(shape);
+    if (st != MOE_OK)
+        return st;
+    const StaticLayout sl = static_layout(*shape);
+    if (sl.total > kStaticScratchBytes)
+        return fail_static(MOE_E_NOMEM,
+                           "this shape needs %zu bytes of scratch; the static scratch array holds %zu "
+                           "(MOE_STATIC_SCRATCH_BYTES): use moe_layer_forward with a workspace instead",
+                           sl.total, kStaticScratchBytes);
+    if (!d_experts || !w || !w->router || !w->shared_blob || !w->shared_gate || !d_x || !d_y)
+        return fail_static(MOE_E_INVALID, "d_experts, the layer weights, d_x and d_y are required");
+    if (misaligned(d_experts, 256) || misaligned(w->router, 16) || misaligned(w->shared_blob, 16) ||
+        misaligned(w->shared_gate, 16) || misaligned(d_x, 16) || misaligned(d_y, 16))
+        return fail_static(MOE_E_INVALID, "d_experts must be 256-byte aligned; weights, d_x and d_y 16-byte aligned");
+    if (n_tokens <= 0)
+        return fail_static(MOE_E_INVALID, "n_tokens must be positive");
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail_static(MOE_E_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    DeviceSetup ds{};
+    if ((st = device_setup(dev, &ds)) != MOE_OK)
+        return st;
+
+    StepParams P{};
+    P.H = shape->hidden;
+    P.E = shape->n_experts;
+    P.k = shape->top_k;
+    P.I = shape->inter;
+    P.Is = shape->shared_inter;
+    P.bits = shape->bits;
+    P.group = shape->group;
+    P.flags = shape->flags;
+    P.geo = blob_geo(P.H, P.I, P.bits, P.group);
+    P.geo_s = blob_geo(P.H, P.Is, P.bits, P.group);
+    P.arena = static_cast<const uint8_t*>(d_experts);
+    P.stride = P.geo.stride;
+    uint8_t* s = ds.scratch;
+    P.table = reinterpret_cast<const int32_t*>(s + sl.table);
+    P.layers = reinterpret_cast<const LayerDesc*>(s + sl.layer);
+    P.logits = reinterpret_cast<float*>(s + sl.logits);
+    P.hbuf = reinterpret_cast<float*>(s + sl.hbuf);
+    P.xbuf = reinterpret_cast<float*>(s + sl.xbuf);
+    P.bar = reinterpret_cast<unsigned long long*>(s + sl.bar);
+    P.status = d_status ? reinterpret_cast<int*>(d_status) : reinterpret_cast<int*>(s + sl.status);
+    P.timeout_ns = kStaticTimeoutNs;
+    for (int j = 0; j < kMaxK; ++j)
+        P.slots[j] = -1;
+    P.mode = kModeFull;
+    P.layer0 = 0;
+    P.n_layers = 1;
+    P.n_tokens = n_tokens;
+    P.x_in = d_x;
+    P.y_out = d_y;
+    P.topk_idx = d_topk_idx;
+    P.topk_w = d_topk_w;
+
+    const uint32_t smem = decode_smem_bytes(P);
+    cudaFuncAttributes fa{};
+    if ((e = cudaFuncGetAttributes(&fa, moe_decode_kernel)) != cudaSuccess)
+        return fail_static(MOE_E_CUDA, "cudaFuncGetAttributes failed: %s", cudaGetErrorString(e));
+    if ((uint32_t)fa.maxDynamicSharedSizeBytes < smem &&
+        (e = cudaFuncSetAttribute(moe_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess)
+        return fail_static(MOE_E_CUDA, "cudaFuncSetAttribute(%u bytes) failed: %s", smem, cudaGetErrorString(e));
+
+    const LayerDesc desc{static_cast<const uint16_t*>(w->router), static_cast<const uint8_t*>(w->shared_blob),
+                         static_cast<const uint16_t*>(w->shared_gate), w->logit_bias};
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    static_prepare<<<1, 256, 0, cs>>>(s, sl, P.E, desc, d_status ? reinterpret_cast<int*>(d_status) : nullptr);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return fail_static(MOE_E_CUDA, "scratch preparation launch failed: %s", cudaGetErrorString(e));
+    void* args[] = {&P};
+    e = cudaLaunchCooperativeKernel((const void*)moe_decode_kernel, dim3(ds.sms), dim3(kThreads), args, smem, cs);
+    if (e != cudaSuccess)
+        return fail_static(MOE_E_CUDA, "decode kernel launch failed: %s", cudaGetErrorString(e));
+    return MOE_OK;
+}

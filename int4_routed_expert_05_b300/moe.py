@@ -25,7 +25,7 @@ ENTRY_POINTS = [
     "moe_pool_sync", "moe_pool_lookup", "moe_pool_load_slot", "moe_pool_wait_loads", "moe_pool_release",
     "moe_pool_stats", "moe_layer_forward", "moe_stack_forward", "moe_route", "moe_experts",
     "moe_layer_forward_scalar", "moe_device_status", "moe_pool_set_timeout", "moe_pool_grid",
-    "moe_last_error", "moe_pool_slot_of", "moe_pool_set_copy_hook",
+    "moe_last_error", "moe_pool_slot_of", "moe_pool_set_copy_hook", "moe_layer_forward_static",
 ]
 
 
@@ -86,6 +86,7 @@ def load() -> ctypes.CDLL:
         "moe_last_error": (ctypes.c_char_p, []),
         "moe_pool_slot_of": (ST, [P, I32, I32, ctypes.POINTER(I32)]),
         "moe_pool_set_copy_hook": (ST, [P, COPY_HOOK, P]),
+        "moe_layer_forward_static": (ST, [PS, P, ctypes.POINTER(LayerWeights), P, I32, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -119,6 +120,16 @@ def _s(stream) -> int | None:
     if isinstance(stream, int):
         return stream or None
     return stream.cuda_stream or None
+
+
+def layer_forward_static(shape: Shape, experts, router, shared_blob, shared_gate, x, n_tokens, y,
+                         topk_idx=None, topk_w=None, status=None, logit_bias=None, stream=None):
+    """moe_layer_forward_static: one layer with the library's fixed scratch array (no device
+    allocation by the library or the caller); experts = the fixed-stride blobs, expert e at
+    experts + e * stride."""
+    w = LayerWeights(_p(router), _p(shared_blob), _p(shared_gate), _p(logit_bias))
+    _check(load().moe_layer_forward_static(ctypes.byref(shape), _p(experts), ctypes.byref(w), _p(x), n_tokens, _p(y),
+                                           _p(topk_idx), _p(topk_w), _p(status), _s(stream)))
 
 
 def make_shape(hidden, n_experts, top_k, inter, shared_inter, bits=4, group=64, flags=RENORM) -> Shape:
