@@ -9,7 +9,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libmoe.so")
 SOURCES = ["api.cu", "decode.cu", "scalar.cu", "noalloc.cu"]
-HEADERS = ["layout.h", "policy.h"]
+HEADERS = ["layout.h", "policy.h", "host.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

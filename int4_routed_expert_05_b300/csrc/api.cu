@@ -8,12 +8,12 @@
 #include <vector>
 
 #include "../../include/moe.h"
+#include "host.h"
 #include "layout.h"
 #include "policy.h"
 
 namespace moe {
 __global__ void moe_decode_kernel(const __grid_constant__ StepParams P);
-__host__ __device__ uint32_t decode_smem_bytes(const StepParams& P);
 __global__ void scalar_router(const StepParams P);
 __global__ void scalar_topk(const StepParams P, int32_t* sel);
 __global__ void scalar_gateup(const StepParams P, const int32_t* sel);
@@ -47,30 +47,28 @@ moe_status fail(moe_status st, const char* fmt, ...)
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t bar, status, table, layers, logits, hbuf, xbuf, sel, total;
+    size_t bar, status, table, layers, logits, hbuf, sel, xlog, xh, xacc, total;
 };
 
 WsLayout ws_layout(const moe_shape& s, int L)
 {
     WsLayout w{};
-    size_t o = 0;
-    w.bar = o;
-    o += 256;
-    w.status = o;
-    o += 256;
-    w.table = o;
-    o = up256(o + sizeof(int32_t) * (size_t)L * s.n_experts);
-    w.layers = o;
-    o = up256(o + sizeof(LayerDesc) * (size_t)L);
-    w.logits = o;
-    o = up256(o + sizeof(float) * (size_t)s.n_experts);
     const int Imax = s.inter > s.shared_inter ? s.inter : s.shared_inter;
-    w.hbuf = o;
-    o = up256(o + sizeof(float) * (size_t)(s.top_k + 1) * Imax);
-    w.xbuf = o;
-    o = up256(o + sizeof(float) * (size_t)s.hidden);
-    w.sel = o;
-    o = up256(o + sizeof(int32_t) * 3 * kMaxK);
+    size_t o = 0;
+    auto take = [&](size_t& field, size_t bytes) {
+        field = o;
+        o = up256(o + bytes);
+    };
+    take(w.bar, 256);
+    take(w.status, 256);
+    take(w.table, sizeof(int32_t) * (size_t)L * s.n_experts);
+    take(w.layers, sizeof(LayerDesc) * (size_t)L);
+    take(w.logits, sizeof(float) * (size_t)s.n_experts);
+    take(w.hbuf, sizeof(float) * (size_t)(s.top_k + 1) * Imax);
+    take(w.sel, sizeof(int32_t) * 3 * kMaxK);
+    take(w.xlog, sizeof(unsigned long long) * (size_t)s.n_experts);
+    take(w.xh, sizeof(unsigned long long) * (size_t)(s.top_k + 1) * Imax);
+    take(w.xacc, sizeof(long long) * 2 * (size_t)s.hidden);
     w.total = o;
     return w;
 }
@@ -114,6 +112,9 @@ struct moe_pool {
     size_t ws_bytes = 0;
     WsLayout wl{};
     BlobGeo geo{}, geo_s{};
+    StageGeo sg{};
+    CUtensorMap tmap[3];
+    uint32_t epoch_next = 1;  // exchange-buffer epochs (the workspace starts zeroed)
     std::vector<LayerDesc> layers;
     SlotPolicy policy;
     int64_t hits = 0, misses = 0, bytes_loaded = 0;
@@ -248,16 +249,18 @@ moe_status moe_pool_create(const moe_shape* s, int32_t n_layers, int32_t n_slots
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess)
         return cleanup(fail(MOE_E_CUDA, "cudaDeviceGetAttribute failed"));
-    StepParams probe{};
-    probe.H = s->hidden;
-    probe.E = s->n_experts;
-    probe.k = s->top_k;
-    probe.I = s->inter;
-    probe.Is = s->shared_inter;
-    probe.bits = s->bits;
-    probe.group = s->group;
-    p->smem = decode_smem_bytes(probe);
-    cudaError_t e = cudaFuncSetAttribute(moe_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem);
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) != cudaSuccess)
+        return cleanup(fail(MOE_E_CUDA, "cudaDeviceGetAttribute failed"));
+    p->smem = fused_smem_bytes(s->hidden, s->n_experts, s->top_k, s->inter, s->shared_inter, s->bits, sms, optin);
+    if (p->smem == 0)
+        return cleanup(fail(MOE_E_SHAPE, "the fused decode kernel cannot stage this shape on %d SMs with %d bytes of "
+                            "shared memory per block", sms, optin));
+    p->sg = stage_geo(s->hidden, s->n_experts, s->top_k, s->inter, s->shared_inter, s->bits, sms);
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, moe_decode_kernel);
+    if (e == cudaSuccess && (uint32_t)fa.maxDynamicSharedSizeBytes < p->smem)
+        e = cudaFuncSetAttribute(moe_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem);
     if (e != cudaSuccess)
         return cleanup(fail(MOE_E_CUDA, "cudaFuncSetAttribute(%u bytes): %s", p->smem, cudaGetErrorString(e)));
     int per_sm = 0;
@@ -265,6 +268,9 @@ moe_status moe_pool_create(const moe_shape* s, int32_t n_layers, int32_t n_slots
     if (e != cudaSuccess || per_sm < 1)
         return cleanup(fail(MOE_E_CUDA, "decode kernel cannot be resident (%d per SM): %s", per_sm,
                             cudaGetErrorString(e)));
+    const int rc = encode_arena_maps(p->tmap, p->arena, n_slots, p->geo, p->sg);
+    if (rc != 0)
+        return cleanup(fail(MOE_E_CUDA, "cuTensorMapEncodeTiled over the arena failed (%d)", rc));
     p->grid = sms;  // one block per SM
     if (cudaMemset(p->ws, 0, p->wl.total) != cudaSuccess ||
         cudaMemset(p->ws + p->wl.table, 0xFF, sizeof(int32_t) * (size_t)n_layers * s->n_experts) != cudaSuccess ||
@@ -477,13 +483,18 @@ StepParams base_params(const moe_pool* p)
     P.flags = s.flags;
     P.geo = p->geo;
     P.geo_s = p->geo_s;
+    P.sg = p->sg;
+    for (int m = 0; m < 3; ++m)
+        P.tmap[m] = p->tmap[m];
     P.arena = p->arena;
     P.stride = p->geo.stride;
     P.table = reinterpret_cast<const int32_t*>(p->ws + p->wl.table);
     P.layers = reinterpret_cast<const LayerDesc*>(p->ws + p->wl.layers);
     P.logits = reinterpret_cast<float*>(p->ws + p->wl.logits);
     P.hbuf = reinterpret_cast<float*>(p->ws + p->wl.hbuf);
-    P.xbuf = reinterpret_cast<float*>(p->ws + p->wl.xbuf);
+    P.xlog = reinterpret_cast<unsigned long long*>(p->ws + p->wl.xlog);
+    P.xh = reinterpret_cast<unsigned long long*>(p->ws + p->wl.xh);
+    P.xacc = reinterpret_cast<long long*>(p->ws + p->wl.xacc);
     P.bar = reinterpret_cast<unsigned long long*>(p->ws + p->wl.bar);
     P.status = reinterpret_cast<int*>(p->ws + p->wl.status);
     P.timeout_ns = p->timeout_ns;
@@ -504,13 +515,18 @@ moe_status check_layers(const moe_pool* p, int layer0, int n)
     return MOE_OK;
 }
 
-moe_status launch(const moe_pool* p, const StepParams& P, cudaStream_t st)
+moe_status launch(moe_pool* p, StepParams& P, cudaStream_t st)
 {
     int dev = -1;
     CUDA_TRY(cudaGetDevice(&dev));
     if (dev != p->device)
         return fail(MOE_E_INVALID, "current device %d differs from the pool's device %d", dev, p->device);
-    void* args[] = {const_cast<StepParams*>(&P)};
+    const uint32_t steps = P.mode == kModeFull ? (uint32_t)(P.n_tokens * P.n_layers) : 1u;
+    if (next_epochs(p->epoch_next, steps, &P.epoch0)) {
+        CUDA_TRY(cudaMemsetAsync(p->ws + p->wl.xlog, 0, p->wl.xh - p->wl.xlog, st));
+        CUDA_TRY(cudaMemsetAsync(p->ws + p->wl.xh, 0, p->wl.xacc - p->wl.xh, st));
+    }
+    void* args[] = {&P};
     CUDA_TRY(cudaLaunchCooperativeKernel((const void*)moe_decode_kernel, dim3(p->grid), dim3(kThreads), args,
                                          p->smem, st));
     return MOE_OK;

@@ -1,0 +1,85 @@
+// host.h -- host-side helpers shared by the entry points: TMA map encoding over an expert arena
+// and the epoch bookkeeping of the exchange buffers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "layout.h"
+
+namespace moe {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
+inline EncodeTiledFn encode_tiled_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// The three code sections (gate.q, up.q, down.q) of every blob of an arena of n_slots blobs as 3D
+// byte tensors [slots][rows][row bytes]; boxes of SR rows by one column block, 128-byte swizzled
+// when rows are at least 128 bytes wide. Returns 0 or a CUresult (-1: no driver entry point).
+inline int encode_arena_maps(CUtensorMap (&maps)[3], const uint8_t* arena, int n_slots, const BlobGeo& geo,
+                             const StageGeo& sg)
+{
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn)
+        return -1;
+    for (int m = 0; m < 3; ++m) {
+        const bool dn = m == 2;
+        const cuuint64_t dims[3] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)geo.rows[m], (cuuint64_t)n_slots};
+        const cuuint64_t strides[2] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)geo.stride};
+        const cuuint32_t box[3] = {(cuuint32_t)(dn ? sg.cbw_d : sg.cbw_gu), (cuuint32_t)sg.SR, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        const CUtensorMapSwizzle swz = (dn ? sg.swz_d : sg.swz_gu) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+        const CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, (void*)(arena + geo.q_off[m]), dims, strides,
+                              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return (int)r;
+    }
+    return 0;
+}
+
+// Shapes the fused kernel takes: the staging plan must fit in shared memory and the grid must
+// hold at least one block per routed expert. Returns the dynamic shared memory bytes, 0 if not.
+inline uint32_t fused_smem_bytes(int H, int E, int k, int I, int Is, int bits, int grid, int smem_optin)
+{
+    if (grid < k)
+        return 0;
+    const StageGeo sg = stage_geo(H, E, k, I, Is, bits, grid);
+    if (sg.SR > kMaxBoxRows)
+        return 0;
+    const uint32_t bytes = smem_plan(H, E, k, I, Is, bits, grid).total + 1024;
+    return bytes <= (uint32_t)smem_optin ? bytes : 0;
+}
+
+// Epochs of the exchange buffers: a launch of n steps takes [epoch0, epoch0 + n). When the 32-bit
+// counter would wrap, the caller clears the buffers (so no stale pair can match) and starts at 1.
+inline bool next_epochs(uint32_t& counter, uint32_t n, uint32_t* epoch0)
+{
+    bool reset = false;
+    if (counter == 0 || (uint64_t)counter + n >= 0xFFFFFFF0ull) {
+        counter = 1;
+        reset = true;
+    }
+    *epoch0 = counter;
+    counter += n;
+    return reset;
+}
+
+}  // namespace moe

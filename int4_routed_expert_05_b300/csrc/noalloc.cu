@@ -2,8 +2,9 @@
 // array, for callers that must not allocate device memory (see include/moe.h).
 //
 // The fused decode kernel needs scratch beyond its inputs and outputs: a grid-barrier counter, a
-// status word, the expert -> blob table, the layer descriptor, the router logits, the
-// intermediate activations h of every selected expert and a residual row. moe_layer_forward takes
+// status word, the expert -> blob table, the layer descriptor, the exchange buffers through which
+// blocks share router logits and intermediate activations, and the output accumulators.
+// moe_layer_forward takes
 // that scratch from a caller-allocated workspace. This entry point takes it from
 // g_static_scratch instead, a fixed-size array that every device loading the library holds until
 // the process exits. The experts are read where the fixed-stride container puts them: expert e at
@@ -15,11 +16,11 @@
 #include <mutex>
 
 #include "../../include/moe.h"
+#include "host.h"
 #include "layout.h"
 
 namespace moe {
 __global__ void moe_decode_kernel(const __grid_constant__ StepParams P);
-__host__ __device__ uint32_t decode_smem_bytes(const StepParams& P);
 void set_last_error(const char* msg);
 }  // namespace moe
 
@@ -42,7 +43,7 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 namespace {
 
 struct StaticLayout {
-    size_t bar, status, table, layer, logits, hbuf, xbuf, total;
+    size_t bar, status, table, layer, xlog, xh, xacc, total;
 };
 
 size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -60,12 +61,12 @@ StaticLayout static_layout(const moe_shape& s)
     o = round256(o + sizeof(int32_t) * (size_t)s.n_experts);
     l.layer = o;
     o = round256(o + sizeof(LayerDesc));
-    l.logits = o;
-    o = round256(o + sizeof(float) * (size_t)s.n_experts);
-    l.hbuf = o;
-    o = round256(o + sizeof(float) * (size_t)(s.top_k + 1) * Imax);
-    l.xbuf = o;
-    o = round256(o + sizeof(float) * (size_t)s.hidden);
+    l.xlog = o;
+    o = round256(o + sizeof(unsigned long long) * (size_t)s.n_experts);
+    l.xh = o;
+    o = round256(o + sizeof(unsigned long long) * (size_t)(s.top_k + 1) * Imax);
+    l.xacc = o;
+    o = round256(o + sizeof(long long) * 2 * (size_t)s.hidden);
     l.total = o;
     return l;
 }
@@ -85,6 +86,8 @@ struct DeviceSetup {
     bool ready;
     uint8_t* scratch;  // device address of g_static_scratch on this device
     int sms;
+    int smem_optin;
+    uint32_t epoch;    // next exchange-buffer epoch on this device (0: buffers not yet cleared)
 };
 
 std::mutex g_setup_mu;
@@ -108,8 +111,14 @@ moe_status device_setup(int dev, DeviceSetup* out)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess || sms <= 0)
             return fail_static(MOE_E_CUDA, "cudaDeviceGetAttribute(SM count) failed: %s", cudaGetErrorString(e));
+        int optin = 0;
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess)
+            return fail_static(MOE_E_CUDA, "cudaDeviceGetAttribute(shared memory) failed: %s", cudaGetErrorString(e));
         d.scratch = static_cast<uint8_t*>(ptr);
         d.sms = sms;
+        d.smem_optin = optin;
+        d.epoch = 0;
         d.ready = true;
     }
     *out = d;
@@ -183,6 +192,10 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     DeviceSetup ds{};
     if ((st = device_setup(dev, &ds)) != MOE_OK)
         return st;
+    const uint32_t smem = fused_smem_bytes(shape->hidden, shape->n_experts, shape->top_k, shape->inter,
+                                           shape->shared_inter, shape->bits, ds.sms, ds.smem_optin);
+    if (smem == 0)
+        return fail_static(MOE_E_SHAPE, "the fused decode kernel cannot stage this shape on this GPU");
 
     StepParams P{};
     P.H = shape->hidden;
@@ -195,14 +208,18 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     P.flags = shape->flags;
     P.geo = blob_geo(P.H, P.I, P.bits, P.group);
     P.geo_s = blob_geo(P.H, P.Is, P.bits, P.group);
+    P.sg = stage_geo(P.H, P.E, P.k, P.I, P.Is, P.bits, ds.sms);
+    const int rc = encode_arena_maps(P.tmap, static_cast<const uint8_t*>(d_experts), P.E, P.geo, P.sg);
+    if (rc != 0)
+        return fail_static(MOE_E_CUDA, "cuTensorMapEncodeTiled over the expert blobs failed (%d)", rc);
     P.arena = static_cast<const uint8_t*>(d_experts);
     P.stride = P.geo.stride;
     uint8_t* s = ds.scratch;
     P.table = reinterpret_cast<const int32_t*>(s + sl.table);
     P.layers = reinterpret_cast<const LayerDesc*>(s + sl.layer);
-    P.logits = reinterpret_cast<float*>(s + sl.logits);
-    P.hbuf = reinterpret_cast<float*>(s + sl.hbuf);
-    P.xbuf = reinterpret_cast<float*>(s + sl.xbuf);
+    P.xlog = reinterpret_cast<unsigned long long*>(s + sl.xlog);
+    P.xh = reinterpret_cast<unsigned long long*>(s + sl.xh);
+    P.xacc = reinterpret_cast<long long*>(s + sl.xacc);
     P.bar = reinterpret_cast<unsigned long long*>(s + sl.bar);
     P.status = d_status ? reinterpret_cast<int*>(d_status) : reinterpret_cast<int*>(s + sl.status);
     P.timeout_ns = kStaticTimeoutNs;
@@ -217,7 +234,6 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     P.topk_idx = d_topk_idx;
     P.topk_w = d_topk_w;
 
-    const uint32_t smem = decode_smem_bytes(P);
     cudaFuncAttributes fa{};
     if ((e = cudaFuncGetAttributes(&fa, moe_decode_kernel)) != cudaSuccess)
         return fail_static(MOE_E_CUDA, "cudaFuncGetAttributes failed: %s", cudaGetErrorString(e));
@@ -229,6 +245,15 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     const LayerDesc desc{static_cast<const uint16_t*>(w->router), static_cast<const uint8_t*>(w->shared_blob),
                          static_cast<const uint16_t*>(w->shared_gate), w->logit_bias};
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    bool clear;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        clear = next_epochs(g_setup[dev].epoch, (uint32_t)n_tokens, &P.epoch0);
+    }
+    if (clear) {  // no earlier pair may carry an epoch of this call
+        if ((e = cudaMemsetAsync(s + sl.xlog, 0, sl.xacc - sl.xlog, cs)) != cudaSuccess)
+            return fail_static(MOE_E_CUDA, "clearing the exchange buffers failed: %s", cudaGetErrorString(e));
+    }
     static_prepare<<<1, 256, 0, cs>>>(s, sl, P.E, desc, d_status ? reinterpret_cast<int*>(d_status) : nullptr);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return fail_static(MOE_E_CUDA, "scratch preparation launch failed: %s", cudaGetErrorString(e));
