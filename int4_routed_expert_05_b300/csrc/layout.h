@@ -91,11 +91,12 @@ struct LayerDesc {
 // Work split (identical on host and device)
 // ------------------------------------------------------------------------------------------
 
-// [part(n, p, i), part(n, p, i + 1)) is part i of [0, n) cut into p nearly equal ranges.
-MOE_HD int part(int n, int parts, int i) { return (int)(((long long)n * i) / parts); }
+// [part(n, p, i), part(n, p, i + 1)) is part i of [0, n) cut into p nearly equal ranges
+// (n * p < 2^32 for every shape the kernels take).
+MOE_HD int part(int n, int parts, int i) { return (int)(((unsigned)n * (unsigned)i) / (unsigned)parts); }
 // Routed expert of rank j is served by the blocks [grp_start(j), grp_start(j + 1)).
-MOE_HD int grp_of(int b, int G, int k) { return (int)(((long long)b * k) / G); }
-MOE_HD int grp_start(int j, int G, int k) { return (int)(((long long)j * G + k - 1) / k); }
+MOE_HD int grp_of(int b, int G, int k) { return (int)(((unsigned)b * (unsigned)k) / (unsigned)G); }
+MOE_HD int grp_start(int j, int G, int k) { return (int)(((unsigned)j * (unsigned)G + (unsigned)k - 1u) / (unsigned)k); }
 MOE_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 // How one block's share of the routed experts is staged: row ranges of gate/up and down rows
@@ -185,13 +186,14 @@ struct StepParams {
 // ------------------------------------------------------------------------------------------
 
 struct SmemPlan {
-    uint32_t mbar, ctl, x, u, up, uc, lg, lkey, lidx;
+    uint32_t ctx, mbar, ctl, x, u, up, uc, lg, lkey, lidx;
     uint32_t rt, wsg, sgq, ssb, sdq, sdsb;
     uint32_t ring, rsb, rdsb;
     uint32_t hs, uhs, hj, uhj, hv, sp, spd;
     uint32_t total;
 };
 
+constexpr uint32_t kCtxBytes = 1024;  // room for the kernel's block context
 constexpr int kNumMbar = kWarps + 3;  // ring slots, routed scales, dense prefetch, shared down
 // control words: sel_idx[kMaxK], sel_w[kMaxK], sel_slot[kMaxK], red[64], misc[16], imisc[16]
 constexpr int kCtlWords = 3 * kMaxK + 64 + 16 + 16;
@@ -215,15 +217,16 @@ MOE_HD SmemPlan smem_plan(int H, int E, int k, int I, int Is, int bits, int G)
         field = o;
         o += bytes;
     };
+    take(s.ctx, kCtxBytes, 16);
     take(s.mbar, 8u * kNumMbar, 16);
     take(s.ctl, 4u * kCtlWords, 16);
     take(s.x, 4u * H, 16);
     take(s.u, 2u * H, 16);
     take(s.up, 2u * KU, 16);
-    take(s.uc, 4u * NCu, 16);
+    take(s.uc, 8u * NCu, 16);
     take(s.lg, 4u * (E > 32 ? E : 32), 16);
-    take(s.lkey, 4u * kWarps * kMaxK, 16);
-    take(s.lidx, 4u * kWarps * kMaxK, 16);
+    take(s.lkey, 4u * (kMaxE + 2 * kWarps + 8), 16);
+    take(s.lidx, 4u * (kMaxE + 2 * kWarps + 8), 16);
     take(s.rt, 2u * sg.Rr * H, 128);
     take(s.wsg, 2u * H, 16);
     take(s.sgq, 2u * sg.Rs * rb_gu, 128);
@@ -234,14 +237,15 @@ MOE_HD SmemPlan smem_plan(int H, int E, int k, int I, int Is, int bits, int G)
     take(s.rsb, 4u * sb_span_max(sg.Rgu, 2 * ngu), 16);
     take(s.rdsb, 2u * sb_span_max(sg.Rd, 2 * ngd), 16);
     take(s.hs, 2u * 2 * KDs, 16);
-    take(s.uhs, 4u * NCds, 16);
+    take(s.uhs, 8u * NCds, 16);
     take(s.hj, 2u * 2 * KD, 16);
-    take(s.uhj, 4u * NCd, 16);
+    take(s.uhj, 8u * NCd, 16);
     take(s.hv, 4u * (I > Is ? I : Is), 16);
     const int spr = sg.Rgu > sg.Rs ? sg.Rgu : sg.Rs;
-    take(s.sp, 4u * spr * 2 * NCu, 16);
+    take(s.sp, 4u * spr * 2 * sg.ncb_gu, 16);
     const int sdr = sg.Rd > sg.Rsd ? sg.Rd : sg.Rsd;
-    const int sdc = NCd > NCds ? NCd : NCds;
+    const int ncb_ds = cdiv(NCds, 4);
+    const int sdc = sg.ncb_d > ncb_ds ? sg.ncb_d : ncb_ds;
     take(s.spd, 4u * sdr * sdc, 16);
     s.total = align_to(o, 16);
     return s;

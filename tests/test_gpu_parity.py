@@ -95,7 +95,10 @@ def test_s80_single_layer(orc):
 
 
 def test_scalar_reference_kernels_agree(orc):
-    """The fused kernel and the plain one-thread-per-output kernels on the same pool."""
+    """The fused kernel and the plain one-thread-per-output kernels on the same pool. The fused
+    kernel reads codes as 1024 + q in fp16 and takes 1024 * sum(u) back out of each 64-element
+    chunk sum in fp32, which costs up to ~2^-11 of that offset term per chunk: the two paths then
+    agree to a few 1e-5 relative, inside the same 1e-4 bound the oracle parity asserts."""
     for sh, seed in [(synth.TINY, 1), (synth.Shape(512, 64, 6, 128, 192, bits=8), 2)]:
         R = Resident(sh, 1, seed)
         x = _bits(synth.activation_bits(sh, seed, 0))
@@ -104,7 +107,7 @@ def test_scalar_reference_kernels_agree(orc):
         torch.cuda.synchronize()
         assert torch.equal(idx, idxs)
         assert torch.allclose(w, ws, rtol=0, atol=1e-6)
-        assert rel_l2(y.cpu().numpy(), ys.cpu().numpy()) < 1e-5
+        assert rel_l2(y.cpu().numpy(), ys.cpu().numpy()) < TIGHT
 
 
 def test_bitwise_reproducible_and_slot_invariant(orc):
