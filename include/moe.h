@@ -203,6 +203,18 @@ moe_status moe_route(moe_pool* pool, int32_t layer, const void* d_x, int32_t* d_
 moe_status moe_experts(moe_pool* pool, int32_t layer, const void* d_x, const float* d_topk_w,
                        const int32_t* h_slots, float* d_y, void* stream);
 
+/* Bounded mode, a whole pre-norm residual stack for one token, driven on the host ([qpack],
+ * [route]): per layer moe_route, a device-to-host read of the k selected experts (synchronous),
+ * moe_pool_lookup, moe_pool_load_slot for every miss from h_blobs on copy_stream, moe_pool_wait_loads,
+ * moe_experts and moe_pool_release. h_blobs: host array [n_layers][n_experts] (indexed from
+ * layer0) of pinned host blob pointers (moe_expert_stride bytes each; entries may repeat).
+ * d_x: fp32 [H] input residual; d_x_out: fp32 [H] final residual (the pool workspace holds the
+ * residuals in between). h_topk_idx: host int32 [n_layers][k] receiving the selections, or NULL.
+ * Returns when the last layer has been enqueued on compute_stream. */
+moe_status moe_stack_forward_streamed(moe_pool* pool, int32_t layer0, int32_t n_layers, const float* d_x,
+                                      float* d_x_out, const void* const* h_blobs, void* compute_stream,
+                                      void* copy_stream, int32_t* h_topk_idx);
+
 /* Reference path: the same layer for one token with plain kernels (one thread per logit, one
  * thread per selection, one thread per output row, fp32 sums in index order). Used to cross-check
  * the fused kernel. Same arguments as moe_layer_forward with n_tokens = 1. */

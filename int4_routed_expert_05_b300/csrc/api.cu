@@ -47,7 +47,7 @@ moe_status fail(moe_status st, const char* fmt, ...)
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t bar, status, table, layers, logits, hbuf, sel, xlog, xh, xacc, total;
+    size_t bar, status, table, layers, logits, hbuf, sel, xlog, xh, xacc, xbuf, total;
 };
 
 WsLayout ws_layout(const moe_shape& s, int L)
@@ -67,8 +67,9 @@ WsLayout ws_layout(const moe_shape& s, int L)
     take(w.hbuf, sizeof(float) * (size_t)(s.top_k + 1) * Imax);
     take(w.sel, sizeof(int32_t) * 3 * kMaxK);
     take(w.xlog, sizeof(unsigned long long) * (size_t)s.n_experts);
-    take(w.xh, sizeof(unsigned long long) * (size_t)(s.top_k + 1) * Imax);
+    take(w.xh, sizeof(unsigned long long) * (size_t)(s.top_k + 1) * xh_stride(s.inter, s.shared_inter));
     take(w.xacc, sizeof(long long) * 2 * (size_t)s.hidden);
+    take(w.xbuf, sizeof(float) * 2 * (size_t)s.hidden);
     w.total = o;
     return w;
 }
@@ -271,6 +272,8 @@ moe_status moe_pool_create(const moe_shape* s, int32_t n_layers, int32_t n_slots
     const int rc = encode_arena_maps(p->tmap, p->arena, n_slots, p->geo, p->sg);
     if (rc != 0)
         return cleanup(fail(MOE_E_CUDA, "cuTensorMapEncodeTiled over the arena failed (%d)", rc));
+    if (sms > kMaxGrid)
+        return cleanup(fail(MOE_E_SHAPE, "%d SMs exceed the %d blocks a decode launch supports", sms, kMaxGrid));
     p->grid = sms;  // one block per SM
     if (cudaMemset(p->ws, 0, p->wl.total) != cudaSuccess ||
         cudaMemset(p->ws + p->wl.table, 0xFF, sizeof(int32_t) * (size_t)n_layers * s->n_experts) != cudaSuccess ||
@@ -679,6 +682,62 @@ moe_status moe_device_status(moe_pool* p, void* stream, int32_t* h_status)
         CUDA_TRY(cudaDeviceSynchronize());
     }
     *h_status = v;
+    return MOE_OK;
+}
+
+moe_status moe_stack_forward_streamed(moe_pool* p, int32_t layer0, int32_t n_layers, const float* d_x, float* d_x_out,
+                                      const void* const* h_blobs, void* compute_stream, void* copy_stream,
+                                      int32_t* h_topk_idx)
+{
+    moe_status st = check_layers(p, layer0, n_layers);
+    if (st != MOE_OK)
+        return st;
+    if ((p->shape.flags & (MOE_PRENORM | MOE_RESIDUAL)) != (MOE_PRENORM | MOE_RESIDUAL))
+        return fail(MOE_E_SHAPE, "a stack needs MOE_PRENORM | MOE_RESIDUAL in the shape flags");
+    if ((st = check_ptr(d_x, 16, "d_x")) != MOE_OK || (st = check_ptr(d_x_out, 16, "d_x_out")) != MOE_OK)
+        return st;
+    if (!h_blobs)
+        return fail(MOE_E_INVALID, "h_blobs is NULL");
+    const int E = p->shape.n_experts, k = p->shape.top_k, H = p->shape.hidden;
+    cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+    int32_t* d_idx = reinterpret_cast<int32_t*>(p->ws + p->wl.sel);
+    float* d_w = reinterpret_cast<float*>(d_idx + kMaxK);
+    float* bufs[2] = {reinterpret_cast<float*>(p->ws + p->wl.xbuf), reinterpret_cast<float*>(p->ws + p->wl.xbuf) + H};
+    const float* cur = d_x;
+    int32_t idx[kMaxK], slots[kMaxK];
+    for (int li = 0; li < n_layers; ++li) {
+        const int l = layer0 + li;
+        float* out = li == n_layers - 1 ? d_x_out : bufs[li & 1];
+        if ((st = moe_route(p, l, cur, d_idx, d_w, cs)) != MOE_OK)
+            return st;
+        CUDA_TRY(cudaMemcpyAsync(idx, d_idx, sizeof(int32_t) * k, cudaMemcpyDeviceToHost, cs));
+        CUDA_TRY(cudaStreamSynchronize(cs));
+        for (int j = 0; j < k; ++j)
+            if (idx[j] < 0 || idx[j] >= E)
+                return fail(MOE_E_CUDA, "routing returned expert %d at layer %d (device status %s)", idx[j], l,
+                            "unknown: read it with moe_device_status");
+        if ((st = moe_pool_lookup(p, l, idx, k, slots)) != MOE_OK)
+            return st;
+        for (int j = 0; j < k; ++j) {
+            if (slots[j] >= 0)
+                continue;
+            const void* blob = h_blobs[(size_t)l * E + idx[j]];
+            if (!blob)
+                return fail(MOE_E_INVALID, "no host blob for expert %d of layer %d", idx[j], l);
+            if ((st = moe_pool_load_slot(p, l, idx[j], blob, copy_stream, &slots[j])) != MOE_OK)
+                return st;
+        }
+        if ((st = moe_pool_wait_loads(p, compute_stream)) != MOE_OK)
+            return st;
+        if ((st = moe_experts(p, l, cur, d_w, slots, out, compute_stream)) != MOE_OK)
+            return st;
+        if ((st = moe_pool_release(p, compute_stream)) != MOE_OK)
+            return st;
+        if (h_topk_idx)
+            for (int j = 0; j < k; ++j)
+                h_topk_idx[(size_t)li * k + j] = idx[j];
+        cur = out;
+    }
     return MOE_OK;
 }
 

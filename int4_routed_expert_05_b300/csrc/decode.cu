@@ -177,6 +177,8 @@ __device__ __forceinline__ void red_add_s64(long long* p, long long v)
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void st_s64(long long* p, long long v)
 {
     asm volatile("st.relaxed.gpu.global.s64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -343,22 +345,6 @@ __device__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base)
     C.span_sd = sb_span_max(C.sg.Rsd, 2 * C.ngds);
 }
 
-__device__ float block_sum(const Ctx& C, float v)
-{
-    v = warp_sum(v);
-    __syncthreads();
-    if (LANE == 0)
-        C.red[WARP] = v;
-    __syncthreads();
-    if (WARP == 0) {
-        float s = LANE < kWarps ? C.red[LANE] : 0.f;
-        s = warp_sum(s);
-        if (LANE == 0)
-            C.red[32] = s;
-    }
-    __syncthreads();
-    return C.red[32];
-}
 
 // Block-uniform time limit check: true once the wait that started at t0 ran past the limit.
 __device__ __forceinline__ bool timed_out(const StepParams& P, long long t0)
@@ -941,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         const int l = P.layer0 + li;
         const LayerDesc L = P.layers[l];
         const uint32_t epoch = P.epoch0 + (uint32_t)step;
-        long long* X = P.xacc + (size_t)(t & 1) * C.H;
+        long long* X = P.xacc + (size_t)(step & 1) * C.H;
         const bool prenorm = (P.flags & kPrenorm) != 0;
 
         // ---------------- 1. layer input ----------------
@@ -1031,10 +1017,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
                     vv += pg[ncb + cb];
                 }
                 const float h = __fdividef(gg, 1.f + __expf(-gg)) * vv;
-                st_pair(P.xh + (size_t)C.k * (C.I > C.Is ? C.I : C.Is) + drow.s0 + TID, epoch, h);
+                st_pair(P.xh + (size_t)C.k * xh_stride(C.I, C.Is) + drow.s0 + TID, epoch, h);
             }
         }
         __syncthreads();
+        if (experts && TID == 0) {
+            // this block's step flag, after a gpu-scope fence: every store of the block so far,
+            // the accumulator base included, is visible to whoever sees the flag
+            fence_gpu();
+            st_pair(P.xh + (size_t)C.k * xh_stride(C.I, C.Is) + C.Is + CTA, epoch, 0.f);
+        }
         // next step's router rows, shared gate vector and shared gate/up rows
         if (step + 1 < n_steps) {
             if (TID == 0) {
@@ -1121,7 +1113,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
 
         // ---------------- 5. shared expert down rows ----------------
         float* hval = C.hv;
-        if (!poll_pairs(limit_cycles(P), P.status, P.xh + (size_t)C.k * (C.I > C.Is ? C.I : C.Is), C.Is, epoch, hval)) {
+        // the shared h values and every block's step flag: past this point the accumulator bases of all
+        // blocks (stored at the end of the previous step, before their flag's fence) are visible
+        if (!poll_pairs(limit_cycles(P), P.status, P.xh + (size_t)C.k * xh_stride(C.I, C.Is), C.Is + GRID, epoch, hval)) {
             ok = false;
             break;
         }
@@ -1149,6 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
                 for (int cb = 0; cb < ncb; ++cb)
                     ys += C.spd[TID * ncb + cb];
                 const float v = C.misc[0] * ys;
+                fence_gpu();  // after the shared h pairs: every block's accumulator base is in place
                 if (!(fabsf(v) < kFixMax))
                     set_status(P.status, kStatusInvalid);
                 else
@@ -1212,7 +1207,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         }
         __syncthreads();
         {
-            const int hdim = C.I > C.Is ? C.I : C.Is;
+            const int hdim = xh_stride(C.I, C.Is);
             unsigned long long* xh = P.xh + (size_t)W.j * hdim;
             if (TID < own) {
                 float h = 0.f;
@@ -1281,6 +1276,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
                 for (int cb = 0; cb < sg.ncb_d; ++cb)
                     yj += C.spd[TID * sg.ncb_d + cb];
                 const float v = C.sel_w[W.j] * yj;
+                fence_gpu();
                 if (!(fabsf(v) < kFixMax))
                     set_status(P.status, kStatusInvalid);
                 else
@@ -1288,20 +1284,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             }
         }
 
-        // next token's accumulator base (ordered before its use by the barrier below)
         const bool last_of_token = li == P.n_layers - 1;
-        if (last_of_token && t + 1 < P.n_tokens) {
-            long long* Xn = P.xacc + (size_t)((t + 1) & 1) * C.H;
-            const bool residual = (P.flags & kResidual) != 0;
-            #pragma unroll 1
-            for (int o = drow.o0 + TID; o < drow.o1; o += kThreads) {
-                float x0 = 0.f;
-                if (residual)
-                    x0 = prenorm ? ((const float*)P.x_in)[(size_t)(t + 1) * C.H + o]
-                                 : bf16f(((const uint16_t*)P.x_in)[(size_t)(t + 1) * C.H + o]);
-                st_s64(Xn + o, (long long)__float2ll_rn(x0 * kFix));
-            }
-        }
 
         // ---------------- 9. layer output ----------------
         if (!grid_barrier(P, C)) {
@@ -1316,6 +1299,24 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             C.sx[o + 1] = __ll2float_rn(b) * kFixInv;
         }
         __syncthreads();
+        // The next step's accumulator starts from this block's slice of its fp32 input: this
+        // layer's output (same token) or the next token's input. These stores reach the other
+        // blocks before any of their atomic adds of the next step: the shared-expert h pairs that
+        // every block waits for are written after a gpu-scope fence (step 2).
+        if (step + 1 < n_steps) {
+            long long* Xn = P.xacc + (size_t)((step + 1) & 1) * C.H;
+            const bool residual = (P.flags & kResidual) != 0;
+            #pragma unroll 1
+            for (int o = drow.o0 + TID; o < drow.o1; o += kThreads) {
+                float x0 = 0.f;
+                if (!last_of_token)
+                    x0 = C.sx[o];
+                else if (residual)
+                    x0 = prenorm ? ((const float*)P.x_in)[(size_t)(t + 1) * C.H + o]
+                                 : bf16f(((const uint16_t*)P.x_in)[(size_t)(t + 1) * C.H + o]);
+                st_s64(Xn + o, (long long)__float2ll_rn(x0 * kFix));
+            }
+        }
         if (last_of_token) {
             #pragma unroll 1
             for (int o = drow.o0 + TID; o < drow.o1; o += kThreads)

@@ -29,6 +29,11 @@ constexpr int kChunk = 64;      // nibbles per MMA chunk (one int4 quantisation 
 constexpr int kCb = 128;        // bytes of one staged column block (the 128-byte swizzle span)
 constexpr int kMaxBoxRows = 256;
 constexpr uint64_t kStrideAlign = 4096;
+constexpr int kMaxGrid = 512;   // most blocks a decode launch may have (one per SM)
+
+// Row stride (in pairs) of the h exchange buffer: rows 0..k-1 hold the routed experts' h, row k the
+// shared expert's h followed by one step flag per block.
+MOE_HD int xh_stride(int I, int Is) { return I > Is + kMaxGrid ? I : Is + kMaxGrid; }
 constexpr float kFix = 4294967296.f;       // fixed-point scale of the output accumulator (2^32)
 constexpr float kFixInv = 2.3283064365386963e-10f;
 constexpr float kFixMax = 1073741824.f;    // largest |contribution| accepted (2^30)
@@ -240,7 +245,7 @@ MOE_HD SmemPlan smem_plan(int H, int E, int k, int I, int Is, int bits, int G)
     take(s.uhs, 8u * NCds, 16);
     take(s.hj, 2u * 2 * KD, 16);
     take(s.uhj, 8u * NCd, 16);
-    take(s.hv, 4u * (I > Is ? I : Is), 16);
+    take(s.hv, 4u * xh_stride(I, Is), 16);
     const int spr = sg.Rgu > sg.Rs ? sg.Rgu : sg.Rs;
     take(s.sp, 4u * spr * 2 * sg.ncb_gu, 16);
     const int sdr = sg.Rd > sg.Rsd ? sg.Rd : sg.Rsd;

@@ -64,7 +64,7 @@ StaticLayout static_layout(const moe_shape& s)
     l.xlog = o;
     o = round256(o + sizeof(unsigned long long) * (size_t)s.n_experts);
     l.xh = o;
-    o = round256(o + sizeof(unsigned long long) * (size_t)(s.top_k + 1) * Imax);
+    o = round256(o + sizeof(unsigned long long) * (size_t)(s.top_k + 1) * xh_stride(s.inter, s.shared_inter));
     l.xacc = o;
     o = round256(o + sizeof(long long) * 2 * (size_t)s.hidden);
     l.total = o;
@@ -192,6 +192,8 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     DeviceSetup ds{};
     if ((st = device_setup(dev, &ds)) != MOE_OK)
         return st;
+    if (ds.sms > kMaxGrid)
+        return fail_static(MOE_E_SHAPE, "%d SMs exceed the %d blocks a decode launch supports", ds.sms, kMaxGrid);
     const uint32_t smem = fused_smem_bytes(shape->hidden, shape->n_experts, shape->top_k, shape->inter,
                                            shape->shared_inter, shape->bits, ds.sms, ds.smem_optin);
     if (smem == 0)

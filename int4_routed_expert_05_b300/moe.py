@@ -26,6 +26,7 @@ ENTRY_POINTS = [
     "moe_pool_stats", "moe_layer_forward", "moe_stack_forward", "moe_route", "moe_experts",
     "moe_layer_forward_scalar", "moe_device_status", "moe_pool_set_timeout", "moe_pool_grid",
     "moe_last_error", "moe_pool_slot_of", "moe_pool_set_copy_hook", "moe_layer_forward_static",
+    "moe_stack_forward_streamed",
 ]
 
 
@@ -87,6 +88,7 @@ def load() -> ctypes.CDLL:
         "moe_pool_slot_of": (ST, [P, I32, I32, ctypes.POINTER(I32)]),
         "moe_pool_set_copy_hook": (ST, [P, COPY_HOOK, P]),
         "moe_layer_forward_static": (ST, [PS, P, ctypes.POINTER(LayerWeights), P, I32, P, P, P, P, P]),
+        "moe_stack_forward_streamed": (ST, [P, I32, I32, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -248,6 +250,15 @@ class Pool:
     def stack_forward(self, layer0, n_layers, x, x_out, trace=None, topk_idx=None, topk_w=None, stream=None):
         _check(self.lib.moe_stack_forward(self.h, layer0, n_layers, _p(x), _p(x_out), _p(trace), _p(topk_idx),
                                           _p(topk_w), _s(stream)))
+
+    def stack_forward_streamed(self, layer0, n_layers, x, x_out, h_blobs: np.ndarray, compute_stream=None,
+                               copy_stream=None, topk_idx: np.ndarray | None = None):
+        """Bounded-mode stack for one token; h_blobs: uint64 array [n_layers][E] of pinned host
+        blob addresses. topk_idx (optional): int32 array [n_layers][k] filled with the selections."""
+        hb = np.ascontiguousarray(h_blobs, dtype=np.uint64)
+        _check(self.lib.moe_stack_forward_streamed(self.h, layer0, n_layers, _p(x), _p(x_out), hb.ctypes.data,
+                                                   _s(compute_stream), _s(copy_stream),
+                                                   None if topk_idx is None else topk_idx.ctypes.data))
 
     def route(self, layer, x, topk_idx, topk_w, stream=None):
         _check(self.lib.moe_route(self.h, layer, _p(x), _p(topk_idx), _p(topk_w), _s(stream)))

@@ -23,6 +23,16 @@ def moe_shape(sh: synth.Shape, flags: int | None = None) -> moe.Shape:
     return moe.make_shape(sh.hidden, sh.n_experts, sh.top_k, sh.inter, sh.shared_inter, sh.bits, sh.group, flags)
 
 
+def dense_layer(sh: synth.Shape, mshape: moe.Shape, seed: int, layer: int, device: str = "cuda"):
+    """Layer ``layer``'s resident weights on the device: router bf16 [E][H], shared-expert blob,
+    shared gate bf16 [H] (all drawn by ``synth``; the blob packed by the library)."""
+    router = torch.from_numpy(synth.router_bits(sh, seed, layer).view(np.int16)).to(device)
+    sb = moe.pack_expert(mshape, synth.expert_tensors(sh, seed, layer, synth.SHARED_EXPERT), shared=True)
+    shared = torch.from_numpy(sb).to(device)
+    gate = torch.from_numpy(synth.shared_gate_bits(sh, seed, layer).view(np.int16)).to(device)
+    return router, shared, gate
+
+
 class Resident:
     """n_layers layers of shape ``sh`` with every expert placed in the pool."""
 
@@ -59,10 +69,10 @@ class Resident:
         # resident dense weights of every layer
         self.router, self.shared, self.gate, self.bias = [], [], [], []
         for l in range(n_layers):
-            self.router.append(torch.from_numpy(synth.router_bits(sh, seed, l).view(np.int16)).to(device))
-            sb = moe.pack_expert(self.mshape, synth.expert_tensors(sh, seed, l, synth.SHARED_EXPERT), shared=True)
-            self.shared.append(torch.from_numpy(sb).to(device))
-            self.gate.append(torch.from_numpy(synth.shared_gate_bits(sh, seed, l).view(np.int16)).to(device))
+            rt, sb, g = dense_layer(sh, self.mshape, seed, l, device)
+            self.router.append(rt)
+            self.shared.append(sb)
+            self.gate.append(g)
             b = None if bias is None or bias[l] is None else torch.as_tensor(bias[l], dtype=torch.float32).to(device)
             self.bias.append(b)
 

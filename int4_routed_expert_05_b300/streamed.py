@@ -1,0 +1,120 @@
+"""Bounded-pool stacks: dense weights resident on the GPU, routed experts streamed on demand from a
+pinned host store into a fixed number of HBM slots (LFU + recency eviction in the library).
+
+torch supplies device memory, pinned host memory and streams; the per-layer host loop (route,
+read back the selection, look up, copy misses, run the experts, release) runs in libmoe
+(``moe_stack_forward_streamed``).
+
+The host store holds ``n_unique`` generated blobs; expert e of layer l is blob ``maps[l][e]`` (the
+same maps as ``Resident``), so a miss always copies one full blob of pinned memory whatever the
+store size. Routing popularity for the workload follows a per-layer Zipf law (see
+:func:`zipf_bias`); it enters the router as the library's ``logit_bias`` hook.
+"""
+from __future__ import annotations
+
+import time
+
+import numpy as np
+import torch
+
+from . import moe, synth
+from .resident import dense_layer, moe_shape
+
+ZIPF_S = 1.1
+
+
+def zipf_bias(sh: synth.Shape, seed: int, layer: int, beta: float, s: float = ZIPF_S) -> np.ndarray:
+    """logit_bias[e] = beta * ln p_e with p_e proportional to (rank_e + 1)^-s, rank a seeded
+    per-layer permutation of the experts. A synthetic routing-popularity hook, not part of the method."""
+    rank = synth.expert_map(sh, seed ^ 0x5A5A, layer, sh.n_experts)  # a permutation of 0..E-1
+    p = (rank.astype(np.float64) + 1.0) ** (-s)
+    p /= p.sum()
+    return (beta * np.log(p)).astype(np.float32)
+
+
+def simulated_hit_rate(sh: synth.Shape, n_layers: int, n_slots: int, beta: float, tokens: int = 96,
+                       warm: int = 32, seed: int = 0, logit_std: float | None = None) -> float:
+    """Hit rate of the library's slot policy (a host-only pool, no device) on a synthetic selection
+    trace: router logits taken as independent N(0, std^2) (std = 0.02 * sqrt(H) for the generator's
+    N(0, 0.02) router rows against an RMS-normalised input) plus the Zipf bias, top-k per layer."""
+    std = 0.02 * np.sqrt(sh.hidden) if logit_std is None else logit_std
+    ms = moe_shape(sh)
+    pool = moe.Pool(ms, n_layers, n_slots)
+    pool.set_copy_hook(lambda slot, blob, n: 0)
+    bias = [zipf_bias(sh, seed, l, beta) for l in range(n_layers)]
+    rng = np.random.default_rng(seed + 7)
+    hits = lookups = 0
+    for t in range(warm + tokens):
+        for l in range(n_layers):
+            lg = rng.standard_normal(sh.n_experts) * std + bias[l]
+            sel = np.argpartition(-lg, sh.top_k)[: sh.top_k].astype(np.int32)
+            slots = pool.lookup(l, sel)
+            for j, e in enumerate(sel):
+                if slots[j] < 0:
+                    pool.load_slot(l, int(e), 1)
+            pool.release()
+            if t >= warm:
+                hits += int((slots >= 0).sum())
+                lookups += sh.top_k
+    pool.close()
+    return hits / lookups
+
+
+def calibrate_beta(sh: synth.Shape, n_layers: int, n_slots: int, target: float = 0.55, seed: int = 0) -> float:
+    """Zipf bias strength whose simulated hit rate is closest to ``target`` (bisection)."""
+    lo, hi = 0.0, 4.0
+    for _ in range(12):
+        mid = 0.5 * (lo + hi)
+        if simulated_hit_rate(sh, n_layers, n_slots, mid, tokens=64, warm=16, seed=seed) < target:
+            lo = mid
+        else:
+            hi = mid
+    return 0.5 * (lo + hi)
+
+
+class Streamed:
+    """n_layers pre-norm residual MoE layers in bounded mode (n_slots expert slots in HBM)."""
+
+    def __init__(self, sh: synth.Shape, n_layers: int, seed: int, n_slots: int, *, n_unique: int | None = None,
+                 beta: float = 0.0, device: str = "cuda", verbose: bool = False):
+        t0 = time.time()
+        self.sh, self.L, self.seed, self.n_slots = sh, n_layers, seed, n_slots
+        E = sh.n_experts
+        self.n_unique = n_unique or E
+        self.mshape = moe_shape(sh, moe.RENORM | moe.PRENORM | moe.RESIDUAL)
+        self.stride = moe.expert_stride(self.mshape)
+        self.maps = [synth.expert_map(sh, seed, l, self.n_unique) for l in range(n_layers)]
+        self.store = torch.empty((self.n_unique, self.stride), dtype=torch.uint8, pin_memory=True)
+        for u in range(self.n_unique):
+            moe.pack_expert(self.mshape, synth.expert_tensors(sh, seed, 0, u), out=self.store[u].numpy())
+        base = self.store.data_ptr()
+        self.h_blobs = np.array([[base + int(self.maps[l][e]) * self.stride for e in range(E)]
+                                 for l in range(n_layers)], dtype=np.uint64)
+        self.beta = beta
+        self.bias = [torch.from_numpy(zipf_bias(sh, seed, l, beta)).to(device) if beta else None for l in range(n_layers)]
+        self.router, self.shared, self.gate = [], [], []
+        for l in range(n_layers):
+            rt, sb, g = dense_layer(sh, self.mshape, seed, l, device)
+            self.router.append(rt)
+            self.shared.append(sb)
+            self.gate.append(g)
+        self.arena = torch.empty(n_slots * self.stride, dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(moe.workspace_bytes(self.mshape, n_layers), dtype=torch.uint8, device=device)
+        self.pool = moe.Pool(self.mshape, n_layers, n_slots, self.arena, self.arena.numel(), self.ws, self.ws.numel())
+        for l in range(n_layers):
+            self.pool.set_layer(l, self.router[l], self.shared[l], self.gate[l], self.bias[l])
+        self.pool.sync()
+        self.copy_stream = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        if verbose:
+            print(f"[streamed] {n_layers} layers x {E} experts, {n_slots} slots ({self.arena.numel() / 2**30:.2f} GiB), "
+                  f"store {self.store.numel() / 1e9:.2f} GB pinned, beta {beta:.3f}, set-up {time.time() - t0:.1f} s",
+                  flush=True)
+
+    def bias_host(self, layer: int):
+        return None if not self.beta else zipf_bias(self.sh, self.seed, layer, self.beta)
+
+    def step(self, x: torch.Tensor, out: torch.Tensor, stream=None, topk_idx: np.ndarray | None = None):
+        """One token through all layers: x, out fp32 device tensors [H]."""
+        s = torch.cuda.current_stream() if stream is None else stream
+        self.pool.stack_forward_streamed(0, self.L, x, out, self.h_blobs, s, self.copy_stream, topk_idx)

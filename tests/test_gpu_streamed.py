@@ -1,0 +1,43 @@
+"""Bounded-pool stacks on the GPU: the per-layer host loop of moe_stack_forward_streamed (route,
+read back, LFU + recency lookup, miss copies from pinned host memory, experts, release) gives
+bit for bit the output of the resident stack, whose layers are checked against the oracle in
+test_gpu_parity (cache hit or miss gives the same answer)."""
+import numpy as np
+import pytest
+import torch
+
+from int4_routed_expert_05_b300 import moe, synth
+from int4_routed_expert_05_b300.resident import Resident
+from int4_routed_expert_05_b300.streamed import Streamed, zipf_bias
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int4_routed_expert_05_b300 import _build
+    _build.build()
+    assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("sh,n_slots", [(synth.Shape(2048, 512, 10, 512, 512), 24), (synth.TINY, 5)])
+def test_streamed_stack_equals_resident(sh, n_slots):
+    L, seed, beta, n_unique = 4, 3, 0.7, 64
+    flags = moe.RENORM | moe.PRENORM | moe.RESIDUAL
+    bias = [zipf_bias(sh, seed, l, beta) for l in range(L)]
+    R = Resident(sh, L, seed, n_unique=min(n_unique, sh.n_experts), flags=flags, bias=bias)
+    S = Streamed(sh, L, seed, n_slots, n_unique=min(n_unique, sh.n_experts), beta=beta)
+    out_s = torch.empty(sh.hidden, dtype=torch.float32, device="cuda")
+    steps = 3
+    for step in range(steps):
+        x0 = torch.from_numpy(synth.activation_f32(sh, seed, step)[0]).cuda()
+        out_r, _, idx_r, _ = R.stack_forward(x0)
+        sel = np.zeros((L, sh.top_k), dtype=np.int32)
+        S.step(x0, out_s, topk_idx=sel)
+        torch.cuda.synchronize()
+        assert R.pool.device_status() == moe.OK and S.pool.device_status() == moe.OK
+        assert np.array_equal(sel, idx_r.cpu().numpy()), step
+        assert torch.equal(out_r, out_s), step
+    hits, misses, nbytes = S.pool.stats()
+    assert hits + misses == steps * L * sh.top_k
+    assert misses > 0 and nbytes == misses * S.stride
