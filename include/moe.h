@@ -215,6 +215,19 @@ moe_status moe_stack_forward_streamed(moe_pool* pool, int32_t layer0, int32_t n_
                                       float* d_x_out, const void* const* h_blobs, void* compute_stream,
                                       void* copy_stream, int32_t* h_topk_idx);
 
+/* Batched tokens (prefill or batched decode), one layer, resident experts: the same layer as
+ * moe_layer_forward for each of n_tokens tokens, computed as GEMMs: router GEMM, per-token top-k,
+ * a sort of the token-expert assignments by expert, grouped gate/up and down GEMMs on the tensor
+ * cores (weights dequantised to fp16 per K-slice), and a per-token combine in rank order.
+ * d_x: bf16 [T][H]; d_y: fp32 [T][H]; d_topk_idx/d_topk_w: [T][k] or NULL.
+ * d_work: caller-owned device workspace of moe_batched_workspace_bytes(shape, T) bytes
+ * (256-byte aligned). Synchronises once with `stream` (the per-expert token counts are read back
+ * to lay out the grouped GEMMs). The shape must not have MOE_PRENORM or MOE_RESIDUAL. */
+size_t moe_batched_workspace_bytes(const moe_shape* shape, int32_t n_tokens);
+moe_status moe_layer_forward_batched(moe_pool* pool, int32_t layer, const void* d_x, int32_t n_tokens, float* d_y,
+                                     int32_t* d_topk_idx, float* d_topk_w, void* d_work, size_t work_bytes,
+                                     void* stream);
+
 /* Reference path: the same layer for one token with plain kernels (one thread per logit, one
  * thread per selection, one thread per output row, fp32 sums in index order). Used to cross-check
  * the fused kernel. Same arguments as moe_layer_forward with n_tokens = 1. */

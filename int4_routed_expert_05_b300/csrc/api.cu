@@ -12,8 +12,39 @@
 #include "layout.h"
 #include "policy.h"
 
+#include <cuda_fp16.h>
+
 namespace moe {
 __global__ void moe_decode_kernel(const __grid_constant__ StepParams P);
+namespace bat {
+struct GemmArgs {
+    int kind;
+    int T, H, E, k, I, Is, bits, n_exp;
+    BlobGeo geo, geo_s;
+    const uint8_t* arena;
+    uint64_t stride;
+    const int32_t* table;
+    const uint16_t* router;
+    const uint8_t* shared_blob;
+    const uint16_t* u_bf16;
+    const __half* u_h;
+    const int32_t* list;
+    const int32_t* offs;
+    const float* aw;
+    __half* hbuf;
+    float* ypart;
+    float* logits;
+    int* status;
+};
+void launch_to_half(const uint16_t* x, __half* y, size_t n, cudaStream_t st);
+void launch_gemm(int kind, const GemmArgs& A, const int4* tasks, int n_tasks, int grid, cudaStream_t st);
+void launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm, const uint16_t* u,
+                 const uint16_t* wsg, int H, int32_t* idx, float* w, float* gamma, int32_t* counts, cudaStream_t st);
+void launch_scan(const int32_t* counts, int E, int T, int32_t* offs, int32_t* cursor, cudaStream_t st);
+void launch_place(const int32_t* idx, const float* w, const float* gamma, int T, int E, int k, int32_t* cursor,
+                  int32_t* list, float* aw, int32_t* pos, cudaStream_t st);
+void launch_combine(const float* ypart, const int32_t* pos, int T, int H, int k, float* y, cudaStream_t st);
+}  // namespace bat
 __global__ void scalar_router(const StepParams P);
 __global__ void scalar_topk(const StepParams P, int32_t* sel);
 __global__ void scalar_gateup(const StepParams P, const int32_t* sel);
@@ -738,6 +769,167 @@ moe_status moe_stack_forward_streamed(moe_pool* p, int32_t layer0, int32_t n_lay
                 h_topk_idx[(size_t)li * k + j] = idx[j];
         cur = out;
     }
+    return MOE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+struct BatLayout {
+    size_t u_h, logits, idx, w, gamma, counts, offs, cursor, list, aw, pos, hbuf, ypart, tasks, total;
+    size_t max_tasks;
+};
+
+BatLayout bat_layout(const moe_shape& s, int T)
+{
+    BatLayout b{};
+    const size_t H = s.hidden, E = s.n_experts, k = s.top_k;
+    const size_t Imax = s.inter > s.shared_inter ? s.inter : s.shared_inter;
+    const size_t A = (size_t)T * (k + 1);
+    size_t o = 0;
+    auto take = [&](size_t& f, size_t bytes) {
+        f = o;
+        o = up256(o + bytes);
+    };
+    take(b.u_h, 2 * (size_t)T * H);
+    take(b.logits, 4 * (size_t)T * E);
+    take(b.idx, 4 * (size_t)T * k);
+    take(b.w, 4 * (size_t)T * k);
+    take(b.gamma, 4 * (size_t)T);
+    take(b.counts, 4 * (E + 2));
+    take(b.offs, 4 * (E + 2));
+    take(b.cursor, 4 * (E + 2));
+    take(b.list, 4 * A);
+    take(b.aw, 4 * A);
+    take(b.pos, 4 * A);
+    take(b.hbuf, 2 * A * Imax);
+    take(b.ypart, 4 * A * H);
+    const size_t ntile = (A + 63) / 64 + E + 1;  // N-tiles over all experts (one partial tile each)
+    const size_t r_tasks = ((E + 127) / 128) * (((size_t)T + 63) / 64);
+    const size_t gu_tasks = ((Imax + 63) / 64) * ntile, dn_tasks = ((H + 127) / 128) * ntile;
+    b.max_tasks = r_tasks > gu_tasks + dn_tasks ? r_tasks : gu_tasks + dn_tasks;
+    take(b.tasks, 16 * b.max_tasks);
+    b.total = o;
+    return b;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_batched_workspace_bytes(const moe_shape* s, int32_t n_tokens)
+{
+    if (!s || n_tokens <= 0)
+        return 0;
+    return bat_layout(*s, n_tokens).total;
+}
+
+moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x, int32_t T, float* d_y,
+                                     int32_t* d_topk_idx, float* d_topk_w, void* d_work, size_t work_bytes,
+                                     void* stream)
+{
+    moe_status st = check_layers(p, layer, 1);
+    if (st != MOE_OK)
+        return st;
+    if (p->shape.flags & (MOE_PRENORM | MOE_RESIDUAL))
+        return fail(MOE_E_SHAPE, "the batched path takes a bf16 layer input (no pre-norm, no residual)");
+    if (T <= 0)
+        return fail(MOE_E_INVALID, "n_tokens must be positive");
+    if ((st = check_ptr(d_x, 16, "d_x")) != MOE_OK || (st = check_ptr(d_y, 16, "d_y")) != MOE_OK ||
+        (st = check_ptr(d_work, 256, "d_work")) != MOE_OK)
+        return st;
+    const moe_shape& sh = p->shape;
+    if (sh.hidden % 32 != 0 || sh.inter % 64 != 0 || sh.shared_inter % 64 != 0)
+        return fail(MOE_E_SHAPE, "batched path needs hidden % 32 == 0 and inter % 64 == 0");
+    const BatLayout bl = bat_layout(sh, T);
+    if (work_bytes < bl.total)
+        return fail(MOE_E_NOMEM, "batched workspace holds %zu bytes, needs %zu (moe_batched_workspace_bytes)",
+                    work_bytes, bl.total);
+    int dev = -1;
+    CUDA_TRY(cudaGetDevice(&dev));
+    if (dev != p->device)
+        return fail(MOE_E_INVALID, "current device %d differs from the pool's device %d", dev, p->device);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    uint8_t* w = static_cast<uint8_t*>(d_work);
+    const int H = sh.hidden, E = sh.n_experts, k = sh.top_k, I = sh.inter, Is = sh.shared_inter;
+    const int Imax = I > Is ? I : Is;
+    const LayerDesc& L = p->layers[layer];
+    bat::GemmArgs A{};
+    A.T = T;
+    A.H = H;
+    A.E = E;
+    A.k = k;
+    A.I = I;
+    A.Is = Is;
+    A.bits = sh.bits;
+    A.geo = p->geo;
+    A.geo_s = p->geo_s;
+    A.arena = p->arena;
+    A.stride = p->geo.stride;
+    A.table = reinterpret_cast<const int32_t*>(p->ws + p->wl.table) + (size_t)layer * E;
+    A.router = L.router;
+    A.shared_blob = L.shared_blob;
+    A.u_bf16 = static_cast<const uint16_t*>(d_x);
+    A.u_h = reinterpret_cast<const __half*>(w + bl.u_h);
+    A.list = reinterpret_cast<const int32_t*>(w + bl.list);
+    A.offs = reinterpret_cast<const int32_t*>(w + bl.offs);
+    A.aw = reinterpret_cast<const float*>(w + bl.aw);
+    A.hbuf = reinterpret_cast<__half*>(w + bl.hbuf);
+    A.ypart = reinterpret_cast<float*>(w + bl.ypart);
+    A.logits = reinterpret_cast<float*>(w + bl.logits);
+    A.status = reinterpret_cast<int*>(p->ws + p->wl.status);
+    int4* d_tasks = reinterpret_cast<int4*>(w + bl.tasks);
+    const int grid = p->grid * 3;
+    int32_t* idx = d_topk_idx ? d_topk_idx : reinterpret_cast<int32_t*>(w + bl.idx);
+    float* wts = d_topk_w ? d_topk_w : reinterpret_cast<float*>(w + bl.w);
+    float* gamma = reinterpret_cast<float*>(w + bl.gamma);
+    int32_t* counts = reinterpret_cast<int32_t*>(w + bl.counts);
+    int32_t* offs = reinterpret_cast<int32_t*>(w + bl.offs);
+    int32_t* cursor = reinterpret_cast<int32_t*>(w + bl.cursor);
+
+    bat::launch_to_half(A.u_bf16, reinterpret_cast<__half*>(w + bl.u_h), (size_t)T * H, cs);
+    // router GEMM
+    std::vector<int4> tasks;
+    for (int m0 = 0; m0 < E; m0 += 128)
+        for (int n0 = 0; n0 < T; n0 += 64)
+            tasks.push_back(make_int4(-1, m0, n0, T - n0 < 64 ? T - n0 : 64));
+    CUDA_TRY(cudaMemcpyAsync(d_tasks, tasks.data(), tasks.size() * sizeof(int4), cudaMemcpyHostToDevice, cs));
+    bat::launch_gemm(0, A, d_tasks, (int)tasks.size(), grid, cs);
+    // routing and the sort by expert
+    CUDA_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * (E + 2), cs));
+    bat::launch_topk(A.logits, L.logit_bias, T, E, k, (sh.flags & MOE_RENORM) ? 1 : 0, A.u_bf16, L.shared_gate, H, idx,
+                     wts, gamma, counts, cs);
+    bat::launch_scan(counts, E, T, offs, cursor, cs);
+    bat::launch_place(idx, wts, gamma, T, E, k, cursor, const_cast<int32_t*>(A.list), const_cast<float*>(A.aw),
+                      reinterpret_cast<int32_t*>(w + bl.pos), cs);
+    std::vector<int32_t> h_offs(E + 2);
+    CUDA_TRY(cudaMemcpyAsync(h_offs.data(), offs, sizeof(int32_t) * (E + 2), cudaMemcpyDeviceToHost, cs));
+    CUDA_TRY(cudaStreamSynchronize(cs));
+    // grouped GEMM tasks: (expert, M-tile, N-tile); gate/up tiles are 64 rows of each matrix
+    std::vector<int4> gu, dn;
+    for (int e = 0; e <= E; ++e) {
+        const int a0 = h_offs[e], a1 = h_offs[e + 1];
+        if (a1 <= a0)
+            continue;
+        const int rows = e < E ? I : Is;
+        for (int m0 = 0; m0 < rows; m0 += 64)
+            for (int n0 = a0; n0 < a1; n0 += 64)
+                gu.push_back(make_int4(e, m0, n0, a1 - n0 < 64 ? a1 - n0 : 64));
+        for (int m0 = 0; m0 < H; m0 += 128)
+            for (int n0 = a0; n0 < a1; n0 += 64)
+                dn.push_back(make_int4(e, m0, n0, a1 - n0 < 64 ? a1 - n0 : 64));
+    }
+    if (gu.size() + dn.size() > bl.max_tasks)
+        return fail(MOE_E_NOMEM, "task list overflow (%zu tasks)", gu.size() + dn.size());
+    std::vector<int4> all(gu);
+    all.insert(all.end(), dn.begin(), dn.end());
+    CUDA_TRY(cudaMemcpyAsync(d_tasks, all.data(), all.size() * sizeof(int4), cudaMemcpyHostToDevice, cs));
+    bat::launch_gemm(1, A, d_tasks, (int)gu.size(), grid, cs);
+    bat::launch_gemm(2, A, d_tasks + gu.size(), (int)dn.size(), grid, cs);
+    bat::launch_combine(A.ypart, reinterpret_cast<const int32_t*>(w + bl.pos), T, H, k, d_y, cs);
+    CUDA_TRY(cudaGetLastError());
+    (void)Imax;
     return MOE_OK;
 }
 

@@ -26,7 +26,7 @@ ENTRY_POINTS = [
     "moe_pool_stats", "moe_layer_forward", "moe_stack_forward", "moe_route", "moe_experts",
     "moe_layer_forward_scalar", "moe_device_status", "moe_pool_set_timeout", "moe_pool_grid",
     "moe_last_error", "moe_pool_slot_of", "moe_pool_set_copy_hook", "moe_layer_forward_static",
-    "moe_stack_forward_streamed",
+    "moe_stack_forward_streamed", "moe_batched_workspace_bytes", "moe_layer_forward_batched",
 ]
 
 
@@ -89,6 +89,8 @@ def load() -> ctypes.CDLL:
         "moe_pool_set_copy_hook": (ST, [P, COPY_HOOK, P]),
         "moe_layer_forward_static": (ST, [PS, P, ctypes.POINTER(LayerWeights), P, I32, P, P, P, P, P]),
         "moe_stack_forward_streamed": (ST, [P, I32, I32, P, P, P, P, P, P]),
+        "moe_batched_workspace_bytes": (SZ, [PS, I32]),
+        "moe_layer_forward_batched": (ST, [P, I32, P, I32, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -132,6 +134,10 @@ def layer_forward_static(shape: Shape, experts, router, shared_blob, shared_gate
     w = LayerWeights(_p(router), _p(shared_blob), _p(shared_gate), _p(logit_bias))
     _check(load().moe_layer_forward_static(ctypes.byref(shape), _p(experts), ctypes.byref(w), _p(x), n_tokens, _p(y),
                                            _p(topk_idx), _p(topk_w), _p(status), _s(stream)))
+
+
+def batched_workspace_bytes(shape: Shape, n_tokens: int) -> int:
+    return int(load().moe_batched_workspace_bytes(ctypes.byref(shape), n_tokens))
 
 
 def make_shape(hidden, n_experts, top_k, inter, shared_inter, bits=4, group=64, flags=RENORM) -> Shape:
@@ -259,6 +265,12 @@ class Pool:
         _check(self.lib.moe_stack_forward_streamed(self.h, layer0, n_layers, _p(x), _p(x_out), hb.ctypes.data,
                                                    _s(compute_stream), _s(copy_stream),
                                                    None if topk_idx is None else topk_idx.ctypes.data))
+
+    def layer_forward_batched(self, layer, x, n_tokens, y, work, topk_idx=None, topk_w=None, stream=None):
+        """moe_layer_forward_batched: x bf16 [T][H] -> y fp32 [T][H]; work: device buffer of
+        batched_workspace_bytes(shape, T) bytes."""
+        _check(self.lib.moe_layer_forward_batched(self.h, layer, _p(x), n_tokens, _p(y), _p(topk_idx), _p(topk_w),
+                                                  _p(work), work.numel() if hasattr(work, "numel") else 0, _s(stream)))
 
     def route(self, layer, x, topk_idx, topk_w, stream=None):
         _check(self.lib.moe_route(self.h, layer, _p(x), _p(topk_idx), _p(topk_w), _s(stream)))

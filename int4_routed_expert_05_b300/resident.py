@@ -106,6 +106,17 @@ class Resident:
         self.pool.layer_forward(layer, x_bits, T, y, idx, w, stream)
         return y, idx, w
 
+    def layer_forward_batched(self, layer: int, x_bits: torch.Tensor, stream=None, work: torch.Tensor | None = None):
+        """The batched (GEMM) path: x_bits int16 [T][H] bf16 patterns -> (y fp32 [T][H], idx, w)."""
+        T = x_bits.shape[0]
+        y = torch.empty((T, self.sh.hidden), dtype=torch.float32, device=self.device)
+        idx = torch.empty((T, self.sh.top_k), dtype=torch.int32, device=self.device)
+        w = torch.empty((T, self.sh.top_k), dtype=torch.float32, device=self.device)
+        if work is None:
+            work = torch.empty(moe.batched_workspace_bytes(self.mshape, T), dtype=torch.uint8, device=self.device)
+        self.pool.layer_forward_batched(layer, x_bits, T, y, work, idx, w, stream)
+        return y, idx, w
+
     def stack_forward(self, x: torch.Tensor, layer0: int = 0, n_layers: int | None = None, trace: bool = False,
                       stream=None):
         """x: fp32 device tensor [H] -> (x_out, trace [n+1][H] or None, idx [n][k], w [n][k])."""

@@ -111,6 +111,45 @@ class Streamed:
                   f"store {self.store.numel() / 1e9:.2f} GB pinned, beta {beta:.3f}, set-up {time.time() - t0:.1f} s",
                   flush=True)
 
+    def set_beta(self, beta: float):
+        """Change the Zipf routing bias strength (re-registers the layers' bias vectors)."""
+        self.beta = beta
+        self.bias = [torch.from_numpy(zipf_bias(self.sh, self.seed, l, beta)).to(self.arena.device) if beta else None
+                     for l in range(self.L)]
+        for l in range(self.L):
+            self.pool.set_layer(l, self.router[l], self.shared[l], self.gate[l], self.bias[l])
+        self.pool.sync()
+        torch.cuda.synchronize()
+
+    def measure_hit_rate(self, xs: torch.Tensor, warm: int = 16, tokens: int = 24) -> float:
+        """Hit rate of this pool over `tokens` decode steps after `warm` steps (inputs xs[i % len])."""
+        out = torch.empty(self.sh.hidden, dtype=torch.float32, device=xs.device)
+        for i in range(warm):
+            self.step(xs[i % xs.shape[0]], out)
+        torch.cuda.synchronize()
+        h0, m0, _ = self.pool.stats()
+        for i in range(tokens):
+            self.step(xs[(warm + i) % xs.shape[0]], out)
+        torch.cuda.synchronize()
+        h1, m1, _ = self.pool.stats()
+        return (h1 - h0) / max(1, (h1 - h0) + (m1 - m0))
+
+    def calibrate_beta(self, xs: torch.Tensor, target: float = 0.55, iters: int = 6, lo: float = 0.0,
+                       hi: float = 1.5) -> tuple[float, float]:
+        """Bisect the Zipf strength on the real routing of this stack until the measured hit rate
+        is near `target`; returns (beta, hit rate)."""
+        best = (self.beta, None)
+        for _ in range(iters):
+            mid = 0.5 * (lo + hi)
+            self.set_beta(mid)
+            hr = self.measure_hit_rate(xs)
+            best = (mid, hr)
+            if hr < target:
+                lo = mid
+            else:
+                hi = mid
+        return best
+
     def bias_host(self, layer: int):
         return None if not self.beta else zipf_bias(self.sh, self.seed, layer, self.beta)
 
