@@ -556,7 +556,7 @@ def run_batched(args):
         ach = bytes_step / (ms_step / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
                 "peak_kind": hbm_kind, "bytes_per_launch": bytes_step}
-    roof.update({"traffic": None, "kernel": "moe_layer_forward_batched (all its launches, one step)"})
+    roof.update({"traffic": None, "kernel": "moe_layer_forward_batched (all 7 launches of one step)"})
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         v, info = cpu_oracle_batched(sh, T, budget_s=args.ref_budget)
@@ -579,7 +579,7 @@ def run_batched(args):
         "cpu_baseline": cpu,
         "e2e": {"value": ws * T * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 2 * T * H,
                 "d2h_bytes_per_step": 4 * T * H, "steps": n_e2e},
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": 7 * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -14,36 +14,18 @@
 
 #include <cuda_fp16.h>
 
+#include "grouped.h"
+
 namespace moe {
 __global__ void moe_decode_kernel(const __grid_constant__ StepParams P);
 namespace bat {
-struct GemmArgs {
-    int kind;
-    int T, H, E, k, I, Is, bits, n_exp;
-    BlobGeo geo, geo_s;
-    const uint8_t* arena;
-    uint64_t stride;
-    const int32_t* table;
-    const uint16_t* router;
-    const uint8_t* shared_blob;
-    const uint16_t* u_bf16;
-    const __half* u_h;
-    const int32_t* list;
-    const int32_t* offs;
-    const float* aw;
-    __half* hbuf;
-    float* ypart;
-    float* logits;
-    int* status;
-};
-void launch_to_half(const uint16_t* x, __half* y, size_t n, cudaStream_t st);
-void launch_gemm(int kind, const GemmArgs& A, const int4* tasks, int n_tasks, int grid, cudaStream_t st);
+void launch_to_half(const uint16_t* x, __half* y, size_t n, int bits, cudaStream_t st);
 void launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm, const uint16_t* u,
                  const uint16_t* wsg, int H, int32_t* idx, float* w, float* gamma, int32_t* counts, cudaStream_t st);
-void launch_scan(const int32_t* counts, int E, int T, int32_t* offs, int32_t* cursor, cudaStream_t st);
+void launch_plan(const int32_t* counts, int E, int T, int I, int Is, int H, int32_t* offs, int32_t* cursor,
+                 int4* tasks_gu, int4* tasks_dn, int32_t* n_tasks, cudaStream_t st);
 void launch_place(const int32_t* idx, const float* w, const float* gamma, int T, int E, int k, int32_t* cursor,
-                  int32_t* list, float* aw, int32_t* pos, cudaStream_t st);
-void launch_combine(const float* ypart, const int32_t* pos, int T, int H, int k, float* y, cudaStream_t st);
+                  int32_t* list, float* aw, cudaStream_t st);
 }  // namespace bat
 __global__ void scalar_router(const StepParams P);
 __global__ void scalar_topk(const StepParams P, int32_t* sel);
@@ -152,6 +134,7 @@ struct moe_pool {
     int64_t hits = 0, misses = 0, bytes_loaded = 0;
     int device = -1, grid = 0;
     uint32_t smem = 0;
+    int smem_optin = 0;
     uint64_t timeout_ns = 2000000000ull;
     // bounded mode: events
     std::vector<cudaEvent_t> ring;   // last-use events, reused round robin
@@ -306,6 +289,7 @@ moe_status moe_pool_create(const moe_shape* s, int32_t n_layers, int32_t n_slots
     if (sms > kMaxGrid)
         return cleanup(fail(MOE_E_SHAPE, "%d SMs exceed the %d blocks a decode launch supports", sms, kMaxGrid));
     p->grid = sms;  // one block per SM
+    p->smem_optin = optin;
     if (cudaMemset(p->ws, 0, p->wl.total) != cudaSuccess ||
         cudaMemset(p->ws + p->wl.table, 0xFF, sizeof(int32_t) * (size_t)n_layers * s->n_experts) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
@@ -777,8 +761,8 @@ moe_status moe_stack_forward_streamed(moe_pool* p, int32_t layer0, int32_t n_lay
 namespace {
 
 struct BatLayout {
-    size_t u_h, logits, idx, w, gamma, counts, offs, cursor, list, aw, pos, hbuf, ypart, tasks, total;
-    size_t max_tasks;
+    size_t u_h, logits, idx, w, gamma, counts, offs, cursor, list, aw, hbuf, tasks_gu, tasks_dn, n_tasks, total;
+    size_t max_gu, max_dn;
 };
 
 BatLayout bat_layout(const moe_shape& s, int T)
@@ -802,14 +786,13 @@ BatLayout bat_layout(const moe_shape& s, int T)
     take(b.cursor, 4 * (E + 2));
     take(b.list, 4 * A);
     take(b.aw, 4 * A);
-    take(b.pos, 4 * A);
     take(b.hbuf, 2 * A * Imax);
-    take(b.ypart, 4 * A * H);
-    const size_t ntile = (A + 63) / 64 + E + 1;  // N-tiles over all experts (one partial tile each)
-    const size_t r_tasks = ((E + 127) / 128) * (((size_t)T + 63) / 64);
-    const size_t gu_tasks = ((Imax + 63) / 64) * ntile, dn_tasks = ((H + 127) / 128) * ntile;
-    b.max_tasks = r_tasks > gu_tasks + dn_tasks ? r_tasks : gu_tasks + dn_tasks;
-    take(b.tasks, 16 * b.max_tasks);
+    const size_t chunks = A / tc::kNT + E + 1;  // 128-token chunks over all experts (one partial each)
+    b.max_gu = chunks * (Imax / 64);
+    b.max_dn = chunks * ((H + 127) / 128);
+    take(b.tasks_gu, 16 * b.max_gu);
+    take(b.tasks_dn, 16 * b.max_dn);
+    take(b.n_tasks, 16);
     b.total = o;
     return b;
 }
@@ -840,8 +823,12 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
         (st = check_ptr(d_work, 256, "d_work")) != MOE_OK)
         return st;
     const moe_shape& sh = p->shape;
-    if (sh.hidden % 32 != 0 || sh.inter % 64 != 0 || sh.shared_inter % 64 != 0)
-        return fail(MOE_E_SHAPE, "batched path needs hidden % 32 == 0 and inter % 64 == 0");
+    const int H = sh.hidden, E = sh.n_experts, k = sh.top_k, I = sh.inter, Is = sh.shared_inter;
+    const int Imax = I > Is ? I : Is;
+    if (H % 64 != 0 || I % 64 != 0 || Is % 64 != 0)
+        return fail(MOE_E_SHAPE, "batched path needs hidden, inter and shared_inter multiples of 64");
+    if (tc::expert_smem_bytes(H, Imax, sh.bits) > (size_t)p->smem_optin)
+        return fail(MOE_E_SHAPE, "batched path: staging for hidden %d does not fit in shared memory", H);
     const BatLayout bl = bat_layout(sh, T);
     if (work_bytes < bl.total)
         return fail(MOE_E_NOMEM, "batched workspace holds %zu bytes, needs %zu (moe_batched_workspace_bytes)",
@@ -852,10 +839,20 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
         return fail(MOE_E_INVALID, "current device %d differs from the pool's device %d", dev, p->device);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     uint8_t* w = static_cast<uint8_t*>(d_work);
-    const int H = sh.hidden, E = sh.n_experts, k = sh.top_k, I = sh.inter, Is = sh.shared_inter;
-    const int Imax = I > Is ? I : Is;
     const LayerDesc& L = p->layers[layer];
-    bat::GemmArgs A{};
+
+    tc::GroupedArgs A{};
+    int rc = encode_slice_maps(A.map_q[0], p->arena, p->S, p->geo.stride, p->geo, sh.bits);
+    if (rc == 0)
+        rc = encode_slice_maps(A.map_q[1], L.shared_blob, 1, p->geo_s.stride, p->geo_s, sh.bits);
+    if (rc == 0)
+        rc = encode_bf16_tiles(&A.map_wr, L.router, H, E, 128);
+    if (rc == 0)
+        rc = encode_bf16_tiles(&A.map_u, d_x, H, T, tc::kNT);
+    if (rc != 0)
+        return fail(MOE_E_CUDA, "tensor map encoding failed (%d)", rc);
+    A.geo = p->geo;
+    A.geo_s = p->geo_s;
     A.T = T;
     A.H = H;
     A.E = E;
@@ -863,73 +860,44 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     A.I = I;
     A.Is = Is;
     A.bits = sh.bits;
-    A.geo = p->geo;
-    A.geo_s = p->geo_s;
+    A.Imax = Imax;
     A.arena = p->arena;
     A.stride = p->geo.stride;
     A.table = reinterpret_cast<const int32_t*>(p->ws + p->wl.table) + (size_t)layer * E;
-    A.router = L.router;
     A.shared_blob = L.shared_blob;
-    A.u_bf16 = static_cast<const uint16_t*>(d_x);
     A.u_h = reinterpret_cast<const __half*>(w + bl.u_h);
     A.list = reinterpret_cast<const int32_t*>(w + bl.list);
-    A.offs = reinterpret_cast<const int32_t*>(w + bl.offs);
     A.aw = reinterpret_cast<const float*>(w + bl.aw);
     A.hbuf = reinterpret_cast<__half*>(w + bl.hbuf);
-    A.ypart = reinterpret_cast<float*>(w + bl.ypart);
+    A.y = d_y;
     A.logits = reinterpret_cast<float*>(w + bl.logits);
     A.status = reinterpret_cast<int*>(p->ws + p->wl.status);
-    int4* d_tasks = reinterpret_cast<int4*>(w + bl.tasks);
-    const int grid = p->grid * 3;
+    A.timeout_cycles = 2 * (long long)p->timeout_ns;
+
     int32_t* idx = d_topk_idx ? d_topk_idx : reinterpret_cast<int32_t*>(w + bl.idx);
     float* wts = d_topk_w ? d_topk_w : reinterpret_cast<float*>(w + bl.w);
     float* gamma = reinterpret_cast<float*>(w + bl.gamma);
     int32_t* counts = reinterpret_cast<int32_t*>(w + bl.counts);
     int32_t* offs = reinterpret_cast<int32_t*>(w + bl.offs);
     int32_t* cursor = reinterpret_cast<int32_t*>(w + bl.cursor);
+    int4* tgu = reinterpret_cast<int4*>(w + bl.tasks_gu);
+    int4* tdn = reinterpret_cast<int4*>(w + bl.tasks_dn);
+    int32_t* ntasks = reinterpret_cast<int32_t*>(w + bl.n_tasks);
+    const int grid = p->grid;
 
-    bat::launch_to_half(A.u_bf16, reinterpret_cast<__half*>(w + bl.u_h), (size_t)T * H, cs);
-    // router GEMM
-    std::vector<int4> tasks;
-    for (int m0 = 0; m0 < E; m0 += 128)
-        for (int n0 = 0; n0 < T; n0 += 64)
-            tasks.push_back(make_int4(-1, m0, n0, T - n0 < 64 ? T - n0 : 64));
-    CUDA_TRY(cudaMemcpyAsync(d_tasks, tasks.data(), tasks.size() * sizeof(int4), cudaMemcpyHostToDevice, cs));
-    bat::launch_gemm(0, A, d_tasks, (int)tasks.size(), grid, cs);
-    // routing and the sort by expert
     CUDA_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * (E + 2), cs));
-    bat::launch_topk(A.logits, L.logit_bias, T, E, k, (sh.flags & MOE_RENORM) ? 1 : 0, A.u_bf16, L.shared_gate, H, idx,
-                     wts, gamma, counts, cs);
-    bat::launch_scan(counts, E, T, offs, cursor, cs);
-    bat::launch_place(idx, wts, gamma, T, E, k, cursor, const_cast<int32_t*>(A.list), const_cast<float*>(A.aw),
-                      reinterpret_cast<int32_t*>(w + bl.pos), cs);
-    std::vector<int32_t> h_offs(E + 2);
-    CUDA_TRY(cudaMemcpyAsync(h_offs.data(), offs, sizeof(int32_t) * (E + 2), cudaMemcpyDeviceToHost, cs));
-    CUDA_TRY(cudaStreamSynchronize(cs));
-    // grouped GEMM tasks: (expert, M-tile, N-tile); gate/up tiles are 64 rows of each matrix
-    std::vector<int4> gu, dn;
-    for (int e = 0; e <= E; ++e) {
-        const int a0 = h_offs[e], a1 = h_offs[e + 1];
-        if (a1 <= a0)
-            continue;
-        const int rows = e < E ? I : Is;
-        for (int m0 = 0; m0 < rows; m0 += 64)
-            for (int n0 = a0; n0 < a1; n0 += 64)
-                gu.push_back(make_int4(e, m0, n0, a1 - n0 < 64 ? a1 - n0 : 64));
-        for (int m0 = 0; m0 < H; m0 += 128)
-            for (int n0 = a0; n0 < a1; n0 += 64)
-                dn.push_back(make_int4(e, m0, n0, a1 - n0 < 64 ? a1 - n0 : 64));
-    }
-    if (gu.size() + dn.size() > bl.max_tasks)
-        return fail(MOE_E_NOMEM, "task list overflow (%zu tasks)", gu.size() + dn.size());
-    std::vector<int4> all(gu);
-    all.insert(all.end(), dn.begin(), dn.end());
-    CUDA_TRY(cudaMemcpyAsync(d_tasks, all.data(), all.size() * sizeof(int4), cudaMemcpyHostToDevice, cs));
-    bat::launch_gemm(1, A, d_tasks, (int)gu.size(), grid, cs);
-    bat::launch_gemm(2, A, d_tasks + gu.size(), (int)dn.size(), grid, cs);
-    bat::launch_combine(A.ypart, reinterpret_cast<const int32_t*>(w + bl.pos), T, H, k, d_y, cs);
+    CUDA_TRY(cudaMemsetAsync(d_y, 0, sizeof(float) * (size_t)T * H, cs));
+    bat::launch_to_half(static_cast<const uint16_t*>(d_x), reinterpret_cast<__half*>(w + bl.u_h), (size_t)T * H,
+                        sh.bits, cs);
+    const int r_tasks = ((E + 127) / 128) * ((T + tc::kNT - 1) / tc::kNT);
+    tc::launch_router_gemm(A, r_tasks < grid ? r_tasks : grid, cs);
+    bat::launch_topk(A.logits, L.logit_bias, T, E, k, (sh.flags & MOE_RENORM) ? 1 : 0,
+                     static_cast<const uint16_t*>(d_x), L.shared_gate, H, idx, wts, gamma, counts, cs);
+    bat::launch_plan(counts, E, T, I, Is, H, offs, cursor, tgu, tdn, ntasks, cs);
+    bat::launch_place(idx, wts, gamma, T, E, k, cursor, const_cast<int32_t*>(A.list), const_cast<float*>(A.aw), cs);
+    tc::launch_expert_gemm(1, A, tgu, ntasks, grid, cs);
+    tc::launch_expert_gemm(2, A, tdn, ntasks + 1, grid, cs);
     CUDA_TRY(cudaGetLastError());
-    (void)Imax;
     return MOE_OK;
 }
 

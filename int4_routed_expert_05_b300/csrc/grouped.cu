@@ -1,0 +1,750 @@
+// grouped.cu -- the GEMMs of the batched MoE layer on the fifth-generation tensor cores (sm_103a).
+//
+// The layer is the one of the decode kernel (cheshm.ai item "Swiftlet fits an 80B-level Qwen giant
+// into Mac": router, top-k of E experts, SwiGLU experts with MLX-style group-64 int4/int8 codes and
+// per-group scale and bias, weighted combine, sigmoid-gated shared expert), here for T tokens at
+// once, where the expert matrices are real GEMMs over the tokens routed to each expert.
+//
+// Both kernels are persistent (one CTA per SM) and warp-specialised around one MMA-issuing thread:
+//   * operands sit in shared memory as 128-row x 64-element K-major tiles in the 128-byte swizzled
+//     layout; tcgen05.mma (M = 128, N = tokens rounded up to 16, K = 16, fp32 accumulate) reads
+//     them through shared-memory descriptors and accumulates in tensor memory (two accumulators, so
+//     the epilogue of one task overlaps the main loop of the next);
+//   * router GEMM: A = router rows (bf16) and B = token rows (bf16), both brought in by TMA with
+//     the hardware swizzle, so a slice goes global -> shared -> tensor core untouched;
+//   * expert GEMMs: TMA stages the packed codes; four dequantising warps turn them into fp16
+//     weights w = s * q + b (one rounding, s and b exact in fp16 for the workloads' ranges) in the
+//     swizzled layout; four gathering warps copy the routed tokens' activation rows into the B
+//     tile; four epilogue warps read the accumulators with tcgen05.ld and apply SwiGLU
+//     (gate/up: h to a per-assignment buffer) or the combine weight (down: fp32 reductions into y).
+// Every wait is bounded: on expiry the kernel records MOE timeout status, drains its own copies and
+// frees its tensor memory.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "grouped.h"
+#include "layout.h"
+
+namespace moe {
+namespace tc {
+
+namespace {
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// ---- mbarriers ----
+__device__ __forceinline__ void bar_init(uint64_t* m, int n)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(m)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* m)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(m)) : "memory");
+}
+__device__ __forceinline__ void bar_expect(uint64_t* m, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(m)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* m, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok)
+                 : "r"(su32(m)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Shared block state: the abort flag every wait checks, the tensor-memory base address.
+struct Ctl {
+    volatile int abort;
+    uint32_t tmem;
+};
+
+// Bounded wait on phase `parity` of m. False on timeout or when another role gave up.
+__device__ __noinline__ bool bar_wait(uint64_t* m, uint32_t parity, Ctl* ctl, int* status, long long limit)
+{
+    if (bar_try(m, parity))
+        return true;
+    const long long t0 = clock64();
+    for (int it = 1;; ++it) {
+        if (bar_try(m, parity))
+            return true;
+        if ((it & 255) == 0) {
+            if (ctl->abort)
+                return false;
+            if (clock64() - t0 > limit) {
+                ctl->abort = 1;
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// ---- copies ----
+__device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* m)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            su32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(su32(m))
+        : "memory");
+}
+__device__ __forceinline__ void tma3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* m)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(su32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(su32(m))
+        : "memory");
+}
+__device__ __forceinline__ void bulk(void* dst, const void* src, uint32_t bytes, uint64_t* m)
+{
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(su32(dst)),
+                 "l"(src), "r"(bytes), "r"(su32(m))
+                 : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ---- tcgen05 ----
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand tile, 128-byte swizzle, 8-row groups 1024 bytes
+// apart (start address and offsets in 16-byte units; bits 46-48 hold the fixed value 1).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc(int n, bool bf16)
+{
+    const uint32_t f = bf16 ? 1u : 0u;
+    return (1u << 4) | (f << 7) | (f << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc)
+{
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* m)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(m))
+                 : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's accumulator row (lane = row)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free(uint32_t base)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(kTmemCols) : "memory");
+}
+
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// 8 int4 codes of one 32-bit word -> 4 fp16 pairs w = s * q + b, pair j = (code j, code j + 4):
+// (word >> 4j) & 0x000F000F | 0x6400_6400 is the fp16 pair (1024 + q_j, 1024 + q_{j+4}); taking
+// 1024 back off is exact, and the fma rounds s * q + b once.
+__device__ __forceinline__ uint4 deq_int4(uint32_t w, __half2 s, __half2 b)
+{
+    const __half2 k1024 = u2h(0x64006400u);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t x;
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(x) : "r"(w >> (4 * j)), "r"(0x000F000Fu), "r"(0x64006400u));
+        o[j] = h2u(__hfma2(__hsub2(u2h(x), k1024), s, b));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 8 int8 codes of two 32-bit words -> 4 fp16 pairs, pair order (0,2), (1,3) within each word.
+__device__ __forceinline__ uint4 deq_int8(uint32_t w0, uint32_t w1, __half2 s, __half2 b)
+{
+    const __half2 k1024 = u2h(0x64006400u);
+    uint32_t o[4];
+    const uint32_t w[2] = {w0, w1};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t x = __byte_perm(w[j >> 1], 0x64646464u, (j & 1) ? 0x4341u : 0x4240u);
+        o[j] = h2u(__hfma2(__hsub2(u2h(x), k1024), s, b));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint16_t pick16(const uint4& v, int i)
+{
+    const uint32_t w = (i & 4) ? ((i & 2) ? v.w : v.z) : ((i & 2) ? v.y : v.x);
+    return (uint16_t)((i & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
+struct TaskX {
+    int e, m0, n0, nn, nk, shared, slot;
+    const uint8_t* blob;
+};
+
+__device__ __forceinline__ TaskX decode_task(const GroupedArgs& P, int kind, int4 t)
+{
+    TaskX x;
+    x.e = t.x;
+    x.m0 = t.y;
+    x.n0 = t.z;
+    x.nn = t.w;
+    x.shared = x.e == P.E;
+    x.slot = 0;
+    if (x.shared) {
+        x.blob = P.shared_blob;
+    } else {
+        int s = P.table[x.e];
+        if (s < 0) {
+            atomicOr(P.status, kStatusNotResident);
+            s = 0;
+        }
+        x.slot = s;
+        x.blob = P.arena + (uint64_t)s * P.stride;
+    }
+    const BlobGeo& g = x.shared ? P.geo_s : P.geo;
+    x.nk = (kind == 1 ? P.H : g.cols[2]) / kKS;
+    return x;
+}
+
+__device__ __forceinline__ int n_mma(int nn) { return (nn + 15) & ~15; }
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------------------
+// Router GEMM: logits[t][e] = sum_h Wr[e][h] u[t][h], tiles of 128 experts x 128 tokens.
+// ------------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreadsR, 1) router_kernel(const __grid_constant__ GroupedArgs P)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sa = sm;                                   // kStagesR A tiles
+    uint8_t* sbuf = sm + kStagesR * kTileBytes;         // kStagesR B tiles
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 2 * kStagesR * kTileBytes);
+    uint64_t* full = bars;                 // [kStagesR]
+    uint64_t* empty = bars + kStagesR;     // [kStagesR]
+    uint64_t* acc_full = bars + 2 * kStagesR;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* fin = acc_empty + 2;
+    Ctl* ctl = reinterpret_cast<Ctl*>(fin + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = (P.E + 127) / 128, n_tasks = mt * ((P.T + kNT - 1) / kNT);
+    const int nk = P.H / kKS;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStagesR; ++i) {
+            bar_init(full + i, 1);
+            bar_init(empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            bar_init(acc_full + i, 1);
+            bar_init(acc_empty + i, 128);
+        }
+        bar_init(fin, 1);
+        ctl->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 5)
+        tmem_alloc(&ctl->tmem);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+    const long long lim = P.timeout_cycles;
+
+    if (warp == 4) {
+        if (lane == 0) {  // TMA producer
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&P.map_wr) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&P.map_u) : "memory");
+            uint32_t it = 0;
+            for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x) {
+                const int m0 = (ti % mt) * 128, n0 = (ti / mt) * kNT;
+                for (int g = 0; g < nk; ++g, ++it) {
+                    const int s = it % kStagesR;
+                    if (!bar_wait(empty + s, ((it / kStagesR) & 1) ^ 1, ctl, P.status, lim))
+                        goto tma_done;
+                    bar_expect(full + s, 2 * kTileBytes);
+                    tma2d(sa + s * kTileBytes, &P.map_wr, g * kKS, m0, full + s);
+                    tma2d(sbuf + s * kTileBytes, &P.map_u, g * kKS, n0, full + s);
+                }
+            }
+        tma_done:
+            // every issued copy has landed before the block can exit
+            for (uint32_t i = it > (uint32_t)kStagesR ? it - kStagesR : 0; i < it; ++i)
+                bar_wait(full + i % kStagesR, (i / kStagesR) & 1, ctl, P.status, lim);
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {  // MMA issuer
+            uint32_t it = 0, j = 0;
+            for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
+                const int n0 = (ti / mt) * kNT;
+                const int nn = min(kNT, P.T - n0);
+                const uint32_t id = idesc(n_mma(nn), true);
+                const int ab = j & 1;
+                if (!bar_wait(acc_empty + ab, ((j >> 1) & 1) ^ 1, ctl, P.status, lim))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + ab * kNT;
+                bool ok = true;
+                for (int g = 0; g < nk; ++g, ++it) {
+                    const int s = it % kStagesR;
+                    if (!bar_wait(full + s, (it / kStagesR) & 1, ctl, P.status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a = sdesc(su32(sa + s * kTileBytes)), b = sdesc(su32(sbuf + s * kTileBytes));
+#pragma unroll
+                    for (int kk = 0; kk < kKS / 16; ++kk)
+                        mma(d, a + 2 * kk, b + 2 * kk, id, (g | kk) != 0);
+                    mma_commit(empty + s);
+                }
+                if (!ok)
+                    break;
+                mma_commit(acc_full + ab);
+            }
+            mma_commit(fin);
+            bar_wait(fin, 0, ctl, P.status, lim);
+        }
+    } else {  // epilogue warps 0-3: TMEM lanes 32 * warp ..
+        const int r = warp * 32 + lane;
+        uint32_t j = 0;
+        for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
+            const int m0 = (ti % mt) * 128, n0 = (ti / mt) * kNT;
+            const int nn = min(kNT, P.T - n0);
+            const int ab = j & 1;
+            if (!bar_wait(acc_full + ab, (j >> 1) & 1, ctl, P.status, lim))
+                break;
+            tc_fence_after();
+            const int row = m0 + r;
+            for (int c0 = 0; c0 < n_mma(nn); c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + ab * kNT + c0, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (row < P.E && c0 + i < nn)
+                        P.logits[(size_t)(n0 + c0 + i) * P.E + row] = v[i];
+            }
+            tc_fence_before();
+            bar_arrive(acc_empty + ab);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_free(tmem);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Expert GEMMs. kind 1: gate/up tiles (64 gate rows + the same 64 up rows) against the expert's
+// tokens, SwiGLU epilogue -> hbuf. kind 2: down tiles (128 rows) against the expert's h rows,
+// epilogue y[token] += weight * acc.
+// ------------------------------------------------------------------------------------------------
+template <int kKind>
+__global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_constant__ GroupedArgs P)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const XPlan pl = xplan(P.H, P.Imax, P.bits);
+    uint8_t* sa = sm + pl.a;
+    uint8_t* sbt = sm + pl.b;
+    uint8_t* scode = sm + pl.code;
+    uint8_t* ssc = sm + pl.sc;
+    float* xch = reinterpret_cast<float*>(sm + pl.xch);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + pl.bar);
+    const int NC = (int)pl.n_code;
+    uint64_t* full_a = bars;
+    uint64_t* full_b = bars + kStages;
+    uint64_t* empty = bars + 2 * kStages;
+    uint64_t* code_full = bars + 3 * kStages;
+    uint64_t* code_empty = code_full + 8;
+    uint64_t* sc_full = code_empty + 8;
+    uint64_t* sc_empty = sc_full + 2;
+    uint64_t* acc_full = sc_empty + 2;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* fin = acc_empty + 2;
+    Ctl* ctl = reinterpret_cast<Ctl*>(bars + 64);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tasks = *P.n_tasks;
+    const long long lim = P.timeout_cycles;
+    const uint32_t sbytes = kKS * P.bits / 8;  // code bytes of one row in one slice
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            bar_init(full_a + i, 128);
+            bar_init(full_b + i, 128);
+            bar_init(empty + i, 1);
+        }
+        for (int i = 0; i < NC; ++i) {
+            bar_init(code_full + i, 1);
+            bar_init(code_empty + i, 128);
+        }
+        for (int i = 0; i < 2; ++i) {
+            bar_init(sc_full + i, 1);
+            bar_init(sc_empty + i, 128);
+            bar_init(acc_full + i, 1);
+            bar_init(acc_empty + i, 128);
+        }
+        bar_init(fin, 1);
+        ctl->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 13)
+        tmem_alloc(&ctl->tmem);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+
+    if (warp < 4) {
+        // ---- dequantising producers: thread r owns row r of the A tile ----
+        const int r = threadIdx.x;
+        uint32_t it = 0, j = 0;
+        for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
+            const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+            const BlobGeo& geo = t.shared ? P.geo_s : P.geo;
+            const int G = kKind == 1 ? geo.groups[0] : geo.groups[2];
+            const int sb = j & 1;
+            if (!bar_wait(sc_full + sb, (j >> 1) & 1, ctl, P.status, lim))
+                break;
+            // row r's scales and biases in the staged block: gate/up [gs 64][gb 64][us 64][ub 64] x G,
+            // down [s 128][b 128] x G
+            const uint16_t* scb = reinterpret_cast<const uint16_t*>(ssc + sb * pl.sc_bytes);
+            const uint16_t* srow;
+            const uint16_t* brow;
+            if (kKind == 1) {
+                const int half = r >> 6, rr = r & 63;
+                srow = scb + (size_t)(2 * half) * 64 * G + rr * G;
+                brow = srow + 64 * G;
+            } else {
+                srow = scb + (size_t)r * G;
+                brow = scb + (size_t)128 * G + r * G;
+            }
+            const bool vec = (G & 7) == 0;
+            uint4 sv = make_uint4(0, 0, 0, 0), bv = sv;
+            bool ok = true;
+            for (int g = 0; g < t.nk; ++g, ++it) {
+                const int c = it % NC;
+                if (!bar_wait(code_full + c, (it / NC) & 1, ctl, P.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                const uint4* cp = reinterpret_cast<const uint4*>(scode + c * pl.code_stage + r * sbytes);
+                uint4 q0 = cp[0], q1 = cp[1], q2 = make_uint4(0, 0, 0, 0), q3 = q2;
+                if (P.bits == 8) {
+                    q2 = cp[2];
+                    q3 = cp[3];
+                }
+                bar_arrive(code_empty + c);
+                uint16_t s16, b16;
+                if (vec) {
+                    if ((g & 7) == 0) {
+                        sv = *reinterpret_cast<const uint4*>(srow + g);
+                        bv = *reinterpret_cast<const uint4*>(brow + g);
+                    }
+                    s16 = pick16(sv, g & 7);
+                    b16 = pick16(bv, g & 7);
+                } else {
+                    s16 = srow[g];
+                    b16 = brow[g];
+                }
+                const __half2 s2 = __half2half2(__float2half_rn(bf2f(s16)));
+                const __half2 b2 = __half2half2(__float2half_rn(bf2f(b16)));
+                const int st = it % kStages;
+                if (!bar_wait(empty + st, ((it / kStages) & 1) ^ 1, ctl, P.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* arow = sa + st * kTileBytes + r * 128;
+                const uint32_t sw = r & 7;
+                if (P.bits == 4) {
+                    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        *reinterpret_cast<uint4*>(arow + ((ch ^ sw) << 4)) = deq_int4(w[ch], s2, b2);
+                } else {
+                    const uint32_t w[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
+                                            q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        *reinterpret_cast<uint4*>(arow + ((ch ^ sw) << 4)) = deq_int8(w[2 * ch], w[2 * ch + 1], s2, b2);
+                }
+                fence_async_smem();
+                bar_arrive(full_a + st);
+            }
+            if (!ok)
+                break;
+            bar_arrive(sc_empty + sb);
+        }
+    } else if (warp < 8) {
+        // ---- gathering producers: thread n owns token row n of the B tile ----
+        // Plain 16-byte loads and shared stores, the next slice's row already in flight while this
+        // slice waits for its stage. (Rows written with cp.async and released after
+        // cp.async.wait_group + fence.proxy.async were measured to reach tcgen05.mma stale at
+        // times; stores from registers followed by the proxy fence are reliable.)
+        const int n = threadIdx.x - 128;
+        uint32_t it = 0;
+        for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x) {
+            const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+            const bool act = n < n_mma(t.nn), live = n < t.nn;
+            const __half* src = nullptr;
+            if (live)
+                src = kKind == 1 ? P.u_h + (size_t)P.list[t.n0 + n] * P.H : P.hbuf + (size_t)(t.n0 + n) * P.Imax;
+            uint4 v[8], nv[8];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                v[ch] = live ? __ldg(reinterpret_cast<const uint4*>(src + ch * 8)) : make_uint4(0, 0, 0, 0);
+            bool ok = true;
+            for (int g = 0; g < t.nk; ++g, ++it) {
+                const bool more = live && g + 1 < t.nk;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    nv[ch] = more ? __ldg(reinterpret_cast<const uint4*>(src + (g + 1) * kKS + ch * 8))
+                                  : make_uint4(0, 0, 0, 0);
+                const int st = it % kStages;
+                if (!bar_wait(empty + st, ((it / kStages) & 1) ^ 1, ctl, P.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                if (act) {
+                    uint8_t* brow = sbt + st * kTileBytes + n * 128;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        *reinterpret_cast<uint4*>(brow + ((ch ^ (n & 7)) << 4)) = v[ch];
+                }
+                fence_async_smem();
+                bar_arrive(full_b + st);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    v[ch] = nv[ch];
+            }
+            if (!ok)
+                break;
+        }
+    } else if (warp < 12) {
+        // ---- epilogue: warp 8 + q reads TMEM lanes 32q .. 32q + 31 (tile row = lane) ----
+        const int q = warp - 8, r = q * 32 + lane;
+        uint32_t j = 0;
+        for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
+            const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+            const int ab = j & 1;
+            if (!bar_wait(acc_full + ab, (j >> 1) & 1, ctl, P.status, lim))
+                break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + ab * kNT;
+            const int N = n_mma(t.nn);
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                float v[16];
+                tmem_ld16(tbase + c0, v);
+                if (kKind == 1) {
+                    // rows 64..127 hold the up projections of rows 0..63: hand them over in shared memory
+                    if (q >= 2) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            xch[(r - 64) * 17 + i] = v[i];
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (q < 2) {
+                        const int row = t.m0 + r;
+                        const int pos = (row & ~7) | kperm(row & 7, P.bits);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int n = c0 + i;
+                            if (n < t.nn) {
+                                const float gt = v[i], up = xch[r * 17 + i];
+                                const float h = __fdividef(gt, 1.f + __expf(-gt)) * up;
+                                P.hbuf[(size_t)(t.n0 + n) * P.Imax + pos] = __float2half_rn(h);
+                            }
+                        }
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                } else {
+                    const int o = t.m0 + r;
+                    if (o < P.H) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int n = c0 + i;
+                            if (n < t.nn) {
+                                const int a = t.n0 + n;
+                                atomicAdd(P.y + (size_t)P.list[a] * P.H + o, P.aw[a] * v[i]);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            bar_arrive(acc_empty + ab);
+        }
+    } else if (warp == 12) {
+        if (lane == 0) {
+            // ---- TMA producer: per task the scale/bias block, per slice the code tile ----
+            for (int m = 0; m < 3; ++m) {
+                asm volatile("prefetch.tensormap [%0];" ::"l"(&P.map_q[0][m]) : "memory");
+                asm volatile("prefetch.tensormap [%0];" ::"l"(&P.map_q[1][m]) : "memory");
+            }
+            uint32_t it = 0, j = 0;
+            for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
+                const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+                const BlobGeo& geo = t.shared ? P.geo_s : P.geo;
+                const int sb = j & 1;
+                if (!bar_wait(sc_empty + sb, ((j >> 1) & 1) ^ 1, ctl, P.status, lim))
+                    goto tma_done;
+                {
+                    uint8_t* dst = ssc + sb * pl.sc_bytes;
+                    if (kKind == 1) {
+                        const int G = geo.groups[0];
+                        const uint32_t nb = 64u * G * 2;
+                        bar_expect(sc_full + sb, 4 * nb);
+                        bulk(dst, t.blob + geo.s_off[0] + (size_t)t.m0 * G * 2, nb, sc_full + sb);
+                        bulk(dst + nb, t.blob + geo.b_off[0] + (size_t)t.m0 * G * 2, nb, sc_full + sb);
+                        bulk(dst + 2 * nb, t.blob + geo.s_off[1] + (size_t)t.m0 * G * 2, nb, sc_full + sb);
+                        bulk(dst + 3 * nb, t.blob + geo.b_off[1] + (size_t)t.m0 * G * 2, nb, sc_full + sb);
+                    } else {
+                        const int G = geo.groups[2];
+                        const int rows = min(128, P.H - t.m0);
+                        const uint32_t nb = (uint32_t)rows * G * 2;
+                        bar_expect(sc_full + sb, 2 * nb);
+                        bulk(dst, t.blob + geo.s_off[2] + (size_t)t.m0 * G * 2, nb, sc_full + sb);
+                        bulk(dst + 128u * G * 2, t.blob + geo.b_off[2] + (size_t)t.m0 * G * 2, nb, sc_full + sb);
+                    }
+                }
+                for (int g = 0; g < t.nk; ++g, ++it) {
+                    const int c = it % NC;
+                    if (!bar_wait(code_empty + c, ((it / NC) & 1) ^ 1, ctl, P.status, lim))
+                        goto tma_done;
+                    uint8_t* dst = scode + c * pl.code_stage;
+                    bar_expect(code_full + c, pl.code_stage);
+                    if (kKind == 1) {
+                        tma3d(dst, &P.map_q[t.shared][0], g * sbytes, t.m0, t.slot, code_full + c);
+                        tma3d(dst + 64 * sbytes, &P.map_q[t.shared][1], g * sbytes, t.m0, t.slot, code_full + c);
+                    } else {
+                        tma3d(dst, &P.map_q[t.shared][2], g * sbytes, t.m0, t.slot, code_full + c);
+                    }
+                }
+            }
+        tma_done:
+            for (uint32_t i = it > (uint32_t)NC ? it - NC : 0; i < it; ++i)
+                bar_wait(code_full + i % NC, (i / NC) & 1, ctl, P.status, lim);
+            for (uint32_t i = j > 2 ? j - 2 : 0; i < j; ++i)
+                bar_wait(sc_full + (i & 1), (i >> 1) & 1, ctl, P.status, lim);
+        }
+    } else {
+        if (lane == 0) {
+            // ---- MMA issuer ----
+            uint32_t it = 0, j = 0;
+            for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
+                const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+                const uint32_t id = idesc(n_mma(t.nn), false);
+                const int ab = j & 1;
+                if (!bar_wait(acc_empty + ab, ((j >> 1) & 1) ^ 1, ctl, P.status, lim))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + ab * kNT;
+                bool ok = true;
+                for (int g = 0; g < t.nk; ++g, ++it) {
+                    const int st = it % kStages;
+                    if (!bar_wait(full_a + st, (it / kStages) & 1, ctl, P.status, lim) ||
+                        !bar_wait(full_b + st, (it / kStages) & 1, ctl, P.status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a = sdesc(su32(sa + st * kTileBytes)), b = sdesc(su32(sbt + st * kTileBytes));
+#pragma unroll
+                    for (int kk = 0; kk < kKS / 16; ++kk)
+                        mma(d, a + 2 * kk, b + 2 * kk, id, (g | kk) != 0);
+                    mma_commit(empty + st);
+                }
+                if (!ok)
+                    break;
+                mma_commit(acc_full + ab);
+            }
+            mma_commit(fin);
+            bar_wait(fin, 0, ctl, P.status, lim);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 13) {
+        tc_fence_after();
+        tmem_free(tmem);
+    }
+}
+
+size_t router_smem_bytes() { return 2 * kStagesR * kTileBytes + 64 * 8 + 1024; }
+
+size_t expert_smem_bytes(int H, int Imax, int bits) { return xplan(H, Imax, bits).total + 1024; }
+
+void launch_router_gemm(const GroupedArgs& A, int grid, cudaStream_t st)
+{
+    static bool attr = false;
+    const size_t smem = router_smem_bytes();
+    if (!attr) {
+        cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr = true;
+    }
+    router_kernel<<<grid, kThreadsR, smem, st>>>(A);
+}
+
+void launch_expert_gemm(int kind, const GroupedArgs& A, const int4* tasks, const int32_t* n_tasks, int grid,
+                        cudaStream_t st)
+{
+    static bool attr[2] = {false, false};
+    GroupedArgs P = A;
+    P.tasks = tasks;
+    P.n_tasks = n_tasks;
+    const size_t smem = expert_smem_bytes(A.H, A.Imax, A.bits);
+    if (kind == 1) {
+        if (!attr[0]) {
+            cudaFuncSetAttribute(expert_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+            attr[0] = true;
+        }
+        expert_kernel<1><<<grid, kThreadsX, smem, st>>>(P);
+    } else {
+        if (!attr[1]) {
+            cudaFuncSetAttribute(expert_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+            attr[1] = true;
+        }
+        expert_kernel<2><<<grid, kThreadsX, smem, st>>>(P);
+    }
+}
+
+}  // namespace tc
+}  // namespace moe

@@ -55,6 +55,47 @@ inline int encode_arena_maps(CUtensorMap (&maps)[3], const uint8_t* arena, int n
     return 0;
 }
 
+// Code sections (gate, up, down) as 3D byte tensors [slots][rows][row bytes] with boxes of one
+// 64-element K slice (32 bytes at int4, 64 at int8) by 64 rows (gate, up) or 128 rows (down):
+// the tiles the batched path's dequantising warps read. `base` is the arena (n_slots blobs at
+// `stride`) or one blob (n_slots = 1).
+inline int encode_slice_maps(CUtensorMap (&maps)[3], const uint8_t* base, int n_slots, uint64_t stride,
+                             const BlobGeo& geo, int bits)
+{
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn)
+        return -1;
+    for (int m = 0; m < 3; ++m) {
+        const cuuint64_t dims[3] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)geo.rows[m], (cuuint64_t)n_slots};
+        const cuuint64_t strides[2] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)stride};
+        const cuuint32_t box[3] = {(cuuint32_t)(64 * bits / 8), m == 2 ? 128u : 64u, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        const CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, (void*)(base + geo.q_off[m]), dims, strides,
+                              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return (int)r;
+    }
+    return 0;
+}
+
+// A row-major bf16 matrix [rows][cols] with boxes of 64 columns (128 bytes) x box_rows rows,
+// 128-byte swizzled: the K-major operand tiles of the tensor cores.
+inline int encode_bf16_tiles(CUtensorMap* map, const void* ptr, int cols, int rows, int box_rows)
+{
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn)
+        return -1;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
 // Shapes the fused kernel takes: the staging plan must fit in shared memory and the grid must
 // hold at least one block per routed expert. Returns the dynamic shared memory bytes, 0 if not.
 inline uint32_t fused_smem_bytes(int H, int E, int k, int I, int Is, int bits, int grid, int smem_optin)

@@ -1,9 +1,11 @@
 """GPU parity of the batched (GEMM) path against the CPU oracle, token by token.
 
 The batched path multiplies fp16-rounded weights (w = s * q + b, one rounding of at most 2^-11
-relative each) by fp16 activations, and hands h to the down GEMM in fp16: two independent
-roundings of relative size <= 2^-11 feed each output, whose errors add up like a random walk, so
-the expected rel-L2 is a few 1e-4. Asserted: the stated 2e-3 and a derived 1e-3."""
+relative each) by the fp16 input (bf16 -> fp16 is exact in range), and hands h to the down GEMM
+in fp16: two independent roundings of relative size <= 2^-11 feed each output, whose errors add
+up like a random walk, so the expected rel-L2 is a few 1e-4. Asserted: the stated 2e-3 and a
+derived 1e-3. The k + 1 expert outputs of a token are summed by fp32 reductions in whatever order
+the tiles finish, so outputs agree run to run to fp32 rounding, not bit for bit."""
 import json
 import os
 
@@ -62,9 +64,10 @@ def test_tiny_batched(orc, bits, renorm):
     assert err <= TOL and err <= DERIVED, err
 
 
-@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+@pytest.mark.parametrize("T", [1, 15, 17, 127, 128, 129, 300])
 def test_token_counts(orc, T):
-    """One token, just under/at/over one 64-token tile, and several tiles with a ragged tail."""
+    """One token, around the 16-column MMA granule and the 128-token tile, and several tiles with
+    a ragged tail."""
     _, _, err = _case(orc, synth.TINY, seed=11, T=T, sample=sorted({0, T // 2, T - 1}))
     assert err <= DERIVED, err
 
@@ -126,4 +129,5 @@ def test_batched_workspace_and_errors(orc):
         R.layer_forward_batched(0, x, work=small)
     y1, i1, w1 = R.layer_forward_batched(0, x)
     y2, i2, w2 = R.layer_forward_batched(0, x)
-    assert torch.equal(i1, i2) and torch.equal(w1, w2) and torch.equal(y1, y2)
+    assert torch.equal(i1, i2) and torch.equal(w1, w2)
+    assert rel_l2(y1.cpu().numpy(), y2.cpu().numpy()) < 1e-6
