@@ -475,7 +475,7 @@ def run_batched(args):
     T = BATCHED[args.config]
     name, _, bits, desc = CONFIGS[args.config]
     sh = _shape(name, bits)
-    L = BATCHED_LAYERS
+    L = args.layers or BATCHED_LAYERS
     R = Resident(sh, L, SEED, flags=moe.RENORM, verbose=(rank == 0))
     H, E, k = sh.hidden, sh.n_experts, sh.top_k
     n_x = 4

@@ -19,7 +19,7 @@
 namespace moe {
 __global__ void moe_decode_kernel(const __grid_constant__ StepParams P);
 namespace bat {
-void launch_to_half(const uint16_t* x, __half* y, size_t n, int bits, cudaStream_t st);
+void launch_gather_rows(const uint16_t* x, const int32_t* list, int A, int H, int bits, __half* us, cudaStream_t st);
 void launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm, const uint16_t* u,
                  const uint16_t* wsg, int H, int32_t* idx, float* w, float* gamma, int32_t* counts, cudaStream_t st);
 void launch_plan(const int32_t* counts, int E, int T, int I, int Is, int H, int32_t* offs, int32_t* cursor,
@@ -761,7 +761,7 @@ moe_status moe_stack_forward_streamed(moe_pool* p, int32_t layer0, int32_t n_lay
 namespace {
 
 struct BatLayout {
-    size_t u_h, logits, idx, w, gamma, counts, offs, cursor, list, aw, hbuf, tasks_gu, tasks_dn, n_tasks, total;
+    size_t us, logits, idx, w, gamma, counts, offs, cursor, list, aw, hbuf, tasks_gu, tasks_dn, n_tasks, total;
     size_t max_gu, max_dn;
 };
 
@@ -776,7 +776,7 @@ BatLayout bat_layout(const moe_shape& s, int T)
         f = o;
         o = up256(o + bytes);
     };
-    take(b.u_h, 2 * (size_t)T * H);
+    take(b.us, 2 * A * H);
     take(b.logits, 4 * (size_t)T * E);
     take(b.idx, 4 * (size_t)T * k);
     take(b.w, 4 * (size_t)T * k);
@@ -845,10 +845,15 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     int rc = encode_slice_maps(A.map_q[0], p->arena, p->S, p->geo.stride, p->geo, sh.bits);
     if (rc == 0)
         rc = encode_slice_maps(A.map_q[1], L.shared_blob, 1, p->geo_s.stride, p->geo_s, sh.bits);
+    const int nA = T * (k + 1);
     if (rc == 0)
-        rc = encode_bf16_tiles(&A.map_wr, L.router, H, E, 128);
+        rc = encode_tiles16(&A.map_wr, L.router, H, E, 128, false);
     if (rc == 0)
-        rc = encode_bf16_tiles(&A.map_u, d_x, H, T, tc::kNT);
+        rc = encode_tiles16(&A.map_u, d_x, H, T, tc::kNT, false);
+    if (rc == 0)
+        rc = encode_tiles16(&A.map_b[0], w + bl.us, H, nA, tc::kBRows, true);
+    if (rc == 0)
+        rc = encode_tiles16(&A.map_b[1], w + bl.hbuf, Imax, nA, tc::kBRows, true);
     if (rc != 0)
         return fail(MOE_E_CUDA, "tensor map encoding failed (%d)", rc);
     A.geo = p->geo;
@@ -865,7 +870,6 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     A.stride = p->geo.stride;
     A.table = reinterpret_cast<const int32_t*>(p->ws + p->wl.table) + (size_t)layer * E;
     A.shared_blob = L.shared_blob;
-    A.u_h = reinterpret_cast<const __half*>(w + bl.u_h);
     A.list = reinterpret_cast<const int32_t*>(w + bl.list);
     A.aw = reinterpret_cast<const float*>(w + bl.aw);
     A.hbuf = reinterpret_cast<__half*>(w + bl.hbuf);
@@ -887,14 +891,14 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
 
     CUDA_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * (E + 2), cs));
     CUDA_TRY(cudaMemsetAsync(d_y, 0, sizeof(float) * (size_t)T * H, cs));
-    bat::launch_to_half(static_cast<const uint16_t*>(d_x), reinterpret_cast<__half*>(w + bl.u_h), (size_t)T * H,
-                        sh.bits, cs);
     const int r_tasks = ((E + 127) / 128) * ((T + tc::kNT - 1) / tc::kNT);
     tc::launch_router_gemm(A, r_tasks < grid ? r_tasks : grid, cs);
     bat::launch_topk(A.logits, L.logit_bias, T, E, k, (sh.flags & MOE_RENORM) ? 1 : 0,
                      static_cast<const uint16_t*>(d_x), L.shared_gate, H, idx, wts, gamma, counts, cs);
     bat::launch_plan(counts, E, T, I, Is, H, offs, cursor, tgu, tdn, ntasks, cs);
     bat::launch_place(idx, wts, gamma, T, E, k, cursor, const_cast<int32_t*>(A.list), const_cast<float*>(A.aw), cs);
+    bat::launch_gather_rows(static_cast<const uint16_t*>(d_x), A.list, nA, H, sh.bits, reinterpret_cast<__half*>(w + bl.us),
+                            cs);
     tc::launch_expert_gemm(1, A, tgu, ntasks, grid, cs);
     tc::launch_expert_gemm(2, A, tdn, ntasks + 1, grid, cs);
     CUDA_TRY(cudaGetLastError());

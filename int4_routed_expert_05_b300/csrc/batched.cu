@@ -11,8 +11,8 @@
 //   4. grouped gate/up GEMM per expert with SwiGLU in the epilogue -> h[assignment][I] (fp16);
 //   5. grouped down GEMM per expert, scaled by the assignment's weight -> partial y rows (fp32);
 //   6. per token: y = sum of its partials in rank order, then the shared expert's (fixed order).
-// This file holds everything around the GEMMs (grouped.cu): the fp16 copy of the input, top-k,
-// the device-side plan (offsets per expert, GEMM task lists) and the placement of assignments.
+// This file holds everything around the GEMMs (grouped.cu): top-k, the device-side plan (offsets
+// per expert, GEMM task lists), the placement of assignments and the input rows in assignment order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -27,13 +27,36 @@ namespace bat {
 
 __device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-// bf16 input -> fp16 copy (B operand of the expert GEMMs), K-permuted within 8-element blocks in
-// the order the dequantiser emits weight pairs (tc::kperm). bf16 -> fp16 is exact for |x| in
+// The expert GEMMs' input operand: row p = the fp16 copy of the input row of assignment p's token,
+// K-permuted within 8-element blocks in the order the dequantiser emits weight pairs (tc::kperm).
+// One warp per row, one 8-element block per lane and step. bf16 -> fp16 is exact for |x| in
 // [2^-14, 65504] (bf16's 8-bit significand fits in fp16's 11 bits).
-__global__ void to_half_kernel(const uint16_t* __restrict__ x, __half* __restrict__ y, size_t n, int bits)
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ list, int A, int H,
+                                   int bits, __half* __restrict__ us)
 {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        y[(i & ~(size_t)7) | tc::kperm((int)(i & 7), bits)] = __float2half_rn(bf(x[i]));
+    const int lane = threadIdx.x & 31;
+    for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < A; p += (gridDim.x * blockDim.x) >> 5) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)list[p] * H);
+        uint4* dst = reinterpret_cast<uint4*>(us + (size_t)p * H);
+        for (int c = lane; c < H / 8; c += 32) {
+            const uint4 v = __ldg(src + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            __half h[8], o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                h[j] = __float2half_rn(bf((uint16_t)(w[j >> 1] >> (16 * (j & 1)))));
+            if (bits == 4) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    o[tc::kperm(j, 4)] = h[j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    o[tc::kperm(j, 8)] = h[j];
+            }
+            dst[c] = *reinterpret_cast<const uint4*>(o);
+        }
+    }
 }
 
 __device__ __forceinline__ uint32_t ord_key(float f)
@@ -207,9 +230,9 @@ __global__ void place_kernel(const int32_t* __restrict__ idx, const float* __res
     }
 }
 
-void launch_to_half(const uint16_t* x, __half* y, size_t n, int bits, cudaStream_t st)
+void launch_gather_rows(const uint16_t* x, const int32_t* list, int A, int H, int bits, __half* us, cudaStream_t st)
 {
-    to_half_kernel<<<1184, 256, 0, st>>>(x, y, n, bits);
+    gather_rows_kernel<<<(A + 7) / 8 < 2368 ? (A + 7) / 8 : 2368, 256, 0, st>>>(x, list, A, H, bits, us);
 }
 
 void launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm, const uint16_t* u,

@@ -14,9 +14,13 @@
 //     the hardware swizzle, so a slice goes global -> shared -> tensor core untouched;
 //   * expert GEMMs: TMA stages the packed codes; four dequantising warps turn them into fp16
 //     weights w = s * q + b (one rounding, s and b exact in fp16 for the workloads' ranges) in the
-//     swizzled layout; four gathering warps copy the routed tokens' activation rows into the B
-//     tile; four epilogue warps read the accumulators with tcgen05.ld and apply SwiGLU
-//     (gate/up: h to a per-assignment buffer) or the combine weight (down: fp32 reductions into y).
+//     swizzled layout; TMA brings the expert's token rows (input rows gathered in assignment order
+//     beforehand, or h rows) into the B tile; four epilogue warps read the accumulators with
+//     tcgen05.ld and apply SwiGLU (gate/up: h to a per-assignment buffer) or the combine weight
+//     (down: fp32 reductions into y).
+//   Operand tiles the MMA reads are written either by TMA or by st.shared followed by
+//   fence.proxy.async before the mbarrier release (rows written by cp.async and released after
+//   cp.async.wait_group + fence.proxy.async were measured to reach tcgen05.mma stale at times).
 // Every wait is bounded: on expiry the kernel records MOE timeout status, drains its own copies and
 // frees its tensor memory.
 #include <cuda.h>
@@ -65,11 +69,10 @@ struct Ctl {
     uint32_t tmem;
 };
 
-// Bounded wait on phase `parity` of m. False on timeout or when another role gave up.
-__device__ __noinline__ bool bar_wait(uint64_t* m, uint32_t parity, Ctl* ctl, int* status, long long limit)
+// Bounded wait on phase `parity` of m. False on timeout or when another role gave up. The test of
+// an already completed phase stays inline; only the polling loop is a call.
+__device__ __noinline__ bool bar_wait_slow(uint64_t* m, uint32_t parity, Ctl* ctl, int* status, long long limit)
 {
-    if (bar_try(m, parity))
-        return true;
     const long long t0 = clock64();
     for (int it = 1;; ++it) {
         if (bar_try(m, parity))
@@ -84,6 +87,11 @@ __device__ __noinline__ bool bar_wait(uint64_t* m, uint32_t parity, Ctl* ctl, in
             }
         }
     }
+}
+
+__device__ __forceinline__ bool bar_wait(uint64_t* m, uint32_t parity, Ctl* ctl, int* status, long long limit)
+{
+    return bar_try(m, parity) || bar_wait_slow(m, parity, ctl, status, limit);
 }
 
 // ---- copies ----
@@ -156,6 +164,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+// 4 consecutive fp32 columns of this thread's accumulator row
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4])
+{
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
         v[i] = __uint_as_float(r[i]);
 }
 
@@ -377,12 +399,12 @@ __global__ void __launch_bounds__(kThreadsR, 1) router_kernel(const __grid_const
 // tokens, SwiGLU epilogue -> hbuf. kind 2: down tiles (128 rows) against the expert's h rows,
 // epilogue y[token] += weight * acc.
 // ------------------------------------------------------------------------------------------------
-template <int kKind>
+template <int kKind, int kBits>
 __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_constant__ GroupedArgs P)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const XPlan pl = xplan(P.H, P.Imax, P.bits);
+    const XPlan pl = xplan(P.H, P.Imax, kBits);
     uint8_t* sa = sm + pl.a;
     uint8_t* sbt = sm + pl.b;
     uint8_t* scode = sm + pl.code;
@@ -404,21 +426,21 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tasks = *P.n_tasks;
     const long long lim = P.timeout_cycles;
-    const uint32_t sbytes = kKS * P.bits / 8;  // code bytes of one row in one slice
+    constexpr uint32_t sbytes = kKS * kBits / 8;  // code bytes of one row in one slice
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            bar_init(full_a + i, 128);
-            bar_init(full_b + i, 128);
+            bar_init(full_a + i, 256);
+            bar_init(full_b + i, 1);
             bar_init(empty + i, 1);
         }
         for (int i = 0; i < NC; ++i) {
             bar_init(code_full + i, 1);
-            bar_init(code_empty + i, 128);
+            bar_init(code_empty + i, 256);
         }
         for (int i = 0; i < 2; ++i) {
             bar_init(sc_full + i, 1);
-            bar_init(sc_empty + i, 128);
+            bar_init(sc_empty + i, 256);
             bar_init(acc_full + i, 1);
             bar_init(acc_empty + i, 128);
         }
@@ -433,9 +455,10 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = ctl->tmem;
 
-    if (warp < 4) {
-        // ---- dequantising producers: thread r owns row r of the A tile ----
-        const int r = threadIdx.x;
+    if (warp < 8) {
+        // ---- dequantising producers: thread (hk, r) owns half hk (32 of the 64 K elements) of row
+        // r of the A tile: two warps per SMSP share each slice ----
+        const int r = threadIdx.x & 127, hk = threadIdx.x >> 7;
         uint32_t it = 0, j = 0;
         for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
             const TaskX t = decode_task(P, kKind, P.tasks[ti]);
@@ -459,6 +482,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             }
             const bool vec = (G & 7) == 0;
             uint4 sv = make_uint4(0, 0, 0, 0), bv = sv;
+            int blk = -1;
             bool ok = true;
             for (int g = 0; g < t.nk; ++g, ++it) {
                 const int c = it % NC;
@@ -466,18 +490,17 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                     ok = false;
                     break;
                 }
-                const uint4* cp = reinterpret_cast<const uint4*>(scode + c * pl.code_stage + r * sbytes);
-                uint4 q0 = cp[0], q1 = cp[1], q2 = make_uint4(0, 0, 0, 0), q3 = q2;
-                if (P.bits == 8) {
-                    q2 = cp[2];
-                    q3 = cp[3];
-                }
+                const uint4* cp =
+                    reinterpret_cast<const uint4*>(scode + c * pl.code_stage + r * sbytes + hk * (sbytes / 2));
+                const uint4 q0 = cp[0];
+                const uint4 q1 = kBits == 8 ? cp[1] : make_uint4(0, 0, 0, 0);
                 bar_arrive(code_empty + c);
                 uint16_t s16, b16;
                 if (vec) {
-                    if ((g & 7) == 0) {
-                        sv = *reinterpret_cast<const uint4*>(srow + g);
-                        bv = *reinterpret_cast<const uint4*>(brow + g);
+                    if ((g >> 3) != blk) {
+                        blk = g >> 3;
+                        sv = *reinterpret_cast<const uint4*>(srow + (g & ~7));
+                        bv = *reinterpret_cast<const uint4*>(brow + (g & ~7));
                     }
                     s16 = pick16(sv, g & 7);
                     b16 = pick16(bv, g & 7);
@@ -494,17 +517,17 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                 }
                 uint8_t* arow = sa + st * kTileBytes + r * 128;
                 const uint32_t sw = r & 7;
-                if (P.bits == 4) {
+                if (kBits == 4) {
+                    const uint32_t w[4] = {q0.x, q0.y, q0.z, q0.w};
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+                        *reinterpret_cast<uint4*>(arow + (((hk * 4 + ch) ^ sw) << 4)) = deq_int4(w[ch], s2, b2);
+                } else {
                     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        *reinterpret_cast<uint4*>(arow + ((ch ^ sw) << 4)) = deq_int4(w[ch], s2, b2);
-                } else {
-                    const uint32_t w[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
-                                            q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        *reinterpret_cast<uint4*>(arow + ((ch ^ sw) << 4)) = deq_int8(w[2 * ch], w[2 * ch + 1], s2, b2);
+                    for (int ch = 0; ch < 4; ++ch)
+                        *reinterpret_cast<uint4*>(arow + (((hk * 4 + ch) ^ sw) << 4)) =
+                            deq_int8(w[2 * ch], w[2 * ch + 1], s2, b2);
                 }
                 fence_async_smem();
                 bar_arrive(full_a + st);
@@ -512,51 +535,6 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             if (!ok)
                 break;
             bar_arrive(sc_empty + sb);
-        }
-    } else if (warp < 8) {
-        // ---- gathering producers: thread n owns token row n of the B tile ----
-        // Plain 16-byte loads and shared stores, the next slice's row already in flight while this
-        // slice waits for its stage. (Rows written with cp.async and released after
-        // cp.async.wait_group + fence.proxy.async were measured to reach tcgen05.mma stale at
-        // times; stores from registers followed by the proxy fence are reliable.)
-        const int n = threadIdx.x - 128;
-        uint32_t it = 0;
-        for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x) {
-            const TaskX t = decode_task(P, kKind, P.tasks[ti]);
-            const bool act = n < n_mma(t.nn), live = n < t.nn;
-            const __half* src = nullptr;
-            if (live)
-                src = kKind == 1 ? P.u_h + (size_t)P.list[t.n0 + n] * P.H : P.hbuf + (size_t)(t.n0 + n) * P.Imax;
-            uint4 v[8], nv[8];
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                v[ch] = live ? __ldg(reinterpret_cast<const uint4*>(src + ch * 8)) : make_uint4(0, 0, 0, 0);
-            bool ok = true;
-            for (int g = 0; g < t.nk; ++g, ++it) {
-                const bool more = live && g + 1 < t.nk;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    nv[ch] = more ? __ldg(reinterpret_cast<const uint4*>(src + (g + 1) * kKS + ch * 8))
-                                  : make_uint4(0, 0, 0, 0);
-                const int st = it % kStages;
-                if (!bar_wait(empty + st, ((it / kStages) & 1) ^ 1, ctl, P.status, lim)) {
-                    ok = false;
-                    break;
-                }
-                if (act) {
-                    uint8_t* brow = sbt + st * kTileBytes + n * 128;
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        *reinterpret_cast<uint4*>(brow + ((ch ^ (n & 7)) << 4)) = v[ch];
-                }
-                fence_async_smem();
-                bar_arrive(full_b + st);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    v[ch] = nv[ch];
-            }
-            if (!ok)
-                break;
         }
     } else if (warp < 12) {
         // ---- epilogue: warp 8 + q reads TMEM lanes 32q .. 32q + 31 (tile row = lane) ----
@@ -570,41 +548,53 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + ab * kNT;
             const int N = n_mma(t.nn);
-            for (int c0 = 0; c0 < N; c0 += 16) {
-                float v[16];
-                tmem_ld16(tbase + c0, v);
-                if (kKind == 1) {
-                    // rows 64..127 hold the up projections of rows 0..63: hand them over in shared memory
+            if (kKind == 1) {
+                // rows 64..127 hold the up projections of rows 0..63: handed over in shared memory,
+                // 16 columns at a time
+                const int row = t.m0 + (r & 63);
+                const int pos = (row & ~7) | kperm(row & 7, kBits);
+                for (int c0 = 0; c0 < N; c0 += 16) {
                     if (q >= 2) {
+#pragma unroll 1
+                        for (int c = 0; c < 16; c += 4) {
+                            float v[4];
+                            tmem_ld4(tbase + c0 + c, v);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            xch[(r - 64) * 17 + i] = v[i];
+                            for (int i = 0; i < 4; ++i)
+                                xch[(r - 64) * 17 + c + i] = v[i];
+                        }
                     }
                     asm volatile("bar.sync 1, 128;" ::: "memory");
                     if (q < 2) {
-                        const int row = t.m0 + r;
-                        const int pos = (row & ~7) | kperm(row & 7, P.bits);
+#pragma unroll 1
+                        for (int c = 0; c < 16; c += 4) {
+                            float v[4];
+                            tmem_ld4(tbase + c0 + c, v);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int n = c0 + i;
-                            if (n < t.nn) {
-                                const float gt = v[i], up = xch[r * 17 + i];
-                                const float h = __fdividef(gt, 1.f + __expf(-gt)) * up;
-                                P.hbuf[(size_t)(t.n0 + n) * P.Imax + pos] = __float2half_rn(h);
+                            for (int i = 0; i < 4; ++i) {
+                                const int n = c0 + c + i;
+                                if (n < t.nn) {
+                                    const float gt = v[i], up = xch[r * 17 + c + i];
+                                    const float h = __fdividef(gt, 1.f + __expf(-gt)) * up;
+                                    P.hbuf[(size_t)(t.n0 + n) * P.Imax + pos] = __float2half_rn(h);
+                                }
                             }
                         }
                     }
                     asm volatile("bar.sync 1, 128;" ::: "memory");
-                } else {
-                    const int o = t.m0 + r;
+                }
+            } else {
+                const int o = t.m0 + r;
+#pragma unroll 1
+                for (int c0 = 0; c0 < N; c0 += 4) {
+                    float v[4];
+                    tmem_ld4(tbase + c0, v);
                     if (o < P.H) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int n = c0 + i;
-                            if (n < t.nn) {
-                                const int a = t.n0 + n;
+                        for (int i = 0; i < 4; ++i) {
+                            const int a = t.n0 + c0 + i;
+                            if (c0 + i < t.nn)
                                 atomicAdd(P.y + (size_t)P.list[a] * P.H + o, P.aw[a] * v[i]);
-                            }
                         }
                     }
                 }
@@ -665,9 +655,36 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             for (uint32_t i = j > 2 ? j - 2 : 0; i < j; ++i)
                 bar_wait(sc_full + (i & 1), (i >> 1) & 1, ctl, P.status, lim);
         }
+    } else if (warp == 14) {
+        if (lane == 0) {
+            // ---- B operand: the task's token rows of this K slice, boxes of 16 rows ----
+            const CUtensorMap* mb = &P.map_b[kKind - 1];
+            asm volatile("prefetch.tensormap [%0];" ::"l"(mb) : "memory");
+            uint32_t it = 0;
+            for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x) {
+                const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+                const int nb = n_mma(t.nn) / kBRows;
+                bool ok = true;
+                for (int g = 0; g < t.nk; ++g, ++it) {
+                    const int st = it % kStages;
+                    if (!bar_wait(empty + st, ((it / kStages) & 1) ^ 1, ctl, P.status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    bar_expect(full_b + st, (uint32_t)nb * kBRows * 128);
+                    for (int q = 0; q < nb; ++q)
+                        tma2d(sbt + st * kTileBytes + q * kBRows * 128, mb, g * kKS, t.n0 + q * kBRows, full_b + st);
+                }
+                if (!ok)
+                    break;
+            }
+            // every issued copy has landed before the block can exit
+            for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i)
+                bar_wait(full_b + i % kStages, (i / kStages) & 1, ctl, P.status, lim);
+        }
     } else {
         if (lane == 0) {
-            // ---- MMA issuer ----
+            // ---- MMA issuer (warp 13) ----
             uint32_t it = 0, j = 0;
             for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
                 const TaskX t = decode_task(P, kKind, P.tasks[ti]);
@@ -726,24 +743,19 @@ void launch_router_gemm(const GroupedArgs& A, int grid, cudaStream_t st)
 void launch_expert_gemm(int kind, const GroupedArgs& A, const int4* tasks, const int32_t* n_tasks, int grid,
                         cudaStream_t st)
 {
-    static bool attr[2] = {false, false};
+    static bool attr[4] = {false, false, false, false};
     GroupedArgs P = A;
     P.tasks = tasks;
     P.n_tasks = n_tasks;
     const size_t smem = expert_smem_bytes(A.H, A.Imax, A.bits);
-    if (kind == 1) {
-        if (!attr[0]) {
-            cudaFuncSetAttribute(expert_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-            attr[0] = true;
-        }
-        expert_kernel<1><<<grid, kThreadsX, smem, st>>>(P);
-    } else {
-        if (!attr[1]) {
-            cudaFuncSetAttribute(expert_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-            attr[1] = true;
-        }
-        expert_kernel<2><<<grid, kThreadsX, smem, st>>>(P);
+    void (*k)(const GroupedArgs) = kind == 1 ? (A.bits == 4 ? expert_kernel<1, 4> : expert_kernel<1, 8>)
+                                             : (A.bits == 4 ? expert_kernel<2, 4> : expert_kernel<2, 8>);
+    const int ki = (kind - 1) * 2 + (A.bits == 4 ? 0 : 1);
+    if (!attr[ki]) {
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        attr[ki] = true;
     }
+    k<<<grid, kThreadsX, smem, st>>>(P);
 }
 
 }  // namespace tc

@@ -18,7 +18,8 @@ constexpr int kStages = 4;        // A/B operand stages of the expert GEMMs
 constexpr int kStagesR = 6;       // A/B operand stages of the router GEMM
 constexpr int kTileBytes = 128 * 128;  // one 128-row x 64-element fp16/bf16 operand tile
 constexpr int kCodeRing = 32768;  // bytes of the staged-code ring
-constexpr int kThreadsX = 448;    // expert kernel: 4 dequant, 4 gather, 4 epilogue, 1 TMA, 1 MMA warps
+constexpr int kThreadsX = 480;    // expert kernel: 8 dequant, 4 epilogue, code TMA, MMA, operand-B TMA warps
+constexpr int kBRows = 16;        // rows of one B-operand TMA box
 constexpr int kThreadsR = 192;    // router kernel: 4 epilogue, 1 TMA, 1 MMA warps
 constexpr int kTmemCols = 256;    // two accumulators of kNT fp32 columns
 
@@ -26,16 +27,17 @@ struct GroupedArgs {
     CUtensorMap map_q[2][3];  // codes of gate, up, down: [0] over the arena's slots, [1] over the shared blob
     CUtensorMap map_wr;       // router weights bf16 [E][H], 128B-swizzled boxes of 128 rows x 64
     CUtensorMap map_u;        // layer input bf16 [T][H], boxes of 128 tokens x 64
+    CUtensorMap map_b[2];     // expert B operands, fp16 rows of 64 elements in boxes of 16 rows:
+                              // [0] input rows in assignment order [A][H], [1] h rows [A][Imax]
     BlobGeo geo, geo_s;
     int T, H, E, k, I, Is, bits, Imax;
     const uint8_t* arena;
     uint64_t stride;
     const int32_t* table;     // [E] slot of each routed expert of this layer
     const uint8_t* shared_blob;
-    const __half* u_h;        // [T][H] fp16 input, K-permuted within 8-element blocks (see kperm)
     const int32_t* list;      // [A] token of each assignment, grouped by expert
     const float* aw;          // [A] combine weight of each assignment
-    __half* hbuf;             // [A][Imax] SwiGLU output, K-permuted like u_h
+    __half* hbuf;             // [A][Imax] SwiGLU output, K-permuted (see kperm)
     float* y;                 // [T][H] output, zeroed before the down GEMM (fp32 reductions)
     float* logits;            // [T][E]
     const int4* tasks;        // {expert, m0, n0, n} per task

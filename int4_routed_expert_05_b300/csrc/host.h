@@ -79,9 +79,9 @@ inline int encode_slice_maps(CUtensorMap (&maps)[3], const uint8_t* base, int n_
     return 0;
 }
 
-// A row-major bf16 matrix [rows][cols] with boxes of 64 columns (128 bytes) x box_rows rows,
-// 128-byte swizzled: the K-major operand tiles of the tensor cores.
-inline int encode_bf16_tiles(CUtensorMap* map, const void* ptr, int cols, int rows, int box_rows)
+// A row-major 16-bit matrix [rows][cols] (bf16 or fp16) with boxes of 64 columns (128 bytes) x
+// box_rows rows, 128-byte swizzled: the K-major operand tiles of the tensor cores.
+inline int encode_tiles16(CUtensorMap* map, const void* ptr, int cols, int rows, int box_rows, bool fp16)
 {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn)
@@ -90,7 +90,8 @@ inline int encode_bf16_tiles(CUtensorMap* map, const void* ptr, int cols, int ro
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t es[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+    const CUresult r = fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(ptr), dims, strides, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? 0 : (int)r;
