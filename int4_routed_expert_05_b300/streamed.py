@@ -100,10 +100,8 @@ class Streamed:
             self.gate.append(g)
         self.arena = torch.empty(n_slots * self.stride, dtype=torch.uint8, device=device)
         self.ws = torch.zeros(moe.workspace_bytes(self.mshape, n_layers), dtype=torch.uint8, device=device)
-        self.pool = moe.Pool(self.mshape, n_layers, n_slots, self.arena, self.arena.numel(), self.ws, self.ws.numel())
-        for l in range(n_layers):
-            self.pool.set_layer(l, self.router[l], self.shared[l], self.gate[l], self.bias[l])
-        self.pool.sync()
+        self.pool = None
+        self.reset_pool()
         self.copy_stream = torch.cuda.Stream()
         torch.cuda.synchronize()
         if verbose:
@@ -121,8 +119,21 @@ class Streamed:
         self.pool.sync()
         torch.cuda.synchronize()
 
+    def reset_pool(self):
+        """A fresh, empty pool over the same arena and workspace (counters and slot table cleared)."""
+        if self.pool is not None:
+            torch.cuda.synchronize()
+            self.pool.close()
+        self.ws.zero_()
+        self.pool = moe.Pool(self.mshape, self.L, self.n_slots, self.arena, self.arena.numel(), self.ws, self.ws.numel())
+        for l in range(self.L):
+            self.pool.set_layer(l, self.router[l], self.shared[l], self.gate[l], self.bias[l])
+        self.pool.sync()
+        torch.cuda.synchronize()
+
     def measure_hit_rate(self, xs: torch.Tensor, warm: int = 16, tokens: int = 24) -> float:
-        """Hit rate of this pool over `tokens` decode steps after `warm` steps (inputs xs[i % len])."""
+        """Hit rate of a fresh pool over `tokens` decode steps after `warm` steps (inputs xs[i % len])."""
+        self.reset_pool()
         out = torch.empty(self.sh.hidden, dtype=torch.float32, device=xs.device)
         for i in range(warm):
             self.step(xs[i % xs.shape[0]], out)
@@ -135,14 +146,14 @@ class Streamed:
         return (h1 - h0) / max(1, (h1 - h0) + (m1 - m0))
 
     def calibrate_beta(self, xs: torch.Tensor, target: float = 0.55, iters: int = 6, lo: float = 0.0,
-                       hi: float = 1.5) -> tuple[float, float]:
+                       hi: float = 1.5, warm: int = 16, tokens: int = 24) -> tuple[float, float]:
         """Bisect the Zipf strength on the real routing of this stack until the measured hit rate
         is near `target`; returns (beta, hit rate)."""
         best = (self.beta, None)
         for _ in range(iters):
             mid = 0.5 * (lo + hi)
             self.set_beta(mid)
-            hr = self.measure_hit_rate(xs)
+            hr = self.measure_hit_rate(xs, warm=warm, tokens=tokens)
             best = (mid, hr)
             if hr < target:
                 lo = mid
