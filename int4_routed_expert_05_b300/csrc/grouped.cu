@@ -49,6 +49,13 @@ __device__ __forceinline__ void bar_arrive(uint64_t* m)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(m)) : "memory");
 }
+// One arrival per warp: the warp's lanes are ordered before lane 0's release by __syncwarp.
+__device__ __forceinline__ void bar_arrive_warp(uint64_t* m)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        bar_arrive(m);
+}
 __device__ __forceinline__ void bar_expect(uint64_t* m, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(m)), "r"(bytes) : "memory");
@@ -295,7 +302,7 @@ __global__ void __launch_bounds__(kThreadsR, 1) router_kernel(const __grid_const
         }
         for (int i = 0; i < 2; ++i) {
             bar_init(acc_full + i, 1);
-            bar_init(acc_empty + i, 128);
+            bar_init(acc_empty + i, 4);
         }
         bar_init(fin, 1);
         ctl->abort = 0;
@@ -370,8 +377,7 @@ __global__ void __launch_bounds__(kThreadsR, 1) router_kernel(const __grid_const
             const int m0 = (ti % mt) * 128, n0 = (ti / mt) * kNT;
             const int nn = min(kNT, P.T - n0);
             const int ab = j & 1;
-            if (!bar_wait(acc_full + ab, (j >> 1) & 1, ctl, P.status, lim))
-                break;
+            bar_wait(acc_full + ab, (j >> 1) & 1, ctl, P.status, lim);  // no early exit (warp-collective loads)
             tc_fence_after();
             const int row = m0 + r;
             for (int c0 = 0; c0 < n_mma(nn); c0 += 16) {
@@ -383,7 +389,7 @@ __global__ void __launch_bounds__(kThreadsR, 1) router_kernel(const __grid_const
                         P.logits[(size_t)(n0 + c0 + i) * P.E + row] = v[i];
             }
             tc_fence_before();
-            bar_arrive(acc_empty + ab);
+            bar_arrive_warp(acc_empty + ab);
         }
     }
     tc_fence_before();
@@ -413,7 +419,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + pl.bar);
     const int NC = (int)pl.n_code;
     uint64_t* full_a = bars;
-    uint64_t* full_b = bars + kStages;
+    uint64_t* full_b = full_a;  // the B-operand TMA's arrive.expect_tx joins the producers' arrivals
     uint64_t* empty = bars + 2 * kStages;
     uint64_t* code_full = bars + 3 * kStages;
     uint64_t* code_empty = code_full + 8;
@@ -430,19 +436,18 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            bar_init(full_a + i, 256);
-            bar_init(full_b + i, 1);
+            bar_init(full_a + i, 9);  // 8 dequantising warps + the B-operand TMA
             bar_init(empty + i, 1);
         }
         for (int i = 0; i < NC; ++i) {
             bar_init(code_full + i, 1);
-            bar_init(code_empty + i, 256);
+            bar_init(code_empty + i, 8);
         }
         for (int i = 0; i < 2; ++i) {
             bar_init(sc_full + i, 1);
-            bar_init(sc_empty + i, 256);
+            bar_init(sc_empty + i, 8);
             bar_init(acc_full + i, 1);
-            bar_init(acc_empty + i, 128);
+            bar_init(acc_empty + i, 4);
         }
         bar_init(fin, 1);
         ctl->abort = 0;
@@ -465,8 +470,9 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             const BlobGeo& geo = t.shared ? P.geo_s : P.geo;
             const int G = kKind == 1 ? geo.groups[0] : geo.groups[2];
             const int sb = j & 1;
-            if (!bar_wait(sc_full + sb, (j >> 1) & 1, ctl, P.status, lim))
-                break;
+            // waits of the warp-collective roles never leave the loop early: after a timeout they
+            // return at once, so every lane still reaches every __syncwarp and named barrier
+            bar_wait(sc_full + sb, (j >> 1) & 1, ctl, P.status, lim);
             // row r's scales and biases in the staged block: gate/up [gs 64][gb 64][us 64][ub 64] x G,
             // down [s 128][b 128] x G
             const uint16_t* scb = reinterpret_cast<const uint16_t*>(ssc + sb * pl.sc_bytes);
@@ -483,18 +489,14 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             const bool vec = (G & 7) == 0;
             uint4 sv = make_uint4(0, 0, 0, 0), bv = sv;
             int blk = -1;
-            bool ok = true;
             for (int g = 0; g < t.nk; ++g, ++it) {
                 const int c = it % NC;
-                if (!bar_wait(code_full + c, (it / NC) & 1, ctl, P.status, lim)) {
-                    ok = false;
-                    break;
-                }
+                bar_wait(code_full + c, (it / NC) & 1, ctl, P.status, lim);
                 const uint4* cp =
                     reinterpret_cast<const uint4*>(scode + c * pl.code_stage + r * sbytes + hk * (sbytes / 2));
                 const uint4 q0 = cp[0];
                 const uint4 q1 = kBits == 8 ? cp[1] : make_uint4(0, 0, 0, 0);
-                bar_arrive(code_empty + c);
+                bar_arrive_warp(code_empty + c);
                 uint16_t s16, b16;
                 if (vec) {
                     if ((g >> 3) != blk) {
@@ -511,10 +513,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                 const __half2 s2 = __half2half2(__float2half_rn(bf2f(s16)));
                 const __half2 b2 = __half2half2(__float2half_rn(bf2f(b16)));
                 const int st = it % kStages;
-                if (!bar_wait(empty + st, ((it / kStages) & 1) ^ 1, ctl, P.status, lim)) {
-                    ok = false;
-                    break;
-                }
+                bar_wait(empty + st, ((it / kStages) & 1) ^ 1, ctl, P.status, lim);
                 uint8_t* arow = sa + st * kTileBytes + r * 128;
                 const uint32_t sw = r & 7;
                 if (kBits == 4) {
@@ -530,11 +529,9 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                             deq_int8(w[2 * ch], w[2 * ch + 1], s2, b2);
                 }
                 fence_async_smem();
-                bar_arrive(full_a + st);
+                bar_arrive_warp(full_a + st);
             }
-            if (!ok)
-                break;
-            bar_arrive(sc_empty + sb);
+            bar_arrive_warp(sc_empty + sb);
         }
     } else if (warp < 12) {
         // ---- epilogue: warp 8 + q reads TMEM lanes 32q .. 32q + 31 (tile row = lane) ----
@@ -543,8 +540,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
         for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
             const TaskX t = decode_task(P, kKind, P.tasks[ti]);
             const int ab = j & 1;
-            if (!bar_wait(acc_full + ab, (j >> 1) & 1, ctl, P.status, lim))
-                break;
+            bar_wait(acc_full + ab, (j >> 1) & 1, ctl, P.status, lim);  // no early exit (named barriers below)
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + ab * kNT;
             const int N = n_mma(t.nn);
@@ -600,7 +596,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                 }
             }
             tc_fence_before();
-            bar_arrive(acc_empty + ab);
+            bar_arrive_warp(acc_empty + ab);
         }
     } else if (warp == 12) {
         if (lane == 0) {
@@ -697,8 +693,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                 bool ok = true;
                 for (int g = 0; g < t.nk; ++g, ++it) {
                     const int st = it % kStages;
-                    if (!bar_wait(full_a + st, (it / kStages) & 1, ctl, P.status, lim) ||
-                        !bar_wait(full_b + st, (it / kStages) & 1, ctl, P.status, lim)) {
+                    if (!bar_wait(full_a + st, (it / kStages) & 1, ctl, P.status, lim)) {
                         ok = false;
                         break;
                     }
