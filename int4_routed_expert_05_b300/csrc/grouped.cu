@@ -242,11 +242,11 @@ __device__ __forceinline__ uint16_t pick16(const uint4& v, int i)
 }
 
 struct TaskX {
-    int e, m0, n0, nn, nk, shared, slot;
+    int e, m0, n0, nn, nk, nh, shared, slot;  // nk slices of 128 K; nh = 64-element halves in all
     const uint8_t* blob;
 };
 
-__device__ __forceinline__ TaskX decode_task(const GroupedArgs& P, int kind, int4 t)
+__device__ __forceinline__ TaskX decode_task(const GroupedArgs& P, int kind, int4 t, int sub = 1)
 {
     TaskX x;
     x.e = t.x;
@@ -267,7 +267,8 @@ __device__ __forceinline__ TaskX decode_task(const GroupedArgs& P, int kind, int
         x.blob = P.arena + (uint64_t)s * P.stride;
     }
     const BlobGeo& g = x.shared ? P.geo_s : P.geo;
-    x.nk = (kind == 1 ? P.H : g.cols[2]) / kKS;
+    x.nh = (kind == 1 ? P.H : g.cols[2]) / kKS;
+    x.nk = (x.nh + sub - 1) / sub;
     return x;
 }
 
@@ -420,8 +421,8 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
     const int NC = (int)pl.n_code;
     uint64_t* full_a = bars;
     uint64_t* full_b = full_a;  // the B-operand TMA's arrive.expect_tx joins the producers' arrivals
-    uint64_t* empty = bars + 2 * kStages;
-    uint64_t* code_full = bars + 3 * kStages;
+    uint64_t* empty = bars + kTiles;
+    uint64_t* code_full = bars + 2 * kTiles;
     uint64_t* code_empty = code_full + 8;
     uint64_t* sc_full = code_empty + 8;
     uint64_t* sc_empty = sc_full + 2;
@@ -432,7 +433,8 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tasks = *P.n_tasks;
     const long long lim = P.timeout_cycles;
-    constexpr uint32_t sbytes = kKS * kBits / 8;  // code bytes of one row in one slice
+    constexpr int kSub = slice_sub(kBits);         // sub-tiles per slice
+    constexpr int kStages = kTiles / kSub;         // slices in flight
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -461,12 +463,12 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
     const uint32_t tmem = ctl->tmem;
 
     if (warp < 8) {
-        // ---- dequantising producers: thread (hk, r) owns half hk (32 of the 64 K elements) of row
-        // r of the A tile: two warps per SMSP share each slice ----
+        // ---- dequantising producers: thread (hk, r) owns 32 code bytes of row r in each slice
+        // (int4: group hk of two; int8: half hk of one): two warps per SMSP share each slice ----
         const int r = threadIdx.x & 127, hk = threadIdx.x >> 7;
         uint32_t it = 0, j = 0;
         for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
-            const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+            const TaskX t = decode_task(P, kKind, P.tasks[ti], kSub);
             const BlobGeo& geo = t.shared ? P.geo_s : P.geo;
             const int G = kKind == 1 ? geo.groups[0] : geo.groups[2];
             const int sb = j & 1;
@@ -491,42 +493,48 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             int blk = -1;
             for (int g = 0; g < t.nk; ++g, ++it) {
                 const int c = it % NC;
+                // int4: this thread's quantisation group gg of the slice's two (128 elements); int8:
+                // half hk of the slice's one group
+                const int gg = kSub == 2 ? 2 * g + hk : g;
+                const bool live = gg < t.nh;   // the last int4 slice may hold one group only
                 bar_wait(code_full + c, (it / NC) & 1, ctl, P.status, lim);
-                const uint4* cp =
-                    reinterpret_cast<const uint4*>(scode + c * pl.code_stage + r * sbytes + hk * (sbytes / 2));
-                const uint4 q0 = cp[0];
-                const uint4 q1 = kBits == 8 ? cp[1] : make_uint4(0, 0, 0, 0);
+                const uint4* cp = reinterpret_cast<const uint4*>(scode + c * pl.code_stage + r * kCodeRow + hk * 32);
+                const uint4 q0 = cp[0], q1 = cp[1];
                 bar_arrive_warp(code_empty + c);
-                uint16_t s16, b16;
-                if (vec) {
-                    if ((g >> 3) != blk) {
-                        blk = g >> 3;
-                        sv = *reinterpret_cast<const uint4*>(srow + (g & ~7));
-                        bv = *reinterpret_cast<const uint4*>(brow + (g & ~7));
+                uint16_t s16 = 0, b16 = 0;
+                if (live) {
+                    if (vec) {
+                        if ((gg >> 3) != blk) {
+                            blk = gg >> 3;
+                            sv = *reinterpret_cast<const uint4*>(srow + (gg & ~7));
+                            bv = *reinterpret_cast<const uint4*>(brow + (gg & ~7));
+                        }
+                        s16 = pick16(sv, gg & 7);
+                        b16 = pick16(bv, gg & 7);
+                    } else {
+                        s16 = srow[gg];
+                        b16 = brow[gg];
                     }
-                    s16 = pick16(sv, g & 7);
-                    b16 = pick16(bv, g & 7);
-                } else {
-                    s16 = srow[g];
-                    b16 = brow[g];
                 }
                 const __half2 s2 = __half2half2(__float2half_rn(bf2f(s16)));
                 const __half2 b2 = __half2half2(__float2half_rn(bf2f(b16)));
                 const int st = it % kStages;
                 bar_wait(empty + st, ((it / kStages) & 1) ^ 1, ctl, P.status, lim);
-                uint8_t* arow = sa + st * kTileBytes + r * 128;
-                const uint32_t sw = r & 7;
-                if (kBits == 4) {
-                    const uint32_t w[4] = {q0.x, q0.y, q0.z, q0.w};
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
-                        *reinterpret_cast<uint4*>(arow + (((hk * 4 + ch) ^ sw) << 4)) = deq_int4(w[ch], s2, b2);
-                } else {
+                if (live) {
+                    const uint32_t sw = r & 7;
                     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    if (kBits == 4) {  // 64 codes -> the 8 chunks of sub-tile hk
+                        uint8_t* arow = sa + (st * kSub + hk) * kTileBytes + r * 128;
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
-                        *reinterpret_cast<uint4*>(arow + (((hk * 4 + ch) ^ sw) << 4)) =
-                            deq_int8(w[2 * ch], w[2 * ch + 1], s2, b2);
+                        for (int ch = 0; ch < 8; ++ch)
+                            *reinterpret_cast<uint4*>(arow + ((ch ^ sw) << 4)) = deq_int4(w[ch], s2, b2);
+                    } else {           // 32 codes -> chunks 4 hk .. 4 hk + 3 of the slice's sub-tile
+                        uint8_t* arow = sa + st * kTileBytes + r * 128;
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch)
+                            *reinterpret_cast<uint4*>(arow + (((hk * 4 + ch) ^ sw) << 4)) =
+                                deq_int8(w[2 * ch], w[2 * ch + 1], s2, b2);
+                    }
                 }
                 fence_async_smem();
                 bar_arrive_warp(full_a + st);
@@ -538,7 +546,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
         const int q = warp - 8, r = q * 32 + lane;
         uint32_t j = 0;
         for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
-            const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+            const TaskX t = decode_task(P, kKind, P.tasks[ti], kSub);
             const int ab = j & 1;
             bar_wait(acc_full + ab, (j >> 1) & 1, ctl, P.status, lim);  // no early exit (named barriers below)
             tc_fence_after();
@@ -607,7 +615,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             }
             uint32_t it = 0, j = 0;
             for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
-                const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+                const TaskX t = decode_task(P, kKind, P.tasks[ti], kSub);
                 const BlobGeo& geo = t.shared ? P.geo_s : P.geo;
                 const int sb = j & 1;
                 if (!bar_wait(sc_empty + sb, ((j >> 1) & 1) ^ 1, ctl, P.status, lim))
@@ -637,11 +645,12 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                         goto tma_done;
                     uint8_t* dst = scode + c * pl.code_stage;
                     bar_expect(code_full + c, pl.code_stage);
+                    const int x = g * kCodeRow;
                     if (kKind == 1) {
-                        tma3d(dst, &P.map_q[t.shared][0], g * sbytes, t.m0, t.slot, code_full + c);
-                        tma3d(dst + 64 * sbytes, &P.map_q[t.shared][1], g * sbytes, t.m0, t.slot, code_full + c);
+                        tma3d(dst, &P.map_q[t.shared][0], x, t.m0, t.slot, code_full + c);
+                        tma3d(dst + 64 * kCodeRow, &P.map_q[t.shared][1], x, t.m0, t.slot, code_full + c);
                     } else {
-                        tma3d(dst, &P.map_q[t.shared][2], g * sbytes, t.m0, t.slot, code_full + c);
+                        tma3d(dst, &P.map_q[t.shared][2], x, t.m0, t.slot, code_full + c);
                     }
                 }
             }
@@ -658,7 +667,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             asm volatile("prefetch.tensormap [%0];" ::"l"(mb) : "memory");
             uint32_t it = 0;
             for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x) {
-                const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+                const TaskX t = decode_task(P, kKind, P.tasks[ti], kSub);
                 const int nb = n_mma(t.nn) / kBRows;
                 bool ok = true;
                 for (int g = 0; g < t.nk; ++g, ++it) {
@@ -667,9 +676,12 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                         ok = false;
                         break;
                     }
-                    bar_expect(full_b + st, (uint32_t)nb * kBRows * 128);
-                    for (int q = 0; q < nb; ++q)
-                        tma2d(sbt + st * kTileBytes + q * kBRows * 128, mb, g * kKS, t.n0 + q * kBRows, full_b + st);
+                    const int halves = min(kSub, t.nh - kSub * g);
+                    bar_expect(full_b + st, (uint32_t)(halves * nb) * kBRows * 128);
+                    for (int h = 0; h < halves; ++h)
+                        for (int q = 0; q < nb; ++q)
+                            tma2d(sbt + (st * kSub + h) * kTileBytes + q * kBRows * 128, mb, (kSub * g + h) * kKS,
+                                  t.n0 + q * kBRows, full_b + st);
                 }
                 if (!ok)
                     break;
@@ -683,7 +695,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
             // ---- MMA issuer (warp 13) ----
             uint32_t it = 0, j = 0;
             for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
-                const TaskX t = decode_task(P, kKind, P.tasks[ti]);
+                const TaskX t = decode_task(P, kKind, P.tasks[ti], kSub);
                 const uint32_t id = idesc(n_mma(t.nn), false);
                 const int ab = j & 1;
                 if (!bar_wait(acc_empty + ab, ((j >> 1) & 1) ^ 1, ctl, P.status, lim))
@@ -698,10 +710,14 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a = sdesc(su32(sa + st * kTileBytes)), b = sdesc(su32(sbt + st * kTileBytes));
+                    const int halves = min(kSub, t.nh - kSub * g);
+                    for (int h = 0; h < halves; ++h) {
+                        const uint64_t a = sdesc(su32(sa + (st * kSub + h) * kTileBytes));
+                        const uint64_t b = sdesc(su32(sbt + (st * kSub + h) * kTileBytes));
 #pragma unroll
-                    for (int kk = 0; kk < kKS / 16; ++kk)
-                        mma(d, a + 2 * kk, b + 2 * kk, id, (g | kk) != 0);
+                        for (int kk = 0; kk < kKS / 16; ++kk)
+                            mma(d, a + 2 * kk, b + 2 * kk, id, (g | h | kk) != 0);
+                    }
                     mma_commit(empty + st);
                 }
                 if (!ok)

@@ -13,8 +13,12 @@ namespace moe {
 namespace tc {
 
 constexpr int kNT = 128;          // tokens per task at most (the N of one MMA tile)
-constexpr int kKS = 64;           // K elements per pipeline slice: one quantisation group, one 128-byte row
-constexpr int kStages = 4;        // A/B operand stages of the expert GEMMs
+constexpr int kKS = 64;           // K elements of one operand sub-tile: one quantisation group, one 128-byte row
+constexpr int kTiles = 4;         // operand sub-tiles of A (and of B) in shared memory, grouped into stages
+constexpr int kCodeRow = 64;      // bytes of one row's codes in one pipeline slice (one TMA box row)
+// Expert-GEMM pipeline slice: 64 bytes of codes per row, i.e. 128 K elements (two sub-tiles) at
+// int4 and 64 (one sub-tile) at int8; kTiles / sub stages of sub sub-tiles each.
+__host__ __device__ constexpr int slice_sub(int bits) { return bits == 4 ? 2 : 1; }
 constexpr int kStagesR = 6;       // A/B operand stages of the router GEMM
 constexpr int kTileBytes = 128 * 128;  // one 128-row x 64-element fp16/bf16 operand tile
 constexpr int kCodeRing = 32768;  // bytes of the staged-code ring
@@ -64,11 +68,12 @@ __host__ __device__ inline XPlan xplan(int H, int Imax, int bits)
     XPlan p{};
     uint32_t o = 0;
     p.a = o;
-    o += kStages * kTileBytes;
+    o += kTiles * kTileBytes;
     p.b = o;
-    o += kStages * kTileBytes;
+    o += kTiles * kTileBytes;
     p.code = o;
-    p.code_stage = 128 * (kKS * bits / 8);
+    p.code_stage = 128 * kCodeRow;
+    (void)bits;
     p.n_code = kCodeRing / p.code_stage;
     o += kCodeRing;
     p.sc = o;

@@ -56,11 +56,12 @@ inline int encode_arena_maps(CUtensorMap (&maps)[3], const uint8_t* arena, int n
 }
 
 // Code sections (gate, up, down) as 3D byte tensors [slots][rows][row bytes] with boxes of one
-// 64-element K slice (32 bytes at int4, 64 at int8) by 64 rows (gate, up) or 128 rows (down):
+// pipeline slice (64 bytes of codes: 128 elements at int4, 64 at int8) by 64 rows (gate, up) or
+// 128 rows (down):
 // the tiles the batched path's dequantising warps read. `base` is the arena (n_slots blobs at
 // `stride`) or one blob (n_slots = 1).
 inline int encode_slice_maps(CUtensorMap (&maps)[3], const uint8_t* base, int n_slots, uint64_t stride,
-                             const BlobGeo& geo, int bits)
+                             const BlobGeo& geo, int /*bits*/)
 {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn)
@@ -68,7 +69,7 @@ inline int encode_slice_maps(CUtensorMap (&maps)[3], const uint8_t* base, int n_
     for (int m = 0; m < 3; ++m) {
         const cuuint64_t dims[3] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)geo.rows[m], (cuuint64_t)n_slots};
         const cuuint64_t strides[2] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)stride};
-        const cuuint32_t box[3] = {(cuuint32_t)(64 * bits / 8), m == 2 ? 128u : 64u, 1};
+        const cuuint32_t box[3] = {64u, m == 2 ? 128u : 64u, 1};
         const cuuint32_t es[3] = {1, 1, 1};
         const CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, (void*)(base + geo.q_off[m]), dims, strides,
                               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
