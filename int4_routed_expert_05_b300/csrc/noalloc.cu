@@ -51,7 +51,6 @@ size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
 StaticLayout static_layout(const moe_shape& s)
 {
     StaticLayout l{};
-    const int Imax = s.inter > s.shared_inter ? s.inter : s.shared_inter;
     size_t o = 0;
     l.bar = o;
     o += 256;
