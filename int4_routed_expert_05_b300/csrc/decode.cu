@@ -715,7 +715,7 @@ __device__ __noinline__ void mma_block(const uint8_t* base, uint32_t swzmask, in
 // Each warp ranks its 32 logits; the largest of the warps' k-th best values is a lower bound of
 // the overall k-th best, so only logits at or above it (usually little more than k) take part in
 // the final ranking.
-__device__ void topk_select(const StepParams& P, const Ctx& C)
+__device__ void topk_select(const StepParams& P, const Ctx& C, int my_slot)
 {
     const int E = C.E, k = C.k;
     const int nl = (E + 31) / 32;
@@ -777,8 +777,10 @@ __device__ void topk_select(const StepParams& P, const Ctx& C)
             rank += (kk.x > key || (kk.x == key && ii.x < e)) + (kk.y > key || (kk.y == key && ii.y < e)) +
                     (kk.z > key || (kk.z == key && ii.z < e)) + (kk.w > key || (kk.w == key && ii.w < e));
         }
-        if (rank < k)
+        if (rank < k) {
             C.sel_idx[rank] = e;
+            C.sel_slot[rank] = my_slot;
+        }
     }
     __syncthreads();
     if (WARP == 0) {
@@ -926,6 +928,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         const int t = step / P.n_layers, li = step - t * P.n_layers;
         const int l = P.layer0 + li;
         const LayerDesc L = P.layers[l];
+        // this thread's expert's slot, loaded now so that it is in a register by the time top-k
+        // names the experts (the thread of logit e is thread e)
+        const int my_slot = (route && TID < C.E) ? P.table[(size_t)l * C.E + TID] : -1;
         const uint32_t epoch = P.epoch0 + (uint32_t)step;
         long long* X = P.xacc + (size_t)(step & 1) * C.H;
         const bool prenorm = (P.flags & kPrenorm) != 0;
@@ -1043,7 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
                 ok = false;
                 break;
             }
-            topk_select(P, C);
+            topk_select(P, C, my_slot);
             if (CTA == 0 && TID < C.k) {
                 const size_t o = ((size_t)t * P.n_layers + li) * C.k + TID;
                 if (P.topk_idx)
@@ -1053,12 +1058,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             }
             if (!experts)
                 break;  // a route-only launch has one step
-            if (TID < C.k) {
-                const int s = P.table[(size_t)l * C.E + C.sel_idx[TID]];
-                C.sel_slot[TID] = s;
-                if (s < 0)
-                    set_status(P.status, kStatusNotResident);
-            }
+            if (TID < C.k && C.sel_slot[TID] < 0)
+                set_status(P.status, kStatusNotResident);
         } else if (TID < C.k) {
             C.sel_w[TID] = P.topk_w[TID];
             C.sel_slot[TID] = P.slots[TID];
