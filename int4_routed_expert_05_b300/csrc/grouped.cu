@@ -498,8 +498,11 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                 const int gg = kSub == 2 ? 2 * g + hk : g;
                 const bool live = gg < t.nh;   // the last int4 slice may hold one group only
                 bar_wait(code_full + c, (it / NC) & 1, ctl, P.status, lim);
-                const uint4* cp = reinterpret_cast<const uint4*>(scode + c * pl.code_stage + r * kCodeRow + hk * 32);
-                const uint4 q0 = cp[0], q1 = cp[1];
+                // the stage holds 64-byte rows, 64-byte swizzled: chunk cc of row r at cc ^ ((r >> 1) & 3)
+                const uint8_t* crow = scode + c * pl.code_stage + r * kCodeRow;
+                const int xr = (r >> 1) & 3;
+                const uint4 q0 = *reinterpret_cast<const uint4*>(crow + (((2 * hk) ^ xr) << 4));
+                const uint4 q1 = *reinterpret_cast<const uint4*>(crow + (((2 * hk + 1) ^ xr) << 4));
                 bar_arrive_warp(code_empty + c);
                 uint16_t s16 = 0, b16 = 0;
                 if (live) {

@@ -57,7 +57,8 @@ inline int encode_arena_maps(CUtensorMap (&maps)[3], const uint8_t* arena, int n
 
 // Code sections (gate, up, down) as 3D byte tensors [slots][rows][row bytes] with boxes of one
 // pipeline slice (64 bytes of codes: 128 elements at int4, 64 at int8) by 64 rows (gate, up) or
-// 128 rows (down):
+// 128 rows (down), 64-byte swizzled (16-byte chunk c of row r lands at chunk c ^ ((r >> 1) & 3), so
+// the dequantising threads, one row each, read without bank conflicts):
 // the tiles the batched path's dequantising warps read. `base` is the arena (n_slots blobs at
 // `stride`) or one blob (n_slots = 1).
 inline int encode_slice_maps(CUtensorMap (&maps)[3], const uint8_t* base, int n_slots, uint64_t stride,
@@ -72,7 +73,7 @@ inline int encode_slice_maps(CUtensorMap (&maps)[3], const uint8_t* base, int n_
         const cuuint32_t box[3] = {64u, m == 2 ? 128u : 64u, 1};
         const cuuint32_t es[3] = {1, 1, 1};
         const CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, (void*)(base + geo.q_off[m]), dims, strides,
-                              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS)
             return (int)r;
