@@ -124,7 +124,6 @@ __device__ __forceinline__ void bulk(void* dst, const void* src, uint32_t bytes,
                  "l"(src), "r"(bytes), "r"(su32(m))
                  : "memory");
 }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // ---- tcgen05 ----
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -152,6 +151,27 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t
         "l"(a), "l"(b), "r"(id), "r"(acc)
         : "memory");
 }
+// A operand from tensor memory (lane = row, 32-bit columns holding fp16 pairs along K)
+__device__ __forceinline__ void mma_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc)
+{
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+
+// 16 / 32 consecutive 32-bit columns of this thread's TMEM lane from registers
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void mma_commit(uint64_t* m)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(m))
@@ -188,16 +208,15 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4])
         v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot)
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t cols = kTmemCols)
 {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(slot)),
-                 "r"(kTmemCols)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(slot)), "r"(cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_free(uint32_t base)
+__device__ __forceinline__ void tmem_free(uint32_t base, uint32_t cols = kTmemCols)
 {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols) : "memory");
 }
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -412,7 +431,6 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const XPlan pl = xplan(P.H, P.Imax, kBits);
-    uint8_t* sa = sm + pl.a;
     uint8_t* sbt = sm + pl.b;
     uint8_t* scode = sm + pl.code;
     uint8_t* ssc = sm + pl.sc;
@@ -435,6 +453,8 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
     const long long lim = P.timeout_cycles;
     constexpr int kSub = slice_sub(kBits);         // sub-tiles per slice
     constexpr int kStages = kTiles / kSub;         // slices in flight
+    // tensor memory: two accumulators (columns 0..255), then the A stages (kSub x 32 columns each)
+    constexpr uint32_t kAccCols = 2 * kNT, kAStageCols = kSub * (kKS / 2), kTmemColsX = 512;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -456,7 +476,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 13)
-        tmem_alloc(&ctl->tmem);
+        tmem_alloc(&ctl->tmem, kTmemColsX);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -523,23 +543,39 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                 const __half2 b2 = __half2half2(__float2half_rn(bf2f(b16)));
                 const int st = it % kStages;
                 bar_wait(empty + st, ((it / kStages) & 1) ^ 1, ctl, P.status, lim);
-                if (live) {
-                    const uint32_t sw = r & 7;
-                    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    if (kBits == 4) {  // 64 codes -> the 8 chunks of sub-tile hk
-                        uint8_t* arow = sa + (st * kSub + hk) * kTileBytes + r * 128;
+                // A row segment -> tensor memory (lane r): 32-bit columns of fp16 pairs in K order
+                tc_fence_after();
+                const uint32_t acol = tmem + ((uint32_t)((r >> 5) * 32) << 16) + kAccCols + st * kAStageCols;
+                const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                if (kBits == 4) {  // 64 codes -> 32 columns of sub-tile hk
 #pragma unroll
-                        for (int ch = 0; ch < 8; ++ch)
-                            *reinterpret_cast<uint4*>(arow + ((ch ^ sw) << 4)) = deq_int4(w[ch], s2, b2);
-                    } else {           // 32 codes -> chunks 4 hk .. 4 hk + 3 of the slice's sub-tile
-                        uint8_t* arow = sa + st * kTileBytes + r * 128;
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t v[16];
 #pragma unroll
-                        for (int ch = 0; ch < 4; ++ch)
-                            *reinterpret_cast<uint4*>(arow + (((hk * 4 + ch) ^ sw) << 4)) =
-                                deq_int8(w[2 * ch], w[2 * ch + 1], s2, b2);
+                        for (int ch = 0; ch < 4; ++ch) {
+                            const uint4 o = deq_int4(w[4 * half + ch], s2, b2);
+                            v[4 * ch] = o.x;
+                            v[4 * ch + 1] = o.y;
+                            v[4 * ch + 2] = o.z;
+                            v[4 * ch + 3] = o.w;
+                        }
+                        if (live)
+                            tmem_st16(acol + hk * 32 + half * 16, v);
                     }
+                } else {           // 32 codes -> columns 16 hk .. 16 hk + 15 of the slice
+                    uint32_t v[16];
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const uint4 o = deq_int8(w[2 * ch], w[2 * ch + 1], s2, b2);
+                        v[4 * ch] = o.x;
+                        v[4 * ch + 1] = o.y;
+                        v[4 * ch + 2] = o.z;
+                        v[4 * ch + 3] = o.w;
+                    }
+                    tmem_st16(acol + hk * 16, v);
                 }
-                fence_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
                 bar_arrive_warp(full_a + st);
             }
             bar_arrive_warp(sc_empty + sb);
@@ -715,11 +751,11 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                     tc_fence_after();
                     const int halves = min(kSub, t.nh - kSub * g);
                     for (int h = 0; h < halves; ++h) {
-                        const uint64_t a = sdesc(su32(sa + (st * kSub + h) * kTileBytes));
+                        const uint32_t a = tmem + kAccCols + st * kAStageCols + h * (kKS / 2);
                         const uint64_t b = sdesc(su32(sbt + (st * kSub + h) * kTileBytes));
 #pragma unroll
                         for (int kk = 0; kk < kKS / 16; ++kk)
-                            mma(d, a + 2 * kk, b + 2 * kk, id, (g | h | kk) != 0);
+                            mma_ta(d, a + kk * 8, b + 2 * kk, id, (g | h | kk) != 0);
                     }
                     mma_commit(empty + st);
                 }
@@ -735,7 +771,7 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
     __syncthreads();
     if (warp == 13) {
         tc_fence_after();
-        tmem_free(tmem);
+        tmem_free(tmem, kTmemColsX);
     }
 }
 
