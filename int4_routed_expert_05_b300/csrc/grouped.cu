@@ -730,25 +730,26 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                 bar_wait(full_b + i % kStages, (i / kStages) & 1, ctl, P.status, lim);
         }
     } else {
-        if (lane == 0) {
-            // ---- MMA issuer (warp 13) ----
-            uint32_t it = 0, j = 0;
-            for (int ti = blockIdx.x; ti < n_tasks; ti += gridDim.x, ++j) {
-                const TaskX t = decode_task(P, kKind, P.tasks[ti], kSub);
-                const uint32_t id = idesc(n_mma(t.nn), false);
-                const int ab = j & 1;
-                if (!bar_wait(acc_empty + ab, ((j >> 1) & 1) ^ 1, ctl, P.status, lim))
+        // ---- MMA issuer (warp 13): the whole warp walks the loop (converged); lane 0 issues ----
+        const bool issuer = lane == 0;
+        uint32_t it = 0, j = 0;
+        bool ok = true;
+        for (int ti = blockIdx.x; ti < n_tasks && ok; ti += gridDim.x, ++j) {
+            const TaskX t = decode_task(P, kKind, P.tasks[ti], kSub);
+            const uint32_t id = idesc(n_mma(t.nn), false);
+            const int ab = j & 1;
+            ok = __all_sync(0xffffffffu, bar_wait(acc_empty + ab, ((j >> 1) & 1) ^ 1, ctl, P.status, lim));
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t d = tmem + ab * kNT;
+            for (int g = 0; g < t.nk; ++g, ++it) {
+                const int st = it % kStages;
+                ok = __all_sync(0xffffffffu, bar_wait(full_a + st, (it / kStages) & 1, ctl, P.status, lim));
+                if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t d = tmem + ab * kNT;
-                bool ok = true;
-                for (int g = 0; g < t.nk; ++g, ++it) {
-                    const int st = it % kStages;
-                    if (!bar_wait(full_a + st, (it / kStages) & 1, ctl, P.status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                if (issuer) {
                     const int halves = min(kSub, t.nh - kSub * g);
                     for (int h = 0; h < halves; ++h) {
                         const uint32_t a = tmem + kAccCols + st * kAStageCols + h * (kKS / 2);
@@ -759,13 +760,17 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                     }
                     mma_commit(empty + st);
                 }
-                if (!ok)
-                    break;
-                mma_commit(acc_full + ab);
+                __syncwarp();
             }
+            if (ok && issuer)
+                mma_commit(acc_full + ab);
+            __syncwarp();
+        }
+        if (issuer) {
             mma_commit(fin);
             bar_wait(fin, 0, ctl, P.status, lim);
         }
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
