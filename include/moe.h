@@ -216,13 +216,27 @@ moe_status moe_stack_forward_streamed(moe_pool* pool, int32_t layer0, int32_t n_
                                       void* copy_stream, int32_t* h_topk_idx);
 
 /* Batched tokens (prefill or batched decode), one layer, resident experts: the same layer as
- * moe_layer_forward for each of n_tokens tokens, computed as GEMMs: router GEMM, per-token top-k,
- * a sort of the token-expert assignments by expert, grouped gate/up and down GEMMs on the tensor
- * cores (weights dequantised to fp16 per K-slice), and a per-token combine in rank order.
- * d_x: bf16 [T][H]; d_y: fp32 [T][H]; d_topk_idx/d_topk_w: [T][k] or NULL.
- * d_work: caller-owned device workspace of moe_batched_workspace_bytes(shape, T) bytes
- * (256-byte aligned). Synchronises once with `stream` (the per-expert token counts are read back
- * to lay out the grouped GEMMs). The shape must not have MOE_PRENORM or MOE_RESIDUAL. */
+ * moe_layer_forward for each of n_tokens tokens (cheshm.ai item "Swiftlet fits an 80B-level Qwen
+ * giant into Mac", scheduling and quantisation paragraphs; alphalab.site benchmark article, TTFT
+ * sections: batched prefill is what the pages' runtime lacks), computed as GEMMs on the tensor
+ * cores: router GEMM, per-token top-k (ties to the lower index) with renormalised weights and the
+ * shared gate, a sort of the token-expert assignments by expert (the shared expert takes every
+ * token), grouped gate/up GEMMs with SwiGLU and grouped down GEMMs whose weighted results are
+ * added into d_y. Weights are dequantised to fp16 (w = s*q + b, one rounding); accumulation fp32.
+ * The k + 1 contributions of a token are summed by fp32 reductions in tile completion order, so
+ * d_y agrees run to run to fp32 rounding, not bit for bit.
+ *   d_x        bf16 [T][H] device, 16-byte aligned (read only)
+ *   d_y        fp32 [T][H] device, 16-byte aligned (overwritten)
+ *   d_topk_idx int32 [T][k] device or NULL; d_topk_w fp32 [T][k] device or NULL
+ *   d_work     caller-owned device workspace of at least moe_batched_workspace_bytes(shape, T)
+ *              bytes, 256-byte aligned; its contents need no initialisation
+ *   stream     cudaStream_t (as void*); all work is enqueued on it, no host synchronisation
+ * Errors: MOE_E_SHAPE if the shape has MOE_PRENORM or MOE_RESIDUAL, if hidden, inter or
+ * shared_inter is not a multiple of 64, or if the staging for `hidden` does not fit in shared
+ * memory; MOE_E_NOMEM if work_bytes is too small; MOE_E_INVALID for T <= 0, misaligned pointers or
+ * a device other than the pool's; MOE_E_CUDA for a launch or tensor-map failure. Device-side
+ * problems (non-resident expert, wait timeout) go to the status word (moe_device_status).
+ * moe_batched_workspace_bytes returns 0 for a NULL shape or n_tokens <= 0; it needs no GPU. */
 size_t moe_batched_workspace_bytes(const moe_shape* shape, int32_t n_tokens);
 moe_status moe_layer_forward_batched(moe_pool* pool, int32_t layer, const void* d_x, int32_t n_tokens, float* d_y,
                                      int32_t* d_topk_idx, float* d_topk_w, void* d_work, size_t work_bytes,

@@ -141,3 +141,19 @@ def test_injected_copy_failure_leaves_pool_unchanged(lib):
     assert ei.value.status == moe.E_CUDA
     after = [[pool.slot_of(l, e) for e in range(16)] for l in range(4)]
     assert before == after and pool.slot_of(1, 5) == s and calls == [s]
+
+
+def test_batched_workspace_bytes(lib):
+    """The batched workspace query is host-only: zero for no tokens, grows with the token count,
+    and holds at least the token-major buffers the layout names (input rows and h rows in
+    assignment order, logits)."""
+    ms = moe_shape(synth.S80)
+    assert moe.batched_workspace_bytes(ms, 0) == 0
+    assert moe.batched_workspace_bytes(ms, -3) == 0
+    sizes = [moe.batched_workspace_bytes(ms, t) for t in (1, 8, 64, 512, 4096)]
+    assert all(b % 256 == 0 for b in sizes)
+    assert sizes == sorted(sizes) and len(set(sizes)) == len(sizes)
+    H, E, k, Imax = synth.S80.hidden, synth.S80.n_experts, synth.S80.top_k, synth.S80.inter
+    for t, b in zip((1, 8, 64, 512, 4096), sizes):
+        a = t * (k + 1)
+        assert b >= 2 * a * H + 2 * a * Imax + 4 * t * E
