@@ -1,4 +1,4 @@
-"""Writes config2_seed.json: the first seed whose 80B-shaped router logits (oracle, double) have a
+"""Writes s80_layer_seed.json: the first seed whose 80B-shaped router logits (oracle, double) have a
 top-10 margin (10th minus 11th largest logit) above 1e-2, as the single-layer 80B workload asks.
 Calls only the oracle and the input generator."""
 import json
@@ -22,5 +22,5 @@ for seed in range(1000):
 out = {"source": "seed search over synth seeds 0.. with the oracle's double router logits; accept the first "
                   "seed whose top-10 margin exceeds 1e-2 (80B-shaped single layer workload)",
        "seed": seed, "margin": margin}
-json.dump(out, open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "config2_seed.json"), "w"), indent=1)
+json.dump(out, open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "s80_layer_seed.json"), "w"), indent=1)
 print(out)

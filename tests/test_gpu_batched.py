@@ -96,7 +96,7 @@ def test_logit_bias_batched(orc):
 @pytest.mark.parametrize("T", [64, 512])
 def test_s80_batched_sampled(orc, T):
     """80B-shaped layer, every expert resident; a sample of the tokens checked against the oracle."""
-    seed = json.load(open(os.path.join(GOLDEN, "config2_seed.json")))["seed"]
+    seed = json.load(open(os.path.join(GOLDEN, "s80_layer_seed.json")))["seed"]
     rng = np.random.default_rng(T)
     sample = sorted(set(rng.choice(T, size=6, replace=False).tolist()) | {0, T - 1})
     _, _, err = _case(orc, synth.S80, seed=seed, T=T, sample=sample)

@@ -89,7 +89,7 @@ def test_logit_bias(orc):
 
 def test_s80_single_layer(orc):
     """80B-shaped layer, all 512 expert blobs resident, seed with top-10 margin > 1e-2."""
-    seed = json.load(open(os.path.join(GOLDEN, "config2_seed.json")))["seed"]
+    seed = json.load(open(os.path.join(GOLDEN, "s80_layer_seed.json")))["seed"]
     R, err = _layer_case(orc, synth.S80, seed=seed)
     assert err <= TOL and err <= TIGHT, err
 
