@@ -218,29 +218,40 @@ def run_reference(args):
     t0 = time.perf_counter()
     r = O.layer(0, u)
     t_layer = time.perf_counter() - t0
-    per_layer = (args.warmup + args.steps) * t_layer <= 150.0
+    n_steps = args.warmup + args.steps
     blob = O.blob(0, int(r["idx"][0]))
-    if per_layer:  # every blob written before timing
+    t0 = time.perf_counter()
+    oracle.expert_ffn(sh, blob, u)
+    t_expert = time.perf_counter() - t0
+    # the largest unit whose K + W repetitions fit in about two and a half minutes
+    mode = "layer" if n_steps * t_layer <= 150.0 else ("expert" if n_steps * t_expert <= 150.0 else "router")
+    if mode == "layer":  # every blob written before timing
         for e in range(sh.n_experts):
             O.blob(0, e)
     times = []
-    for i in range(args.warmup + args.steps):
+    for i in range(n_steps):
         t0 = time.perf_counter()
-        if per_layer:
+        if mode == "layer":
             O.layer(0, oracle.rmsnorm_bf16(x + i * 1e-3))
-        else:
+        elif mode == "expert":
             oracle.expert_ffn(sh, blob, u)
+        else:
+            oracle.router_logits(Wr, u)
         times.append(time.perf_counter() - t0)
     t = statistics.mean(times[args.warmup:]) if args.steps else times[-1]
-    if per_layer:
+    if mode == "layer":
         v = 1.0 / (t * L)
         sample = f"one oracle layer (router, top-{sh.top_k}, {sh.top_k + 1} expert FFNs, combine) per step, x{L} layers"
-    else:
+    elif mode == "expert":
         t0 = time.perf_counter()
         oracle.router_logits(Wr, u)
         t_router = time.perf_counter() - t0
         v = 1.0 / (L * ((sh.top_k + 1) * t + t_router))
         sample = f"one expert FFN per step, scaled by {sh.top_k + 1} experts and {L} layers plus the router"
+    else:
+        v = 1.0 / (L * ((sh.top_k + 1) * t_expert + t))
+        sample = (f"the router GEMV per step (one expert FFN timed once: {1e3 * t_expert:.1f} ms), scaled by "
+                  f"{sh.top_k + 1} experts and {L} layers")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
