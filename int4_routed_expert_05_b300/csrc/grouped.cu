@@ -5,22 +5,22 @@
 // per-group scale and bias, weighted combine, sigmoid-gated shared expert), here for T tokens at
 // once, where the expert matrices are real GEMMs over the tokens routed to each expert.
 //
-// Both kernels are persistent (one CTA per SM) and warp-specialised around one MMA-issuing thread:
-//   * operands sit in shared memory as 128-row x 64-element K-major tiles in the 128-byte swizzled
-//     layout; tcgen05.mma (M = 128, N = tokens rounded up to 16, K = 16, fp32 accumulate) reads
-//     them through shared-memory descriptors and accumulates in tensor memory (two accumulators, so
-//     the epilogue of one task overlaps the main loop of the next);
+// Both kernels are persistent (one CTA per SM) and warp-specialised around one MMA-issuing thread;
+// tcgen05.mma (M = 128, N = tokens rounded up to 16, K = 16, fp32 accumulate) accumulates in tensor
+// memory (two accumulators, so the epilogue of one task overlaps the main loop of the next):
 //   * router GEMM: A = router rows (bf16) and B = token rows (bf16), both brought in by TMA with
-//     the hardware swizzle, so a slice goes global -> shared -> tensor core untouched;
-//   * expert GEMMs: TMA stages the packed codes; four dequantising warps turn them into fp16
-//     weights w = s * q + b (one rounding, s and b exact in fp16 for the workloads' ranges) in the
-//     swizzled layout; TMA brings the expert's token rows (input rows gathered in assignment order
-//     beforehand, or h rows) into the B tile; four epilogue warps read the accumulators with
-//     tcgen05.ld and apply SwiGLU (gate/up: h to a per-assignment buffer) or the combine weight
-//     (down: fp32 reductions into y).
-//   Operand tiles the MMA reads are written either by TMA or by st.shared followed by
-//   fence.proxy.async before the mbarrier release (rows written by cp.async and released after
-//   cp.async.wait_group + fence.proxy.async were measured to reach tcgen05.mma stale at times).
+//     the 128-byte swizzle as K-major shared-memory tiles, so a slice goes global -> shared ->
+//     tensor core untouched;
+//   * expert GEMMs: TMA stages the packed codes (64 bytes per row and slice, 64-byte swizzled);
+//     eight dequantising warps turn them into fp16 weights w = s * q + b (one rounding, s and b
+//     exact in fp16 for the workloads' ranges) and write them straight into tensor memory
+//     (tcgen05.st; the MMA reads A from there); TMA brings the expert's token rows (input rows in
+//     assignment order, or h rows) into 128-byte swizzled B tiles in shared memory; four epilogue
+//     warps read the accumulators with tcgen05.ld and apply SwiGLU (gate/up: h to a per-assignment
+//     buffer) or the combine weight (down: fp32 reductions into y).
+//   Operand tiles the MMA reads come from TMA or from tcgen05.st (rows written by cp.async and
+//   released after cp.async.wait_group + fence.proxy.async were measured to reach tcgen05.mma stale
+//   at times, and are not used).
 // Every wait is bounded: on expiry the kernel records MOE timeout status, drains its own copies and
 // frees its tensor memory.
 #include <cuda.h>
