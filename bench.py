@@ -517,6 +517,7 @@ def run_batched(args):
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
+    R.pool.time_batched(args.steps)  # CUDA events around the expert GEMMs of every timed step
     _barrier(ws)
     torch.cuda.synchronize()
     clocks.start()
@@ -531,6 +532,8 @@ def run_batched(args):
     _barrier(ws)
     clk = clocks.stop()
     ms = _max_over_ranks(ws, e0.elapsed_time(e1))
+    gemm_ms, gemm_calls = R.pool.batched_gemm_ms()
+    R.pool.time_batched(0)
     if R.pool.device_status() != moe.OK:
         raise RuntimeError("device status after the timed region is not MOE_OK")
 
@@ -555,22 +558,32 @@ def run_batched(args):
     ms_ = moe_shape(sh)
     blob, blob_s = moe.expert_bytes(ms_), moe.expert_bytes(ms_, shared=True)
     uniq = float(np.mean(touched))
+    A = T * (k + 1)
+    # the expert GEMMs (the dominant kernels, about 90 % of a step): weights of the touched experts
+    # and the shared expert, input rows and h rows in assignment order (fp16), y reductions (fp32)
+    gemm_bytes = uniq * blob + blob_s + 2 * A * H + 2 * 2 * A * sh.inter + 4 * T * H
+    gemm_flops = 2.0 * T * (k * 3 * sh.inter + 3 * sh.shared_inter) * H
     bytes_step = uniq * blob + blob_s + E * H * 2 + H * 2 + T * H * 2 + T * H * 4
     flops_step = 2.0 * T * (E * H + (k * 3 * sh.inter + 3 * sh.shared_inter) * H)
     ms_step = ms / args.steps
+    ms_gemm = gemm_ms / max(1, gemm_calls)
     hbm_peak, hbm_kind = _peaks()
     tc_peak, tc_kind = _tensor_peak()
-    t_hbm = bytes_step / (hbm_peak * 1e9)
-    t_tc = flops_step / (tc_peak * 1e12)
-    if t_tc >= t_hbm:
-        ach = flops_step / (ms_step / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak,
-                "peak_kind": tc_kind, "flops_per_launch": flops_step}
-    else:
-        ach = bytes_step / (ms_step / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                "peak_kind": hbm_kind, "bytes_per_launch": bytes_step}
-    roof.update({"traffic": None, "kernel": "moe_layer_forward_batched (all 7 launches of one step)"})
+
+    def roofline(nbytes, flops, ms_unit):
+        if flops / (tc_peak * 1e12) >= nbytes / (hbm_peak * 1e9):
+            ach = flops / (ms_unit / 1e3) / 1e12
+            return {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak,
+                    "peak_kind": tc_kind, "flops_per_launch": flops}
+        ach = nbytes / (ms_unit / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                "peak_kind": hbm_kind, "bytes_per_launch": nbytes}
+
+    roof = roofline(gemm_bytes, gemm_flops, ms_gemm)
+    roof.update({"traffic": None, "kernel": "expert_kernel<1> + expert_kernel<2> (gate/up and down expert GEMMs)",
+                 "ms_per_launch": ms_gemm, "timed_launches": gemm_calls})
+    step_roof = roofline(bytes_step, flops_step, ms_step)
+    step_roof.update({"kernel": "moe_layer_forward_batched (all 7 launches of one step)"})
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         v, info = cpu_oracle_batched(sh, T, budget_s=args.ref_budget)
@@ -590,6 +603,7 @@ def run_batched(args):
         "experts_touched_per_step": uniq,
         "tflops": flops_step / (ms_step / 1e3) / 1e12,
         "roofline": roof,
+        "step_roofline": step_roof,
         "cpu_baseline": cpu,
         "e2e": {"value": ws * T * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 2 * T * H,
                 "d2h_bytes_per_step": 4 * T * H, "steps": n_e2e},

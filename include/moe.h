@@ -238,6 +238,13 @@ moe_status moe_stack_forward_streamed(moe_pool* pool, int32_t layer0, int32_t n_
  * problems (non-resident expert, wait timeout) go to the status word (moe_device_status).
  * moe_batched_workspace_bytes returns 0 for a NULL shape or n_tokens <= 0; it needs no GPU. */
 size_t moe_batched_workspace_bytes(const moe_shape* shape, int32_t n_tokens);
+/* Timing of the batched path's expert GEMMs (a measurement hook; the pages have no counterpart):
+ * moe_pool_time_batched(pool, n) makes each following moe_layer_forward_batched call record a CUDA
+ * event pair on its stream around its two expert-GEMM launches, in a ring of n pairs owned by the
+ * pool (n = 0 turns it off); moe_pool_batched_gemm_ms waits for the recorded pairs and returns the
+ * sum of their elapsed times (ms) and their count (at most n, the latest calls), then clears them. */
+moe_status moe_pool_time_batched(moe_pool* pool, int32_t n_calls);
+moe_status moe_pool_batched_gemm_ms(moe_pool* pool, float* h_total_ms, int32_t* h_calls);
 moe_status moe_layer_forward_batched(moe_pool* pool, int32_t layer, const void* d_x, int32_t n_tokens, float* d_y,
                                      int32_t* d_topk_idx, float* d_topk_w, void* d_work, size_t work_bytes,
                                      void* stream);

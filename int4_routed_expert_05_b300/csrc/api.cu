@@ -146,6 +146,9 @@ struct moe_pool {
     // test hook replacing the device copy of load_slot
     int (*copy_hook)(void*, int32_t, const void*, size_t) = nullptr;
     void* copy_user = nullptr;
+    // batched-path timing: event pairs around the expert GEMMs of each call, round robin
+    std::vector<cudaEvent_t> gemm_ev;  // [2 * n]
+    int gemm_next = 0, gemm_used = 0;
 };
 
 extern "C" {
@@ -304,6 +307,8 @@ void moe_pool_destroy(moe_pool* p)
         return;
     for (cudaEvent_t ev : p->ring)
         cudaEventDestroy(ev);
+    for (cudaEvent_t ev : p->gemm_ev)
+        cudaEventDestroy(ev);
     if (p->loads_done)
         cudaEventDestroy(p->loads_done);
     delete p;
@@ -317,6 +322,38 @@ void* moe_pool_slot_ptr(const moe_pool* p, int32_t slot)
 }
 
 int32_t moe_pool_grid(const moe_pool* p) { return p ? p->grid : 0; }
+
+moe_status moe_pool_time_batched(moe_pool* p, int32_t n_calls)
+{
+    if (!p || n_calls < 0 || n_calls > 100000)
+        return fail(MOE_E_INVALID, "bad pool or call count");
+    for (cudaEvent_t ev : p->gemm_ev)
+        cudaEventDestroy(ev);
+    p->gemm_ev.assign(2 * (size_t)n_calls, nullptr);
+    for (auto& ev : p->gemm_ev)
+        CUDA_TRY(cudaEventCreate(&ev));
+    p->gemm_next = p->gemm_used = 0;
+    return MOE_OK;
+}
+
+moe_status moe_pool_batched_gemm_ms(moe_pool* p, float* h_total_ms, int32_t* h_calls)
+{
+    if (!p || !h_total_ms || !h_calls)
+        return fail(MOE_E_INVALID, "NULL argument");
+    float total = 0.f;
+    const int n = (int)p->gemm_ev.size() / 2;
+    const int used = p->gemm_used < n ? p->gemm_used : n;
+    for (int i = 0; i < used; ++i) {
+        CUDA_TRY(cudaEventSynchronize(p->gemm_ev[2 * i + 1]));
+        float ms = 0.f;
+        CUDA_TRY(cudaEventElapsedTime(&ms, p->gemm_ev[2 * i], p->gemm_ev[2 * i + 1]));
+        total += ms;
+    }
+    *h_total_ms = total;
+    *h_calls = used;
+    p->gemm_next = p->gemm_used = 0;
+    return MOE_OK;
+}
 
 moe_status moe_pool_set_timeout(moe_pool* p, uint64_t timeout_ns)
 {
@@ -899,8 +936,17 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     bat::launch_place(idx, wts, gamma, T, E, k, cursor, const_cast<int32_t*>(A.list), const_cast<float*>(A.aw), cs);
     bat::launch_gather_rows(static_cast<const uint16_t*>(d_x), A.list, nA, H, sh.bits, reinterpret_cast<__half*>(w + bl.us),
                             cs);
+    const int nev = (int)p->gemm_ev.size() / 2;
+    const int ei = nev ? p->gemm_next : -1;
+    if (ei >= 0)
+        CUDA_TRY(cudaEventRecord(p->gemm_ev[2 * ei], cs));
     tc::launch_expert_gemm(1, A, tgu, ntasks, grid, cs);
     tc::launch_expert_gemm(2, A, tdn, ntasks + 1, grid, cs);
+    if (ei >= 0) {
+        CUDA_TRY(cudaEventRecord(p->gemm_ev[2 * ei + 1], cs));
+        p->gemm_next = (p->gemm_next + 1) % nev;
+        p->gemm_used += 1;
+    }
     CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }

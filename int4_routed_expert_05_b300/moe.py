@@ -27,6 +27,7 @@ ENTRY_POINTS = [
     "moe_layer_forward_scalar", "moe_device_status", "moe_pool_set_timeout", "moe_pool_grid",
     "moe_last_error", "moe_pool_slot_of", "moe_pool_set_copy_hook", "moe_layer_forward_static",
     "moe_stack_forward_streamed", "moe_batched_workspace_bytes", "moe_layer_forward_batched",
+    "moe_pool_time_batched", "moe_pool_batched_gemm_ms",
 ]
 
 
@@ -91,6 +92,8 @@ def load() -> ctypes.CDLL:
         "moe_stack_forward_streamed": (ST, [P, I32, I32, P, P, P, P, P, P]),
         "moe_batched_workspace_bytes": (SZ, [PS, I32]),
         "moe_layer_forward_batched": (ST, [P, I32, P, I32, P, P, P, P, SZ, P]),
+        "moe_pool_time_batched": (ST, [P, I32]),
+        "moe_pool_batched_gemm_ms": (ST, [P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -271,6 +274,16 @@ class Pool:
         batched_workspace_bytes(shape, T) bytes."""
         _check(self.lib.moe_layer_forward_batched(self.h, layer, _p(x), n_tokens, _p(y), _p(topk_idx), _p(topk_w),
                                                   _p(work), work.numel() if hasattr(work, "numel") else 0, _s(stream)))
+
+    def time_batched(self, n_calls: int):
+        """Record CUDA events around the expert GEMMs of the next batched calls (ring of n)."""
+        _check(self.lib.moe_pool_time_batched(self.h, n_calls))
+
+    def batched_gemm_ms(self) -> tuple[float, int]:
+        """(total ms, calls) of the recorded expert-GEMM intervals; waits for them, then clears."""
+        ms, n = ctypes.c_float(0.0), ctypes.c_int32(0)
+        _check(self.lib.moe_pool_batched_gemm_ms(self.h, ctypes.byref(ms), ctypes.byref(n)))
+        return float(ms.value), int(n.value)
 
     def route(self, layer, x, topk_idx, topk_w, stream=None):
         _check(self.lib.moe_route(self.h, layer, _p(x), _p(topk_idx), _p(topk_w), _s(stream)))
