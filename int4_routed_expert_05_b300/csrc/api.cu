@@ -149,6 +149,16 @@ struct moe_pool {
     // batched-path timing: event pairs around the expert GEMMs of each call, round robin
     std::vector<cudaEvent_t> gemm_ev;  // [2 * n]
     int gemm_next = 0, gemm_used = 0;
+    // batched-path tensor maps, re-encoded only when the memory they describe changes
+    struct MapKey {
+        const void* ptr = nullptr;
+        int64_t a = -1, b = -1;
+        bool same(const void* p, int64_t x, int64_t y) const { return ptr == p && a == x && b == y; }
+    };
+    MapKey k_arena, k_u, k_b0, k_b1;
+    CUtensorMap m_arena[3], m_u, m_b0, m_b1;
+    std::vector<MapKey> k_shared, k_router;   // per layer
+    std::vector<CUtensorMap> m_shared, m_router;  // [L][3], [L]
 };
 
 extern "C" {
@@ -879,20 +889,66 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     const LayerDesc& L = p->layers[layer];
 
     tc::GroupedArgs A{};
-    int rc = encode_slice_maps(A.map_q[0], p->arena, p->S, p->geo.stride, p->geo, sh.bits);
-    if (rc == 0)
-        rc = encode_slice_maps(A.map_q[1], L.shared_blob, 1, p->geo_s.stride, p->geo_s, sh.bits);
     const int nA = T * (k + 1);
-    if (rc == 0)
-        rc = encode_tiles16(&A.map_wr, L.router, H, E, 128, false);
-    if (rc == 0)
-        rc = encode_tiles16(&A.map_u, d_x, H, T, tc::kNT, false);
-    if (rc == 0)
-        rc = encode_tiles16(&A.map_b[0], w + bl.us, H, nA, tc::kBRows, true);
-    if (rc == 0)
-        rc = encode_tiles16(&A.map_b[1], w + bl.hbuf, Imax, nA, tc::kBRows, true);
+    if ((int)p->k_shared.size() != p->L) {
+        p->k_shared.assign(p->L, {});
+        p->k_router.assign(p->L, {});
+        p->m_shared.resize(3 * (size_t)p->L);
+        p->m_router.resize(p->L);
+    }
+    int rc = 0;
+    if (!p->k_arena.same(p->arena, p->S, sh.bits)) {
+        p->k_arena = {};
+        rc = encode_slice_maps(p->m_arena, p->arena, p->S, p->geo.stride, p->geo, sh.bits);
+        if (rc == 0)
+            p->k_arena = {p->arena, p->S, sh.bits};
+    }
+    auto& ks = p->k_shared[layer];
+    if (rc == 0 && !ks.same(L.shared_blob, sh.bits, 0)) {
+        ks = {};
+        CUtensorMap tmp[3];
+        rc = encode_slice_maps(tmp, L.shared_blob, 1, p->geo_s.stride, p->geo_s, sh.bits);
+        if (rc == 0) {
+            for (int m = 0; m < 3; ++m)
+                p->m_shared[3 * (size_t)layer + m] = tmp[m];
+            ks = {L.shared_blob, sh.bits, 0};
+        }
+    }
+    auto& kr = p->k_router[layer];
+    if (rc == 0 && !kr.same(L.router, H, E)) {
+        kr = {};
+        rc = encode_tiles16(&p->m_router[layer], L.router, H, E, 128, false);
+        if (rc == 0)
+            kr = {L.router, H, E};
+    }
+    if (rc == 0 && !p->k_u.same(d_x, T, H)) {
+        p->k_u = {};
+        rc = encode_tiles16(&p->m_u, d_x, H, T, tc::kNT, false);
+        if (rc == 0)
+            p->k_u = {d_x, T, H};
+    }
+    if (rc == 0 && !p->k_b0.same(w + bl.us, nA, H)) {
+        p->k_b0 = {};
+        rc = encode_tiles16(&p->m_b0, w + bl.us, H, nA, tc::kBRows, true);
+        if (rc == 0)
+            p->k_b0 = {w + bl.us, nA, H};
+    }
+    if (rc == 0 && !p->k_b1.same(w + bl.hbuf, nA, Imax)) {
+        p->k_b1 = {};
+        rc = encode_tiles16(&p->m_b1, w + bl.hbuf, Imax, nA, tc::kBRows, true);
+        if (rc == 0)
+            p->k_b1 = {w + bl.hbuf, nA, Imax};
+    }
     if (rc != 0)
         return fail(MOE_E_CUDA, "tensor map encoding failed (%d)", rc);
+    for (int m = 0; m < 3; ++m) {
+        A.map_q[0][m] = p->m_arena[m];
+        A.map_q[1][m] = p->m_shared[3 * (size_t)layer + m];
+    }
+    A.map_wr = p->m_router[layer];
+    A.map_u = p->m_u;
+    A.map_b[0] = p->m_b0;
+    A.map_b[1] = p->m_b1;
     A.geo = p->geo;
     A.geo_s = p->geo_s;
     A.T = T;
