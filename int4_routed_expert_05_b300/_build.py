@@ -28,9 +28,17 @@ def stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile when forced or stale. The library is written to a per-process temporary file and
+    renamed into place, so ranks that build at the same time never load a half-written file."""
     if force or stale():
         extra = ["-Xptxas", "-v"] if verbose else []
-        subprocess.run(nvcc_cmd(LIB, extra), check=True)
+        tmp = f"{LIB}.tmp{os.getpid()}"
+        try:
+            subprocess.run(nvcc_cmd(tmp, extra), check=True)
+            os.replace(tmp, LIB)
+        finally:
+            if os.path.exists(tmp):
+                os.remove(tmp)
     return LIB
 
 

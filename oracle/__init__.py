@@ -26,9 +26,15 @@ RMS_EPS = 1e-6
 
 def compile_c(src: str, out: str) -> str:
     """gcc -O2, no fast-math, no floating-point contraction."""
+    tmp = f"{out}.tmp{os.getpid()}"  # written aside and renamed: concurrent builders never see half a file
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
-           "-o", out, src, "-lm"]
-    subprocess.run(cmd, check=True)
+           "-o", tmp, src, "-lm"]
+    try:
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+    finally:
+        if os.path.exists(tmp):
+            os.remove(tmp)
     return out
 
 
