@@ -516,8 +516,42 @@ def run_batched(args):
         touched.append(len(np.unique(idx.cpu().numpy())))
     torch.cuda.synchronize()
 
+    # The layer call does no host synchronisation, so each (layer, input) pair of the rotation is
+    # captured once as a CUDA graph and replayed: the same seven launches, without per-launch host
+    # overhead. Falls back to direct calls if capture is refused. (Events recorded inside a graph
+    # cannot be waited on from the host, so with graphs the expert-GEMM time comes from a second,
+    # direct-call pass below.)
+    n_combo = int(np.lcm(L, n_x))
+    graphs = []
+    if not args.no_graphs:
+        try:
+            R.pool.time_batched(0)
+            gs = torch.cuda.Stream()
+            gs.wait_stream(stream)
+            for c in range(n_combo):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=gs):
+                    R.pool.layer_forward_batched(c % L, xs[c % n_x], T, y, work, idx, w, gs)
+                graphs.append(g)
+            stream.wait_stream(gs)
+            torch.cuda.synchronize()
+        except Exception as exc:  # noqa: BLE001 - any refusal means direct calls
+            print(f"[bench] CUDA graph capture unavailable ({exc}); timing direct calls", file=sys.stderr)
+            graphs = []
+            torch.cuda.synchronize()
+    if not graphs:
+        R.pool.time_batched(args.steps)  # CUDA events around the expert GEMMs of every timed step
+
+    def timed_step(i):
+        if graphs:
+            graphs[i % n_combo].replay()
+        else:
+            step(i)
+
+    for i in range(3):  # replays warm up too
+        timed_step(args.warmup + i)
+    torch.cuda.synchronize()
     clocks = ClockSampler(local)
-    R.pool.time_batched(args.steps)  # CUDA events around the expert GEMMs of every timed step
     _barrier(ws)
     torch.cuda.synchronize()
     clocks.start()
@@ -526,12 +560,17 @@ def run_batched(args):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        step(args.warmup + i)
+        timed_step(args.warmup + i)
     e1.record(stream)
     torch.cuda.synchronize()
     _barrier(ws)
     clk = clocks.stop()
     ms = _max_over_ranks(ws, e0.elapsed_time(e1))
+    if graphs:  # the expert GEMMs' own time, from direct calls with the event hook
+        R.pool.time_batched(args.steps)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        torch.cuda.synchronize()
     gemm_ms, gemm_calls = R.pool.batched_gemm_ms()
     R.pool.time_batched(0)
     if R.pool.device_status() != moe.OK:
@@ -594,6 +633,7 @@ def run_batched(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights, fp16 tensor-core operands, fp32 accumulate",
         "data": "synthetic (seeded generator, random-init weights of the stated shapes)",
         "config": {"workload": args.config, "description": desc, "tokens": T, "layers_rotated": L,
+                   "cuda_graphs": bool(graphs),
                    "hidden": H, "experts": E, "top_k": k, "inter": sh.inter, "shared_inter": sh.shared_inter,
                    "bits": bits, "group": sh.group,
                    "l2": "steps rotate over %d resident layers (%.1f GB of expert blobs), far above the 126 MB L2"
@@ -644,6 +684,7 @@ def main():
     ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true", help="batched workloads: time direct calls, not graph replays")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the stack (small cases for profiling)")
     args = ap.parse_args()
