@@ -280,11 +280,10 @@ moe_status moe_pool_create(const moe_shape* s, int32_t n_layers, int32_t n_slots
     int optin = 0;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) != cudaSuccess)
         return cleanup(fail(MOE_E_CUDA, "cudaDeviceGetAttribute failed"));
-    p->smem = fused_smem_bytes(s->hidden, s->n_experts, s->top_k, s->inter, s->shared_inter, s->bits, sms, optin);
+    p->smem = plan_decode(s->hidden, s->n_experts, s->top_k, s->inter, s->shared_inter, s->bits, sms, optin, &p->sg);
     if (p->smem == 0)
         return cleanup(fail(MOE_E_SHAPE, "the fused decode kernel cannot stage this shape on %d SMs with %d bytes of "
                             "shared memory per block", sms, optin));
-    p->sg = stage_geo(s->hidden, s->n_experts, s->top_k, s->inter, s->shared_inter, s->bits, sms);
     cudaFuncAttributes fa{};
     cudaError_t e = cudaFuncGetAttributes(&fa, moe_decode_kernel);
     if (e == cudaSuccess && (uint32_t)fa.maxDynamicSharedSizeBytes < p->smem)

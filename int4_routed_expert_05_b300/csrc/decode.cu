@@ -10,26 +10,31 @@
 // fixed-stride blob per expert, one read per expert).
 //
 // Design: one cooperative launch covers every layer and token of a call, one 512-thread block per
-// SM. Every step executes the whole body, so the body has to stay small enough for the SM's
-// instruction caches: only the inner chunk loops of the MMA blocks are unrolled. Per step (token, layer) a block
-//   1. holds the layer input x in shared memory and forms u;
-//   2. computes its rows of the router (rows prefetched during the previous step) and publishes
-//      them as epoch-tagged (epoch, value) pairs; computes its rows of the shared expert's gate/up
-//      and publishes h_shared the same way; queues the next step's router and shared rows;
-//   3. polls the logits until every pair carries this step's epoch, takes the top-k itself;
-//   4. joins the group of blocks that serves one routed expert (rank j): fetches its share of the
-//      expert's gate/up rows and down rows as TMA boxes into a ring of 16 slots (one per warp; a
-//      warp refills its slot with its next box as soon as it has consumed it), and in the meantime
-//      finishes the shared expert's down rows;
-//   5. turns its gate/up rows into h_j, publishes them to its group, collects the group's h_j
-//      while the down boxes land, and computes its down rows of y_j;
-//   6. adds w_j y_j (and gamma y_shared) into a fixed-point accumulator with integer atomics, so
-//      the sum is exact and independent of the order in which blocks arrive;
-//   7. waits at one grid barrier and reads the complete layer output back.
-// int4 codes become exact bf16 integers in registers (mask + bf16x2 FMA) and meet the activations
-// on the tensor cores (mma.m16n8k16, fp32 accumulate), one 64-element quantisation group per chunk;
-// the affine dequantisation is applied per chunk as s * (sum q u) + b * (sum u). Every sum runs in
-// a fixed order, so the result depends neither on the grid size nor on pool placement.
+// SM. A layer at batch 1 moves about 20 MB, a few microseconds of HBM time, so the kernel is built
+// around the latency of the layer's three all-to-all dependencies (logits -> top-k, h_j -> down
+// rows, y -> next layer) and around what the copy engine charges per copy (each copy costs tens of
+// cycles to issue, so a block fetches its routed rows in three large copies). Per step (token,
+// layer) a block
+//   1. waits for the previous step's output words, forms x (every block the same) and u;
+//   2. computes its router rows (staged during the previous step) and publishes the logits as
+//      epoch-tagged (epoch, value) pairs;
+//   3. polls the logits and takes the top-k itself (every block, the same result);
+//   4. issues every byte it will read of its routed expert: its gate rows, its up rows and its
+//      down rows (one 4D tensor copy each, 128-byte swizzled) plus their scales, so the layer's
+//      whole routed stream is in flight at once;
+//   5. while those bytes travel: its rows of the shared expert's gate/up (staged during the
+//      previous step) -> h_shared, published; the next step's router and shared rows queued; the
+//      shared h polled and its down rows added as gamma * y_shared;
+//   6. turns its gate/up rows into h_j as the copies land, exchanges h_j within the expert's
+//      block group, and computes its down rows of y_j;
+//   7. adds w_j y_j into the output words: each word collects exactly k + 1 contributions as
+//      fixed-point integers with a contribution count in its low byte, so the sum is exact and
+//      order independent and the count tells every block when the layer output is complete: there
+//      is no grid barrier between layers.
+// int4 codes become fp16 values 1024 + q in registers (one lop3 per pair) and meet the activations
+// on the tensor cores (mma.m16n8k16, fp32 accumulate), one 64-field chunk at a time; the offset
+// and the affine dequantisation are applied per chunk as s * (sum q u) + b * (sum u). Every sum
+// runs in a fixed order, so the result depends neither on arrival order nor on pool placement.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -53,35 +58,6 @@ __device__ __forceinline__ uint16_t f2bf(float v)
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
-// Order-preserving map of a float onto uint32 (larger float -> larger key; finite keys > 0).
-__device__ __forceinline__ uint32_t ord_key(float f)
-{
-    uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Position of element n of an expanded activation vector inside its permuted 16-element block
-// (register order 0,4,1,5,2,6,3,7, 8,12,9,13,10,14,11,15 of the B fragments).
-__device__ __forceinline__ int pslot(int n)
-{
-    const int e = n & 15;
-    return (n & ~15) | (e & 8) | ((e & 3) << 1) | ((e >> 2) & 1);
-}
-
-// SM cycle counter: cheap to read, so waits check their limit on it. A limit of t ns is taken as
-// 2 t cycles (about t ns at the 2.03 GHz maximum SM clock, longer at lower clocks).
-__device__ __forceinline__ long long cycles() { return clock64(); }
-__device__ __forceinline__ long long limit_cycles(const StepParams& P) { return (long long)(2 * P.timeout_ns); }
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-// thread / block coordinates (kept out of the block context, which lives in shared memory)
-#define TID ((int)threadIdx.x)
-#define WARP ((int)threadIdx.x >> 5)
-#define LANE ((int)threadIdx.x & 31)
-#define CTA ((int)blockIdx.x)
-#define GRID ((int)gridDim.x)
-
 __device__ __forceinline__ uint16_t f2h(float v)
 {
     __half h = __float2half_rn(v);
@@ -89,6 +65,25 @@ __device__ __forceinline__ uint16_t f2h(float v)
 }
 
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(*reinterpret_cast<const __half*>(&b)); }
+
+// Order-preserving map of a float onto uint32 (larger float -> larger key; finite keys > 0).
+__device__ __forceinline__ uint32_t ord_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// SM cycle counter: waits check their limit on it. A limit of t ns is taken as 2 t cycles (about
+// t ns at the 2.03 GHz maximum SM clock, longer at lower clocks).
+__device__ __forceinline__ long long cycles() { return clock64(); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+#define TID ((int)threadIdx.x)
+#define WARP ((int)threadIdx.x >> 5)
+#define LANE ((int)threadIdx.x & 31)
+#define CTA ((int)blockIdx.x)
+#define GRID ((int)gridDim.x)
 
 // (a & b) | c in one instruction
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
@@ -121,23 +116,6 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One 64-field chunk of a 16-row tile: thread (g, tq) holds fields [16 tq, 16 tq + 16) of row g
-// (ra) and of row g + 8 (rb); b0/b1 hold the matching 16 B values in permuted register order.
-// c[0] = C[g][2tq], c[1] = C[g][2tq+1], c[2] = C[g+8][2tq], c[3] = C[g+8][2tq+1].
-__device__ __forceinline__ void chunk_mma(float (&c)[4], uint2 ra, uint2 rb, uint4 b0, uint4 b1)
-{
-    uint32_t a[4], b[4];
-    c[0] = c[1] = c[2] = c[3] = 0.f;
-    deq8(ra.x, a);
-    deq8(rb.x, b);
-    mma_f16(c, a[0], b[0], a[1], b[1], b0.x, b0.y);
-    mma_f16(c, a[2], b[2], a[3], b[3], b0.z, b0.w);
-    deq8(ra.y, a);
-    deq8(rb.y, b);
-    mma_f16(c, a[0], b[0], a[1], b[1], b1.x, b1.y);
-    mma_f16(c, a[2], b[2], a[3], b[3], b1.z, b1.w);
-}
-
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -150,7 +128,7 @@ __device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x, float acc)
 {
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
     const uint32_t xx[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll 1
+#pragma unroll
     for (int i = 0; i < 4; ++i) {
         acc = fmaf(__uint_as_float(ww[i] << 16), __uint_as_float(xx[i] << 16), acc);
         acc = fmaf(__uint_as_float(ww[i] & 0xFFFF0000u), __uint_as_float(xx[i] & 0xFFFF0000u), acc);
@@ -172,12 +150,10 @@ __device__ __forceinline__ void ld_pair2(const unsigned long long* p, unsigned l
     asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
-__device__ __forceinline__ void red_add_s64(long long* p, long long v)
+__device__ __forceinline__ void red_add_u64(long long* p, long long v)
 {
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-
-__device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ void st_s64(long long* p, long long v)
 {
@@ -189,6 +165,21 @@ __device__ __forceinline__ void ld_s64x2(const long long* p, long long& a, long 
     asm volatile("ld.relaxed.gpu.global.v2.s64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
+__device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ void ld_acq_pair2(const unsigned long long* p, unsigned long long& a, unsigned long long& b)
+{
+    asm volatile("ld.acquire.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // ---- mbarrier / TMA ----
 __device__ __forceinline__ void mbar_init(uint64_t* m, int n)
@@ -220,13 +211,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                  : "memory");
 }
 
-// 3D tiled TMA load (x in bytes: a multiple of 16)
-__device__ __forceinline__ void tma3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* m)
+// 4D tiled TMA load (coordinates: byte in the column block, row, column block, slot)
+__device__ __forceinline__ void tma4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w, uint64_t* m)
 {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(m))
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(m))
         : "memory");
 }
 
@@ -239,52 +230,57 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map)
 // per-block context
 // ------------------------------------------------------------------------------------------
 
-// Block-uniform context: shape, staging geometry and shared-memory carve-up. One copy per block
-// in shared memory (written by thread 0 at start), so it takes no registers.
+// Block-uniform constants of a launch: shape, this block's share of the work and the
+// shared-memory carve-up. One copy per block in shared memory, written by thread 0 at start; the
+// phases below copy what they need into registers once, at their start.
 struct Ctx {
-    int H, E, k, I, Is, xp, KU, NCu, KD, NCd, KDs, NCds, ngu, ngd, ngds, rb_gu, rb_d, rb_ds;
+    int H, E, k, I, Is, xp, KU, NCu, KD, NCd, KDs, NCds, ngu, ngd, ngds, rb_gu, rb_d, rb_ds, ncb_ds;
+    int e0, e1;       // router rows
+    int s0, s1;       // shared gate/up rows
+    int o0, o1;       // shared down rows, and the slice of the output words this block clears
+    int j;            // rank of the routed expert this block serves
+    int r0, r1;       // its gate/up rows
+    int d0, d1;       // its down rows
     float invH;
-    BlobGeo geo, geo_s;   // routed / shared blob geometry
-    // (Ctx must fit in kCtxBytes; checked below)
-    StageGeo sg;
-    uint64_t* mbar;        // [kNumMbar]: ring slots, routed scales, dense, shared down
-    int* sel_idx;          // [kMaxK]
-    float* sel_w;          // [kMaxK]
-    int* sel_slot;         // [kMaxK]
-    float* red;            // [64]
-    float* misc;           // [16]: [0] gamma
-    int* imisc;            // [16]: staged-span offsets ([0..3] shared gate/up, [4..5] shared down,
-                           //       [8..13] routed gate/up and down)
-    float* sx;             // [H] layer input x (fp32)
-    uint16_t* su;          // [H] u (bf16)
-    uint16_t* sup;         // [KU] B operand of u (fp16, permuted blocks)
-    float2* scs;           // [NCu] per chunk: sum of u, 1024 * sum of B
-    float* slg;            // [E] logits
-    uint32_t* lkey;        // [kWarps][kMaxK]
-    int* lidx;             // [kWarps][kMaxK]
-    uint16_t* srt;         // [Rr][H] router rows
-    uint16_t* swsg;        // [H] shared gate vector
-    uint8_t* sgq;          // [2][Rs][rb_gu] shared gate/up codes
-    uint8_t* ssb;          // 4 spans: shared gate.s, gate.b, up.s, up.b rows
-    uint8_t* sdq;          // [Rsd][rb_ds] shared down codes
-    uint8_t* sdsb;         // 2 spans: shared down.s, down.b rows
-    uint8_t* ring;         // [kWarps][slot_bytes]
-    uint8_t* rsb;          // 4 spans: routed gate.s, gate.b, up.s, up.b rows
-    uint8_t* rdsb;         // 2 spans: routed down.s, down.b rows
-    uint16_t* shs;         // [2][KDs] B operand of h_shared (fp16 hi/lo, permuted blocks)
-    float2* chs;           // [NCds] per chunk: sum of h, 1024 * sum of B
-    uint16_t* shj;         // [2][KD] B operand of h_j
-    float2* chj;           // [NCd]
-    float* hv;             // [max(I, Is)] polled h values
-    float* sp;             // gate/up partials [rows][2][ncb_gu]
-    float* spd;            // down partials [rows][NCd or NCds]
+    uint64_t* mbar;
+    int* sel_idx;     // [kMaxK]
+    float* sel_w;     // [kMaxK]
+    int* sel_slot;    // [kMaxK]
+    float* red;       // [64]
+    float* misc;      // [32]: [0] gamma, [1..kMaxK] selected logits
+    int* imisc;       // [16]: offsets of staged scale spans ([0..3] shared gate/up, [4..5] shared down,
+                      //       [8..13] routed gate.s, gate.b, up.s, up.b, down.s, down.b)
+    float* sx;        // [H] layer input x (fp32)
+    uint16_t* su;     // [H] u (bf16)
+    uint16_t* sup;    // [KU] B operand of u (fp16, permuted blocks)
+    float2* scs;      // [NCu] per chunk: sum of u, 1024 * sum of B
+    float* slg;       // [E] logits
+    uint32_t* tk;     // top-k scratch
+    uint16_t* srt;    // [Rr][H] router rows
+    uint16_t* swsg;   // [H] shared gate vector
+    uint8_t* sgq;     // [2][Rs][rb_gu] shared gate/up codes
+    uint8_t* ssb;     // 4 spans: shared gate.s, gate.b, up.s, up.b rows
+    uint8_t* sdq;     // [Rsd][rb_ds] shared down codes
+    uint8_t* sdsb;    // 2 spans: shared down.s, down.b rows
+    uint8_t* ring;    // gate/up slots [nslot][2][nr_gu][gu_copy], then down [nr_d][d_copy]
+    uint8_t* rsb;     // 4 spans: routed gate.s, gate.b, up.s, up.b rows
+    uint8_t* rdsb;    // 2 spans: routed down.s, down.b rows
+    uint16_t* shs;    // [2][KDs] B operand of h_shared (fp16 hi/lo, permuted blocks)
+    float2* chs;      // [NCds]
+    uint16_t* shj;    // [2][KD] B operand of h_j
+    float2* chj;      // [NCd]
+    float* hv;        // [max(I, Is)] polled h values
+    float* sp;        // gate/up partials [rows][2 * ncb_gu]
+    float* spd;       // down partials [rows][ncb]
+    float* rp;        // router partials [Rr][kRouterParts]
     uint32_t span_gu, span_d, span_sgu, span_sd;  // bytes per staged scale span
 };
 
 static_assert(sizeof(Ctx) <= kCtxBytes, "the block context outgrew its shared-memory slot");
 
-__device__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base)
+__device__ __noinline__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base)
 {
+    const StageGeo& sg = P.sg;
     C.H = P.H;
     C.E = P.E;
     C.k = P.k;
@@ -303,11 +299,22 @@ __device__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base)
     C.rb_gu = P.H * P.bits / 8;
     C.rb_d = P.I * P.bits / 8;
     C.rb_ds = P.Is * P.bits / 8;
-    C.sg = P.sg;
+    C.ncb_ds = cdiv(C.rb_ds, kCb);
     C.invH = 1.f / (float)P.H;
-    C.geo = P.geo;
-    C.geo_s = P.geo_s;
-    const SmemPlan s = smem_plan(P.H, P.E, P.k, P.I, P.Is, P.bits, GRID);
+    const int G = GRID, b = CTA;
+    C.e0 = part(P.E, G, b);
+    C.e1 = part(P.E, G, b + 1);
+    C.s0 = part(P.Is, G, b);
+    C.s1 = part(P.Is, G, b + 1);
+    C.o0 = part(P.H, G, b);
+    C.o1 = part(P.H, G, b + 1);
+    C.j = grp_of(b, G, P.k);
+    const int gi = b - grp_start(C.j, G, P.k);
+    C.r0 = imin(gi * sg.SRgu, P.I);
+    C.r1 = imin(C.r0 + sg.SRgu, P.I);
+    C.d0 = imin(gi * sg.SRd, P.H);
+    C.d1 = imin(C.d0 + sg.SRd, P.H);
+    const SmemPlan s = smem_plan(P.H, P.E, P.k, P.I, P.Is, P.bits, sg);
     C.mbar = (uint64_t*)(base + s.mbar);
     int* ctl = (int*)(base + s.ctl);
     C.sel_idx = ctl;
@@ -315,14 +322,13 @@ __device__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base)
     C.sel_slot = ctl + 2 * kMaxK;
     C.red = (float*)(ctl + 3 * kMaxK);
     C.misc = (float*)(ctl + 3 * kMaxK + 64);
-    C.imisc = ctl + 3 * kMaxK + 64 + 16;
+    C.imisc = ctl + 3 * kMaxK + 64 + 32;
     C.sx = (float*)(base + s.x);
     C.su = (uint16_t*)(base + s.u);
     C.sup = (uint16_t*)(base + s.up);
     C.scs = (float2*)(base + s.uc);
     C.slg = (float*)(base + s.lg);
-    C.lkey = (uint32_t*)(base + s.lkey);
-    C.lidx = (int*)(base + s.lidx);
+    C.tk = (uint32_t*)(base + s.tk);
     C.srt = (uint16_t*)(base + s.rt);
     C.swsg = (uint16_t*)(base + s.wsg);
     C.sgq = base + s.sgq;
@@ -339,58 +345,16 @@ __device__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base)
     C.hv = (float*)(base + s.hv);
     C.sp = (float*)(base + s.sp);
     C.spd = (float*)(base + s.spd);
-    C.span_gu = sb_span_max(C.sg.Rgu, 2 * C.ngu);
-    C.span_d = sb_span_max(C.sg.Rd, 2 * C.ngd);
-    C.span_sgu = sb_span_max(C.sg.Rs, 2 * C.ngu);
-    C.span_sd = sb_span_max(C.sg.Rsd, 2 * C.ngds);
-}
-
-
-// Block-uniform time limit check: true once the wait that started at t0 ran past the limit.
-__device__ __forceinline__ bool timed_out(const StepParams& P, long long t0)
-{
-    return __syncthreads_or(threadIdx.x == 0 && cycles() - t0 > limit_cycles(P)) != 0;
-}
-
-// Issue a 1D copy of rows [r0, r1) of a section whose rows hold row_b bytes (16-byte aligned
-// superset); returns the bytes issued and, in *off, the offset of row r0 inside the copy.
-__device__ __forceinline__ uint32_t copy_rows(void* dst, const uint8_t* sec, int r0, int r1, int row_b, uint64_t* m,
-                                              uint32_t* off)
-{
-    if (r1 <= r0) {
-        *off = 0;
-        return 0;
-    }
-    const uintptr_t a = (uintptr_t)(sec + (size_t)r0 * row_b);
-    const uintptr_t e = (uintptr_t)(sec + (size_t)r1 * row_b);
-    const uintptr_t a16 = a & ~(uintptr_t)15, e16 = (e + 15) & ~(uintptr_t)15;
-    *off = (uint32_t)(a - a16);
-    bulk_g2s(dst, (const void*)a16, (uint32_t)(e16 - a16), m);
-    return (uint32_t)(e16 - a16);
+    C.rp = (float*)(base + s.rp);
+    C.span_gu = sb_span_max(sg.SRgu, 2 * C.ngu);
+    C.span_d = sb_span_max(sg.SRd, 2 * C.ngd);
+    C.span_sgu = sb_span_max(sg.Rs, 2 * C.ngu);
+    C.span_sd = sb_span_max(sg.Rsd, 2 * C.ngds);
 }
 
 // ------------------------------------------------------------------------------------------
-// dense (resident) rows of a step: router rows, shared gate vector, shared gate/up rows, and
-// separately the shared down rows
+// copies
 // ------------------------------------------------------------------------------------------
-
-struct DenseRows {
-    int e0, e1;    // router rows
-    int s0, s1;    // shared gate/up rows
-    int o0, o1;    // shared down rows (= this block's slice of the output)
-};
-
-__device__ __forceinline__ DenseRows dense_rows(const Ctx& C)
-{
-    DenseRows d;
-    d.e0 = part(C.E, GRID, CTA);
-    d.e1 = part(C.E, GRID, CTA + 1);
-    d.s0 = part(C.Is, GRID, CTA);
-    d.s1 = part(C.Is, GRID, CTA + 1);
-    d.o0 = part(C.H, GRID, CTA);
-    d.o1 = part(C.H, GRID, CTA + 1);
-    return d;
-}
 
 // Bytes copy_rows() issues for rows [r0, r1) of a section whose rows hold row_b bytes.
 __device__ __forceinline__ uint32_t span_bytes(const uint8_t* sec, int r0, int r1, int row_b)
@@ -402,223 +366,240 @@ __device__ __forceinline__ uint32_t span_bytes(const uint8_t* sec, int r0, int r
     return (uint32_t)(((e + 15) & ~(uintptr_t)15) - (a & ~(uintptr_t)15));
 }
 
-// Issued by thread 0: the router rows, the shared gate vector and the shared expert's gate/up
-// rows of layer L. Offsets of the staged scale spans go to imisc[0..3].
-__device__ __noinline__ void issue_dense(const StepParams& P, const Ctx& C, const LayerDesc L, bool with_router, bool with_shared)
+// Issue a 1D copy of rows [r0, r1) of a section whose rows hold row_b bytes (16-byte aligned
+// superset); returns, in *off, the offset of row r0 inside the copy.
+__device__ __forceinline__ void copy_rows(void* dst, const uint8_t* sec, int r0, int r1, int row_b, uint64_t* m,
+                                          int* off)
 {
-    const DenseRows d = dense_rows(C);
-    uint64_t* m = C.mbar + kWarps + 1;
-    const BlobGeo& gs = C.geo_s;
-    const bool rt = with_router && d.e1 > d.e0;
-    const bool sh = with_shared && d.s1 > d.s0;
-    // the expected bytes go first: the arrive must not complete the phase before the copies count
-    uint32_t bytes = (uint32_t)C.H * 2;
+    if (r1 <= r0) {
+        *off = 0;
+        return;
+    }
+    const uintptr_t a = (uintptr_t)(sec + (size_t)r0 * row_b);
+    const uintptr_t e = (uintptr_t)(sec + (size_t)r1 * row_b);
+    const uintptr_t a16 = a & ~(uintptr_t)15, e16 = (e + 15) & ~(uintptr_t)15;
+    *off = (int)(a - a16);
+    bulk_g2s(dst, (const void*)a16, (uint32_t)(e16 - a16), m);
+}
+
+// One thread: the router rows, the shared gate vector and the shared expert's gate/up rows and
+// scales of layer L (only the parts the launch's mode uses).
+__device__ __noinline__ void issue_dense(const StepParams& P, const Ctx& C, const LayerDesc L, bool rt, bool sh)
+{
+    uint64_t* m = C.mbar + kMbDense;
+    const uint8_t* sb = L.shared_blob;
+    const int ns = C.s1 - C.s0, H = C.H, rb = C.rb_gu, ngu2 = C.ngu * 2;
+    rt = rt && C.e1 > C.e0;
+    const bool shr = sh && ns > 0;
+    uint32_t bytes = sh ? (uint32_t)H * 2 : 0u;
     if (rt)
-        bytes += (uint32_t)(d.e1 - d.e0) * C.H * 2;
-    if (sh) {
-        bytes += 2u * (uint32_t)(d.s1 - d.s0) * C.rb_gu;
-        #pragma unroll 1
+        bytes += (uint32_t)(C.e1 - C.e0) * H * 2;
+    if (shr) {
+        bytes += 2u * (uint32_t)ns * rb;
+#pragma unroll 1
         for (int i = 0; i < 4; ++i)
-            bytes += span_bytes(L.shared_blob + ((i & 1) ? gs.b_off[i >> 1] : gs.s_off[i >> 1]), d.s0, d.s1, C.ngu * 2);
+            bytes += span_bytes(sb + ((i & 1) ? P.geo_s.b_off[i >> 1] : P.geo_s.s_off[i >> 1]), C.s0, C.s1, ngu2);
     }
     mbar_expect(m, bytes);
     if (rt)
-        bulk_g2s(C.srt, L.router + (size_t)d.e0 * C.H, (uint32_t)(d.e1 - d.e0) * C.H * 2, m);
-    bulk_g2s(C.swsg, L.shared_gate, (uint32_t)C.H * 2, m);
-    if (sh) {
-        const uint32_t nq = (uint32_t)(d.s1 - d.s0) * C.rb_gu;
-        bulk_g2s(C.sgq, L.shared_blob + gs.q_off[0] + (size_t)d.s0 * C.rb_gu, nq, m);
-        bulk_g2s(C.sgq + (size_t)C.sg.Rs * C.rb_gu, L.shared_blob + gs.q_off[1] + (size_t)d.s0 * C.rb_gu, nq, m);
-        #pragma unroll 1
-        for (int i = 0; i < 4; ++i) {
-            uint32_t off;
-            copy_rows(C.ssb + i * C.span_sgu, L.shared_blob + ((i & 1) ? gs.b_off[i >> 1] : gs.s_off[i >> 1]), d.s0, d.s1,
-                      C.ngu * 2, m, &off);
-            C.imisc[i] = (int)off;
-        }
+        bulk_g2s(C.srt, L.router + (size_t)C.e0 * H, (uint32_t)(C.e1 - C.e0) * H * 2, m);
+    if (sh)
+        bulk_g2s(C.swsg, L.shared_gate, (uint32_t)H * 2, m);
+    if (shr) {
+        const uint32_t nq = (uint32_t)ns * rb;
+        bulk_g2s(C.sgq, sb + P.geo_s.q_off[0] + (size_t)C.s0 * rb, nq, m);
+        bulk_g2s(C.sgq + (size_t)P.sg.Rs * rb, sb + P.geo_s.q_off[1] + (size_t)C.s0 * rb, nq, m);
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i)
+            copy_rows(C.ssb + i * C.span_sgu, sb + ((i & 1) ? P.geo_s.b_off[i >> 1] : P.geo_s.s_off[i >> 1]), C.s0,
+                      C.s1, ngu2, m, &C.imisc[i]);
     }
 }
 
-__device__ __noinline__ void issue_shared_down(const StepParams& P, const Ctx& C, const LayerDesc L)
+// One thread: the shared expert's down rows [o0, o1) and their scales of layer L.
+__device__ __noinline__ void issue_sdown(const StepParams& P, const Ctx& C, const LayerDesc L)
 {
-    const DenseRows d = dense_rows(C);
-    uint64_t* m = C.mbar + kWarps + 2;
-    const BlobGeo& gs = C.geo_s;
+    uint64_t* m = C.mbar + kMbSdown;
+    const uint8_t* sb = L.shared_blob;
     const int rowb = C.ngds * 2;
     uint32_t bytes = 0;
-    if (d.o1 > d.o0)
-        bytes = (uint32_t)(d.o1 - d.o0) * C.rb_ds + span_bytes(L.shared_blob + gs.s_off[2], d.o0, d.o1, rowb) +
-                span_bytes(L.shared_blob + gs.b_off[2], d.o0, d.o1, rowb);
+    if (C.o1 > C.o0)
+        bytes = (uint32_t)(C.o1 - C.o0) * C.rb_ds + span_bytes(sb + P.geo_s.s_off[2], C.o0, C.o1, rowb) +
+                span_bytes(sb + P.geo_s.b_off[2], C.o0, C.o1, rowb);
     mbar_expect(m, bytes);
-    if (d.o1 > d.o0) {
-        uint32_t off;
-        bulk_g2s(C.sdq, L.shared_blob + gs.q_off[2] + (size_t)d.o0 * C.rb_ds, (uint32_t)(d.o1 - d.o0) * C.rb_ds, m);
-        copy_rows(C.sdsb, L.shared_blob + gs.s_off[2], d.o0, d.o1, rowb, m, &off);
-        C.imisc[4] = (int)off;
-        copy_rows(C.sdsb + C.span_sd, L.shared_blob + gs.b_off[2], d.o0, d.o1, rowb, m, &off);
-        C.imisc[5] = (int)off;
+    if (C.o1 > C.o0) {
+        bulk_g2s(C.sdq, sb + P.geo_s.q_off[2] + (size_t)C.o0 * C.rb_ds, (uint32_t)(C.o1 - C.o0) * C.rb_ds, m);
+        copy_rows(C.sdsb, sb + P.geo_s.s_off[2], C.o0, C.o1, rowb, m, &C.imisc[4]);
+        copy_rows(C.sdsb + C.span_sd, sb + P.geo_s.b_off[2], C.o0, C.o1, rowb, m, &C.imisc[5]);
     }
 }
 
-// ------------------------------------------------------------------------------------------
-// A-fragment loads from staged rows
-// ------------------------------------------------------------------------------------------
-
-// Rows staged in shared memory. Swizzled (TMA boxes of 128-byte rows, slots 1024-byte aligned):
-// the 16-byte chunk j of row R sits at chunk j ^ (R & 7); linear: rows of `width` bytes one after
-// another. swzmask is 7 for swizzled rows (width 128) and 0 for linear ones, so both layouts share
-// one branch-free address computation.
-__device__ __forceinline__ uint2 lds_a(const uint8_t* base, uint32_t swzmask, int width, int R, int byte)
+// Staging address of gate/up copy (slot sl, matrix m, row box rc) and of down copy rc.
+__device__ __forceinline__ uint8_t* gu_copy_at(const Ctx& C, const StageGeo& sg, int sl, int m, int rc)
 {
-    const uint32_t off = (uint32_t)R * (uint32_t)width + ((((uint32_t)byte >> 4) ^ ((uint32_t)R & swzmask)) << 4) +
-                         ((uint32_t)byte & 15u);
-    return *reinterpret_cast<const uint2*>(base + off);
+    return C.ring + (size_t)((sl * 2 + m) * sg.nr_gu + rc) * sg.gu_copy;
+}
+__device__ __forceinline__ uint8_t* d_copy_at(const Ctx& C, const StageGeo& sg, int rc)
+{
+    return C.ring + (size_t)sg.nslot_gu * 2 * sg.nr_gu * sg.gu_copy + (size_t)rc * sg.d_copy;
+}
+
+// One thread: the gate and up copies of column group cg of the block's gate/up rows, into slot sl.
+__device__ __noinline__ void issue_gu_group(const StepParams& P, const Ctx& C, int slot, int cg, int sl)
+{
+    const StageGeo& sg = P.sg;
+    const int nrc = cdiv(C.r1 - C.r0, sg.bh_gu);
+#pragma unroll 1
+    for (int m = 0; m < 2; ++m) {
+        uint64_t* mb = C.mbar + 2 * sl + m;
+        mbar_expect(mb, (uint32_t)nrc * sg.cbw_gu * sg.bh_gu * sg.cpg_gu);
+#pragma unroll 1
+        for (int rc = 0; rc < nrc; ++rc)
+            tma4d(gu_copy_at(C, sg, sl, m, rc), &P.tmap[m], 0, C.r0 + rc * sg.bh_gu, cg * sg.cpg_gu, slot, mb);
+    }
+}
+
+// One thread: the scales of the block's routed rows, its first gate/up column groups and all of
+// its down rows.
+__device__ __noinline__ void issue_routed(const StepParams& P, const Ctx& C, int slot)
+{
+    const StageGeo& sg = P.sg;
+    const uint8_t* blob = P.arena + (uint64_t)slot * P.stride;
+    const bool gu = C.r1 > C.r0, dn = C.d1 > C.d0;
+    uint64_t* m = C.mbar + kMbRsc;
+    uint32_t bytes = 0;
+#pragma unroll 1
+    for (int i = 0; i < 6; ++i) {
+        const bool d = i >= 4;
+        const uint64_t sec = (i & 1) ? P.geo.b_off[i >> 1] : P.geo.s_off[i >> 1];
+        bytes += span_bytes(blob + sec, d ? C.d0 : C.r0, d ? C.d1 : C.r1, d ? C.ngd * 2 : C.ngu * 2);
+    }
+    mbar_expect(m, bytes);
+    // gate scales, then the gate/up codes of the first groups, then the rest: the copy engine
+    // takes copies in order, and the gate/up rows are needed first
+#pragma unroll 1
+    for (int i = 0; i < 6; ++i) {
+        const bool d = i >= 4;
+        uint8_t* dst = d ? C.rdsb + (i - 4) * C.span_d : C.rsb + i * C.span_gu;
+        const uint64_t sec = (i & 1) ? P.geo.b_off[i >> 1] : P.geo.s_off[i >> 1];
+        copy_rows(dst, blob + sec, d ? C.d0 : C.r0, d ? C.d1 : C.r1, d ? C.ngd * 2 : C.ngu * 2, m, &C.imisc[8 + i]);
+        if (i == 3 && gu)
+#pragma unroll 1
+            for (int cg = 0; cg < sg.nslot_gu; ++cg)
+                issue_gu_group(P, C, slot, cg, cg);
+    }
+    if (dn) {
+        const int nrc = cdiv(C.d1 - C.d0, sg.bh_d);
+        uint64_t* md = C.mbar + kMbDown;
+        mbar_expect(md, (uint32_t)nrc * sg.cbw_d * sg.bh_d * sg.cpg_d);
+#pragma unroll 1
+        for (int rc = 0; rc < nrc; ++rc)
+            tma4d(d_copy_at(C, sg, rc), &P.tmap[2], 0, C.d0 + rc * sg.bh_d, 0, slot, md);
+    }
 }
 
 // ------------------------------------------------------------------------------------------
-// input, u, expanded u
+// waits and exchanges
 // ------------------------------------------------------------------------------------------
 
-// The B operand of one chunk: fp16 activations in the MMA's register order (pslot). For int4 the
-// odd fields of a word enter A multiplied by 16, so their activations are divided by 16; an int8
-// code is read as two fields (low, 16 x high), both paired with the code's activation.
-
-// x (in sx) or the bf16 input u_bits -> su (bf16 u), sup (B operand), scs (per chunk sums)
-__device__ void make_u(const StepParams& P, const Ctx& C, bool prenorm, const uint16_t* u_bits)
+// Block-uniform wait for a block-level mbarrier phase (all threads).
+__device__ __forceinline__ bool wait_block(uint64_t* m, uint32_t parity, long long limit, int* status)
 {
-    const int H = C.H;
-    float rinv = 1.f;
-    if (prenorm) {
-        float ss = 0.f;
-        #pragma unroll 1
-        for (int i = TID; i < H; i += kThreads)
-            ss = fmaf(C.sx[i], C.sx[i], ss);
-        ss = warp_sum(ss);
-        if (LANE == 0)
-            C.red[WARP] = ss;
-        __syncthreads();
-        float tot = 0.f;
-        #pragma unroll 1
-        for (int w = 0; w < kWarps; ++w)
-            tot += C.red[w];
-        rinv = rsqrtf(tot * C.invH + 1e-6f);
-    }
-    const int cpc = kChunk / C.xp;  // codes per chunk
-    const int lpc = cpc / 4;        // threads per chunk (4 codes each)
-    #pragma unroll 1
-    for (int q0 = 0; q0 < H / 4; q0 += kThreads) {
-        const int q = q0 + TID;
-        float us = 0.f, bs = 0.f;
-        if (q < H / 4) {
-            #pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                const int i = 4 * q + j;
-                const uint16_t ub = prenorm ? f2bf(C.sx[i] * rinv) : u_bits[i];
-                const float uv = bf16f(ub);
-                C.su[i] = ub;
-                us += uv;
-                if (C.xp == 1) {
-                    const uint16_t bh = f2h((i & 1) ? uv * 0.0625f : uv);
-                    C.sup[pslot(i)] = bh;
-                    bs += h2f(bh);
-                } else {
-                    const uint16_t bh = f2h(uv);
-                    C.sup[pslot(2 * i)] = bh;
-                    C.sup[pslot(2 * i + 1)] = bh;
-                    bs += 2.f * h2f(bh);
-                }
-            }
+    const long long t0 = cycles();
+    bool ok = true;
+    while (!mbar_try(m, parity))
+        if (cycles() - t0 > limit) {
+            ok = false;
+            break;
         }
-        #pragma unroll 1
-        for (int o = lpc / 2; o; o >>= 1) {
-            us += __shfl_xor_sync(0xffffffffu, us, o);
-            bs += __shfl_xor_sync(0xffffffffu, bs, o);
-        }
-        if (q < H / 4 && (LANE % lpc) == 0)
-            C.scs[4 * q / cpc] = make_float2(us, 1024.f * bs);
+    if (__syncthreads_or(!ok)) {
+        if (TID == 0)
+            set_status(status, kStatusTimeout);
+        return false;
     }
-    __syncthreads();
+    return true;
 }
 
-// h values hv[0, n) -> B operand hi/lo parts (sh: [2][n * xp]) and per chunk {sum of h, 1024 *
-// sum of (hi + lo)}; hi + lo carries h to about 22 bits.
-__device__ __noinline__ void stage_h(int xp, const float* hv, int n, uint16_t* sh, float2* chs)
-{
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int KD = n * xp;
-    uint16_t* hi = sh;
-    uint16_t* lo = sh + KD;
-    const int cpc = kChunk / xp;
-    const int lpc = cpc / 4;
-    #pragma unroll 1
-    for (int q0 = 0; q0 < n / 4; q0 += kThreads) {
-        const int q = q0 + tid;
-        float hs = 0.f, bs = 0.f;
-        if (q < n / 4) {
-            #pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                const int i = 4 * q + j;
-                const float v = hv[i];
-                hs += v;
-                if (xp == 1) {
-                    const float e = (i & 1) ? v * 0.0625f : v;
-                    const uint16_t hb = f2h(e);
-                    const uint16_t lb = f2h(e - h2f(hb));
-                    hi[pslot(i)] = hb;
-                    lo[pslot(i)] = lb;
-                    bs += h2f(hb) + h2f(lb);
-                } else {
-                    const uint16_t hb = f2h(v);
-                    const uint16_t lb = f2h(v - h2f(hb));
-                    hi[pslot(2 * i)] = hb;
-                    hi[pslot(2 * i + 1)] = hb;
-                    lo[pslot(2 * i)] = lb;
-                    lo[pslot(2 * i + 1)] = lb;
-                    bs += 2.f * (h2f(hb) + h2f(lb));
-                }
-            }
-        }
-        #pragma unroll 1
-        for (int o = lpc / 2; o; o >>= 1) {
-            hs += __shfl_xor_sync(0xffffffffu, hs, o);
-            bs += __shfl_xor_sync(0xffffffffu, bs, o);
-        }
-        if (q < n / 4 && (lane % lpc) == 0)
-            chs[4 * q / cpc] = make_float2(hs, 1024.f * bs);
-    }
-    __syncthreads();
-}
-
-// Poll n epoch-tagged pairs until all carry `epoch`; values -> dst (fp32). Block-uniform.
-__device__ __noinline__ bool poll_pairs(long long limit, int* status, const unsigned long long* src, int n,
-                                        uint32_t epoch, float* dst)
+// Warp-uniform wait for an mbarrier phase; false after the limit.
+__device__ __forceinline__ bool wait_warp(uint64_t* m, uint32_t parity, long long limit)
 {
     const long long t0 = cycles();
     while (true) {
-        int bad = 0;
-        #pragma unroll 1
-        for (int e = 2 * (int)threadIdx.x; e < n; e += 2 * kThreads) {
-            unsigned long long a, b;
-            ld_pair2(src + e, a, b);
-            bad |= (uint32_t)(a >> 32) != epoch;
-            dst[e] = __uint_as_float((uint32_t)a);
-            if (e + 1 < n) {
-                bad |= (uint32_t)(b >> 32) != epoch;
-                dst[e + 1] = __uint_as_float((uint32_t)b);
-            }
-        }
-        if (!__syncthreads_or(bad))
+        if (__all_sync(0xffffffffu, mbar_try(m, parity)))
             return true;
-        if (__syncthreads_or(threadIdx.x == 0 && cycles() - t0 > limit)) {
-            if (threadIdx.x == 0)
-                set_status(status, kStatusTimeout);
+        if (__any_sync(0xffffffffu, cycles() - t0 > limit))
             return false;
-        }
     }
 }
 
-// Grid barrier on a monotonically increasing counter (a multiple of the grid between launches).
-__device__ __noinline__ bool grid_barrier(const StepParams& P, const Ctx& C)
+// Poll n epoch-tagged pairs until each carries `epoch`; values -> dst (fp32). Each thread spins on
+// its own 16-byte pieces, so only stale pieces are read again. With `acquire`, the loads are
+// acquire loads: what a publisher stored before its pair is visible to this block afterwards.
+// Block-uniform.
+__device__ __forceinline__ bool poll_pairs(const unsigned long long* src, int n, uint32_t epoch, float* dst,
+                                        bool acquire, long long limit, int* status)
+{
+    const long long t0 = cycles();
+    bool ok = true;
+#pragma unroll 1
+    for (int e = 2 * TID; ok && e < n; e += 2 * kThreads) {
+        unsigned long long a, b;
+        while (true) {
+            if (acquire)
+                ld_acq_pair2(src + e, a, b);
+            else
+                ld_pair2(src + e, a, b);
+            if ((uint32_t)(a >> 32) == epoch && (e + 1 >= n || (uint32_t)(b >> 32) == epoch))
+                break;
+            if (cycles() - t0 > limit) {
+                ok = false;
+                break;
+            }
+        }
+        dst[e] = __uint_as_float((uint32_t)a);
+        if (e + 1 < n)
+            dst[e + 1] = __uint_as_float((uint32_t)b);
+    }
+    if (__syncthreads_or(!ok)) {
+        if (TID == 0)
+            set_status(status, kStatusTimeout);
+        return false;
+    }
+    return true;
+}
+
+// Output words of elements [4q, 4q + 4) once each holds `want` contributions; false after the
+// limit.
+__device__ __forceinline__ bool poll_out4(const long long* X, int q, int want, long long t0, long long limit, float4& y)
+{
+    long long a, b, c, d;
+    while (true) {
+        ld_s64x2(X + 4 * q, a, b);
+        ld_s64x2(X + 4 * q + 2, c, d);
+        if ((int)(a & 0xFF) == want && (int)(b & 0xFF) == want && (int)(c & 0xFF) == want && (int)(d & 0xFF) == want)
+            break;
+        if (cycles() - t0 > limit)
+            return false;
+    }
+    y = make_float4(__ll2float_rn(a >> kCountBits) * kFixInv, __ll2float_rn(b >> kCountBits) * kFixInv,
+                    __ll2float_rn(c >> kCountBits) * kFixInv, __ll2float_rn(d >> kCountBits) * kFixInv);
+    return true;
+}
+
+// One contribution v to output word p (count + 1, value in fixed point).
+__device__ __forceinline__ void add_out(long long* p, float v, int* status)
+{
+    long long fx = 0;
+    if (fabsf(v) < kFixMax)
+        fx = __float2ll_rn(v * kFix);
+    else
+        set_status(status, kStatusInvalid);
+    red_add_u64(p, (long long)((unsigned long long)fx << kCountBits) + 1);
+}
+
+// Launch-start barrier on a monotonically increasing counter (a multiple of the grid between
+// launches).
+__device__ __noinline__ bool grid_barrier(const StepParams& P, long long limit)
 {
     __syncthreads();
     int ok = 1;
@@ -633,7 +614,7 @@ __device__ __noinline__ bool grid_barrier(const StepParams& P, const Ctx& C)
             asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(P.bar) : "memory");
             if (v >= target)
                 break;
-            if (cycles() - t0 > limit_cycles(P)) {
+            if (cycles() - t0 > limit) {
                 ok = 0;
                 set_status(P.status, kStatusTimeout);
                 break;
@@ -644,87 +625,378 @@ __device__ __noinline__ bool grid_barrier(const StepParams& P, const Ctx& C)
 }
 
 // ------------------------------------------------------------------------------------------
-// the chunk work items
+// the GEMV tiles
 // ------------------------------------------------------------------------------------------
 
-__device__ __forceinline__ float bf16_at(const uint8_t* p) { return bf16f(*reinterpret_cast<const uint16_t*>(p)); }
-
-// One block of up to four chunks (one 128-byte column block) of staged rows. Rows [0, nstaged) of
-// the staged set are local rows rloc0 + R; chunk c0 + i starts at byte cbyte0 + 32 i of a staged
-// row. For every local row r < nrows it writes s * (sum q v) + b * (sum v), summed over the
-// chunks, to out[r * ostride], where v is u (gate/up rows) or h (down rows; kDown: B holds h's hi
-// parts in the even columns and lo parts in the odd ones). The B operands and chunk sums are
-// loaded once for all row tiles, and the four chunks of a tile run as independent MMA chains.
-template <bool kDown>
-__device__ __noinline__ void mma_block(const uint8_t* base, uint32_t swzmask, int width, int nstaged, int rloc0,
-                                          int nrows, int c0, int nch, int cbyte0, const uint16_t* bsrc, int KD,
-                                          const float2* csum, const uint8_t* sc, const uint8_t* bi, int sbrow,
-                                          float* out, int ostride, int gsh)
+// Tiles [t0, t1) (16 rows each) of one staged column block, of which rows [0, nvalid) are real: row
+// R at base + R * width. With swz = 7 the rows are 128-byte swizzled TMA rows (16-byte piece q of
+// a row at shared address bits 7..9 XOR q; the copy's destination is 1024-byte aligned); with
+// swz = 0 they are linear. Chunks c0 .. c0 + nch - 1 (nch <= 4) of the B operand start at byte
+// 32 (c - c0) of a row. For each real row R this writes out[R * ostride] = sum over the chunks (in
+// chunk order) of s * (sum q v) + b * (sum v), with v the activation: the B operand `bsrc`
+// (lo_off = 0: u, every column the same) or h (lo_off = KD: hi parts in the even columns, lo parts
+// at bsrc + KD in the odd ones). Scales: sc / bi + R * sbrow, one bf16 per group (a group is one
+// chunk at int4, two at int8: gsh). The column block's B fragments and chunk sums are loaded once
+// for all tiles; its chunks run as independent MMA chains. Rows g and g + 8 of every tile share one
+// swizzle key (a tile is 16 rows), so each thread's four piece offsets are fixed for the call.
+__device__ __forceinline__ void box_mma(const uint8_t* base, uint32_t swz, int width, int nvalid, int t0, int t1,
+                                        int c0, int nch, const uint16_t* bsrc, int lo_off, const float2* csum,
+                                        const uint8_t* sc, const uint8_t* bi, int sbrow, int gsh, float* out,
+                                        int ostride)
 {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
-    const uint16_t* bb = kDown ? bsrc + (size_t)(g & 1) * KD : bsrc;
-    const int ntile = (nstaged + 15) >> 4;
+    const uint16_t* bb = bsrc + (size_t)(g & 1) * lo_off;
+    const uint32_t b0 = smem_u32(base);
+    uint4 Bx[4], By[4];
+    float2 cs[4];
+    uint32_t off[4];
+    const uint32_t key = ((b0 >> 7) + (uint32_t)(t0 * 16 + g) * ((uint32_t)width >> 7)) & swz;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int cc = c0 + (c < nch ? c : 0);
+        const uint4* bp = reinterpret_cast<const uint4*>(bb + kChunk * cc + 16 * tq);
+        Bx[c] = bp[0];
+        By[c] = bp[1];
+        cs[c] = csum[cc];
+        off[c] = ((((uint32_t)(2 * c + (tq >> 1))) ^ key) << 4) | (uint32_t)(8 * (tq & 1));
+    }
+    const int nsc = 4 >> gsh;  // scale groups of the column block
 #pragma unroll 1
-    for (int tile = 0; tile < ntile; ++tile) {
+    for (int tile = t0; tile < t1; ++tile) {
         const int Ra = tile * 16 + g, Rb = Ra + 8;
         const int R = tq == 0 ? Ra : Rb;
-        const int r = rloc0 + R;
-        const bool mine = tq < 2 && R < nstaged && r < nrows;
-        float part = 0.f;
-#pragma unroll 1
-        for (int cp = 0; cp < 4; cp += 2) {  // two chunks at a time: two independent MMA chains
-            uint2 ra[2], rb[2];
-            uint4 B0[2], B1[2];
-            float sv[2], bv[2];
-            float2 cs[2];
+        const bool mine = tq < 2 && R < nvalid;
+        const uint32_t aa = b0 + (uint32_t)Ra * (uint32_t)width, ab = aa + 8u * (uint32_t)width;
+        uint2 ra[4], rb[4];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int cl = cp + h;
-                const bool on = cl < nch;
-                const int c = c0 + (on ? cl : 0);
-                const int byte = cbyte0 + 32 * cl + 8 * tq;
-                ra[h] = (on && Ra < nstaged) ? lds_a(base, swzmask, width, Ra, byte) : make_uint2(0, 0);
-                rb[h] = (on && Rb < nstaged) ? lds_a(base, swzmask, width, Rb, byte) : make_uint2(0, 0);
-                const uint4* bp = reinterpret_cast<const uint4*>(bb + kChunk * c + 16 * tq);
-                B0[h] = bp[0];
-                B1[h] = bp[1];
-                cs[h] = csum[c];
-                const int gi = c >> gsh;
-                sv[h] = (mine && on) ? bf16_at(sc + r * sbrow + 2 * gi) : 0.f;
-                bv[h] = (mine && on) ? bf16_at(bi + r * sbrow + 2 * gi) : 0.f;
-            }
+        for (int c = 0; c < 4; ++c) {
+            const bool on = c < nch;
+            ra[c] = (on && Ra < nvalid) ? lds64(aa + off[c]) : make_uint2(0, 0);
+            rb[c] = (on && Rb < nvalid) ? lds64(ab + off[c]) : make_uint2(0, 0);
+        }
+        // this thread's row's scales and biases of the column block's groups (4 at int4, 2 at int8)
+        float sv[4], bv[4];
+        {
+            const uint16_t* sp = reinterpret_cast<const uint16_t*>(sc + R * sbrow) + (c0 >> gsh);
+            const uint16_t* bp = reinterpret_cast<const uint16_t*>(bi + R * sbrow) + (c0 >> gsh);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float acc[4];
-                chunk_mma(acc, ra[h], rb[h], B0[h], B1[h]);
-                const float a = kDown ? (tq == 0 ? acc[0] + acc[1] : acc[2] + acc[3]) : (tq == 0 ? acc[0] : acc[2]);
-                part = fmaf(sv[h], a - cs[h].y, fmaf(bv[h], cs[h].x, part));
+            for (int q = 0; q < 4; ++q) {
+                const bool on = mine && q < nsc && (q << gsh) < nch;
+                sv[q] = on ? bf16f(sp[q]) : 0.f;
+                bv[q] = on ? bf16f(bp[q]) : 0.f;
             }
         }
+        float acc[4][4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+        // first 32 fields of each chunk, then the second 32: four independent chains
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t a[4], b[4];
+            deq8(ra[c].x, a);
+            deq8(rb[c].x, b);
+            mma_f16(acc[c], a[0], b[0], a[1], b[1], Bx[c].x, Bx[c].y);
+            mma_f16(acc[c], a[2], b[2], a[3], b[3], Bx[c].z, Bx[c].w);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t a[4], b[4];
+            deq8(ra[c].y, a);
+            deq8(rb[c].y, b);
+            mma_f16(acc[c], a[0], b[0], a[1], b[1], By[c].x, By[c].y);
+            mma_f16(acc[c], a[2], b[2], a[3], b[3], By[c].z, By[c].w);
+        }
+        float part = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float v = tq == 0 ? acc[c][0] : acc[c][2];
+            if (lo_off)
+                v += tq == 0 ? acc[c][1] : acc[c][3];
+            part = fmaf(sv[c >> gsh], v - cs[c].y, fmaf(bv[c >> gsh], cs[c].x, part));
+        }
         if (mine)
-            out[r * ostride] = part;
+            out[R * ostride] = part;
     }
+}
+
+// ------------------------------------------------------------------------------------------
+// layer input, u, h operands
+// ------------------------------------------------------------------------------------------
+
+// The B operand of a chunk: fp16 activations in the MMA's register order (pslot).
+
+// Eight fp16 B entries of elements [8o, 8o + 8) in pslot order (see put_b8): int4 at positions [8o, 8o + 8) in the order 0,4,1,5,2,6,3,7;
+// int8 (two fields per code) at [16o, 16o + 16).
+__device__ __forceinline__ void store_b8(uint16_t* __restrict__ bop, int xp, int o, const uint32_t (&hb)[8])
+{
+    if (xp == 1) {
+        reinterpret_cast<uint4*>(bop)[o] = make_uint4(hb[0] | (hb[4] << 16), hb[1] | (hb[5] << 16), hb[2] | (hb[6] << 16),
+                                                      hb[3] | (hb[7] << 16));
+    } else {
+        const uint32_t w0 = hb[0] | (hb[2] << 16), w1 = hb[1] | (hb[3] << 16), w2 = hb[4] | (hb[6] << 16),
+                       w3 = hb[5] | (hb[7] << 16);
+        reinterpret_cast<uint4*>(bop)[2 * o] = make_uint4(w0, w0, w1, w1);
+        reinterpret_cast<uint4*>(bop)[2 * o + 1] = make_uint4(w2, w2, w3, w3);
+    }
+}
+
+// The B operand entries of the eight activations v of elements [8o, 8o + 8) and their chunk-sum
+// contributions {sum v, sum B}. For int4 the odd fields of a code word enter A multiplied by 16,
+// so their activations are divided by 16; an int8 code is read as two fields (low, 16 x high),
+// both paired with the code's activation.
+__device__ __forceinline__ float2 put_b8(uint16_t* __restrict__ bop, int xp, int o, const float (&v)[8])
+{
+    float us = 0.f, bs = 0.f;
+    uint32_t hb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        us += v[j];
+        hb[j] = f2h((xp == 1 && (j & 1)) ? v[j] * 0.0625f : v[j]);
+        bs += h2f((uint16_t)hb[j]);
+    }
+    store_b8(bop, xp, o, hb);
+    return make_float2(us, xp == 1 ? bs : 2.f * bs);
+}
+
+// Chunk sums of a chunk whose elements are held by lpc consecutive lanes.
+__device__ __forceinline__ float2 chunk_reduce(float2 v, int lpc)
+{
+#pragma unroll 1
+    for (int o = lpc / 2; o; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    }
+    return v;
+}
+
+// Layer input of a step. When the previous step exists, waits for its output words (want
+// contributions each) and forms its output xo = (x if residual) + y. x becomes xo, or the next
+// token's input x_in (fp32, or bf16 bits) when `fresh`. Block 0 writes xo to out_prev (the
+// previous token's output, when non-null) and to trace_prev, and x to trace_cur. Then u =
+// bf16(x / rms(x)) (norm), bf16(x) (from_x) or the bf16 input bits as given, its B operand and
+// chunk sums. Each thread takes 8 consecutive elements. Block-uniform; false (status set) after
+// the limit.
+__device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev, int want, bool residual, bool fresh,
+                                            const void* x_in, bool in_f32, bool from_x, bool norm, float* out_prev,
+                                            float* trace_prev, float* trace_cur, long long limit, int* status)
+{
+    const int H = C.H, xp = C.xp, n8 = H / 8;
+    float4* __restrict__ sx = reinterpret_cast<float4*>(C.sx);
+    uint16_t* __restrict__ su = C.su;
+    uint16_t* __restrict__ bop = C.sup;
+    float2* __restrict__ scs = C.scs;
+    float* __restrict__ red = C.red;
+    const bool w0 = CTA == 0;
+    const long long t0 = cycles();
+    bool ok = true;
+    float ss = 0.f;
+    float4 k0 = make_float4(0.f, 0.f, 0.f, 0.f), k1 = k0;
+#pragma unroll 1
+    for (int o = TID; o < n8; o += kThreads) {
+        float4 x0 = sx[2 * o], x1 = sx[2 * o + 1];
+        if (Xprev) {
+            float4 y0, y1;
+            if (!poll_out4(Xprev, 2 * o, want, t0, limit, y0) || !poll_out4(Xprev, 2 * o + 1, want, t0, limit, y1)) {
+                ok = false;
+                break;
+            }
+            if (residual) {
+                x0 = make_float4(x0.x + y0.x, x0.y + y0.y, x0.z + y0.z, x0.w + y0.w);
+                x1 = make_float4(x1.x + y1.x, x1.y + y1.y, x1.z + y1.z, x1.w + y1.w);
+            } else {
+                x0 = y0;
+                x1 = y1;
+            }
+            if (w0 && out_prev) {
+                reinterpret_cast<float4*>(out_prev)[2 * o] = x0;
+                reinterpret_cast<float4*>(out_prev)[2 * o + 1] = x1;
+            }
+            if (w0 && trace_prev) {
+                reinterpret_cast<float4*>(trace_prev)[2 * o] = x0;
+                reinterpret_cast<float4*>(trace_prev)[2 * o + 1] = x1;
+            }
+        }
+        if (fresh) {
+            if (in_f32) {
+                x0 = reinterpret_cast<const float4*>(x_in)[2 * o];
+                x1 = reinterpret_cast<const float4*>(x_in)[2 * o + 1];
+            } else {
+                const uint4 bits = reinterpret_cast<const uint4*>(x_in)[o];
+                x0 = make_float4(bf16f((uint16_t)bits.x), bf16f((uint16_t)(bits.x >> 16)), bf16f((uint16_t)bits.y),
+                                 bf16f((uint16_t)(bits.y >> 16)));
+                x1 = make_float4(bf16f((uint16_t)bits.z), bf16f((uint16_t)(bits.z >> 16)), bf16f((uint16_t)bits.w),
+                                 bf16f((uint16_t)(bits.w >> 16)));
+            }
+        }
+        sx[2 * o] = x0;
+        sx[2 * o + 1] = x1;
+        if (w0 && trace_cur) {
+            reinterpret_cast<float4*>(trace_cur)[2 * o] = x0;
+            reinterpret_cast<float4*>(trace_cur)[2 * o + 1] = x1;
+        }
+        ss = fmaf(x0.x, x0.x, fmaf(x0.y, x0.y, fmaf(x0.z, x0.z, fmaf(x0.w, x0.w, ss))));
+        ss = fmaf(x1.x, x1.x, fmaf(x1.y, x1.y, fmaf(x1.z, x1.z, fmaf(x1.w, x1.w, ss))));
+        if (o == TID) {
+            k0 = x0;
+            k1 = x1;
+        }
+    }
+    if (__syncthreads_or(!ok)) {
+        if (TID == 0)
+            set_status(status, kStatusTimeout);
+        return false;
+    }
+    float rinv = 1.f;
+    if (norm) {
+        ss = warp_sum(ss);
+        if ((TID & 31) == 0)
+            red[TID >> 5] = ss;
+        __syncthreads();
+        const float4* r4 = reinterpret_cast<const float4*>(red);
+        const float4 a = r4[0], b = r4[1], c = r4[2], d = r4[3];
+        const float tot = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w)) + ((c.x + c.y) + (c.z + c.w)) +
+                          ((d.x + d.y) + (d.z + d.w));
+        rinv = rsqrtf(tot * C.invH + 1e-6f);
+    }
+    const int lpc = 8 / xp;  // lanes per chunk (a chunk is 64 fields)
+    // every lane of a warp runs every iteration: the chunk sums are shuffled across lanes
+#pragma unroll 1
+    for (int o0 = 0; o0 < n8; o0 += kThreads) {
+        const int o = o0 + TID;
+        const bool on = o < n8;
+        float2 part = make_float2(0.f, 0.f);
+        if (on) {
+            float4 x0 = k0, x1 = k1;
+            if (o != TID) {
+                x0 = sx[2 * o];
+                x1 = sx[2 * o + 1];
+            }
+            uint16_t ub[8];
+            if (from_x) {
+                const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    ub[j] = f2bf(xs[j] * rinv);
+            } else {
+                const uint4 bits = reinterpret_cast<const uint4*>(x_in)[o];
+                const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    ub[2 * j] = (uint16_t)bw[j];
+                    ub[2 * j + 1] = (uint16_t)(bw[j] >> 16);
+                }
+            }
+            reinterpret_cast<uint4*>(su)[o] =
+                make_uint4((uint32_t)ub[0] | ((uint32_t)ub[1] << 16), (uint32_t)ub[2] | ((uint32_t)ub[3] << 16),
+                           (uint32_t)ub[4] | ((uint32_t)ub[5] << 16), (uint32_t)ub[6] | ((uint32_t)ub[7] << 16));
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = bf16f(ub[j]);
+            part = put_b8(bop, xp, o, v);
+        }
+        const float2 cs = chunk_reduce(part, lpc);
+        if (on && o % lpc == 0)
+            scs[o / lpc] = make_float2(cs.x, 1024.f * cs.y);
+    }
+    __syncthreads();
+    return true;
+}
+
+// h values hv[0, n) -> B operand hi/lo parts (sh: [2][n * xp]) and per chunk {sum of h, 1024 *
+// sum of (hi + lo)}; hi + lo carries h to about 22 bits. Each thread takes 8 consecutive values.
+__device__ __forceinline__ void stage_h(int xp, const float* __restrict__ hv, int n, uint16_t* __restrict__ sh,
+                                        float2* __restrict__ chs)
+{
+    const int n8 = n / 8, lpc = 8 / xp;
+    uint16_t* __restrict__ hi = sh;
+    uint16_t* __restrict__ lo = sh + n * xp;
+    // every lane of a warp runs every iteration: the chunk sums are shuffled across lanes
+#pragma unroll 1
+    for (int o0 = 0; o0 < n8; o0 += kThreads) {
+        const int o = o0 + TID;
+        const bool on = o < n8;
+        float hs = 0.f, bs = 0.f;
+        if (on) {
+            const float4 a = reinterpret_cast<const float4*>(hv)[2 * o], b = reinterpret_cast<const float4*>(hv)[2 * o + 1];
+            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t hb[8], lb[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                hs += v[j];
+                const float e = (xp == 1 && (j & 1)) ? v[j] * 0.0625f : v[j];
+                hb[j] = f2h(e);
+                lb[j] = f2h(e - h2f((uint16_t)hb[j]));
+                bs += h2f((uint16_t)hb[j]) + h2f((uint16_t)lb[j]);
+            }
+            if (xp == 2)
+                bs *= 2.f;
+            store_b8(hi, xp, o, hb);
+            store_b8(lo, xp, o, lb);
+        }
+        const float2 cs = chunk_reduce(make_float2(hs, bs), lpc);
+        if (on && o % lpc == 0)
+            chs[o / lpc] = make_float2(cs.x, 1024.f * cs.y);
+    }
+    __syncthreads();
 }
 
 // ------------------------------------------------------------------------------------------
 // routing
 // ------------------------------------------------------------------------------------------
 
-// slg (logits) -> sel_idx / sel_w (rank order: larger fp32 logit first, ties -> lower index).
-// Each warp ranks its 32 logits; the largest of the warps' k-th best values is a lower bound of
-// the overall k-th best, so only logits at or above it (usually little more than k) take part in
-// the final ranking.
-__device__ void topk_select(const StepParams& P, const Ctx& C, int my_slot)
+// This block's router rows -> logits, published as epoch-tagged pairs. Each row's dot product is
+// cut into kRouterParts fixed parts (one warp each, lane-strided bf16 FMAs, butterfly sum) added
+// in part order, so a logit does not depend on the grid. `bias`: this thread's logit bias (thread
+// r < rows holds row r's).
+__device__ __forceinline__ void router_rows(const Ctx& C, unsigned long long* xlog, uint32_t epoch, float bias)
+{
+    const int nr = C.e1 - C.e0, H = C.H, e0 = C.e0;
+    const uint16_t* __restrict__ srt = C.srt;
+    const uint16_t* __restrict__ su = C.su;
+    float* __restrict__ rp = C.rp;
+    const int nv = H / 8;  // 16-byte vectors per row
+#pragma unroll 1
+    for (int it = WARP; it < nr * kRouterParts; it += kWarps) {
+        const int r = it / kRouterParts, p = it - r * kRouterParts;
+        const uint16_t* row = srt + (size_t)r * H;
+        const int v1 = part(nv, kRouterParts, p + 1);
+        float acc = 0.f;
+#pragma unroll 2
+        for (int v = part(nv, kRouterParts, p) + LANE; v < v1; v += 32)
+            acc = dot8_bf16(*reinterpret_cast<const uint4*>(row + 8 * v), *reinterpret_cast<const uint4*>(su + 8 * v),
+                            acc);
+        acc = warp_sum(acc);
+        if (LANE == 0)
+            rp[it] = acc;
+    }
+    __syncthreads();
+    if (TID < nr) {
+        const float4 p4 = reinterpret_cast<const float4*>(rp)[TID];
+        st_pair(xlog + e0 + TID, epoch, (((p4.x + p4.y) + p4.z) + p4.w) + bias);
+    }
+}
+
+// slg (logits) -> sel_idx / sel_w / sel_slot (rank order: larger fp32 logit first, equal logits ->
+// lower index). Each warp ranks its 32 logits (31 shuffles; equal keys go to the lower lane, i.e.
+// the lower index) and lists its top-k in rank order; warp 0 then merges the sorted lists: k
+// rounds, each taking the largest list head (a warp max reduction; equal heads go to the lower
+// list, i.e. the lower index). my_slot: the pool slot of this thread's expert (thread e holds
+// expert e).
+__device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, int my_slot)
 {
     const int E = C.E, k = C.k;
+    const float* __restrict__ slg = C.slg;
+    uint2* __restrict__ cand = reinterpret_cast<uint2*>(C.tk);            // [kWarps][kMaxK] (key, index)
+    int* __restrict__ slot_of = reinterpret_cast<int*>(C.tk) + 2 * kWarps * kMaxK;  // [kMaxE]
+    const int e = TID;
+    const bool valid = e < E;
+    const uint32_t key = valid ? ord_key(slg[e]) : 0u;  // finite logits map to keys > 0
     const int nl = (E + 31) / 32;
-    uint32_t* wkth = C.lkey;                 // [kWarps] k-th best key of each warp
-    uint32_t* skey = C.lkey + kWarps;        // [E] survivors
-    int* sidx = C.lidx;                      // [E]
-    int* wcnt = C.lidx + kMaxE + 8;          // [kWarps] survivors per warp
-    const int e = 32 * WARP + LANE;
-    const uint32_t key = (WARP < nl && e < E) ? ord_key(C.slg[e]) : 0u;
+    if (valid)
+        slot_of[e] = my_slot;
     if (WARP < nl) {
         int rank = 0;
 #pragma unroll
@@ -733,324 +1005,149 @@ __device__ void topk_select(const StepParams& P, const Ctx& C, int my_slot)
             const uint32_t o = __shfl_sync(0xffffffffu, key, src);
             rank += (o > key) || (o == key && src < LANE);
         }
-        const unsigned kth = __ballot_sync(0xffffffffu, rank == k - 1);
-        const uint32_t kv = __shfl_sync(0xffffffffu, key, kth ? __ffs(kth) - 1 : 0);
-        if (LANE == 0)
-            wkth[WARP] = kth ? kv : 0u;
-    }
-    __syncthreads();
-    uint32_t t0 = 0;
-#pragma unroll 1
-    for (int w = 0; w < nl; ++w)
-        t0 = max(t0, wkth[w]);
-    const bool surv = WARP < nl && e < E && key >= t0;
-    const unsigned bal = __ballot_sync(0xffffffffu, surv);
-    if (LANE == 0)
-        wcnt[WARP] = __popc(bal);
-    __syncthreads();
-    int pos = 0, ns = 0;
-#pragma unroll 1
-    for (int w = 0; w < kWarps; ++w) {
-        const int c = wcnt[w];
-        pos += w < WARP ? c : 0;
-        ns += c;
-    }
-    if (surv) {
-        const int p = pos + __popc(bal & ((1u << LANE) - 1u));
-        skey[p] = key;
-        sidx[p] = e;
-    }
-    __syncthreads();
-    if (TID >= ns && TID < ((ns + 3) & ~3)) {  // pad the survivor list to a multiple of 4
-        skey[TID] = 0u;
-        sidx[TID] = 0x7fffffff;
-    }
-    __syncthreads();
-    if (surv) {
-        int rank = 0;
-        const uint4* k4 = reinterpret_cast<const uint4*>(skey);
-        const int4* i4 = reinterpret_cast<const int4*>(sidx);
-#pragma unroll 4
-        for (int i = 0; i < (ns + 3) >> 2; ++i) {
-            const uint4 kk = k4[i];
-            const int4 ii = i4[i];
-            rank += (kk.x > key || (kk.x == key && ii.x < e)) + (kk.y > key || (kk.y == key && ii.y < e)) +
-                    (kk.z > key || (kk.z == key && ii.z < e)) + (kk.w > key || (kk.w == key && ii.w < e));
-        }
-        if (rank < k) {
-            C.sel_idx[rank] = e;
-            C.sel_slot[rank] = my_slot;
-        }
+        if (rank < k)  // lanes past E carry key 0: they pad a short list
+            cand[WARP * kMaxK + rank] = make_uint2(key, (uint32_t)e);
     }
     __syncthreads();
     if (WARP == 0) {
-        const float lmax = C.slg[C.sel_idx[0]];
-        const float p = LANE < k ? __expf(C.slg[C.sel_idx[LANE]] - lmax) : 0.f;
-        float denom = 0.f;
-        if (P.flags & kRenorm) {
-            #pragma unroll 1
-            for (int j = 0; j < k; ++j)
-                denom += __shfl_sync(0xffffffffu, p, j);
-        } else {
-            float s = 0.f;
-            #pragma unroll 1
-            for (int e = LANE; e < E; e += 32)
-                s += __expf(C.slg[e] - lmax);
-            denom = __shfl_sync(0xffffffffu, warp_sum(s), 0);
+        int ptr = 0;
+        uint2 head = LANE < nl ? cand[LANE * kMaxK] : make_uint2(0u, 0u);
+        float lsel = 0.f, lmax = 0.f;
+        int isel = 0;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, head.x);
+            const unsigned eq = __ballot_sync(0xffffffffu, LANE < nl && head.x == mx);
+            const int win = __ffs(eq) - 1;
+            const int ei = __shfl_sync(0xffffffffu, (int)head.y, win);
+            if (LANE == j)
+                isel = ei;
+            if (LANE == win) {
+                ++ptr;
+                head = ptr < k ? cand[LANE * kMaxK + ptr] : make_uint2(0u, 0u);
+            }
         }
         if (LANE < k)
-            C.sel_w[LANE] = __fdividef(p, denom);
+            lsel = slg[isel];
+        lmax = __shfl_sync(0xffffffffu, lsel, 0);
+        const float pj = LANE < k ? __expf(lsel - lmax) : 0.f;
+        float denom;
+        if (renorm) {
+            denom = warp_sum(pj);
+        } else {
+            float sum = 0.f;
+#pragma unroll 1
+            for (int e2 = LANE; e2 < E; e2 += 32)
+                sum += __expf(slg[e2] - lmax);
+            denom = warp_sum(sum);
+        }
+        if (LANE < k) {
+            C.sel_idx[LANE] = isel;
+            C.sel_w[LANE] = __fdividef(pj, denom);
+            C.sel_slot[LANE] = slot_of[isel];
+        }
     }
     __syncthreads();
-}
-
-// ------------------------------------------------------------------------------------------
-// routed stages
-// ------------------------------------------------------------------------------------------
-
-struct Routed {
-    int j;                 // expert rank served by this block
-    const uint8_t* blob;   // its blob (null: not resident)
-    int slot;
-    int r0, r1;            // own gate/up rows
-    int d0, d1;            // own down rows
-    uint32_t off[6];       // offsets of the staged scale spans: gate.s, gate.b, up.s, up.b, down.s, down.b
-};
-
-// Stage s of the block's routed work -> TMA box into ring slot (s % kWarps).
-__device__ __noinline__ void issue_stage(const StepParams& P, const Ctx& C, int wslot, int r0, int d0, int s)
-{
-    const StageGeo& sg = C.sg;
-    uint8_t* dst = C.ring + (size_t)(s % kWarps) * sg.slot_bytes;
-    uint64_t* m = C.mbar + (s % kWarps);
-    if (s < sg.n_gu) {
-        const int rc = s % sg.nrc_gu, q = s / sg.nrc_gu, mat = q & 1, cb = q >> 1;
-        mbar_expect(m, (uint32_t)sg.SR * sg.cbw_gu);
-        tma3d(dst, &P.tmap[mat], cb * sg.cbw_gu, r0 + rc * sg.SR, wslot, m);
-    } else {
-        const int sd = s - sg.n_gu, rc = sd % sg.nrc_d, cb = sd / sg.nrc_d;
-        mbar_expect(m, (uint32_t)sg.SR * sg.cbw_d);
-        tma3d(dst, &P.tmap[2], cb * sg.cbw_d, d0 + rc * sg.SR, wslot, m);
-    }
-}
-
-// Wait for ring slot `slot` to complete phase `parity` (warp-uniform; false after the limit).
-__device__ __noinline__ bool wait_slot(const StepParams& P, const Ctx& C, int slot, uint32_t parity)
-{
-    const long long t0 = cycles();
-    while (true) {
-        if (__all_sync(0xffffffffu, mbar_try(C.mbar + slot, parity)))
-            return true;
-        if (__any_sync(0xffffffffu, cycles() - t0 > limit_cycles(P)))
-            return false;
-    }
-}
-
-// Block-uniform wait for a block-level mbarrier (all threads).
-__device__ __noinline__ bool wait_block(const StepParams& P, const Ctx& C, uint64_t* m, uint32_t parity)
-{
-    const long long t0 = cycles();
-    while (true) {
-        const int ok = mbar_try(m, parity);
-        if (__syncthreads_and(ok))
-            return true;
-        if (timed_out(P, t0))
-            return false;
-    }
 }
 
 }  // namespace
 
-// Dynamic shared memory of the fused kernel: the plan plus 1024 bytes to align the ring.
-__host__ __device__ uint32_t decode_smem_bytes(const StepParams& P, int grid)
+// Dynamic shared memory of the fused kernel: the plan plus 1024 bytes to align the staging slots.
+__host__ __device__ uint32_t decode_smem_bytes(const StepParams& P)
 {
-    return smem_plan(P.H, P.E, P.k, P.I, P.Is, P.bits, grid).total + 1024;
+    return smem_plan(P.H, P.E, P.k, P.I, P.Is, P.bits, P.sg).total + 1024;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_constant__ StepParams P)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const SmemPlan plan0 = smem_plan(P.H, P.E, P.k, P.I, P.Is, P.bits, GRID);
-    Ctx& C = *reinterpret_cast<Ctx*>(base + plan0.ctx);
+    Ctx& C = *reinterpret_cast<Ctx*>(base);  // the plan puts the context first
     if (TID == 0)
         make_ctx(P, C, base);
     __syncthreads();
-    const StageGeo& sg = C.sg;
+    const StageGeo& sg = P.sg;
     const bool route = P.mode != kModeExperts;
     const bool experts = P.mode != kModeRoute;
-    const int n_steps = P.n_tokens * P.n_layers;
+    const bool prenorm = (P.flags & kPrenorm) != 0;
+    const bool residual = (P.flags & kResidual) != 0;
+    const int n_steps = P.mode == kModeFull ? P.n_tokens * P.n_layers : 1;
+    const long long limit = (long long)(2 * P.timeout_ns);
+    const int H = C.H, K = C.k, hdim = xh_stride(C.I, C.Is);
+    // warps with side duties: the issuing thread is lane 0 of warp 0 (routed copies) and of warp
+    // kWarps - 1 (the next step's dense rows); the output words are cleared by warp kWarps - 2
+    constexpr int kIssueWarp = kWarps - 1, kClearWarp = kWarps - 2;
 
     if (TID == 0) {
-        #pragma unroll
+#pragma unroll 1
         for (int i = 0; i < kNumMbar; ++i)
             mbar_init(C.mbar + i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (experts)
-            #pragma unroll
+#pragma unroll 1
             for (int i = 0; i < 3; ++i)
                 prefetch_map(&P.tmap[i]);
-    }
-    __syncthreads();
-
-    // phase counters of the mbarriers (uniform in the block / warp)
-    uint32_t ph_dense = 0, ph_sdown = 0, ph_rsc = 0, ph_slot = 0;
-    bool dense_pending = false, sdown_pending = false, rsc_pending = false;
-    int slot_pending = 0;  // this warp's issued-but-unconsumed stages (at most one per slot)
-
-    if (TID == 0) {
         const LayerDesc L0 = P.layers[P.layer0];
         issue_dense(P, C, L0, route, experts);
         if (experts)
-            issue_shared_down(P, C, L0);
+            issue_sdown(P, C, L0);
     }
-    dense_pending = true;
-    sdown_pending = experts;
-
-    const DenseRows drow = dense_rows(C);
-    bool ok = true;
-
-    // X init for token 0: this block's slice of the accumulator holds the residual base
-    if (experts) {
-        const bool residual = (P.flags & kResidual) != 0;
-        #pragma unroll 1
-        for (int o = drow.o0 + TID; o < drow.o1; o += kThreads) {
-            float x0 = 0.f;
-            if (residual)
-                x0 = (P.flags & kPrenorm) ? ((const float*)P.x_in)[o] : bf16f(((const uint16_t*)P.x_in)[o]);
-            st_s64(P.xacc + o, (long long)__float2ll_rn(x0 * kFix));
-        }
-        ok = grid_barrier(P, C);
+    // this block's slice of the first step's output words starts at zero
+    if (experts && WARP == kClearWarp) {
+#pragma unroll 1
+        for (int o = C.o0 + LANE; o < C.o1; o += 32)
+            st_s64(P.xacc + o, 0);
+        fence_gpu();
     }
 
-    #pragma unroll 1
+    // mbarrier phases (block-uniform)
+    uint32_t ph_dense = 0, ph_sdown = 0, ph_rsc = 0, ph_down = 0, ph_gu = 0;  // ph_gu: bit 2s + m
+    bool dense_pending = true, sdown_pending = experts, rsc_pending = false, down_pending = false;
+    uint32_t gu_pending = 0;
+
+    bool ok = grid_barrier(P, limit);
+
+#pragma unroll 1
     for (int step = 0; ok && step < n_steps; ++step) {
         const int t = step / P.n_layers, li = step - t * P.n_layers;
         const int l = P.layer0 + li;
         const LayerDesc L = P.layers[l];
-        // this thread's expert's slot, loaded now so that it is in a register by the time top-k
-        // names the experts (the thread of logit e is thread e)
-        const int my_slot = (route && TID < C.E) ? P.table[(size_t)l * C.E + TID] : -1;
+        const LayerDesc Ln = P.layers[P.layer0 + (step + 1) % P.n_layers];
+        // this thread's expert's slot and this thread's router row's bias, loaded now so that they
+        // are in registers by the time they are needed
+        const int my_slot = (P.mode == kModeFull && TID < C.E) ? P.table[(size_t)l * C.E + TID] : -1;
+        const float bias = (route && L.logit_bias && TID < C.e1 - C.e0) ? __ldg(L.logit_bias + C.e0 + TID) : 0.f;
         const uint32_t epoch = P.epoch0 + (uint32_t)step;
-        long long* X = P.xacc + (size_t)(step & 1) * C.H;
-        const bool prenorm = (P.flags & kPrenorm) != 0;
+        long long* X = P.xacc + (size_t)(step & 1) * H;
 
-        // ---------------- 1. layer input ----------------
-        if (li == 0) {
-            if (prenorm) {
-                const float* src = (const float*)P.x_in + (size_t)t * C.H;
-                #pragma unroll 1
-                for (int i = TID; i < C.H; i += kThreads)
-                    C.sx[i] = src[i];
-            } else {
-                const uint16_t* src = (const uint16_t*)P.x_in + (size_t)t * C.H;
-                #pragma unroll 1
-                for (int i = TID; i < C.H; i += kThreads)
-                    C.sx[i] = bf16f(src[i]);
-            }
-            __syncthreads();
+        // ---------------- 1. layer input, u ----------------
+        {
+            const bool fresh = li == 0;
+            const size_t trow = (size_t)P.n_layers + 1;
+            float* tr_prev = (step > 0 && fresh && P.trace) ? P.trace + ((size_t)(t - 1) * trow + P.n_layers) * H : nullptr;
+            float* tr_cur = P.trace ? P.trace + ((size_t)t * trow + li) * H : nullptr;
+            const bool in_f32 = prenorm;
+            const char* xin = (const char*)P.x_in + (size_t)t * H * (in_f32 ? 4 : 2);
+            if (!(ok = layer_input(C, (step > 0 && experts) ? P.xacc + (size_t)((step - 1) & 1) * H : nullptr, K + 1,
+                                   residual, fresh, xin, in_f32, prenorm || li > 0, prenorm,
+                                   (step > 0 && fresh) ? P.y_out + (size_t)(t - 1) * H : nullptr, tr_prev, tr_cur,
+                                   limit, P.status)))
+                break;
         }
-        if (P.trace && CTA == 0)
-            #pragma unroll 1
-            for (int i = TID; i < C.H; i += kThreads)
-                P.trace[((size_t)t * (P.n_layers + 1) + li) * C.H + i] = C.sx[i];
-        make_u(P, C, prenorm, (const uint16_t*)P.x_in + (size_t)t * C.H);
 
-        // ---------------- 2. router rows, gamma, shared gate/up ----------------
-        if (!wait_block(P, C, C.mbar + kWarps + 1, ph_dense & 1)) {
-            ok = false;
+        // ---------------- 2. router rows -> logits ----------------
+        if (!(ok = wait_block(C.mbar + kMbDense, ph_dense & 1, limit, P.status)))
             break;
-        }
         ++ph_dense;
         dense_pending = false;
         if (route) {
-            const int nr = drow.e1 - drow.e0;
-            #pragma unroll 1
-            for (int r = WARP; r < nr; r += kWarps) {
-                const uint16_t* row = C.srt + (size_t)r * C.H;
-                float acc = 0.f;
-                #pragma unroll 1
-                for (int i = 0; i < C.H / 256; ++i) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(row + 256 * i + 8 * LANE);
-                    const uint4 x = *reinterpret_cast<const uint4*>(C.su + 256 * i + 8 * LANE);
-                    acc = dot8_bf16(w, x, acc);
-                }
-                acc = warp_sum(acc);
-                if (LANE == 0) {
-                    const int e = drow.e0 + r;
-                    if (L.logit_bias)
-                        acc += __ldg(L.logit_bias + e);
-                    st_pair(P.xlog + e, epoch, acc);
-                }
-            }
-        }
-        if (experts) {
-            if (WARP == kWarps - 1) {
-                float z = 0.f;
-                #pragma unroll 1
-                for (int i = 0; i < C.H / 256; ++i) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(C.swsg + 256 * i + 8 * LANE);
-                    const uint4 x = *reinterpret_cast<const uint4*>(C.su + 256 * i + 8 * LANE);
-                    z = dot8_bf16(w, x, z);
-                }
-                z = warp_sum(z);
-                if (LANE == 0)
-                    C.misc[0] = __fdividef(1.f, 1.f + __expf(-z));
-            }
-            // shared gate/up rows [s0, s1): one item per (matrix, 128-byte column block)
-            const int ns = drow.s1 - drow.s0;
-            const int ncb = sg.ncb_gu;
-            if (ns > 0) {
-                #pragma unroll 1
-                for (int it = WARP; it < 2 * ncb; it += kWarps) {
-                    const int m = it / ncb, cb = it - m * ncb;
-                    const uint8_t* q = C.sgq + (size_t)m * sg.Rs * C.rb_gu;
-                    const uint8_t* sc = C.ssb + (2 * m) * C.span_sgu + C.imisc[2 * m];
-                    const uint8_t* bi = C.ssb + (2 * m + 1) * C.span_sgu + C.imisc[2 * m + 1];
-                    const int c0 = cb * 4;
-                    mma_block<false>(q, 0u, C.rb_gu, ns, 0, ns, c0, min(4, C.NCu - c0), cb * kCb, C.sup, 0, C.scs, sc,
-                                     bi, C.ngu * 2, C.sp + m * ncb + cb, 2 * ncb, C.xp - 1);
-                }
-            }
-            __syncthreads();
-            if (TID < ns) {
-                const float* pg = C.sp + TID * 2 * ncb;
-                float gg = 0.f, vv = 0.f;
-                #pragma unroll 1
-                for (int cb = 0; cb < ncb; ++cb) {
-                    gg += pg[cb];
-                    vv += pg[ncb + cb];
-                }
-                const float h = __fdividef(gg, 1.f + __expf(-gg)) * vv;
-                st_pair(P.xh + (size_t)C.k * xh_stride(C.I, C.Is) + drow.s0 + TID, epoch, h);
-            }
-        }
-        __syncthreads();
-        if (experts && TID == 0) {
-            // this block's step flag, after a gpu-scope fence: every store of the block so far,
-            // the accumulator base included, is visible to whoever sees the flag
-            fence_gpu();
-            st_pair(P.xh + (size_t)C.k * xh_stride(C.I, C.Is) + C.Is + CTA, epoch, 0.f);
-        }
-        // next step's router rows, shared gate vector and shared gate/up rows
-        if (step + 1 < n_steps) {
-            if (TID == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                const int ln = P.layer0 + (step + 1) % P.n_layers;
-                issue_dense(P, C, P.layers[ln], route, experts);
-            }
-            dense_pending = true;
-        }
-
-        // ---------------- 3. routing ----------------
-        if (route) {
-            if (!poll_pairs(limit_cycles(P), P.status, P.xlog, C.E, epoch, C.slg)) {
-                ok = false;
+            router_rows(C, P.xlog, epoch, bias);
+            // ---------------- 3. top-k ----------------
+            if (!(ok = poll_pairs(P.xlog, C.E, epoch, C.slg, false, limit, P.status)))
                 break;
-            }
-            topk_select(P, C, my_slot);
-            if (CTA == 0 && TID < C.k) {
-                const size_t o = ((size_t)t * P.n_layers + li) * C.k + TID;
+            topk_select(C, (P.flags & kRenorm) != 0, my_slot);
+            if (CTA == 0 && TID < K) {
+                const size_t o = ((size_t)t * P.n_layers + li) * K + TID;
                 if (P.topk_idx)
                     P.topk_idx[o] = C.sel_idx[TID];
                 if (P.topk_w)
@@ -1058,294 +1155,263 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             }
             if (!experts)
                 break;  // a route-only launch has one step
-            if (TID < C.k && C.sel_slot[TID] < 0)
+            if (TID < K && C.sel_slot[TID] < 0)
                 set_status(P.status, kStatusNotResident);
-        } else if (TID < C.k) {
-            C.sel_w[TID] = P.topk_w[TID];
-            C.sel_slot[TID] = P.slots[TID];
-            C.sel_idx[TID] = -1;
-        }
-        __syncthreads();
-
-        // ---------------- 4. routed work of this block: issue its boxes ----------------
-        Routed W;
-        {
-            W.j = grp_of(CTA, GRID, C.k);
-            const int gs0 = grp_start(W.j, GRID, C.k), gs1 = grp_start(W.j + 1, GRID, C.k);
-            const int n = gs1 - gs0, mi = CTA - gs0;
-            W.slot = C.sel_slot[W.j];
-            W.blob = W.slot >= 0 ? P.arena + (uint64_t)W.slot * P.stride : nullptr;
-            W.r0 = part(C.I, n, mi);
-            W.r1 = part(C.I, n, mi + 1);
-            W.d0 = part(C.H, n, mi);
-            W.d1 = part(C.H, n, mi + 1);
-        }
-        if (W.blob) {
-            if (WARP == 0 && LANE == 0) {
-                // scale / bias rows of the block's gate/up rows and down rows
-                uint64_t* m = C.mbar + kWarps;
-                const BlobGeo& geo = C.geo;
-                uint32_t bytes = 0;
-                #pragma unroll 1
-                for (int i = 0; i < 6; ++i) {
-                    const bool dn = i >= 4;
-                    const uint64_t sec = (i & 1) ? geo.b_off[i >> 1] : geo.s_off[i >> 1];
-                    bytes += span_bytes(W.blob + sec, dn ? W.d0 : W.r0, dn ? W.d1 : W.r1, dn ? C.ngd * 2 : C.ngu * 2);
-                }
-                mbar_expect(m, bytes);
-                #pragma unroll 1
-                for (int i = 0; i < 6; ++i) {
-                    const bool dn = i >= 4;
-                    uint8_t* dst = dn ? C.rdsb + (i - 4) * C.span_d : C.rsb + i * C.span_gu;
-                    uint32_t off;
-                    const uint64_t sec = (i & 1) ? geo.b_off[i >> 1] : geo.s_off[i >> 1];
-                    copy_rows(dst, W.blob + sec, dn ? W.d0 : W.r0, dn ? W.d1 : W.r1, dn ? C.ngd * 2 : C.ngu * 2, m, &off);
-                    C.imisc[8 + i] = (int)off;
-                }
+        } else {
+            if (TID < K) {
+                C.sel_w[TID] = P.topk_w[TID];
+                C.sel_slot[TID] = P.slots[TID];
+                C.sel_idx[TID] = -1;
             }
-            rsc_pending = true;
-            if (LANE == 0 && WARP < sg.n_stages) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue_stage(P, C, W.slot, W.r0, W.d0, WARP);
-            }
-            if (WARP < sg.n_stages)
-                slot_pending = 1;
+            __syncthreads();
         }
 
-        // ---------------- 5. shared expert down rows ----------------
-        float* hval = C.hv;
-        // the shared h values and every block's step flag: past this point the accumulator bases of all
-        // blocks (stored at the end of the previous step, before their flag's fence) are visible
-        if (!poll_pairs(limit_cycles(P), P.status, P.xh + (size_t)C.k * xh_stride(C.I, C.Is), C.Is + GRID, epoch, hval)) {
-            ok = false;
-            break;
+        // ---------------- 4. this block's routed bytes, all issued now ----------------
+        const int rslot = C.sel_slot[C.j];
+        const bool blob = rslot >= 0;
+        const bool have_gu = blob && C.r1 > C.r0, have_d = blob && C.d1 > C.d0;
+        if (blob && TID == 0) {
+            fence_async_smem();
+            issue_routed(P, C, rslot);
         }
-        stage_h(C.xp, hval, C.Is, C.shs, C.chs);
-        if (!wait_block(P, C, C.mbar + kWarps + 2, ph_sdown & 1)) {
-            ok = false;
-            break;
-        }
-        ++ph_sdown;
-        sdown_pending = false;
+        rsc_pending = blob;
+        down_pending = have_d;
+        if (have_gu)
+            gu_pending = (1u << (2 * sg.nslot_gu)) - 1u;
+
+        // ---------------- 5. shared expert, next step's dense rows ----------------
         {
-            const int nd = drow.o1 - drow.o0;
-            const int ncb = (C.NCds + 3) / 4;
-            const uint8_t* sc = C.sdsb + C.imisc[4];
-            const uint8_t* bi = C.sdsb + C.span_sd + C.imisc[5];
-            if (nd > 0)
-                #pragma unroll 1
-                for (int cb = WARP; cb < ncb; cb += kWarps)
-                    mma_block<true>(C.sdq, 0u, C.rb_ds, nd, 0, nd, 4 * cb, min(4, C.NCds - 4 * cb), cb * kCb, C.shs,
-                                    C.KDs, C.chs, sc, bi, C.ngds * 2, C.spd + cb, ncb, C.xp - 1);
+            // gamma = sigmoid(w_sg . u): one warp
+            if (WARP == 1) {
+                float z = 0.f;
+#pragma unroll 2
+                for (int v = LANE; v < H / 8; v += 32)
+                    z = dot8_bf16(*reinterpret_cast<const uint4*>(C.swsg + 8 * v),
+                                  *reinterpret_cast<const uint4*>(C.su + 8 * v), z);
+                z = warp_sum(z);
+                if (LANE == 0)
+                    C.misc[0] = __fdividef(1.f, 1.f + __expf(-z));
+            }
+            // shared gate/up rows [s0, s1): items (matrix, column block, tile)
+            const int ns = C.s1 - C.s0;
+            const int ncb = sg.ncb_gu, nt = cdiv(ns, 16);
+            const int cpb = sg.cbw_gu / 32;
+#pragma unroll 1
+            for (int it = WARP; ns > 0 && it < 2 * ncb; it += kWarps) {
+                const int m = it / ncb, cb = it - m * ncb;
+                const int c0 = cb * cpb;
+                box_mma(C.sgq + (size_t)m * sg.Rs * C.rb_gu + cb * kCb, 0u, C.rb_gu, ns, 0, nt, c0,
+                        imin(cpb, C.NCu - c0), C.sup, 0, C.scs, C.ssb + (2 * m) * C.span_sgu + C.imisc[2 * m],
+                        C.ssb + (2 * m + 1) * C.span_sgu + C.imisc[2 * m + 1], C.ngu * 2, C.xp - 1,
+                        C.sp + m * ncb + cb, 2 * ncb);
+            }
+            __syncthreads();
+            if (TID < ns) {
+                const float* pg = C.sp + TID * 2 * ncb;
+                float gg = 0.f, vv = 0.f;
+#pragma unroll 4
+                for (int cb = 0; cb < ncb; ++cb) {
+                    gg += pg[cb];
+                    vv += pg[ncb + cb];
+                }
+                st_pair(P.xh + (size_t)K * hdim + C.s0 + TID, epoch, __fdividef(gg, 1.f + __expf(-gg)) * vv);
+            }
+            // the router rows, gate vector and shared gate/up rows are consumed: the next step's
+            if (step + 1 < n_steps && WARP == kIssueWarp && LANE == 0) {
+                fence_async_smem();
+                issue_dense(P, C, Ln, route, experts);
+            }
+            dense_pending = step + 1 < n_steps;
+            // the shared expert's h, then its down rows [o0, o1)
+            if (!(ok = poll_pairs(P.xh + (size_t)K * hdim, C.Is, epoch, C.hv, true, limit, P.status)))
+                break;
+            // every block has read the previous step's output words (it published h_shared after):
+            // clear this block's slice of them for the next step, and order that before this
+            // warp's later stores
+            if (step + 1 < n_steps && WARP == kClearWarp) {
+#pragma unroll 1
+                for (int o = C.o0 + LANE; o < C.o1; o += 32)
+                    st_s64(P.xacc + (size_t)((step + 1) & 1) * H + o, 0);
+                fence_gpu();
+            }
+            stage_h(C.xp, C.hv, C.Is, C.shs, C.chs);
+            if (!(ok = wait_block(C.mbar + kMbSdown, ph_sdown & 1, limit, P.status)))
+                break;
+            ++ph_sdown;
+            sdown_pending = false;
+            const int nd = C.o1 - C.o0, ntd = cdiv(nd, 16);
+            const int cw = imin(kCb, C.rb_ds), cpd = cw / 32;
+#pragma unroll 1
+            for (int it = WARP; nd > 0 && it < C.ncb_ds; it += kWarps) {
+                const int cb = it, c0 = cb * cpd;
+                box_mma(C.sdq + cb * kCb, 0u, C.rb_ds, nd, 0, ntd, c0, imin(cpd, C.NCds - c0), C.shs, C.KDs,
+                        C.chs, C.sdsb + C.imisc[4], C.sdsb + C.span_sd + C.imisc[5], C.ngds * 2, C.xp - 1, C.spd + cb,
+                        C.ncb_ds);
+            }
             __syncthreads();
             if (TID < nd) {
                 float ys = 0.f;
-                #pragma unroll 1
-                for (int cb = 0; cb < ncb; ++cb)
-                    ys += C.spd[TID * ncb + cb];
-                const float v = C.misc[0] * ys;
-                fence_gpu();  // after the shared h pairs: every block's accumulator base is in place
-                if (!(fabsf(v) < kFixMax))
-                    set_status(P.status, kStatusInvalid);
-                else
-                    red_add_s64(X + drow.o0 + TID, (long long)__float2ll_rn(v * kFix));
+#pragma unroll 1
+                for (int cb = 0; cb < C.ncb_ds; ++cb)
+                    ys += C.spd[TID * C.ncb_ds + cb];
+                add_out(X + C.o0 + TID, C.misc[0] * ys, P.status);
             }
             __syncthreads();
-        }
-        if (step + 1 < n_steps) {
-            if (TID == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue_shared_down(P, C, P.layers[P.layer0 + (step + 1) % P.n_layers]);
+            if (step + 1 < n_steps && WARP == kIssueWarp) {
+                if (LANE == 0) {
+                    fence_async_smem();
+                    issue_sdown(P, C, Ln);
+                }
             }
-            sdown_pending = true;
+            sdown_pending = step + 1 < n_steps;
         }
 
         // ---------------- 6. routed gate/up -> h_j ----------------
-        const int own = W.r1 - W.r0, own_d = W.d1 - W.d0;
-        if (W.blob) {
-            if (!wait_block(P, C, C.mbar + kWarps, ph_rsc & 1)) {
-                ok = false;
+        if (blob) {
+            if (!(ok = wait_block(C.mbar + kMbRsc, ph_rsc & 1, limit, P.status)))
                 break;
-            }
             ++ph_rsc;
             rsc_pending = false;
+        }
+        if (have_gu) {
+            const int nrc = cdiv(C.r1 - C.r0, sg.bh_gu), cpb = sg.cbw_gu / 32;
+            const int per_m = nrc * sg.cpg_gu;  // items per matrix of a column group: (row box, column block)
             bool wok = true;
-            // every warp works through its gate/up stages (s = warp, warp + 16, ...)
-            #pragma unroll 1
-            for (int s = WARP; s < sg.n_gu; s += kWarps) {
-                if (!wait_slot(P, C, WARP, ph_slot & 1)) {
-                    wok = false;
+#pragma unroll 1
+            for (int cg = 0; cg < sg.ncs_gu; ++cg) {
+                const int sl = cg % sg.nslot_gu;
+#pragma unroll 1
+                for (int it = WARP; wok && it < 2 * per_m; it += kWarps) {
+                    const int m = it >= per_m, q = it - m * per_m;
+                    const int cbl = q % sg.cpg_gu, rc = q / sg.cpg_gu;
+                    const int cb = cg * sg.cpg_gu + cbl;
+                    const int nvalid = imin(sg.bh_gu, C.r1 - C.r0 - rc * sg.bh_gu);
+                    if (cb >= sg.ncb_gu)
+                        continue;
+                    if (!(wok = wait_warp(C.mbar + 2 * sl + m, (ph_gu >> (2 * sl + m)) & 1, limit)))
+                        break;
+                    const int c0 = cb * cpb;
+                    box_mma(gu_copy_at(C, sg, sl, m, rc) + (size_t)cbl * sg.bh_gu * sg.cbw_gu, sg.swz_gu ? 7u : 0u,
+                            sg.cbw_gu, nvalid, 0, cdiv(nvalid, 16), c0, imin(cpb, C.NCu - c0), C.sup, 0, C.scs,
+                            C.rsb + (2 * m) * C.span_gu + C.imisc[8 + 2 * m] + rc * sg.bh_gu * C.ngu * 2,
+                            C.rsb + (2 * m + 1) * C.span_gu + C.imisc[9 + 2 * m] + rc * sg.bh_gu * C.ngu * 2, C.ngu * 2,
+                            C.xp - 1, C.sp + (rc * sg.bh_gu) * 2 * sg.ncb_gu + m * sg.ncb_gu + cb, 2 * sg.ncb_gu);
+                }
+                if (__syncthreads_or(!wok)) {
+                    if (TID == 0)
+                        set_status(P.status, kStatusTimeout);
+                    ok = false;
                     break;
                 }
-                ++ph_slot;
-                slot_pending = 0;
-                const uint8_t* slotp = C.ring + (size_t)WARP * sg.slot_bytes;
-                const int rc = s % sg.nrc_gu, q = s / sg.nrc_gu, m = q & 1, cb = q >> 1;
-                const int rloc0 = rc * sg.SR;
-                const int nstaged = min(sg.SR, own - rloc0);
-                const uint8_t* sc = C.rsb + (2 * m) * C.span_gu + C.imisc[8 + 2 * m];
-                const uint8_t* bi = C.rsb + (2 * m + 1) * C.span_gu + C.imisc[8 + 2 * m + 1];
-                const int cpb = sg.cbw_gu / 32;  // chunks per column block
-                const int c0 = cb * cpb;
-                if (nstaged > 0 && c0 < C.NCu)
-                    mma_block<false>(slotp, sg.swz_gu ? 7u : 0u, sg.cbw_gu, nstaged, rloc0, own, c0, min(cpb, C.NCu - c0), 0,
-                                     C.sup, 0, C.scs, sc, bi, C.ngu * 2, C.sp + m * sg.ncb_gu + cb, 2 * sg.ncb_gu, C.xp - 1);
-                __syncwarp();
-                const int s2 = s + kWarps;
-                if (s2 < sg.n_stages) {
-                    if (LANE == 0) {
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        issue_stage(P, C, W.slot, W.r0, W.d0, s2);
+                ph_gu ^= 3u << (2 * sl);
+                gu_pending &= ~(3u << (2 * sl));
+                // slot sl is free again: its next column group (when the groups take turns)
+                if (cg + sg.nslot_gu < sg.ncs_gu) {
+                    if (TID == 0) {
+                        fence_async_smem();
+                        issue_gu_group(P, C, rslot, cg + sg.nslot_gu, sl);
                     }
-                    slot_pending = 1;
+                    gu_pending |= 3u << (2 * sl);
                 }
             }
-            if (__syncthreads_or(!wok)) {
-                set_status(P.status, kStatusTimeout);
-                ok = false;
+            if (!ok)
                 break;
-            }
         }
         __syncthreads();
-        {
-            const int hdim = xh_stride(C.I, C.Is);
-            unsigned long long* xh = P.xh + (size_t)W.j * hdim;
-            if (TID < own) {
-                float h = 0.f;
-                if (W.blob) {
-                    const int ncb = sg.ncb_gu;
-                    const float* pg = C.sp + TID * 2 * ncb;
-                    float gg = 0.f, vv = 0.f;
-                    #pragma unroll 1
-                    for (int cb = 0; cb < ncb; ++cb) {
-                        gg += pg[cb];
-                        vv += pg[ncb + cb];
-                    }
-                    h = __fdividef(gg, 1.f + __expf(-gg)) * vv;
+        unsigned long long* xh = P.xh + (size_t)C.j * hdim;
+#pragma unroll 1
+        for (int r = TID; r < C.r1 - C.r0; r += kThreads) {
+            float h = 0.f;
+            if (blob) {
+                const int ncb = sg.ncb_gu;
+                const float* pg = C.sp + r * 2 * ncb;
+                float gg = 0.f, vv = 0.f;
+#pragma unroll 4
+                for (int cb = 0; cb < ncb; ++cb) {
+                    gg += pg[cb];
+                    vv += pg[ncb + cb];
                 }
-                st_pair(xh + W.r0 + TID, epoch, h);
+                h = __fdividef(gg, 1.f + __expf(-gg)) * vv;
             }
-            __syncthreads();
-            // ---------------- 7. the group's h_j, down rows ----------------
-            if (!poll_pairs(limit_cycles(P), P.status, xh, C.I, epoch, hval)) {
-                ok = false;
-                break;
-            }
+            st_pair(xh + C.r0 + r, epoch, h);
         }
-        if (W.blob) {
-            stage_h(C.xp, hval, C.I, C.shj, C.chj);
-            bool wok = true;
-            const int s_first = sg.n_gu + ((WARP - sg.n_gu % kWarps + kWarps) % kWarps);
-            #pragma unroll 1
-            for (int s = s_first; s < sg.n_stages; s += kWarps) {
-                if (!wait_slot(P, C, WARP, ph_slot & 1)) {
-                    wok = false;
+
+        // ---------------- 7. the group's h_j, down rows, contributions ----------------
+        if (C.d1 > C.d0) {
+            if (!(ok = poll_pairs(xh, C.I, epoch, C.hv, false, limit, P.status)))
+                break;
+            if (have_d) {
+                stage_h(C.xp, C.hv, C.I, C.shj, C.chj);
+                const int nrc = cdiv(C.d1 - C.d0, sg.bh_d), tb = cdiv(sg.bh_d, 16), cpd = sg.cbw_d / 32;
+                // items (row box, column block, group of tpi tiles), about one per warp
+                const int tpi = cdiv(nrc * sg.cpg_d * tb, kWarps), ntg = cdiv(tb, tpi);
+                bool wok = true;
+#pragma unroll 1
+                for (int it = WARP; it < nrc * sg.cpg_d * ntg; it += kWarps) {
+                    const int tg = it % ntg, q = it / ntg, cb = q % sg.cpg_d, rc = q / sg.cpg_d;
+                    const int nvalid = imin(sg.bh_d, C.d1 - C.d0 - rc * sg.bh_d);
+                    const int tt0 = tg * tpi, tt1 = imin(tt0 + tpi, cdiv(nvalid, 16));
+                    if (tt0 >= tt1)
+                        continue;
+                    if (!(wok = wait_warp(C.mbar + kMbDown, ph_down & 1, limit)))
+                        break;
+                    const int c0 = cb * cpd;
+                    box_mma(d_copy_at(C, sg, rc) + (size_t)cb * sg.bh_d * sg.cbw_d, sg.swz_d ? 7u : 0u, sg.cbw_d, nvalid,
+                            tt0, tt1, c0, imin(cpd, C.NCd - c0), C.shj, C.KD, C.chj,
+                            C.rdsb + C.imisc[12] + rc * sg.bh_d * C.ngd * 2,
+                            C.rdsb + C.span_d + C.imisc[13] + rc * sg.bh_d * C.ngd * 2, C.ngd * 2, C.xp - 1,
+                            C.spd + (rc * sg.bh_d) * sg.ncb_d + cb, sg.ncb_d);
+                }
+                if (__syncthreads_or(!wok)) {
+                    if (TID == 0)
+                        set_status(P.status, kStatusTimeout);
+                    ok = false;
                     break;
                 }
-                ++ph_slot;
-                slot_pending = 0;
-                const uint8_t* slotp = C.ring + (size_t)WARP * sg.slot_bytes;
-                const int sd = s - sg.n_gu, rc = sd % sg.nrc_d, cb = sd / sg.nrc_d;
-                const int rloc0 = rc * sg.SR;
-                const int nstaged = min(sg.SR, own_d - rloc0);
-                const uint8_t* sc = C.rdsb + C.imisc[12];
-                const uint8_t* bi = C.rdsb + C.span_d + C.imisc[13];
-                const int cpb = sg.cbw_d / 32;
-                const int c0 = cb * cpb;
-                if (nstaged > 0 && c0 < C.NCd)
-                    mma_block<true>(slotp, sg.swz_d ? 7u : 0u, sg.cbw_d, nstaged, rloc0, own_d, c0, min(cpb, C.NCd - c0), 0,
-                                    C.shj, C.KD, C.chj, sc, bi, C.ngd * 2, C.spd + cb, sg.ncb_d, C.xp - 1);
-                __syncwarp();
-                const int s2 = s + kWarps;
-                if (s2 < sg.n_stages) {
-                    if (LANE == 0) {
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        issue_stage(P, C, W.slot, W.r0, W.d0, s2);
-                    }
-                    slot_pending = 1;
-                }
+                ++ph_down;
+                down_pending = false;
             }
-            if (__syncthreads_or(!wok)) {
-                set_status(P.status, kStatusTimeout);
-                ok = false;
-                break;
-            }
-            // ---------------- 8. weighted contributions ----------------
-            if (TID < own_d) {
+#pragma unroll 1
+            for (int r = TID; r < C.d1 - C.d0; r += kThreads) {
                 float yj = 0.f;
-                #pragma unroll 1
-                for (int cb = 0; cb < sg.ncb_d; ++cb)
-                    yj += C.spd[TID * sg.ncb_d + cb];
-                const float v = C.sel_w[W.j] * yj;
-                fence_gpu();
-                if (!(fabsf(v) < kFixMax))
-                    set_status(P.status, kStatusInvalid);
-                else
-                    red_add_s64(X + W.d0 + TID, (long long)__float2ll_rn(v * kFix));
+                if (have_d)
+#pragma unroll 1
+                    for (int cb = 0; cb < sg.ncb_d; ++cb)
+                        yj += C.spd[r * sg.ncb_d + cb];
+                add_out(X + C.d0 + r, C.sel_w[C.j] * yj, P.status);
             }
-        }
-
-        const bool last_of_token = li == P.n_layers - 1;
-
-        // ---------------- 9. layer output ----------------
-        if (!grid_barrier(P, C)) {
-            ok = false;
-            break;
-        }
-        #pragma unroll 1
-        for (int o = 2 * TID; o < C.H; o += 2 * kThreads) {
-            long long a, b;
-            ld_s64x2(X + o, a, b);
-            C.sx[o] = __ll2float_rn(a) * kFixInv;
-            C.sx[o + 1] = __ll2float_rn(b) * kFixInv;
         }
         __syncthreads();
-        // The next step's accumulator starts from this block's slice of its fp32 input: this
-        // layer's output (same token) or the next token's input. These stores reach the other
-        // blocks before any of their atomic adds of the next step: the shared-expert h pairs that
-        // every block waits for are written after a gpu-scope fence (step 2).
-        if (step + 1 < n_steps) {
-            long long* Xn = P.xacc + (size_t)((step + 1) & 1) * C.H;
-            const bool residual = (P.flags & kResidual) != 0;
-            #pragma unroll 1
-            for (int o = drow.o0 + TID; o < drow.o1; o += kThreads) {
-                float x0 = 0.f;
-                if (!last_of_token)
-                    x0 = C.sx[o];
-                else if (residual)
-                    x0 = prenorm ? ((const float*)P.x_in)[(size_t)(t + 1) * C.H + o]
-                                 : bf16f(((const uint16_t*)P.x_in)[(size_t)(t + 1) * C.H + o]);
-                st_s64(Xn + o, (long long)__float2ll_rn(x0 * kFix));
-            }
-        }
-        if (last_of_token) {
-            #pragma unroll 1
-            for (int o = drow.o0 + TID; o < drow.o1; o += kThreads)
-                P.y_out[(size_t)t * C.H + o] = C.sx[o];
-            if (P.trace)
-                #pragma unroll 1
-                for (int o = drow.o0 + TID; o < drow.o1; o += kThreads)
-                    P.trace[((size_t)t * (P.n_layers + 1) + P.n_layers) * C.H + o] = C.sx[o];
-        }
+    }
+
+    // the last step's output
+    if (ok && experts) {
+        const int s = n_steps - 1, t = s / P.n_layers;
+        ok = layer_input(C, P.xacc + (size_t)(s & 1) * H, K + 1, residual, false, nullptr, false, true, false,
+                         P.y_out + (size_t)t * H,
+                         P.trace ? P.trace + ((size_t)t * (P.n_layers + 1) + P.n_layers) * H : nullptr, nullptr, limit,
+                         P.status);
     }
 
     // drain: copies still in flight into this block's shared memory finish before it exits
-    {
+    if (TID == 0) {
         const long long t0 = cycles();
         auto drain = [&](uint64_t* m, uint32_t parity) {
-            while (!mbar_try(m, parity) && cycles() - t0 < 4 * limit_cycles(P)) {
+            while (!mbar_try(m, parity) && cycles() - t0 < 4 * limit) {
             }
         };
-        if (LANE == 0 && slot_pending)
-            drain(C.mbar + WARP, ph_slot & 1);
-        if (TID == 0) {
-            if (dense_pending)
-                drain(C.mbar + kWarps + 1, ph_dense & 1);
-            if (sdown_pending)
-                drain(C.mbar + kWarps + 2, ph_sdown & 1);
-            if (rsc_pending)
-                drain(C.mbar + kWarps, ph_rsc & 1);
-        }
+#pragma unroll 1
+        for (int i = 0; i < 2 * kMaxGuSlots; ++i)
+            if (gu_pending & (1u << i))
+                drain(C.mbar + i, (ph_gu >> i) & 1);
+        if (rsc_pending)
+            drain(C.mbar + kMbRsc, ph_rsc & 1);
+        if (down_pending)
+            drain(C.mbar + kMbDown, ph_down & 1);
+        if (dense_pending)
+            drain(C.mbar + kMbDense, ph_dense & 1);
+        if (sdown_pending)
+            drain(C.mbar + kMbSdown, ph_sdown & 1);
     }
 }
 

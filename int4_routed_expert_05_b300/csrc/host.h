@@ -30,9 +30,11 @@ inline EncodeTiledFn encode_tiled_fn()
     return fn;
 }
 
-// The three code sections (gate.q, up.q, down.q) of every blob of an arena of n_slots blobs as 3D
-// byte tensors [slots][rows][row bytes]; boxes of SR rows by one column block, 128-byte swizzled
-// when rows are at least 128 bytes wide. Returns 0 or a CUresult (-1: no driver entry point).
+// The three code sections (gate.q, up.q, down.q) of every blob of an arena of n_slots blobs as 4D
+// byte tensors: (byte in a column block, row, column block, slot) with strides (row bytes, column
+// block bytes, blob stride); a box is the decode kernel's copy of bh rows by cpg column blocks,
+// 128-byte swizzled when rows are at least 128 bytes wide. Returns 0 or a CUresult (-1: no driver
+// entry point).
 inline int encode_arena_maps(CUtensorMap (&maps)[3], const uint8_t* arena, int n_slots, const BlobGeo& geo,
                              const StageGeo& sg)
 {
@@ -41,12 +43,14 @@ inline int encode_arena_maps(CUtensorMap (&maps)[3], const uint8_t* arena, int n
         return -1;
     for (int m = 0; m < 3; ++m) {
         const bool dn = m == 2;
-        const cuuint64_t dims[3] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)geo.rows[m], (cuuint64_t)n_slots};
-        const cuuint64_t strides[2] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)geo.stride};
-        const cuuint32_t box[3] = {(cuuint32_t)(dn ? sg.cbw_d : sg.cbw_gu), (cuuint32_t)sg.SR, 1};
-        const cuuint32_t es[3] = {1, 1, 1};
+        const int cbw = dn ? sg.cbw_d : sg.cbw_gu, ncb = dn ? sg.ncb_d : sg.ncb_gu;
+        const cuuint64_t dims[4] = {(cuuint64_t)cbw, (cuuint64_t)geo.rows[m], (cuuint64_t)ncb, (cuuint64_t)n_slots};
+        const cuuint64_t strides[3] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)cbw, (cuuint64_t)geo.stride};
+        const cuuint32_t box[4] = {(cuuint32_t)cbw, (cuuint32_t)(dn ? sg.bh_d : sg.bh_gu),
+                                   (cuuint32_t)(dn ? sg.cpg_d : sg.cpg_gu), 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
         const CUtensorMapSwizzle swz = (dn ? sg.swz_d : sg.swz_gu) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-        const CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, (void*)(arena + geo.q_off[m]), dims, strides,
+        const CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, (void*)(arena + geo.q_off[m]), dims, strides,
                               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS)
@@ -99,17 +103,26 @@ inline int encode_tiles16(CUtensorMap* map, const void* ptr, int cols, int rows,
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
-// Shapes the fused kernel takes: the staging plan must fit in shared memory and the grid must
-// hold at least one block per routed expert. Returns the dynamic shared memory bytes, 0 if not.
-inline uint32_t fused_smem_bytes(int H, int E, int k, int I, int Is, int bits, int grid, int smem_optin)
+// Staging plan of the fused kernel for a shape on `grid` blocks (one per SM): every routed byte of
+// a block fetched at once when that fits in shared memory, else the gate/up rows in column groups
+// that take turns in fewer slots. Returns the dynamic shared memory bytes and the geometry in *sg,
+// or 0 when the shape cannot be staged (grid smaller than top_k, or too little shared memory).
+inline uint32_t plan_decode(int H, int E, int k, int I, int Is, int bits, int grid, int smem_optin, StageGeo* sg)
 {
-    if (grid < k)
+    if (grid < k || grid > kMaxGrid)
         return 0;
-    const StageGeo sg = stage_geo(H, E, k, I, Is, bits, grid);
-    if (sg.SR > kMaxBoxRows)
-        return 0;
-    const uint32_t bytes = smem_plan(H, E, k, I, Is, bits, grid).total + 1024;
-    return bytes <= (uint32_t)smem_optin ? bytes : 0;
+    for (int ncs = 1; ncs <= 16; ncs *= 2)
+        for (int nslot = ncs; nslot >= 1; nslot /= 2) {
+            const StageGeo g = stage_geo(H, E, k, I, Is, bits, grid, ncs, nslot);
+            if (g.nslot_gu > kMaxGuSlots || g.ncs_gu != ncs)
+                continue;
+            const uint32_t bytes = smem_plan(H, E, k, I, Is, bits, g).total + 1024;
+            if (bytes <= (uint32_t)smem_optin) {
+                *sg = g;
+                return bytes;
+            }
+        }
+    return 0;
 }
 
 // Epochs of the exchange buffers: a launch of n steps takes [epoch0, epoch0 + n). When the 32-bit

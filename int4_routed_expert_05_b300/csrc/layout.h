@@ -1,5 +1,5 @@
 // layout.h -- blob geometry, launch parameters, work split and shared-memory plan of the decode
-// kernels.
+// kernel.
 //
 // Blob format (one expert = one contiguous blob fetched at arena + slot * stride; paotong.dev
 // commentary on Swiftlet, the fixed-stride .qpack container): sections gate.q | up.q | down.q |
@@ -25,18 +25,24 @@ constexpr int kThreads = 512;   // threads per block of the fused decode kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxK = 16;       // top-k limit
 constexpr int kMaxE = 512;      // experts per layer limit
-constexpr int kChunk = 64;      // nibbles per MMA chunk (one int4 quantisation group)
+constexpr int kChunk = 64;      // 4-bit fields per MMA chunk (one int4 quantisation group)
 constexpr int kCb = 128;        // bytes of one staged column block (the 128-byte swizzle span)
 constexpr int kMaxBoxRows = 256;
 constexpr uint64_t kStrideAlign = 4096;
 constexpr int kMaxGrid = 512;   // most blocks a decode launch may have (one per SM)
+constexpr int kRouterParts = 4; // a router row's dot product is cut into this many fixed parts
 
-// Row stride (in pairs) of the h exchange buffer: rows 0..k-1 hold the routed experts' h, row k the
-// shared expert's h followed by one step flag per block.
-MOE_HD int xh_stride(int I, int Is) { return I > Is + kMaxGrid ? I : Is + kMaxGrid; }
-constexpr float kFix = 4294967296.f;       // fixed-point scale of the output accumulator (2^32)
+// Row stride (in pairs) of the h exchange buffer: rows 0..k-1 hold the routed experts' h, row k
+// the shared expert's.
+MOE_HD int xh_stride(int I, int Is) { return I > Is ? I : Is; }
+
+// Output words: each of the k + 1 expert contributions to output element o adds
+// (round(v * 2^32) << 8) + 1 to word o, so the low byte counts the contributions that have
+// landed and the upper 56 bits hold their exact fixed-point sum, whatever the arrival order.
+constexpr float kFix = 4294967296.f;       // 2^32
 constexpr float kFixInv = 2.3283064365386963e-10f;
-constexpr float kFixMax = 1073741824.f;    // largest |contribution| accepted (2^30)
+constexpr float kFixMax = 4194304.f;       // largest |contribution| accepted (2^22)
+constexpr int kCountBits = 8;
 
 // device status codes (same values as moe_status)
 constexpr int kStatusInvalid = 1;
@@ -103,33 +109,49 @@ MOE_HD int part(int n, int parts, int i) { return (int)(((unsigned)n * (unsigned
 MOE_HD int grp_of(int b, int G, int k) { return (int)(((unsigned)b * (unsigned)k) / (unsigned)G); }
 MOE_HD int grp_start(int j, int G, int k) { return (int)(((unsigned)j * (unsigned)G + (unsigned)k - 1u) / (unsigned)k); }
 MOE_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
+MOE_HD int imin(int a, int b) { return a < b ? a : b; }
+MOE_HD int imax(int a, int b) { return a > b ? a : b; }
 
-// How one block's share of the routed experts is staged: row ranges of gate/up and down rows
-// are fetched as TMA boxes of SR rows x one 128-byte column block (or the whole row when a row
-// is narrower), one box per stage, through a ring of kWarps slots.
+// How one block's share of a routed expert is staged. Block i of an expert's group owns gate/up
+// rows [i * SRgu, (i + 1) * SRgu) and down rows [i * SRd, (i + 1) * SRd), clipped to the matrix.
+// They are fetched by a few large tensor copies: a copy is a box of bh rows by cpg column blocks
+// (a column block is 128 bytes, 128-byte swizzled, or the whole row when rows are narrower) and
+// lands as [column block][row][column-block bytes]. Rows a box reads beyond the block's range lie
+// past the end of the matrix (zero-filled by the copy engine, no memory traffic), because SRgu
+// and SRd are whole multiples of the box heights. Gate and up rows are fetched in ncs_gu column
+// groups; a slot holds the gate and the up copies of one group, and with fewer slots than groups
+// (nslot_gu < ncs_gu) the groups take turns (a slot is refilled once the block is done with it).
+// Down rows are fetched all at once.
 struct StageGeo {
-    int SR;              // box rows
-    int nrc_gu, nrc_d;   // row chunks of a block's gate/up rows / down rows
-    int ncb_gu, ncb_d;   // column blocks per gate/up row / down row
-    int cbw_gu, cbw_d;   // bytes per column block
-    int swz_gu, swz_d;   // 1: 128-byte swizzled boxes, 0: linear boxes
-    int n_gu, n_stages;  // gate/up stages, all stages
-    int Rgu, Rd;         // most gate/up rows / down rows one block owns
-    int Rr, Rs, Rsd;     // most router rows, shared gate/up rows, shared down rows per block
-    uint32_t slot_bytes; // one ring slot (1024-byte multiple)
+    int SRgu, SRd;         // gate/up rows and down rows per block of a group
+    int bh_gu, bh_d;       // box rows (<= 256)
+    int nr_gu, nr_d;       // boxes along the rows: SRgu = nr_gu * bh_gu, SRd = nr_d * bh_d
+    int cbw_gu, cbw_d;     // bytes per column block
+    int swz_gu, swz_d;     // 1: 128-byte swizzled boxes, 0: linear boxes
+    int ncb_gu, ncb_d;     // column blocks per gate/up row / down row
+    int cpg_gu, cpg_d;     // column blocks per copy
+    int ncs_gu, ncs_d;     // column groups
+    int nslot_gu;          // gate/up column-group slots
+    uint32_t gu_copy;      // shared-memory bytes of one gate (or up) copy, 1024-aligned
+    uint32_t d_copy;       // shared-memory bytes of one down copy, 1024-aligned
+    int Rr, Rs, Rsd;       // most router rows, shared gate/up rows, shared down rows per block
 };
 
-MOE_HD StageGeo stage_geo(int H, int E, int k, int I, int Is, int bits, int G)
+MOE_HD uint32_t align1k(uint32_t v) { return (v + 1023u) & ~1023u; }
+
+// ncs_gu / nslot_gu: column groups and slots of the gate/up rows (1 / 1 fetches every gate/up
+// byte of the block at once).
+MOE_HD StageGeo stage_geo(int H, int E, int k, int I, int Is, int bits, int G, int ncs_gu, int nslot_gu)
 {
     StageGeo s{};
-    const int nmin = G / k;  // smallest group
-    s.Rgu = cdiv(I, nmin);
-    s.Rd = cdiv(H, nmin);
-    s.SR = s.Rgu < kMaxBoxRows ? s.Rgu : kMaxBoxRows;
-    if (s.SR < 1)
-        s.SR = 1;
-    s.nrc_gu = cdiv(s.Rgu, s.SR);
-    s.nrc_d = cdiv(s.Rd, s.SR);
+    const int nmin = imax(1, G / k);  // smallest group
+    const int rgu = cdiv(I, nmin), rd = cdiv(H, nmin);
+    s.nr_gu = cdiv(rgu, kMaxBoxRows);
+    s.bh_gu = cdiv(rgu, s.nr_gu);
+    s.SRgu = s.nr_gu * s.bh_gu;
+    s.nr_d = cdiv(rd, kMaxBoxRows);
+    s.bh_d = cdiv(rd, s.nr_d);
+    s.SRd = s.nr_d * s.bh_d;
     const int rb_gu = H * bits / 8, rb_d = I * bits / 8;
     s.swz_gu = rb_gu >= kCb;
     s.swz_d = rb_d >= kCb;
@@ -137,13 +159,17 @@ MOE_HD StageGeo stage_geo(int H, int E, int k, int I, int Is, int bits, int G)
     s.cbw_d = s.swz_d ? kCb : rb_d;
     s.ncb_gu = cdiv(rb_gu, s.cbw_gu);
     s.ncb_d = cdiv(rb_d, s.cbw_d);
-    s.n_gu = 2 * s.ncb_gu * s.nrc_gu;
-    s.n_stages = s.n_gu + s.ncb_d * s.nrc_d;
+    s.ncs_gu = imax(1, imin(ncs_gu, s.ncb_gu));
+    s.cpg_gu = cdiv(s.ncb_gu, s.ncs_gu);
+    s.ncs_gu = cdiv(s.ncb_gu, s.cpg_gu);
+    s.nslot_gu = imax(1, imin(nslot_gu, s.ncs_gu));
+    s.ncs_d = 1;
+    s.cpg_d = s.ncb_d;
+    s.gu_copy = align1k((uint32_t)s.cbw_gu * s.bh_gu * s.cpg_gu);
+    s.d_copy = align1k((uint32_t)s.cbw_d * s.bh_d * s.cpg_d);
     s.Rr = cdiv(E, G);
     s.Rs = cdiv(Is, G);
     s.Rsd = cdiv(H, G);
-    const uint32_t box = (uint32_t)s.SR * kCb;
-    s.slot_bytes = (box + 1023u) & ~1023u;
     return s;
 }
 
@@ -157,7 +183,8 @@ MOE_HD uint32_t sb_span_max(int nrows, int row_b) { return ((uint32_t)(nrows * r
 // ------------------------------------------------------------------------------------------
 
 struct StepParams {
-    // 3D TMA maps over the arena: bytes of a row x rows x slots, for gate.q, up.q and down.q
+    // 4D TMA maps over the arena: bytes of a column block x rows x column blocks x slots, for
+    // gate.q, up.q and down.q
     CUtensorMap tmap[3];
     int H, E, k, I, Is, bits, group, flags;
     BlobGeo geo, geo_s;           // routed / shared blob geometry
@@ -176,8 +203,8 @@ struct StepParams {
     // exchange buffers (workspace)
     unsigned long long* xlog;     // [E] (epoch << 32 | fp32 logit)
     unsigned long long* xh;       // [k + 1][max(I, Is)] (epoch << 32 | fp32 h); row k: shared expert
-    long long* xacc;              // [2][H] fixed-point output accumulators (token parity)
-    unsigned long long* bar;      // grid-barrier counter (a multiple of the grid between launches)
+    long long* xacc;              // [2][H] counted fixed-point output words (step parity)
+    unsigned long long* bar;      // launch-start barrier counter (a multiple of the grid between launches)
     int* status;
     uint32_t epoch0;              // epoch of the launch's first step (>= 1)
     unsigned long long timeout_ns;
@@ -191,30 +218,34 @@ struct StepParams {
 // ------------------------------------------------------------------------------------------
 
 struct SmemPlan {
-    uint32_t ctx, mbar, ctl, x, u, up, uc, lg, lkey, lidx;
+    uint32_t ctx, mbar, ctl, x, u, up, uc, lg, tk;
     uint32_t rt, wsg, sgq, ssb, sdq, sdsb;
     uint32_t ring, rsb, rdsb;
-    uint32_t hs, uhs, hj, uhj, hv, sp, spd;
+    uint32_t hs, uhs, hj, uhj, hv, sp, spd, rp;
     uint32_t total;
 };
 
-constexpr uint32_t kCtxBytes = 1024;  // room for the kernel's block context
-constexpr int kNumMbar = kWarps + 3;  // ring slots, routed scales, dense prefetch, shared down
-// control words: sel_idx[kMaxK], sel_w[kMaxK], sel_slot[kMaxK], red[64], misc[16], imisc[16]
-constexpr int kCtlWords = 3 * kMaxK + 64 + 16 + 16;
+constexpr uint32_t kCtxBytes = 1024;   // room for the kernel's block context
+// mbarriers: gate/up copies [2 * kMaxGuSlots] (slot s: gate 2s, up 2s + 1), then down copies,
+// routed scales, dense rows, shared down rows
+constexpr int kMaxGuSlots = 8;
+constexpr int kMbDown = 2 * kMaxGuSlots, kMbRsc = kMbDown + 1, kMbDense = kMbDown + 2, kMbSdown = kMbDown + 3;
+constexpr int kNumMbar = kMbDown + 4;
+// control words: sel_idx[kMaxK], sel_w[kMaxK], sel_slot[kMaxK], red[64], misc[32], imisc[16]
+constexpr int kCtlWords = 3 * kMaxK + 64 + 32 + 16;
 
 MOE_HD uint32_t align_to(uint32_t v, uint32_t a) { return (v + a - 1) & ~(a - 1); }
 
-MOE_HD SmemPlan smem_plan(int H, int E, int k, int I, int Is, int bits, int G)
+MOE_HD SmemPlan smem_plan(int H, int E, int k, int I, int Is, int bits, const StageGeo& sg)
 {
-    const StageGeo sg = stage_geo(H, E, k, I, Is, bits, G);
-    const int xp = (bits == 8) ? 2 : 1;           // int8 codes are read as two nibbles
+    const int xp = (bits == 8) ? 2 : 1;           // int8 codes are read as two 4-bit fields
     const int KU = H * xp;                         // expanded length of u
     const int NCu = KU / kChunk;
     const int KD = I * xp, KDs = Is * xp;
     const int NCd = KD / kChunk, NCds = KDs / kChunk;
     const int ngu = H / 64, ngd = I / 64, ngds = Is / 64;
     const int rb_gu = H * bits / 8, rb_ds = Is * bits / 8;
+    const int ncb_ds = cdiv(rb_ds, kCb);
     SmemPlan s{};
     uint32_t o = 0;
     auto take = [&](uint32_t& field, uint32_t bytes, uint32_t a) {
@@ -229,29 +260,25 @@ MOE_HD SmemPlan smem_plan(int H, int E, int k, int I, int Is, int bits, int G)
     take(s.u, 2u * H, 16);
     take(s.up, 2u * KU, 16);
     take(s.uc, 8u * NCu, 16);
-    take(s.lg, 4u * (E > 32 ? E : 32), 16);
-    take(s.lkey, 4u * (kMaxE + 2 * kWarps + 8), 16);
-    take(s.lidx, 4u * (kMaxE + 2 * kWarps + 8), 16);
+    take(s.lg, 4u * imax(E, 32), 16);
+    take(s.tk, 8u * (kMaxE + 2 * kWarps + 8), 16);
     take(s.rt, 2u * sg.Rr * H, 128);
     take(s.wsg, 2u * H, 16);
     take(s.sgq, 2u * sg.Rs * rb_gu, 128);
     take(s.ssb, 4u * sb_span_max(sg.Rs, 2 * ngu), 16);
     take(s.sdq, (uint32_t)sg.Rsd * rb_ds, 128);
     take(s.sdsb, 2u * sb_span_max(sg.Rsd, 2 * ngds), 16);
-    take(s.ring, (uint32_t)kWarps * sg.slot_bytes, 1024);
-    take(s.rsb, 4u * sb_span_max(sg.Rgu, 2 * ngu), 16);
-    take(s.rdsb, 2u * sb_span_max(sg.Rd, 2 * ngd), 16);
+    take(s.ring, (uint32_t)sg.nslot_gu * 2 * sg.nr_gu * sg.gu_copy + (uint32_t)sg.nr_d * sg.d_copy, 1024);
+    take(s.rsb, 4u * sb_span_max(sg.SRgu, 2 * ngu), 16);
+    take(s.rdsb, 2u * sb_span_max(sg.SRd, 2 * ngd), 16);
     take(s.hs, 2u * 2 * KDs, 16);
     take(s.uhs, 8u * NCds, 16);
     take(s.hj, 2u * 2 * KD, 16);
     take(s.uhj, 8u * NCd, 16);
     take(s.hv, 4u * xh_stride(I, Is), 16);
-    const int spr = sg.Rgu > sg.Rs ? sg.Rgu : sg.Rs;
-    take(s.sp, 4u * spr * 2 * sg.ncb_gu, 16);
-    const int sdr = sg.Rd > sg.Rsd ? sg.Rd : sg.Rsd;
-    const int ncb_ds = cdiv(NCds, 4);
-    const int sdc = sg.ncb_d > ncb_ds ? sg.ncb_d : ncb_ds;
-    take(s.spd, 4u * sdr * sdc, 16);
+    take(s.sp, 4u * imax(sg.SRgu, sg.Rs) * 2 * sg.ncb_gu, 16);
+    take(s.spd, 4u * imax(sg.SRd, sg.Rsd) * imax(sg.ncb_d, ncb_ds), 16);
+    take(s.rp, 4u * imax(sg.Rr, 1) * kRouterParts, 16);
     s.total = align_to(o, 16);
     return s;
 }

@@ -87,7 +87,14 @@ struct DeviceSetup {
     int sms;
     int smem_optin;
     uint32_t epoch;    // next exchange-buffer epoch on this device (0: buffers not yet cleared)
+    StaticLayout last; // layout of the previous call on this device (all zero before the first)
 };
+
+bool same_layout(const StaticLayout& a, const StaticLayout& b)
+{
+    return a.bar == b.bar && a.status == b.status && a.table == b.table && a.layer == b.layer && a.xlog == b.xlog &&
+           a.xh == b.xh && a.xacc == b.xacc && a.total == b.total;
+}
 
 std::mutex g_setup_mu;
 DeviceSetup g_setup[kMaxDevices];
@@ -118,6 +125,7 @@ moe_status device_setup(int dev, DeviceSetup* out)
         d.sms = sms;
         d.smem_optin = optin;
         d.epoch = 0;
+        d.last = StaticLayout{};
         d.ready = true;
     }
     *out = d;
@@ -176,8 +184,10 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
                            "this shape needs %zu bytes of scratch; the static scratch array holds %zu "
                            "(MOE_STATIC_SCRATCH_BYTES): use moe_layer_forward with a workspace instead",
                            sl.total, kStaticScratchBytes);
-    if (!d_experts || !w || !w->router || !w->shared_blob || !w->shared_gate || !d_x || !d_y)
-        return fail_static(MOE_E_INVALID, "d_experts, the layer weights, d_x and d_y are required");
+    if (!d_experts || !w || !w->router || !w->shared_blob || !w->shared_gate || !d_x || !d_y || !d_status)
+        return fail_static(MOE_E_INVALID, "d_experts, the layer weights, d_x, d_y and d_status are required");
+    if (misaligned(d_status, 4))
+        return fail_static(MOE_E_INVALID, "d_status must be 4-byte aligned");
     if (misaligned(d_experts, 256) || misaligned(w->router, 16) || misaligned(w->shared_blob, 16) ||
         misaligned(w->shared_gate, 16) || misaligned(d_x, 16) || misaligned(d_y, 16))
         return fail_static(MOE_E_INVALID, "d_experts must be 256-byte aligned; weights, d_x and d_y 16-byte aligned");
@@ -193,8 +203,9 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
         return st;
     if (ds.sms > kMaxGrid)
         return fail_static(MOE_E_SHAPE, "%d SMs exceed the %d blocks a decode launch supports", ds.sms, kMaxGrid);
-    const uint32_t smem = fused_smem_bytes(shape->hidden, shape->n_experts, shape->top_k, shape->inter,
-                                           shape->shared_inter, shape->bits, ds.sms, ds.smem_optin);
+    StageGeo sg{};
+    const uint32_t smem = plan_decode(shape->hidden, shape->n_experts, shape->top_k, shape->inter,
+                                      shape->shared_inter, shape->bits, ds.sms, ds.smem_optin, &sg);
     if (smem == 0)
         return fail_static(MOE_E_SHAPE, "the fused decode kernel cannot stage this shape on this GPU");
 
@@ -209,7 +220,7 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     P.flags = shape->flags;
     P.geo = blob_geo(P.H, P.I, P.bits, P.group);
     P.geo_s = blob_geo(P.H, P.Is, P.bits, P.group);
-    P.sg = stage_geo(P.H, P.E, P.k, P.I, P.Is, P.bits, ds.sms);
+    P.sg = sg;
     const int rc = encode_arena_maps(P.tmap, static_cast<const uint8_t*>(d_experts), P.E, P.geo, P.sg);
     if (rc != 0)
         return fail_static(MOE_E_CUDA, "cuTensorMapEncodeTiled over the expert blobs failed (%d)", rc);
@@ -222,7 +233,7 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     P.xh = reinterpret_cast<unsigned long long*>(s + sl.xh);
     P.xacc = reinterpret_cast<long long*>(s + sl.xacc);
     P.bar = reinterpret_cast<unsigned long long*>(s + sl.bar);
-    P.status = d_status ? reinterpret_cast<int*>(d_status) : reinterpret_cast<int*>(s + sl.status);
+    P.status = reinterpret_cast<int*>(d_status);
     P.timeout_ns = kStaticTimeoutNs;
     for (int j = 0; j < kMaxK; ++j)
         P.slots[j] = -1;
@@ -248,14 +259,23 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     bool clear;
     {
+        // The exchange buffers are cleared when the epoch counter starts over and whenever this
+        // call's layout differs from the previous call's: the buffers then sit on bytes that the
+        // previous call used for something else (output words, the expert table), which could
+        // read as a pair carrying one of this call's epochs.
         std::lock_guard<std::mutex> lock(g_setup_mu);
-        clear = next_epochs(g_setup[dev].epoch, (uint32_t)n_tokens, &P.epoch0);
+        DeviceSetup& d = g_setup[dev];
+        clear = next_epochs(d.epoch, (uint32_t)n_tokens, &P.epoch0);
+        if (!same_layout(d.last, sl)) {
+            clear = true;
+            d.last = sl;
+        }
     }
     if (clear) {  // no earlier pair may carry an epoch of this call
         if ((e = cudaMemsetAsync(s + sl.xlog, 0, sl.xacc - sl.xlog, cs)) != cudaSuccess)
             return fail_static(MOE_E_CUDA, "clearing the exchange buffers failed: %s", cudaGetErrorString(e));
     }
-    static_prepare<<<1, 256, 0, cs>>>(s, sl, P.E, desc, d_status ? reinterpret_cast<int*>(d_status) : nullptr);
+    static_prepare<<<1, 256, 0, cs>>>(s, sl, P.E, desc, reinterpret_cast<int*>(d_status));
     if ((e = cudaGetLastError()) != cudaSuccess)
         return fail_static(MOE_E_CUDA, "scratch preparation launch failed: %s", cudaGetErrorString(e));
     void* args[] = {&P};
