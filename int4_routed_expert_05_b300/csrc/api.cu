@@ -60,7 +60,7 @@ moe_status fail(moe_status st, const char* fmt, ...)
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t bar, status, table, layers, logits, hbuf, sel, xlog, xh, xacc, xbuf, total;
+    size_t bar, status, table, layers, smaps, logits, hbuf, sel, xlog, xh, xflag, xacc, xbuf, total;
 };
 
 WsLayout ws_layout(const moe_shape& s, int L)
@@ -76,11 +76,13 @@ WsLayout ws_layout(const moe_shape& s, int L)
     take(w.status, 256);
     take(w.table, sizeof(int32_t) * (size_t)L * s.n_experts);
     take(w.layers, sizeof(LayerDesc) * (size_t)L);
+    take(w.smaps, sizeof(CUtensorMap) * 3 * (size_t)L);
     take(w.logits, sizeof(float) * (size_t)s.n_experts);
     take(w.hbuf, sizeof(float) * (size_t)(s.top_k + 1) * Imax);
     take(w.sel, sizeof(int32_t) * 3 * kMaxK);
     take(w.xlog, sizeof(unsigned long long) * (size_t)s.n_experts);
     take(w.xh, sizeof(unsigned long long) * (size_t)(s.top_k + 1) * xh_stride(s.inter, s.shared_inter));
+    take(w.xflag, sizeof(unsigned long long) * (size_t)kMaxGrid);
     take(w.xacc, sizeof(long long) * 2 * (size_t)s.hidden);
     take(w.xbuf, sizeof(float) * 2 * (size_t)s.hidden);
     w.total = o;
@@ -126,8 +128,9 @@ struct moe_pool {
     size_t ws_bytes = 0;
     WsLayout wl{};
     BlobGeo geo{}, geo_s{};
-    StageGeo sg{};
+    StageGeo sg{}, sgs{};
     CUtensorMap tmap[3];
+    std::vector<CUtensorMap> smaps;  // [L][3] decode-kernel maps over each layer's shared blob
     uint32_t epoch_next = 1;  // exchange-buffer epochs (the workspace starts zeroed)
     std::vector<LayerDesc> layers;
     SlotPolicy policy;
@@ -262,6 +265,7 @@ moe_status moe_pool_create(const moe_shape* s, int32_t n_layers, int32_t n_slots
     p->geo = geo;
     p->geo_s = blob_geo(s->hidden, s->shared_inter, s->bits, s->group);
     p->layers.assign(n_layers, LayerDesc{nullptr, nullptr, nullptr, nullptr});
+    p->smaps.assign(3 * (size_t)n_layers, CUtensorMap{});
     p->policy = SlotPolicy(n_layers, s->n_experts, n_slots);
     p->slot_last_use.assign(n_slots, nullptr);
     if (!d_workspace) {  // host-only pool: slot policy without a device
@@ -280,7 +284,8 @@ moe_status moe_pool_create(const moe_shape* s, int32_t n_layers, int32_t n_slots
     int optin = 0;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) != cudaSuccess)
         return cleanup(fail(MOE_E_CUDA, "cudaDeviceGetAttribute failed"));
-    p->smem = plan_decode(s->hidden, s->n_experts, s->top_k, s->inter, s->shared_inter, s->bits, sms, optin, &p->sg);
+    p->smem = plan_decode(s->hidden, s->n_experts, s->top_k, s->inter, s->shared_inter, s->bits, sms, optin, &p->sg,
+                          &p->sgs);
     if (p->smem == 0)
         return cleanup(fail(MOE_E_SHAPE, "the fused decode kernel cannot stage this shape on %d SMs with %d bytes of "
                             "shared memory per block", sms, optin));
@@ -383,6 +388,14 @@ moe_status moe_pool_set_layer(moe_pool* p, int32_t layer, const moe_layer_weight
     if (reinterpret_cast<uintptr_t>(w->router) % 16 || reinterpret_cast<uintptr_t>(w->shared_blob) % 16 ||
         reinterpret_cast<uintptr_t>(w->shared_gate) % 16)
         return fail(MOE_E_INVALID, "layer weights must be 16-byte aligned");
+    if (p->ws) {  // the decode kernel's maps over this layer's shared blob
+        CUtensorMap m[3];
+        const int rc = encode_arena_maps(m, static_cast<const uint8_t*>(w->shared_blob), 1, p->geo_s, p->sgs);
+        if (rc != 0)
+            return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled over the shared blob of layer %d failed (%d)", layer, rc);
+        for (int i = 0; i < 3; ++i)
+            p->smaps[3 * (size_t)layer + i] = m[i];
+    }
     p->layers[layer] = LayerDesc{static_cast<const uint16_t*>(w->router), static_cast<const uint8_t*>(w->shared_blob),
                                  static_cast<const uint16_t*>(w->shared_gate), w->logit_bias};
     return MOE_OK;
@@ -406,6 +419,8 @@ moe_status moe_pool_sync(moe_pool* p, void* stream)
     const auto& t = p->policy.table();
     CUDA_TRY(cudaMemcpyAsync(p->ws + p->wl.table, t.data(), sizeof(int32_t) * t.size(), cudaMemcpyHostToDevice, st));
     CUDA_TRY(cudaMemcpyAsync(p->ws + p->wl.layers, p->layers.data(), sizeof(LayerDesc) * p->layers.size(),
+                             cudaMemcpyHostToDevice, st));
+    CUDA_TRY(cudaMemcpyAsync(p->ws + p->wl.smaps, p->smaps.data(), sizeof(CUtensorMap) * p->smaps.size(),
                              cudaMemcpyHostToDevice, st));
     return MOE_OK;
 }
@@ -548,6 +563,9 @@ StepParams base_params(const moe_pool* p)
     P.geo = p->geo;
     P.geo_s = p->geo_s;
     P.sg = p->sg;
+    P.sgs = p->sgs;
+    P.smaps = reinterpret_cast<const CUtensorMap*>(p->ws + p->wl.smaps);
+    P.xflag = reinterpret_cast<unsigned long long*>(p->ws + p->wl.xflag);
     for (int m = 0; m < 3; ++m)
         P.tmap[m] = p->tmap[m];
     P.arena = p->arena;

@@ -100,7 +100,7 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
 // per-chunk correction.
 __device__ __forceinline__ void deq8(uint32_t w, uint32_t (&r)[4])
 {
-    const uint32_t w8 = w >> 8;
+    const uint32_t w8 = __umulhi(w, 1u << 24);  // w >> 8, as a multiply (off the integer-logic pipe)
     r[0] = and_or(w, 0x000F000Fu, 0x64006400u);
     r[1] = and_or(w, 0x00F000F0u, 0x64006400u);
     r[2] = and_or(w8, 0x000F000Fu, 0x64006400u);
@@ -179,8 +179,6 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
 // ---- mbarrier / TMA ----
 __device__ __forceinline__ void mbar_init(uint64_t* m, int n)
 {
@@ -230,26 +228,28 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map)
 // per-block context
 // ------------------------------------------------------------------------------------------
 
-// Block-uniform constants of a launch: shape, this block's share of the work and the
-// shared-memory carve-up. One copy per block in shared memory, written by thread 0 at start; the
-// phases below copy what they need into registers once, at their start.
+// Block-uniform constants of a launch: shape, the expert group this block serves, its rows, its
+// copies and the shared-memory carve-up. One copy per block in shared memory, written by thread 0
+// at start; the phases below copy what they need into registers at their start.
 struct Ctx {
-    int H, E, k, I, Is, xp, KU, NCu, KD, NCd, KDs, NCds, ngu, ngd, ngds, rb_gu, rb_d, rb_ds, ncb_ds;
+    int H, E, k, I, Is, xp, KU, NCu, ngu;
+    int j;            // group rank: the routed expert of rank j (j < k) or the shared expert (j = k)
+    int sh;           // 1 when this block serves the shared expert
+    int Ie, KD, NCd, ngd;  // intermediate size of the served expert and the derived sizes
     int e0, e1;       // router rows
-    int s0, s1;       // shared gate/up rows
-    int o0, o1;       // shared down rows, and the slice of the output words this block clears
-    int j;            // rank of the routed expert this block serves
-    int r0, r1;       // its gate/up rows
-    int d0, d1;       // its down rows
+    int o0, o1;       // the slice of the output words this block clears
+    int r0, r1;       // gate/up rows of the served expert
+    int d0, d1;       // down rows
+    StageGeo g;       // staging geometry of the served expert
+    uint32_t sc_src[6], sc_bytes[6];  // scale spans: offset in the blob, bytes (16-byte aligned)
+    int sc_off[6];    // offset of the first row inside each span
     float invH;
     uint64_t* mbar;
     int* sel_idx;     // [kMaxK]
     float* sel_w;     // [kMaxK]
     int* sel_slot;    // [kMaxK]
     float* red;       // [64]
-    float* misc;      // [32]: [0] gamma, [1..kMaxK] selected logits
-    int* imisc;       // [16]: offsets of staged scale spans ([0..3] shared gate/up, [4..5] shared down,
-                      //       [8..13] routed gate.s, gate.b, up.s, up.b, down.s, down.b)
+    float* misc;      // [32]: [0] gamma
     float* sx;        // [H] layer input x (fp32)
     uint16_t* su;     // [H] u (bf16)
     uint16_t* sup;    // [KU] B operand of u (fp16, permuted blocks)
@@ -258,29 +258,27 @@ struct Ctx {
     uint32_t* tk;     // top-k scratch
     uint16_t* srt;    // [Rr][H] router rows
     uint16_t* swsg;   // [H] shared gate vector
-    uint8_t* sgq;     // [2][Rs][rb_gu] shared gate/up codes
-    uint8_t* ssb;     // 4 spans: shared gate.s, gate.b, up.s, up.b rows
-    uint8_t* sdq;     // [Rsd][rb_ds] shared down codes
-    uint8_t* sdsb;    // 2 spans: shared down.s, down.b rows
+    int32_t* stab;    // the layer's slot-table row (16-byte aligned superset of [E])
+    float* sbias;     // the layer's logit bias [E] (when staged)
+    LayerDesc cur;    // the step's layer descriptor
+    int tab_off;      // offset (entries) of the row inside stab
+    int bias_staged;  // 1: sbias holds the bias, 0: read it from global memory
     uint8_t* ring;    // gate/up slots [nslot][2][nr_gu][gu_copy], then down [nr_d][d_copy]
-    uint8_t* rsb;     // 4 spans: routed gate.s, gate.b, up.s, up.b rows
-    uint8_t* rdsb;    // 2 spans: routed down.s, down.b rows
-    uint16_t* shs;    // [2][KDs] B operand of h_shared (fp16 hi/lo, permuted blocks)
-    float2* chs;      // [NCds]
-    uint16_t* shj;    // [2][KD] B operand of h_j
+    uint8_t* rsb;     // 4 spans: gate.s, gate.b, up.s, up.b rows
+    uint8_t* rdsb;    // 2 spans: down.s, down.b rows
+    uint16_t* shj;    // [2][KD] B operand of h
     float2* chj;      // [NCd]
-    float* hv;        // [max(I, Is)] polled h values
+    float* hv;        // [Ie] polled h values
     float* sp;        // gate/up partials [rows][2 * ncb_gu]
-    float* spd;       // down partials [rows][ncb]
+    float* spd;       // down partials [rows][ncb_d]
     float* rp;        // router partials [Rr][kRouterParts]
-    uint32_t span_gu, span_d, span_sgu, span_sd;  // bytes per staged scale span
+    uint32_t span_gu, span_d;  // bytes per staged scale span
 };
 
 static_assert(sizeof(Ctx) <= kCtxBytes, "the block context outgrew its shared-memory slot");
 
 __device__ __noinline__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base)
 {
-    const StageGeo& sg = P.sg;
     C.H = P.H;
     C.E = P.E;
     C.k = P.k;
@@ -289,32 +287,45 @@ __device__ __noinline__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base
     C.xp = P.bits == 8 ? 2 : 1;
     C.KU = P.H * C.xp;
     C.NCu = C.KU / kChunk;
-    C.KD = P.I * C.xp;
-    C.NCd = C.KD / kChunk;
-    C.KDs = P.Is * C.xp;
-    C.NCds = C.KDs / kChunk;
     C.ngu = P.H / 64;
-    C.ngd = P.I / 64;
-    C.ngds = P.Is / 64;
-    C.rb_gu = P.H * P.bits / 8;
-    C.rb_d = P.I * P.bits / 8;
-    C.rb_ds = P.Is * P.bits / 8;
-    C.ncb_ds = cdiv(C.rb_ds, kCb);
     C.invH = 1.f / (float)P.H;
-    const int G = GRID, b = CTA;
+    const int G = GRID, b = CTA, ng = P.k + 1;
     C.e0 = part(P.E, G, b);
     C.e1 = part(P.E, G, b + 1);
-    C.s0 = part(P.Is, G, b);
-    C.s1 = part(P.Is, G, b + 1);
     C.o0 = part(P.H, G, b);
     C.o1 = part(P.H, G, b + 1);
-    C.j = grp_of(b, G, P.k);
-    const int gi = b - grp_start(C.j, G, P.k);
-    C.r0 = imin(gi * sg.SRgu, P.I);
-    C.r1 = imin(C.r0 + sg.SRgu, P.I);
-    C.d0 = imin(gi * sg.SRd, P.H);
-    C.d1 = imin(C.d0 + sg.SRd, P.H);
-    const SmemPlan s = smem_plan(P.H, P.E, P.k, P.I, P.Is, P.bits, sg);
+    C.j = grp_of(b, G, ng);
+    C.sh = C.j == P.k;
+    C.g = C.sh ? P.sgs : P.sg;
+    const BlobGeo& bg = C.sh ? P.geo_s : P.geo;
+    C.Ie = C.sh ? P.Is : P.I;
+    C.KD = C.Ie * C.xp;
+    C.NCd = C.KD / kChunk;
+    C.ngd = C.Ie / 64;
+    const int gi = b - grp_start(C.j, G, ng);
+    C.r0 = imin(gi * C.g.SRgu, C.Ie);
+    C.r1 = imin(C.r0 + C.g.SRgu, C.Ie);
+    C.d0 = imin(gi * C.g.SRd, P.H);
+    C.d1 = imin(C.d0 + C.g.SRd, P.H);
+    // scale spans of the block's rows: gate.s, gate.b, up.s, up.b, down.s, down.b (blob bases are
+    // 16-byte aligned, so the spans' alignment does not depend on the blob)
+#pragma unroll 1
+    for (int i = 0; i < 6; ++i) {
+        const bool d = i >= 4;
+        const uint64_t sec = (i & 1) ? bg.b_off[i >> 1] : bg.s_off[i >> 1];
+        const int rb = d ? C.ngd * 2 : C.ngu * 2, r0 = d ? C.d0 : C.r0, r1 = d ? C.d1 : C.r1;
+        if (r1 <= r0) {
+            C.sc_src[i] = C.sc_bytes[i] = 0;
+            C.sc_off[i] = 0;
+            continue;
+        }
+        const uint64_t a = sec + (uint64_t)r0 * rb, e = sec + (uint64_t)r1 * rb;
+        const uint64_t a16 = a & ~(uint64_t)15, e16 = (e + 15) & ~(uint64_t)15;
+        C.sc_src[i] = (uint32_t)a16;
+        C.sc_bytes[i] = (uint32_t)(e16 - a16);
+        C.sc_off[i] = (int)(a - a16);
+    }
+    const SmemPlan s = smem_plan(P.H, P.E, P.I, P.Is, P.bits, G, P.sg, P.sgs);
     C.mbar = (uint64_t*)(base + s.mbar);
     int* ctl = (int*)(base + s.ctl);
     C.sel_idx = ctl;
@@ -322,7 +333,6 @@ __device__ __noinline__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base
     C.sel_slot = ctl + 2 * kMaxK;
     C.red = (float*)(ctl + 3 * kMaxK);
     C.misc = (float*)(ctl + 3 * kMaxK + 64);
-    C.imisc = ctl + 3 * kMaxK + 64 + 32;
     C.sx = (float*)(base + s.x);
     C.su = (uint16_t*)(base + s.u);
     C.sup = (uint16_t*)(base + s.up);
@@ -331,170 +341,111 @@ __device__ __noinline__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base
     C.tk = (uint32_t*)(base + s.tk);
     C.srt = (uint16_t*)(base + s.rt);
     C.swsg = (uint16_t*)(base + s.wsg);
-    C.sgq = base + s.sgq;
-    C.ssb = base + s.ssb;
-    C.sdq = base + s.sdq;
-    C.sdsb = base + s.sdsb;
+    C.stab = (int32_t*)(base + s.tab);
+    C.sbias = (float*)(base + s.bias);
     C.ring = base + s.ring;
     C.rsb = base + s.rsb;
     C.rdsb = base + s.rdsb;
-    C.shs = (uint16_t*)(base + s.hs);
-    C.chs = (float2*)(base + s.uhs);
     C.shj = (uint16_t*)(base + s.hj);
     C.chj = (float2*)(base + s.uhj);
     C.hv = (float*)(base + s.hv);
     C.sp = (float*)(base + s.sp);
     C.spd = (float*)(base + s.spd);
     C.rp = (float*)(base + s.rp);
-    C.span_gu = sb_span_max(sg.SRgu, 2 * C.ngu);
-    C.span_d = sb_span_max(sg.SRd, 2 * C.ngd);
-    C.span_sgu = sb_span_max(sg.Rs, 2 * C.ngu);
-    C.span_sd = sb_span_max(sg.Rsd, 2 * C.ngds);
+    const int Im = imax(P.I, P.Is);
+    C.span_gu = sb_span_max(imax(P.sg.SRgu, P.sgs.SRgu), 2 * C.ngu);
+    C.span_d = sb_span_max(imax(P.sg.SRd, P.sgs.SRd), 2 * (Im / 64));
 }
 
 // ------------------------------------------------------------------------------------------
 // copies
 // ------------------------------------------------------------------------------------------
 
-// Bytes copy_rows() issues for rows [r0, r1) of a section whose rows hold row_b bytes.
-__device__ __forceinline__ uint32_t span_bytes(const uint8_t* sec, int r0, int r1, int row_b)
-{
-    if (r1 <= r0)
-        return 0;
-    const uintptr_t a = (uintptr_t)(sec + (size_t)r0 * row_b);
-    const uintptr_t e = (uintptr_t)(sec + (size_t)r1 * row_b);
-    return (uint32_t)(((e + 15) & ~(uintptr_t)15) - (a & ~(uintptr_t)15));
-}
-
-// Issue a 1D copy of rows [r0, r1) of a section whose rows hold row_b bytes (16-byte aligned
-// superset); returns, in *off, the offset of row r0 inside the copy.
-__device__ __forceinline__ void copy_rows(void* dst, const uint8_t* sec, int r0, int r1, int row_b, uint64_t* m,
-                                          int* off)
-{
-    if (r1 <= r0) {
-        *off = 0;
-        return;
-    }
-    const uintptr_t a = (uintptr_t)(sec + (size_t)r0 * row_b);
-    const uintptr_t e = (uintptr_t)(sec + (size_t)r1 * row_b);
-    const uintptr_t a16 = a & ~(uintptr_t)15, e16 = (e + 15) & ~(uintptr_t)15;
-    *off = (int)(a - a16);
-    bulk_g2s(dst, (const void*)a16, (uint32_t)(e16 - a16), m);
-}
-
-// One thread: the router rows, the shared gate vector and the shared expert's gate/up rows and
-// scales of layer L (only the parts the launch's mode uses).
-__device__ __noinline__ void issue_dense(const StepParams& P, const Ctx& C, const LayerDesc L, bool rt, bool sh)
+// One thread: what a step reads of layer l besides its experts: the router rows [e0, e1), the
+// layer's slot-table row and logit bias (rt), and the shared gate vector (wsg). Also records the
+// layer's descriptor for the step.
+__device__ __noinline__ void issue_dense(const StepParams& P, Ctx& C, int l, bool rt, bool wsg)
 {
     uint64_t* m = C.mbar + kMbDense;
-    const uint8_t* sb = L.shared_blob;
-    const int ns = C.s1 - C.s0, H = C.H, rb = C.rb_gu, ngu2 = C.ngu * 2;
-    rt = rt && C.e1 > C.e0;
-    const bool shr = sh && ns > 0;
-    uint32_t bytes = sh ? (uint32_t)H * 2 : 0u;
+    const LayerDesc L = P.layers[l];
+    C.cur = L;
+    const int H = C.H, E = C.E;
+    const bool rr = rt && C.e1 > C.e0;
+    uint32_t bytes = (rr ? (uint32_t)(C.e1 - C.e0) * H * 2 : 0u) + (wsg ? (uint32_t)H * 2 : 0u);
+    // the slot-table row: its 16-byte aligned superset (inside the table's buffer)
+    const int32_t* row = P.table + (size_t)l * E;
+    const uintptr_t ta = reinterpret_cast<uintptr_t>(row) & ~(uintptr_t)15;
+    const uint32_t tb = (uint32_t)(((reinterpret_cast<uintptr_t>(row + E) + 15) & ~(uintptr_t)15) - ta);
+    C.tab_off = (int)((reinterpret_cast<uintptr_t>(row) - ta) / 4);
+    C.bias_staged = rt && L.logit_bias && (reinterpret_cast<uintptr_t>(L.logit_bias) & 15) == 0 && (E & 3) == 0;
     if (rt)
-        bytes += (uint32_t)(C.e1 - C.e0) * H * 2;
-    if (shr) {
-        bytes += 2u * (uint32_t)ns * rb;
-#pragma unroll 1
-        for (int i = 0; i < 4; ++i)
-            bytes += span_bytes(sb + ((i & 1) ? P.geo_s.b_off[i >> 1] : P.geo_s.s_off[i >> 1]), C.s0, C.s1, ngu2);
-    }
+        bytes += tb + (C.bias_staged ? (uint32_t)E * 4 : 0u);
     mbar_expect(m, bytes);
-    if (rt)
+    if (rr)
         bulk_g2s(C.srt, L.router + (size_t)C.e0 * H, (uint32_t)(C.e1 - C.e0) * H * 2, m);
-    if (sh)
+    if (wsg)
         bulk_g2s(C.swsg, L.shared_gate, (uint32_t)H * 2, m);
-    if (shr) {
-        const uint32_t nq = (uint32_t)ns * rb;
-        bulk_g2s(C.sgq, sb + P.geo_s.q_off[0] + (size_t)C.s0 * rb, nq, m);
-        bulk_g2s(C.sgq + (size_t)P.sg.Rs * rb, sb + P.geo_s.q_off[1] + (size_t)C.s0 * rb, nq, m);
-#pragma unroll 1
-        for (int i = 0; i < 4; ++i)
-            copy_rows(C.ssb + i * C.span_sgu, sb + ((i & 1) ? P.geo_s.b_off[i >> 1] : P.geo_s.s_off[i >> 1]), C.s0,
-                      C.s1, ngu2, m, &C.imisc[i]);
-    }
-}
-
-// One thread: the shared expert's down rows [o0, o1) and their scales of layer L.
-__device__ __noinline__ void issue_sdown(const StepParams& P, const Ctx& C, const LayerDesc L)
-{
-    uint64_t* m = C.mbar + kMbSdown;
-    const uint8_t* sb = L.shared_blob;
-    const int rowb = C.ngds * 2;
-    uint32_t bytes = 0;
-    if (C.o1 > C.o0)
-        bytes = (uint32_t)(C.o1 - C.o0) * C.rb_ds + span_bytes(sb + P.geo_s.s_off[2], C.o0, C.o1, rowb) +
-                span_bytes(sb + P.geo_s.b_off[2], C.o0, C.o1, rowb);
-    mbar_expect(m, bytes);
-    if (C.o1 > C.o0) {
-        bulk_g2s(C.sdq, sb + P.geo_s.q_off[2] + (size_t)C.o0 * C.rb_ds, (uint32_t)(C.o1 - C.o0) * C.rb_ds, m);
-        copy_rows(C.sdsb, sb + P.geo_s.s_off[2], C.o0, C.o1, rowb, m, &C.imisc[4]);
-        copy_rows(C.sdsb + C.span_sd, sb + P.geo_s.b_off[2], C.o0, C.o1, rowb, m, &C.imisc[5]);
+    if (rt) {
+        bulk_g2s(C.stab, reinterpret_cast<const void*>(ta), tb, m);
+        if (C.bias_staged)
+            bulk_g2s(C.sbias, L.logit_bias, (uint32_t)E * 4, m);
     }
 }
 
 // Staging address of gate/up copy (slot sl, matrix m, row box rc) and of down copy rc.
-__device__ __forceinline__ uint8_t* gu_copy_at(const Ctx& C, const StageGeo& sg, int sl, int m, int rc)
+__device__ __forceinline__ uint8_t* gu_copy_at(const Ctx& C, int sl, int m, int rc)
 {
-    return C.ring + (size_t)((sl * 2 + m) * sg.nr_gu + rc) * sg.gu_copy;
+    return C.ring + (size_t)((sl * 2 + m) * C.g.nr_gu + rc) * C.g.gu_copy;
 }
-__device__ __forceinline__ uint8_t* d_copy_at(const Ctx& C, const StageGeo& sg, int rc)
+__device__ __forceinline__ uint8_t* d_copy_at(const Ctx& C, int rc)
 {
-    return C.ring + (size_t)sg.nslot_gu * 2 * sg.nr_gu * sg.gu_copy + (size_t)rc * sg.d_copy;
-}
-
-// One thread: the gate and up copies of column group cg of the block's gate/up rows, into slot sl.
-__device__ __noinline__ void issue_gu_group(const StepParams& P, const Ctx& C, int slot, int cg, int sl)
-{
-    const StageGeo& sg = P.sg;
-    const int nrc = cdiv(C.r1 - C.r0, sg.bh_gu);
-#pragma unroll 1
-    for (int m = 0; m < 2; ++m) {
-        uint64_t* mb = C.mbar + 2 * sl + m;
-        mbar_expect(mb, (uint32_t)nrc * sg.cbw_gu * sg.bh_gu * sg.cpg_gu);
-#pragma unroll 1
-        for (int rc = 0; rc < nrc; ++rc)
-            tma4d(gu_copy_at(C, sg, sl, m, rc), &P.tmap[m], 0, C.r0 + rc * sg.bh_gu, cg * sg.cpg_gu, slot, mb);
-    }
+    return C.ring + (size_t)C.g.nslot_gu * 2 * C.g.nr_gu * C.g.gu_copy + (size_t)rc * C.g.d_copy;
 }
 
-// One thread: the scales of the block's routed rows, its first gate/up column groups and all of
-// its down rows.
-__device__ __noinline__ void issue_routed(const StepParams& P, const Ctx& C, int slot)
+// One thread: the gate (m = 0) or up (m = 1) copy of column group cg of the block's gate/up rows,
+// into slot sl; with the matrix's scale and bias rows when `scales` (the first group).
+// maps: the expert's gate/up/down maps; w: the blob's coordinate in them; blob: the blob itself.
+__device__ __noinline__ void issue_gu(const Ctx& C, const uint8_t* blob, const CUtensorMap* maps, int w, int cg, int sl,
+                                      int m, bool scales)
 {
-    const StageGeo& sg = P.sg;
-    const uint8_t* blob = P.arena + (uint64_t)slot * P.stride;
-    const bool gu = C.r1 > C.r0, dn = C.d1 > C.d0;
-    uint64_t* m = C.mbar + kMbRsc;
-    uint32_t bytes = 0;
+    const StageGeo& g = C.g;
+    const int nrc = cdiv(C.r1 - C.r0, g.bh_gu);
+    uint64_t* mb = C.mbar + 2 * sl + m;
+    mbar_expect(mb, (uint32_t)nrc * g.cbw_gu * g.bh_gu * g.cpg_gu +
+                        (scales ? C.sc_bytes[2 * m] + C.sc_bytes[2 * m + 1] : 0u));
 #pragma unroll 1
-    for (int i = 0; i < 6; ++i) {
-        const bool d = i >= 4;
-        const uint64_t sec = (i & 1) ? P.geo.b_off[i >> 1] : P.geo.s_off[i >> 1];
-        bytes += span_bytes(blob + sec, d ? C.d0 : C.r0, d ? C.d1 : C.r1, d ? C.ngd * 2 : C.ngu * 2);
-    }
-    mbar_expect(m, bytes);
-    // gate scales, then the gate/up codes of the first groups, then the rest: the copy engine
-    // takes copies in order, and the gate/up rows are needed first
+    for (int rc = 0; rc < nrc; ++rc)
+        tma4d(gu_copy_at(C, sl, m, rc), maps + m, 0, C.r0 + rc * g.bh_gu, cg * g.cpg_gu, w, mb);
+    if (scales)
 #pragma unroll 1
-    for (int i = 0; i < 6; ++i) {
-        const bool d = i >= 4;
-        uint8_t* dst = d ? C.rdsb + (i - 4) * C.span_d : C.rsb + i * C.span_gu;
-        const uint64_t sec = (i & 1) ? P.geo.b_off[i >> 1] : P.geo.s_off[i >> 1];
-        copy_rows(dst, blob + sec, d ? C.d0 : C.r0, d ? C.d1 : C.r1, d ? C.ngd * 2 : C.ngu * 2, m, &C.imisc[8 + i]);
-        if (i == 3 && gu)
+        for (int i = 2 * m; i < 2 * m + 2; ++i)
+            if (C.sc_bytes[i])
+                bulk_g2s(C.rsb + i * C.span_gu, blob + C.sc_src[i], C.sc_bytes[i], mb);
+}
+
+// One thread: every byte the block reads of its expert in a step, gate rows first, then up rows,
+// then down rows (the copy engine takes copies in order), each matrix's codes and scales on one
+// mbarrier; gate/up rows of the first column groups only when the groups take turns.
+__device__ __noinline__ void issue_expert(const Ctx& C, const uint8_t* blob, const CUtensorMap* maps, int w)
+{
+    const StageGeo& g = C.g;
+    if (C.r1 > C.r0)
 #pragma unroll 1
-            for (int cg = 0; cg < sg.nslot_gu; ++cg)
-                issue_gu_group(P, C, slot, cg, cg);
-    }
-    if (dn) {
-        const int nrc = cdiv(C.d1 - C.d0, sg.bh_d);
+        for (int cg = 0; cg < g.nslot_gu; ++cg)
+#pragma unroll 1
+            for (int m = 0; m < 2; ++m)
+                issue_gu(C, blob, maps, w, cg, cg, m, cg == 0);
+    if (C.d1 > C.d0) {
+        const int nrc = cdiv(C.d1 - C.d0, g.bh_d);
         uint64_t* md = C.mbar + kMbDown;
-        mbar_expect(md, (uint32_t)nrc * sg.cbw_d * sg.bh_d * sg.cpg_d);
+        mbar_expect(md, (uint32_t)nrc * g.cbw_d * g.bh_d * g.cpg_d + C.sc_bytes[4] + C.sc_bytes[5]);
 #pragma unroll 1
         for (int rc = 0; rc < nrc; ++rc)
-            tma4d(d_copy_at(C, sg, rc), &P.tmap[2], 0, C.d0 + rc * sg.bh_d, 0, slot, md);
+            tma4d(d_copy_at(C, rc), maps + 2, 0, C.d0 + rc * g.bh_d, 0, w, md);
+#pragma unroll 1
+        for (int i = 4; i < 6; ++i)
+            if (C.sc_bytes[i])
+                bulk_g2s(C.rdsb + (i - 4) * C.span_d, blob + C.sc_src[i], C.sc_bytes[i], md);
     }
 }
 
@@ -568,6 +519,36 @@ __device__ __forceinline__ bool poll_pairs(const unsigned long long* src, int n,
     return true;
 }
 
+// Wait until the n completion flags carry `epoch` (one warp polls them with acquire loads; the
+// block then reads what the flagging blocks stored before their flags). Block-uniform.
+__device__ __forceinline__ bool wait_flags(const unsigned long long* flags, int n, uint32_t epoch, long long limit,
+                                           int* status)
+{
+    bool ok = true;
+    if (WARP == 0) {
+        const long long t0 = cycles();
+#pragma unroll 1
+        for (int f = LANE; ok && f < n; f += 32) {
+            while (true) {
+                unsigned long long v;
+                asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(flags + f) : "memory");
+                if ((uint32_t)v == epoch)
+                    break;
+                if (cycles() - t0 > limit) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+    if (__syncthreads_or(!ok)) {
+        if (TID == 0)
+            set_status(status, kStatusTimeout);
+        return false;
+    }
+    return true;
+}
+
 // Output words of elements [4q, 4q + 4) once each holds `want` contributions; false after the
 // limit.
 __device__ __forceinline__ bool poll_out4(const long long* X, int q, int want, long long t0, long long limit, float4& y)
@@ -628,21 +609,66 @@ __device__ __noinline__ bool grid_barrier(const StepParams& P, long long limit)
 // the GEMV tiles
 // ------------------------------------------------------------------------------------------
 
+// One 16-row tile: A fragments of the nch chunks (rows Ra, Rb present when ha / hb), scales sv / bv
+// of the thread's row, the four MMA chains, and the thread's row partial.
+__device__ __forceinline__ float tile_mma(uint32_t aa, uint32_t ab, bool ha, bool hb, int nch, const uint32_t (&off)[4],
+                                          const uint4 (&Bx)[4], const uint4 (&By)[4], const float2 (&cs)[4],
+                                          const float (&sv)[4], const float (&bv)[4], int gsh, bool lo, int tq)
+{
+    uint2 ra[4], rb[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const bool on = c < nch;
+        ra[c] = (on && ha) ? lds64(aa + off[c]) : make_uint2(0, 0);
+        rb[c] = (on && hb) ? lds64(ab + off[c]) : make_uint2(0, 0);
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+    // first 32 fields of each chunk, then the second 32: four independent chains
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t a[4], b[4];
+        deq8(ra[c].x, a);
+        deq8(rb[c].x, b);
+        mma_f16(acc[c], a[0], b[0], a[1], b[1], Bx[c].x, Bx[c].y);
+        mma_f16(acc[c], a[2], b[2], a[3], b[3], Bx[c].z, Bx[c].w);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t a[4], b[4];
+        deq8(ra[c].y, a);
+        deq8(rb[c].y, b);
+        mma_f16(acc[c], a[0], b[0], a[1], b[1], By[c].x, By[c].y);
+        mma_f16(acc[c], a[2], b[2], a[3], b[3], By[c].z, By[c].w);
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float v = tq == 0 ? acc[c][0] : acc[c][2];
+        if (lo)
+            v += tq == 0 ? acc[c][1] : acc[c][3];
+        part = fmaf(sv[c >> gsh], v - cs[c].y, fmaf(bv[c >> gsh], cs[c].x, part));
+    }
+    return part;
+}
+
 // Tiles [t0, t1) (16 rows each) of one staged column block, of which rows [0, nvalid) are real: row
 // R at base + R * width. With swz = 7 the rows are 128-byte swizzled TMA rows (16-byte piece q of
 // a row at shared address bits 7..9 XOR q; the copy's destination is 1024-byte aligned); with
 // swz = 0 they are linear. Chunks c0 .. c0 + nch - 1 (nch <= 4) of the B operand start at byte
-// 32 (c - c0) of a row. For each real row R this writes out[R * ostride] = sum over the chunks (in
-// chunk order) of s * (sum q v) + b * (sum v), with v the activation: the B operand `bsrc`
-// (lo_off = 0: u, every column the same) or h (lo_off = KD: hi parts in the even columns, lo parts
-// at bsrc + KD in the odd ones). Scales: sc / bi + R * sbrow, one bf16 per group (a group is one
-// chunk at int4, two at int8: gsh). The column block's B fragments and chunk sums are loaded once
-// for all tiles; its chunks run as independent MMA chains. Rows g and g + 8 of every tile share one
+// 32 (cofs + c - c0) of a row. For each real row R this writes out[R * ostride] = sum over the
+// chunks (in chunk order) of s * (sum q v) + b * (sum v), with v the activation: the B operand
+// `bsrc` (lo_off = 0: u, every column the same) or h (lo_off = KD: hi parts in the even columns, lo
+// parts at bsrc + KD in the odd ones). Scales: sc / bi + R * sbrow, one bf16 per group (a group is
+// one chunk at int4, two at int8: gsh). The B fragments and chunk sums are loaded once for all
+// tiles; the chunks run as independent MMA chains. Rows g and g + 8 of every tile share one
 // swizzle key (a tile is 16 rows), so each thread's four piece offsets are fixed for the call.
 __device__ __forceinline__ void box_mma(const uint8_t* base, uint32_t swz, int width, int nvalid, int t0, int t1,
                                         int c0, int nch, const uint16_t* bsrc, int lo_off, const float2* csum,
                                         const uint8_t* sc, const uint8_t* bi, int sbrow, int gsh, float* out,
-                                        int ostride)
+                                        int ostride, int cofs = 0)
 {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
@@ -659,63 +685,49 @@ __device__ __forceinline__ void box_mma(const uint8_t* base, uint32_t swz, int w
         Bx[c] = bp[0];
         By[c] = bp[1];
         cs[c] = csum[cc];
-        off[c] = ((((uint32_t)(2 * c + (tq >> 1))) ^ key) << 4) | (uint32_t)(8 * (tq & 1));
+        off[c] = ((((uint32_t)(2 * (cofs + c) + (tq >> 1))) ^ key) << 4) | (uint32_t)(8 * (tq & 1));
     }
-    const int nsc = 4 >> gsh;  // scale groups of the column block
+    const int nsc = (nch + (1 << gsh) - 1) >> gsh;  // scale groups the chunks touch
+    const int q0 = c0 >> gsh;
+    // 8-byte scale loads when the four groups of every row are 8-byte aligned
+    const bool vec = gsh == 0 && nch == 4 && ((reinterpret_cast<uintptr_t>(sc) | reinterpret_cast<uintptr_t>(bi) |
+                                               (uintptr_t)sbrow | (uintptr_t)(2 * q0)) & 7) == 0;
 #pragma unroll 1
     for (int tile = t0; tile < t1; ++tile) {
         const int Ra = tile * 16 + g, Rb = Ra + 8;
         const int R = tq == 0 ? Ra : Rb;
         const bool mine = tq < 2 && R < nvalid;
         const uint32_t aa = b0 + (uint32_t)Ra * (uint32_t)width, ab = aa + 8u * (uint32_t)width;
-        uint2 ra[4], rb[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const bool on = c < nch;
-            ra[c] = (on && Ra < nvalid) ? lds64(aa + off[c]) : make_uint2(0, 0);
-            rb[c] = (on && Rb < nvalid) ? lds64(ab + off[c]) : make_uint2(0, 0);
-        }
-        // this thread's row's scales and biases of the column block's groups (4 at int4, 2 at int8)
         float sv[4], bv[4];
-        {
-            const uint16_t* sp = reinterpret_cast<const uint16_t*>(sc + R * sbrow) + (c0 >> gsh);
-            const uint16_t* bp = reinterpret_cast<const uint16_t*>(bi + R * sbrow) + (c0 >> gsh);
+        if (vec) {
+            uint2 s2 = make_uint2(0, 0), b2 = make_uint2(0, 0);
+            if (mine) {
+                s2 = *reinterpret_cast<const uint2*>(sc + R * sbrow + 2 * q0);
+                b2 = *reinterpret_cast<const uint2*>(bi + R * sbrow + 2 * q0);
+            }
+            sv[0] = __uint_as_float(s2.x << 16);
+            sv[1] = __uint_as_float(s2.x & 0xFFFF0000u);
+            sv[2] = __uint_as_float(s2.y << 16);
+            sv[3] = __uint_as_float(s2.y & 0xFFFF0000u);
+            bv[0] = __uint_as_float(b2.x << 16);
+            bv[1] = __uint_as_float(b2.x & 0xFFFF0000u);
+            bv[2] = __uint_as_float(b2.y << 16);
+            bv[3] = __uint_as_float(b2.y & 0xFFFF0000u);
+        } else {
+            const uint16_t* sp = reinterpret_cast<const uint16_t*>(sc + R * sbrow) + q0;
+            const uint16_t* bp = reinterpret_cast<const uint16_t*>(bi + R * sbrow) + q0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const bool on = mine && q < nsc && (q << gsh) < nch;
+                const bool on = mine && q < nsc;
                 sv[q] = on ? bf16f(sp[q]) : 0.f;
                 bv[q] = on ? bf16f(bp[q]) : 0.f;
             }
         }
-        float acc[4][4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
-        // first 32 fields of each chunk, then the second 32: four independent chains
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t a[4], b[4];
-            deq8(ra[c].x, a);
-            deq8(rb[c].x, b);
-            mma_f16(acc[c], a[0], b[0], a[1], b[1], Bx[c].x, Bx[c].y);
-            mma_f16(acc[c], a[2], b[2], a[3], b[3], Bx[c].z, Bx[c].w);
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t a[4], b[4];
-            deq8(ra[c].y, a);
-            deq8(rb[c].y, b);
-            mma_f16(acc[c], a[0], b[0], a[1], b[1], By[c].x, By[c].y);
-            mma_f16(acc[c], a[2], b[2], a[3], b[3], By[c].z, By[c].w);
-        }
-        float part = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float v = tq == 0 ? acc[c][0] : acc[c][2];
-            if (lo_off)
-                v += tq == 0 ? acc[c][1] : acc[c][3];
-            part = fmaf(sv[c >> gsh], v - cs[c].y, fmaf(bv[c >> gsh], cs[c].x, part));
-        }
+        float part;
+        if (tile * 16 + 16 <= nvalid && nch == 4)  // a full tile: no per-load checks
+            part = tile_mma(aa, ab, true, true, 4, off, Bx, By, cs, sv, bv, gsh, lo_off != 0, tq);
+        else
+            part = tile_mma(aa, ab, Ra < nvalid, Rb < nvalid, nch, off, Bx, By, cs, sv, bv, gsh, lo_off != 0, tq);
         if (mine)
             out[R * ostride] = part;
     }
@@ -949,9 +961,8 @@ __device__ __forceinline__ void stage_h(int xp, const float* __restrict__ hv, in
 
 // This block's router rows -> logits, published as epoch-tagged pairs. Each row's dot product is
 // cut into kRouterParts fixed parts (one warp each, lane-strided bf16 FMAs, butterfly sum) added
-// in part order, so a logit does not depend on the grid. `bias`: this thread's logit bias (thread
-// r < rows holds row r's).
-__device__ __forceinline__ void router_rows(const Ctx& C, unsigned long long* xlog, uint32_t epoch, float bias)
+// in part order, so a logit does not depend on the grid.
+__device__ __forceinline__ void router_rows(const Ctx& C, unsigned long long* xlog, uint32_t epoch)
 {
     const int nr = C.e1 - C.e0, H = C.H, e0 = C.e0;
     const uint16_t* __restrict__ srt = C.srt;
@@ -975,61 +986,93 @@ __device__ __forceinline__ void router_rows(const Ctx& C, unsigned long long* xl
     __syncthreads();
     if (TID < nr) {
         const float4 p4 = reinterpret_cast<const float4*>(rp)[TID];
+        float bias = 0.f;
+        if (C.cur.logit_bias)
+            bias = C.bias_staged ? C.sbias[e0 + TID] : __ldg(C.cur.logit_bias + e0 + TID);
         st_pair(xlog + e0 + TID, epoch, (((p4.x + p4.y) + p4.z) + p4.w) + bias);
     }
 }
 
 // slg (logits) -> sel_idx / sel_w / sel_slot (rank order: larger fp32 logit first, equal logits ->
-// lower index). Each warp ranks its 32 logits (31 shuffles; equal keys go to the lower lane, i.e.
-// the lower index) and lists its top-k in rank order; warp 0 then merges the sorted lists: k
-// rounds, each taking the largest list head (a warp max reduction; equal heads go to the lower
-// list, i.e. the lower index). my_slot: the pool slot of this thread's expert (thread e holds
-// expert e).
-__device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, int my_slot)
+// lower index). Each warp takes its own top-k by k rounds of a warp max reduction (equal keys go to
+// the lower lane, i.e. the lower index). Two lower bounds of the overall k-th key follow: the
+// largest of the warps' k-th keys, and the k-th largest of the warps' maxima (k warps hold a key
+// at least that large). Only members of a warp's top-k at or above the larger bound can be
+// selected; they are compacted and each is ranked by counting the larger ones. slots: look the
+// selected experts' pool slots up in the staged slot-table row.
+__device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, bool slots)
 {
     const int E = C.E, k = C.k;
     const float* __restrict__ slg = C.slg;
-    uint2* __restrict__ cand = reinterpret_cast<uint2*>(C.tk);            // [kWarps][kMaxK] (key, index)
-    int* __restrict__ slot_of = reinterpret_cast<int*>(C.tk) + 2 * kWarps * kMaxK;  // [kMaxE]
+    uint2* __restrict__ wk = reinterpret_cast<uint2*>(C.tk);                       // [kWarps] (k-th key, max key)
+    int* __restrict__ wcnt = reinterpret_cast<int*>(C.tk) + 2 * kWarps + kMaxE;    // [kWarps]
+    unsigned long long* __restrict__ skey = reinterpret_cast<unsigned long long*>(C.tk + 2 * kWarps + kMaxE + kWarps);
     const int e = TID;
     const bool valid = e < E;
     const uint32_t key = valid ? ord_key(slg[e]) : 0u;  // finite logits map to keys > 0
     const int nl = (E + 31) / 32;
-    if (valid)
-        slot_of[e] = my_slot;
+    bool taken = false;
     if (WARP < nl) {
+        uint32_t kv = 0, mx = 0;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            kv = __reduce_max_sync(0xffffffffu, taken ? 0u : key);
+            const unsigned eq = __ballot_sync(0xffffffffu, !taken && key == kv && kv != 0u);
+            taken |= eq != 0u && LANE == __ffs(eq) - 1;
+            if (j == 0)
+                mx = kv;
+        }
+        if (LANE == 0)
+            wk[WARP] = make_uint2(kv, mx);  // kv is 0 when the warp holds fewer than k keys
+    }
+    __syncthreads();
+    uint32_t thr;
+    {
+        const uint2 v = LANE < nl ? wk[LANE] : make_uint2(0u, 0u);
+        const uint32_t t1 = __reduce_max_sync(0xffffffffu, v.x);
+        // rank of this lane's warp maximum among the maxima (equal ones by lane)
         int rank = 0;
 #pragma unroll
-        for (int d = 1; d < 32; ++d) {
+        for (int d = 1; d < kWarps; ++d) {
             const int src = (LANE + d) & 31;
-            const uint32_t o = __shfl_sync(0xffffffffu, key, src);
-            rank += (o > key) || (o == key && src < LANE);
+            const uint32_t o = __shfl_sync(0xffffffffu, v.y, src);
+            rank += src < nl && ((o > v.y) || (o == v.y && src < LANE));
         }
-        if (rank < k)  // lanes past E carry key 0: they pad a short list
-            cand[WARP * kMaxK + rank] = make_uint2(key, (uint32_t)e);
+        const unsigned hit = __ballot_sync(0xffffffffu, LANE < nl && rank == k - 1);
+        const uint32_t t2 = hit ? __shfl_sync(0xffffffffu, v.y, __ffs(hit) - 1) : 0u;
+        thr = max(t1, t2);
+    }
+    const bool surv = taken && key >= thr;
+    const unsigned bal = __ballot_sync(0xffffffffu, surv);
+    if (LANE == 0)
+        wcnt[WARP] = __popc(bal);
+    __syncthreads();
+    int pos = 0, ns = 0;
+#pragma unroll
+    for (int q = 0; q < kWarps; q += 4) {
+        const int4 c4 = *reinterpret_cast<const int4*>(wcnt + q);
+        pos += (q < WARP ? c4.x : 0) + (q + 1 < WARP ? c4.y : 0) + (q + 2 < WARP ? c4.z : 0) + (q + 3 < WARP ? c4.w : 0);
+        ns += c4.x + c4.y + c4.z + c4.w;
+    }
+    // composite keys: logit key above, the complement of the index below (equal logits -> the
+    // lower index ranks first); unique, so a survivor's rank is the number of larger keys
+    if (surv)
+        skey[pos + __popc(bal & ((1u << LANE) - 1u))] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)e);
+    __syncthreads();
+    if (TID < ns) {
+        const unsigned long long mine = skey[TID];
+        int rank = 0;
+#pragma unroll 4
+        for (int q = 0; q < ns; ++q)
+            rank += skey[q] > mine;
+        if (rank < k)
+            C.sel_idx[rank] = (int)(0xFFFFFFFFu - (uint32_t)mine);
     }
     __syncthreads();
     if (WARP == 0) {
-        int ptr = 0;
-        uint2 head = LANE < nl ? cand[LANE * kMaxK] : make_uint2(0u, 0u);
-        float lsel = 0.f, lmax = 0.f;
-        int isel = 0;
-#pragma unroll 1
-        for (int j = 0; j < k; ++j) {
-            const uint32_t mx = __reduce_max_sync(0xffffffffu, head.x);
-            const unsigned eq = __ballot_sync(0xffffffffu, LANE < nl && head.x == mx);
-            const int win = __ffs(eq) - 1;
-            const int ei = __shfl_sync(0xffffffffu, (int)head.y, win);
-            if (LANE == j)
-                isel = ei;
-            if (LANE == win) {
-                ++ptr;
-                head = ptr < k ? cand[LANE * kMaxK + ptr] : make_uint2(0u, 0u);
-            }
-        }
-        if (LANE < k)
-            lsel = slg[isel];
-        lmax = __shfl_sync(0xffffffffu, lsel, 0);
+        const int isel = LANE < k ? C.sel_idx[LANE] : 0;
+        const float lsel = LANE < k ? slg[isel] : 0.f;
+        const float lmax = __shfl_sync(0xffffffffu, lsel, 0);
         const float pj = LANE < k ? __expf(lsel - lmax) : 0.f;
         float denom;
         if (renorm) {
@@ -1042,9 +1085,8 @@ __device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, int my_sl
             denom = warp_sum(sum);
         }
         if (LANE < k) {
-            C.sel_idx[LANE] = isel;
             C.sel_w[LANE] = __fdividef(pj, denom);
-            C.sel_slot[LANE] = slot_of[isel];
+            C.sel_slot[LANE] = slots ? C.stab[C.tab_off + isel] : -1;
         }
     }
     __syncthreads();
@@ -1053,9 +1095,9 @@ __device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, int my_sl
 }  // namespace
 
 // Dynamic shared memory of the fused kernel: the plan plus 1024 bytes to align the staging slots.
-__host__ __device__ uint32_t decode_smem_bytes(const StepParams& P)
+__host__ __device__ uint32_t decode_smem_bytes(const StepParams& P, int grid)
 {
-    return smem_plan(P.H, P.E, P.k, P.I, P.Is, P.bits, P.sg).total + 1024;
+    return smem_plan(P.H, P.E, P.I, P.Is, P.bits, grid, P.sg, P.sgs).total + 1024;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_constant__ StepParams P)
@@ -1066,7 +1108,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     if (TID == 0)
         make_ctx(P, C, base);
     __syncthreads();
-    const StageGeo& sg = P.sg;
     const bool route = P.mode != kModeExperts;
     const bool experts = P.mode != kModeRoute;
     const bool prenorm = (P.flags & kPrenorm) != 0;
@@ -1074,9 +1115,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     const int n_steps = P.mode == kModeFull ? P.n_tokens * P.n_layers : 1;
     const long long limit = (long long)(2 * P.timeout_ns);
     const int H = C.H, K = C.k, hdim = xh_stride(C.I, C.Is);
-    // warps with side duties: the issuing thread is lane 0 of warp 0 (routed copies) and of warp
-    // kWarps - 1 (the next step's dense rows); the output words are cleared by warp kWarps - 2
-    constexpr int kIssueWarp = kWarps - 1, kClearWarp = kWarps - 2;
+    const bool shb = experts && C.sh;  // this block serves the shared expert
+    const StageGeo& g = C.g;
+    // the warp that clears this block's slice of the output words
+    constexpr int kClearWarp = kWarps - 2;
 
     if (TID == 0) {
 #pragma unroll 1
@@ -1087,10 +1129,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
 #pragma unroll 1
             for (int i = 0; i < 3; ++i)
                 prefetch_map(&P.tmap[i]);
-        const LayerDesc L0 = P.layers[P.layer0];
-        issue_dense(P, C, L0, route, experts);
-        if (experts)
-            issue_sdown(P, C, L0);
+        issue_dense(P, C, P.layer0, route, shb);
+        if (shb)
+            issue_expert(C, C.cur.shared_blob, P.smaps + 3 * P.layer0, 0);
     }
     // this block's slice of the first step's output words starts at zero
     if (experts && WARP == kClearWarp) {
@@ -1101,9 +1142,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     }
 
     // mbarrier phases (block-uniform)
-    uint32_t ph_dense = 0, ph_sdown = 0, ph_rsc = 0, ph_down = 0, ph_gu = 0;  // ph_gu: bit 2s + m
-    bool dense_pending = true, sdown_pending = experts, rsc_pending = false, down_pending = false;
-    uint32_t gu_pending = 0;
+    uint32_t ph_dense = 0, ph_down = 0, ph_gu = 0;  // ph_gu: bit 2s + m
+    bool dense_pending = true, down_pending = shb && C.d1 > C.d0;
+    uint32_t gu_pending = (shb && C.r1 > C.r0) ? (1u << (2 * g.nslot_gu)) - 1u : 0u;
 
     bool ok = grid_barrier(P, limit);
 
@@ -1111,12 +1152,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     for (int step = 0; ok && step < n_steps; ++step) {
         const int t = step / P.n_layers, li = step - t * P.n_layers;
         const int l = P.layer0 + li;
-        const LayerDesc L = P.layers[l];
-        const LayerDesc Ln = P.layers[P.layer0 + (step + 1) % P.n_layers];
-        // this thread's expert's slot and this thread's router row's bias, loaded now so that they
-        // are in registers by the time they are needed
-        const int my_slot = (P.mode == kModeFull && TID < C.E) ? P.table[(size_t)l * C.E + TID] : -1;
-        const float bias = (route && L.logit_bias && TID < C.e1 - C.e0) ? __ldg(L.logit_bias + C.e0 + TID) : 0.f;
+        const int ln = P.layer0 + (step + 1) % P.n_layers;
         const uint32_t epoch = P.epoch0 + (uint32_t)step;
         long long* X = P.xacc + (size_t)(step & 1) * H;
 
@@ -1124,243 +1160,193 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         {
             const bool fresh = li == 0;
             const size_t trow = (size_t)P.n_layers + 1;
+            if (step > 0 && experts && !(ok = wait_flags(P.xflag, GRID, epoch - 1, limit, P.status)))
+                break;
             float* tr_prev = (step > 0 && fresh && P.trace) ? P.trace + ((size_t)(t - 1) * trow + P.n_layers) * H : nullptr;
             float* tr_cur = P.trace ? P.trace + ((size_t)t * trow + li) * H : nullptr;
-            const bool in_f32 = prenorm;
-            const char* xin = (const char*)P.x_in + (size_t)t * H * (in_f32 ? 4 : 2);
+            const char* xin = (const char*)P.x_in + (size_t)t * H * (prenorm ? 4 : 2);
             if (!(ok = layer_input(C, (step > 0 && experts) ? P.xacc + (size_t)((step - 1) & 1) * H : nullptr, K + 1,
-                                   residual, fresh, xin, in_f32, prenorm || li > 0, prenorm,
+                                   residual, fresh, xin, prenorm, prenorm || li > 0, prenorm,
                                    (step > 0 && fresh) ? P.y_out + (size_t)(t - 1) * H : nullptr, tr_prev, tr_cur,
                                    limit, P.status)))
                 break;
         }
 
-        // ---------------- 2. router rows -> logits ----------------
+        // ---------------- 2. router rows -> logits; gamma ----------------
         if (!(ok = wait_block(C.mbar + kMbDense, ph_dense & 1, limit, P.status)))
             break;
         ++ph_dense;
         dense_pending = false;
-        if (route) {
-            router_rows(C, P.xlog, epoch, bias);
-            // ---------------- 3. top-k ----------------
-            if (!(ok = poll_pairs(P.xlog, C.E, epoch, C.slg, false, limit, P.status)))
-                break;
-            topk_select(C, (P.flags & kRenorm) != 0, my_slot);
-            if (CTA == 0 && TID < K) {
-                const size_t o = ((size_t)t * P.n_layers + li) * K + TID;
-                if (P.topk_idx)
-                    P.topk_idx[o] = C.sel_idx[TID];
-                if (P.topk_w)
-                    P.topk_w[o] = C.sel_w[TID];
-            }
-            if (!experts)
-                break;  // a route-only launch has one step
-            if (TID < K && C.sel_slot[TID] < 0)
-                set_status(P.status, kStatusNotResident);
-        } else {
-            if (TID < K) {
-                C.sel_w[TID] = P.topk_w[TID];
-                C.sel_slot[TID] = P.slots[TID];
-                C.sel_idx[TID] = -1;
-            }
-            __syncthreads();
-        }
-
-        // ---------------- 4. this block's routed bytes, all issued now ----------------
-        const int rslot = C.sel_slot[C.j];
-        const bool blob = rslot >= 0;
-        const bool have_gu = blob && C.r1 > C.r0, have_d = blob && C.d1 > C.d0;
-        if (blob && TID == 0) {
-            fence_async_smem();
-            issue_routed(P, C, rslot);
-        }
-        rsc_pending = blob;
-        down_pending = have_d;
-        if (have_gu)
-            gu_pending = (1u << (2 * sg.nslot_gu)) - 1u;
-
-        // ---------------- 5. shared expert, next step's dense rows ----------------
-        {
-            // gamma = sigmoid(w_sg . u): one warp
-            if (WARP == 1) {
-                float z = 0.f;
+        if (route)
+            router_rows(C, P.xlog, epoch);
+        if (shb && WARP == 1) {
+            float z = 0.f;
 #pragma unroll 2
-                for (int v = LANE; v < H / 8; v += 32)
-                    z = dot8_bf16(*reinterpret_cast<const uint4*>(C.swsg + 8 * v),
-                                  *reinterpret_cast<const uint4*>(C.su + 8 * v), z);
-                z = warp_sum(z);
-                if (LANE == 0)
-                    C.misc[0] = __fdividef(1.f, 1.f + __expf(-z));
-            }
-            // shared gate/up rows [s0, s1): items (matrix, column block, tile)
-            const int ns = C.s1 - C.s0;
-            const int ncb = sg.ncb_gu, nt = cdiv(ns, 16);
-            const int cpb = sg.cbw_gu / 32;
-#pragma unroll 1
-            for (int it = WARP; ns > 0 && it < 2 * ncb; it += kWarps) {
-                const int m = it / ncb, cb = it - m * ncb;
-                const int c0 = cb * cpb;
-                box_mma(C.sgq + (size_t)m * sg.Rs * C.rb_gu + cb * kCb, 0u, C.rb_gu, ns, 0, nt, c0,
-                        imin(cpb, C.NCu - c0), C.sup, 0, C.scs, C.ssb + (2 * m) * C.span_sgu + C.imisc[2 * m],
-                        C.ssb + (2 * m + 1) * C.span_sgu + C.imisc[2 * m + 1], C.ngu * 2, C.xp - 1,
-                        C.sp + m * ncb + cb, 2 * ncb);
-            }
-            __syncthreads();
-            if (TID < ns) {
-                const float* pg = C.sp + TID * 2 * ncb;
-                float gg = 0.f, vv = 0.f;
-#pragma unroll 4
-                for (int cb = 0; cb < ncb; ++cb) {
-                    gg += pg[cb];
-                    vv += pg[ncb + cb];
-                }
-                st_pair(P.xh + (size_t)K * hdim + C.s0 + TID, epoch, __fdividef(gg, 1.f + __expf(-gg)) * vv);
-            }
-            // the router rows, gate vector and shared gate/up rows are consumed: the next step's
-            if (step + 1 < n_steps && WARP == kIssueWarp && LANE == 0) {
-                fence_async_smem();
-                issue_dense(P, C, Ln, route, experts);
-            }
-            dense_pending = step + 1 < n_steps;
-            // the shared expert's h, then its down rows [o0, o1)
-            if (!(ok = poll_pairs(P.xh + (size_t)K * hdim, C.Is, epoch, C.hv, true, limit, P.status)))
-                break;
-            // every block has read the previous step's output words (it published h_shared after):
-            // clear this block's slice of them for the next step, and order that before this
-            // warp's later stores
-            if (step + 1 < n_steps && WARP == kClearWarp) {
-#pragma unroll 1
-                for (int o = C.o0 + LANE; o < C.o1; o += 32)
-                    st_s64(P.xacc + (size_t)((step + 1) & 1) * H + o, 0);
-                fence_gpu();
-            }
-            stage_h(C.xp, C.hv, C.Is, C.shs, C.chs);
-            if (!(ok = wait_block(C.mbar + kMbSdown, ph_sdown & 1, limit, P.status)))
-                break;
-            ++ph_sdown;
-            sdown_pending = false;
-            const int nd = C.o1 - C.o0, ntd = cdiv(nd, 16);
-            const int cw = imin(kCb, C.rb_ds), cpd = cw / 32;
-#pragma unroll 1
-            for (int it = WARP; nd > 0 && it < C.ncb_ds; it += kWarps) {
-                const int cb = it, c0 = cb * cpd;
-                box_mma(C.sdq + cb * kCb, 0u, C.rb_ds, nd, 0, ntd, c0, imin(cpd, C.NCds - c0), C.shs, C.KDs,
-                        C.chs, C.sdsb + C.imisc[4], C.sdsb + C.span_sd + C.imisc[5], C.ngds * 2, C.xp - 1, C.spd + cb,
-                        C.ncb_ds);
-            }
-            __syncthreads();
-            if (TID < nd) {
-                float ys = 0.f;
-#pragma unroll 1
-                for (int cb = 0; cb < C.ncb_ds; ++cb)
-                    ys += C.spd[TID * C.ncb_ds + cb];
-                add_out(X + C.o0 + TID, C.misc[0] * ys, P.status);
-            }
-            __syncthreads();
-            if (step + 1 < n_steps && WARP == kIssueWarp) {
-                if (LANE == 0) {
-                    fence_async_smem();
-                    issue_sdown(P, C, Ln);
-                }
-            }
-            sdown_pending = step + 1 < n_steps;
+            for (int v = LANE; v < H / 8; v += 32)
+                z = dot8_bf16(*reinterpret_cast<const uint4*>(C.swsg + 8 * v), *reinterpret_cast<const uint4*>(C.su + 8 * v),
+                              z);
+            z = warp_sum(z);
+            if (LANE == 0)
+                C.misc[0] = __fdividef(1.f, 1.f + __expf(-z));
         }
 
-        // ---------------- 6. routed gate/up -> h_j ----------------
-        if (blob) {
-            if (!(ok = wait_block(C.mbar + kMbRsc, ph_rsc & 1, limit, P.status)))
-                break;
-            ++ph_rsc;
-            rsc_pending = false;
-        }
-        if (have_gu) {
-            const int nrc = cdiv(C.r1 - C.r0, sg.bh_gu), cpb = sg.cbw_gu / 32;
-            const int per_m = nrc * sg.cpg_gu;  // items per matrix of a column group: (row box, column block)
-            bool wok = true;
+        // ---------------- 3. the expert's gate/up rows -> h (shared expert: now) ----------------
+        // (the routed experts' come after the top-k; the code is shared through this lambda-free
+        // loop body, run at most once per step)
+        bool blob = false;
+        int rslot = -1;
+        const CUtensorMap* maps = nullptr;
 #pragma unroll 1
-            for (int cg = 0; cg < sg.ncs_gu; ++cg) {
-                const int sl = cg % sg.nslot_gu;
-#pragma unroll 1
-                for (int it = WARP; wok && it < 2 * per_m; it += kWarps) {
-                    const int m = it >= per_m, q = it - m * per_m;
-                    const int cbl = q % sg.cpg_gu, rc = q / sg.cpg_gu;
-                    const int cb = cg * sg.cpg_gu + cbl;
-                    const int nvalid = imin(sg.bh_gu, C.r1 - C.r0 - rc * sg.bh_gu);
-                    if (cb >= sg.ncb_gu)
-                        continue;
-                    if (!(wok = wait_warp(C.mbar + 2 * sl + m, (ph_gu >> (2 * sl + m)) & 1, limit)))
+        for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1) {
+                // ---------------- 4. top-k ----------------
+                if (route) {
+                    if (!(ok = poll_pairs(P.xlog, C.E, epoch, C.slg, true, limit, P.status)))
                         break;
-                    const int c0 = cb * cpb;
-                    box_mma(gu_copy_at(C, sg, sl, m, rc) + (size_t)cbl * sg.bh_gu * sg.cbw_gu, sg.swz_gu ? 7u : 0u,
-                            sg.cbw_gu, nvalid, 0, cdiv(nvalid, 16), c0, imin(cpb, C.NCu - c0), C.sup, 0, C.scs,
-                            C.rsb + (2 * m) * C.span_gu + C.imisc[8 + 2 * m] + rc * sg.bh_gu * C.ngu * 2,
-                            C.rsb + (2 * m + 1) * C.span_gu + C.imisc[9 + 2 * m] + rc * sg.bh_gu * C.ngu * 2, C.ngu * 2,
-                            C.xp - 1, C.sp + (rc * sg.bh_gu) * 2 * sg.ncb_gu + m * sg.ncb_gu + cb, 2 * sg.ncb_gu);
-                }
-                if (__syncthreads_or(!wok)) {
-                    if (TID == 0)
-                        set_status(P.status, kStatusTimeout);
-                    ok = false;
-                    break;
-                }
-                ph_gu ^= 3u << (2 * sl);
-                gu_pending &= ~(3u << (2 * sl));
-                // slot sl is free again: its next column group (when the groups take turns)
-                if (cg + sg.nslot_gu < sg.ncs_gu) {
-                    if (TID == 0) {
-                        fence_async_smem();
-                        issue_gu_group(P, C, rslot, cg + sg.nslot_gu, sl);
+                    topk_select(C, (P.flags & kRenorm) != 0, P.mode == kModeFull);
+                    if (CTA == 0 && TID < K) {
+                        const size_t o = ((size_t)t * P.n_layers + li) * K + TID;
+                        if (P.topk_idx)
+                            P.topk_idx[o] = C.sel_idx[TID];
+                        if (P.topk_w)
+                            P.topk_w[o] = C.sel_w[TID];
                     }
-                    gu_pending |= 3u << (2 * sl);
+                    if (!experts)
+                        break;  // a route-only launch has one step
+                    if (TID < K && C.sel_slot[TID] < 0)
+                        set_status(P.status, kStatusNotResident);
+                } else {
+                    if (TID < K) {
+                        C.sel_w[TID] = P.topk_w[TID];
+                        C.sel_slot[TID] = P.slots[TID];
+                        C.sel_idx[TID] = -1;
+                    }
+                    __syncthreads();
                 }
-            }
-            if (!ok)
-                break;
-        }
-        __syncthreads();
-        unsigned long long* xh = P.xh + (size_t)C.j * hdim;
+                // the router rows and gate vector are consumed: the next step's; every block has
+                // read the previous step's output words (it published its logits after): clear
+                // this block's slice of them for the next step, ordered before this warp's later
+                // stores
+                if (step + 1 < n_steps) {
+                    if (WARP == kClearWarp) {
 #pragma unroll 1
-        for (int r = TID; r < C.r1 - C.r0; r += kThreads) {
-            float h = 0.f;
-            if (blob) {
-                const int ncb = sg.ncb_gu;
-                const float* pg = C.sp + r * 2 * ncb;
-                float gg = 0.f, vv = 0.f;
-#pragma unroll 4
-                for (int cb = 0; cb < ncb; ++cb) {
-                    gg += pg[cb];
-                    vv += pg[ncb + cb];
+                        for (int o = C.o0 + LANE; o < C.o1; o += 32)
+                            st_s64(P.xacc + (size_t)((step + 1) & 1) * H + o, 0);
+                        fence_gpu();
+                    }
                 }
-                h = __fdividef(gg, 1.f + __expf(-gg)) * vv;
+                if (shb)
+                    break;  // the shared expert's rows are done
+                // this block's routed expert: every byte it reads of it, issued now
+                rslot = C.sel_slot[C.j];
+                blob = rslot >= 0;
+                maps = P.tmap;
+                if (blob && TID == 0)
+                    issue_expert(C, P.arena + (uint64_t)rslot * P.stride, maps, rslot);
+                down_pending = blob && C.d1 > C.d0;
+                if (blob && C.r1 > C.r0)
+                    gu_pending = (1u << (2 * g.nslot_gu)) - 1u;
+            } else {
+                if (!shb)
+                    continue;
+                blob = true;
+                maps = P.smaps + 3 * l;
             }
-            st_pair(xh + C.r0 + r, epoch, h);
-        }
-
-        // ---------------- 7. the group's h_j, down rows, contributions ----------------
-        if (C.d1 > C.d0) {
-            if (!(ok = poll_pairs(xh, C.I, epoch, C.hv, false, limit, P.status)))
-                break;
-            if (have_d) {
-                stage_h(C.xp, C.hv, C.I, C.shj, C.chj);
-                const int nrc = cdiv(C.d1 - C.d0, sg.bh_d), tb = cdiv(sg.bh_d, 16), cpd = sg.cbw_d / 32;
-                // items (row box, column block, group of tpi tiles), about one per warp
-                const int tpi = cdiv(nrc * sg.cpg_d * tb, kWarps), ntg = cdiv(tb, tpi);
+            const bool have_gu = blob && C.r1 > C.r0;
+            if (have_gu) {
+                const int nrc = cdiv(C.r1 - C.r0, g.bh_gu), cpb = g.cbw_gu / 32;
+                const int per_m = nrc * g.cpg_gu;  // items per matrix of a column group: (row box, column block)
                 bool wok = true;
 #pragma unroll 1
-                for (int it = WARP; it < nrc * sg.cpg_d * ntg; it += kWarps) {
-                    const int tg = it % ntg, q = it / ntg, cb = q % sg.cpg_d, rc = q / sg.cpg_d;
-                    const int nvalid = imin(sg.bh_d, C.d1 - C.d0 - rc * sg.bh_d);
+                for (int cg = 0; cg < g.ncs_gu; ++cg) {
+                    const int sl = cg % g.nslot_gu;
+#pragma unroll 1
+                    for (int it = WARP; wok && it < 2 * per_m; it += kWarps) {
+                        const int m = it >= per_m, q = it - m * per_m;
+                        const int cbl = q % g.cpg_gu, rc = q / g.cpg_gu;
+                        const int cb = cg * g.cpg_gu + cbl;
+                        const int nvalid = imin(g.bh_gu, C.r1 - C.r0 - rc * g.bh_gu);
+                        if (cb >= g.ncb_gu)
+                            continue;
+                        if (!(wok = wait_warp(C.mbar + 2 * sl + m, (ph_gu >> (2 * sl + m)) & 1, limit)))
+                            break;
+                        const int c0 = cb * cpb;
+                        box_mma(gu_copy_at(C, sl, m, rc) + (size_t)cbl * g.bh_gu * g.cbw_gu, g.swz_gu ? 7u : 0u, g.cbw_gu,
+                                nvalid, 0, cdiv(nvalid, 16), c0, imin(cpb, C.NCu - c0), C.sup, 0, C.scs,
+                                C.rsb + (2 * m) * C.span_gu + C.sc_off[2 * m] + rc * g.bh_gu * C.ngu * 2,
+                                C.rsb + (2 * m + 1) * C.span_gu + C.sc_off[2 * m + 1] + rc * g.bh_gu * C.ngu * 2,
+                                C.ngu * 2, C.xp - 1, C.sp + (rc * g.bh_gu) * 2 * g.ncb_gu + m * g.ncb_gu + cb,
+                                2 * g.ncb_gu);
+                    }
+                    if (__syncthreads_or(!wok)) {
+                        if (TID == 0)
+                            set_status(P.status, kStatusTimeout);
+                        ok = false;
+                        break;
+                    }
+                    ph_gu ^= 3u << (2 * sl);
+                    gu_pending &= ~(3u << (2 * sl));
+                    // slot sl is free again: its next column group (when the groups take turns)
+                    if (cg + g.nslot_gu < g.ncs_gu) {
+                        if (TID == 0)
+#pragma unroll 1
+                            for (int m = 0; m < 2; ++m)
+                                issue_gu(C, shb ? C.cur.shared_blob : P.arena + (uint64_t)rslot * P.stride, maps,
+                                         shb ? 0 : rslot, cg + g.nslot_gu, sl, m, false);
+                        gu_pending |= 3u << (2 * sl);
+                    }
+                }
+                if (!ok)
+                    break;
+            }
+            __syncthreads();
+            unsigned long long* xh = P.xh + (size_t)C.j * hdim;
+#pragma unroll 1
+            for (int r = TID; r < C.r1 - C.r0; r += kThreads) {
+                float h = 0.f;
+                if (blob) {
+                    const int ncb = g.ncb_gu;
+                    const float* pg = C.sp + r * 2 * ncb;
+                    float gg = 0.f, vv = 0.f;
+#pragma unroll 4
+                    for (int cb = 0; cb < ncb; ++cb) {
+                        gg += pg[cb];
+                        vv += pg[ncb + cb];
+                    }
+                    h = __fdividef(gg, 1.f + __expf(-gg)) * vv;
+                }
+                st_pair(xh + C.r0 + r, epoch, h);
+            }
+        }
+        if (!ok || !experts)
+            break;
+
+        // ---------------- 5. the group's h, down rows, contributions ----------------
+        const bool have_d = blob && C.d1 > C.d0;
+        if (C.d1 > C.d0) {
+            unsigned long long* xh = P.xh + (size_t)C.j * hdim;
+            if (!(ok = poll_pairs(xh, C.Ie, epoch, C.hv, false, limit, P.status)))
+                break;
+            if (have_d) {
+                stage_h(C.xp, C.hv, C.Ie, C.shj, C.chj);
+                const int nrc = cdiv(C.d1 - C.d0, g.bh_d), tb = cdiv(g.bh_d, 16), cpd = g.cbw_d / 32;
+                // items (row box, column block, group of tpi tiles), about one per warp
+                const int tpi = cdiv(nrc * g.cpg_d * tb, kWarps), ntg = cdiv(tb, tpi);
+                bool wok = true;
+#pragma unroll 1
+                for (int it = WARP; it < nrc * g.cpg_d * ntg; it += kWarps) {
+                    const int tg = it % ntg, q = it / ntg, cb = q % g.cpg_d, rc = q / g.cpg_d;
+                    const int nvalid = imin(g.bh_d, C.d1 - C.d0 - rc * g.bh_d);
                     const int tt0 = tg * tpi, tt1 = imin(tt0 + tpi, cdiv(nvalid, 16));
                     if (tt0 >= tt1)
                         continue;
                     if (!(wok = wait_warp(C.mbar + kMbDown, ph_down & 1, limit)))
                         break;
                     const int c0 = cb * cpd;
-                    box_mma(d_copy_at(C, sg, rc) + (size_t)cb * sg.bh_d * sg.cbw_d, sg.swz_d ? 7u : 0u, sg.cbw_d, nvalid,
-                            tt0, tt1, c0, imin(cpd, C.NCd - c0), C.shj, C.KD, C.chj,
-                            C.rdsb + C.imisc[12] + rc * sg.bh_d * C.ngd * 2,
-                            C.rdsb + C.span_d + C.imisc[13] + rc * sg.bh_d * C.ngd * 2, C.ngd * 2, C.xp - 1,
-                            C.spd + (rc * sg.bh_d) * sg.ncb_d + cb, sg.ncb_d);
+                    box_mma(d_copy_at(C, rc) + (size_t)cb * g.bh_d * g.cbw_d, g.swz_d ? 7u : 0u, g.cbw_d, nvalid, tt0, tt1,
+                            c0, imin(cpd, C.NCd - c0), C.shj, C.KD, C.chj, C.rdsb + C.sc_off[4] + rc * g.bh_d * C.ngd * 2,
+                            C.rdsb + C.span_d + C.sc_off[5] + rc * g.bh_d * C.ngd * 2, C.ngd * 2, C.xp - 1,
+                            C.spd + (rc * g.bh_d) * g.ncb_d + cb, g.ncb_d);
                 }
                 if (__syncthreads_or(!wok)) {
                     if (TID == 0)
@@ -1371,23 +1357,44 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
                 ++ph_down;
                 down_pending = false;
             }
+            const float wj = C.sh ? C.misc[0] : C.sel_w[C.j];
 #pragma unroll 1
             for (int r = TID; r < C.d1 - C.d0; r += kThreads) {
                 float yj = 0.f;
                 if (have_d)
 #pragma unroll 1
-                    for (int cb = 0; cb < sg.ncb_d; ++cb)
-                        yj += C.spd[r * sg.ncb_d + cb];
-                add_out(X + C.d0 + r, C.sel_w[C.j] * yj, P.status);
+                    for (int cb = 0; cb < g.ncb_d; ++cb)
+                        yj += C.spd[r * g.ncb_d + cb];
+                add_out(X + C.d0 + r, wj * yj, P.status);
             }
         }
         __syncthreads();
+        // the next step's router rows, slot-table row, bias, gate vector and (the shared expert's
+        // blocks) shared rows: the staging is free again
+        if (step + 1 < n_steps) {
+            if (TID == 0) {
+                issue_dense(P, C, ln, route, shb);
+                if (shb)
+                    issue_expert(C, C.cur.shared_blob, P.smaps + 3 * ln, 0);
+            }
+            dense_pending = true;
+        }
+        if (shb && step + 1 < n_steps) {
+            down_pending = C.d1 > C.d0;
+            if (C.r1 > C.r0)
+                gu_pending = (1u << (2 * g.nslot_gu)) - 1u;
+        }
+        // this block's contributions to the step's output words are in: its flag
+        if (TID == 0)
+            asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(P.xflag + CTA), "l"((unsigned long long)epoch)
+                         : "memory");
     }
 
     // the last step's output
     if (ok && experts) {
         const int s = n_steps - 1, t = s / P.n_layers;
-        ok = layer_input(C, P.xacc + (size_t)(s & 1) * H, K + 1, residual, false, nullptr, false, true, false,
+        ok = wait_flags(P.xflag, GRID, P.epoch0 + (uint32_t)s, limit, P.status) &&
+             layer_input(C, P.xacc + (size_t)(s & 1) * H, K + 1, residual, false, nullptr, false, true, false,
                          P.y_out + (size_t)t * H,
                          P.trace ? P.trace + ((size_t)t * (P.n_layers + 1) + P.n_layers) * H : nullptr, nullptr, limit,
                          P.status);
@@ -1404,14 +1411,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         for (int i = 0; i < 2 * kMaxGuSlots; ++i)
             if (gu_pending & (1u << i))
                 drain(C.mbar + i, (ph_gu >> i) & 1);
-        if (rsc_pending)
-            drain(C.mbar + kMbRsc, ph_rsc & 1);
         if (down_pending)
             drain(C.mbar + kMbDown, ph_down & 1);
         if (dense_pending)
             drain(C.mbar + kMbDense, ph_dense & 1);
-        if (sdown_pending)
-            drain(C.mbar + kMbSdown, ph_sdown & 1);
     }
 }
 

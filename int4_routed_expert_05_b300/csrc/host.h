@@ -103,22 +103,26 @@ inline int encode_tiles16(CUtensorMap* map, const void* ptr, int cols, int rows,
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
-// Staging plan of the fused kernel for a shape on `grid` blocks (one per SM): every routed byte of
-// a block fetched at once when that fits in shared memory, else the gate/up rows in column groups
-// that take turns in fewer slots. Returns the dynamic shared memory bytes and the geometry in *sg,
-// or 0 when the shape cannot be staged (grid smaller than top_k, or too little shared memory).
-inline uint32_t plan_decode(int H, int E, int k, int I, int Is, int bits, int grid, int smem_optin, StageGeo* sg)
+// Staging plan of the fused kernel for a shape on `grid` blocks (one per SM): k + 1 groups of
+// blocks (the routed experts and the shared expert); every byte a block reads of its expert
+// fetched at once when that fits in shared memory, else the gate/up rows in column groups that
+// take turns in fewer slots. Returns the dynamic shared memory bytes and the two geometries, or 0
+// when the shape cannot be staged (fewer blocks than groups, or too little shared memory).
+inline uint32_t plan_decode(int H, int E, int k, int I, int Is, int bits, int grid, int smem_optin, StageGeo* sg,
+                            StageGeo* sgs)
 {
-    if (grid < k || grid > kMaxGrid)
+    if (grid < k + 1 || grid > kMaxGrid)
         return 0;
     for (int ncs = 1; ncs <= 16; ncs *= 2)
         for (int nslot = ncs; nslot >= 1; nslot /= 2) {
-            const StageGeo g = stage_geo(H, E, k, I, Is, bits, grid, ncs, nslot);
-            if (g.nslot_gu > kMaxGuSlots || g.ncs_gu != ncs)
+            const StageGeo g = stage_geo(H, I, bits, grid, k + 1, ncs, nslot);
+            const StageGeo gs = stage_geo(H, Is, bits, grid, k + 1, ncs, nslot);
+            if (g.nslot_gu > kMaxGuSlots || gs.nslot_gu > kMaxGuSlots || g.ncs_gu != ncs)
                 continue;
-            const uint32_t bytes = smem_plan(H, E, k, I, Is, bits, g).total + 1024;
+            const uint32_t bytes = smem_plan(H, E, I, Is, bits, grid, g, gs).total + 1024;
             if (bytes <= (uint32_t)smem_optin) {
                 *sg = g;
+                *sgs = gs;
                 return bytes;
             }
         }

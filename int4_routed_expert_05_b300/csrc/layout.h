@@ -112,16 +112,19 @@ MOE_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
 MOE_HD int imin(int a, int b) { return a < b ? a : b; }
 MOE_HD int imax(int a, int b) { return a > b ? a : b; }
 
-// How one block's share of a routed expert is staged. Block i of an expert's group owns gate/up
-// rows [i * SRgu, (i + 1) * SRgu) and down rows [i * SRd, (i + 1) * SRd), clipped to the matrix.
-// They are fetched by a few large tensor copies: a copy is a box of bh rows by cpg column blocks
-// (a column block is 128 bytes, 128-byte swizzled, or the whole row when rows are narrower) and
-// lands as [column block][row][column-block bytes]. Rows a box reads beyond the block's range lie
-// past the end of the matrix (zero-filled by the copy engine, no memory traffic), because SRgu
-// and SRd are whole multiples of the box heights. Gate and up rows are fetched in ncs_gu column
-// groups; a slot holds the gate and the up copies of one group, and with fewer slots than groups
+// The k routed experts of a step and the shared expert are served by k + 1 groups of blocks:
+// group j < k serves the expert of rank j, group k the shared expert.
+// How one block's share of an expert is staged. Block i of a group owns gate/up rows
+// [i * SRgu, (i + 1) * SRgu) and down rows [i * SRd, (i + 1) * SRd), clipped to the matrix. They
+// are fetched by a few large tensor copies: a copy is a box of bh rows by cpg column blocks (a
+// column block is 128 bytes, 128-byte swizzled, or the whole row when rows are narrower) and lands
+// as [column block][row][column-block bytes]. Rows a box reads beyond the block's range lie past
+// the end of the matrix (zero-filled by the copy engine, no memory traffic), because SRgu and SRd
+// are whole multiples of the box heights. Gate and up rows are fetched in ncs_gu column groups; a
+// slot holds the gate and the up copies of one group, and with fewer slots than groups
 // (nslot_gu < ncs_gu) the groups take turns (a slot is refilled once the block is done with it).
-// Down rows are fetched all at once.
+// Down rows are fetched all at once. Routed and shared experts have one geometry each (their
+// intermediate sizes may differ).
 struct StageGeo {
     int SRgu, SRd;         // gate/up rows and down rows per block of a group
     int bh_gu, bh_d;       // box rows (<= 256)
@@ -134,25 +137,25 @@ struct StageGeo {
     int nslot_gu;          // gate/up column-group slots
     uint32_t gu_copy;      // shared-memory bytes of one gate (or up) copy, 1024-aligned
     uint32_t d_copy;       // shared-memory bytes of one down copy, 1024-aligned
-    int Rr, Rs, Rsd;       // most router rows, shared gate/up rows, shared down rows per block
 };
 
 MOE_HD uint32_t align1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 
-// ncs_gu / nslot_gu: column groups and slots of the gate/up rows (1 / 1 fetches every gate/up
-// byte of the block at once).
-MOE_HD StageGeo stage_geo(int H, int E, int k, int I, int Is, int bits, int G, int ncs_gu, int nslot_gu)
+// Geometry of an expert with intermediate size Ie served by groups of at least G / ngroups
+// blocks. ncs_gu / nslot_gu: column groups and slots of the gate/up rows (1 / 1 fetches every
+// gate/up byte of the block at once).
+MOE_HD StageGeo stage_geo(int H, int Ie, int bits, int G, int ngroups, int ncs_gu, int nslot_gu)
 {
     StageGeo s{};
-    const int nmin = imax(1, G / k);  // smallest group
-    const int rgu = cdiv(I, nmin), rd = cdiv(H, nmin);
+    const int nmin = imax(1, G / ngroups);  // smallest group
+    const int rgu = cdiv(Ie, nmin), rd = cdiv(H, nmin);
     s.nr_gu = cdiv(rgu, kMaxBoxRows);
     s.bh_gu = cdiv(rgu, s.nr_gu);
     s.SRgu = s.nr_gu * s.bh_gu;
     s.nr_d = cdiv(rd, kMaxBoxRows);
     s.bh_d = cdiv(rd, s.nr_d);
     s.SRd = s.nr_d * s.bh_d;
-    const int rb_gu = H * bits / 8, rb_d = I * bits / 8;
+    const int rb_gu = H * bits / 8, rb_d = Ie * bits / 8;
     s.swz_gu = rb_gu >= kCb;
     s.swz_d = rb_d >= kCb;
     s.cbw_gu = s.swz_gu ? kCb : rb_gu;
@@ -167,10 +170,13 @@ MOE_HD StageGeo stage_geo(int H, int E, int k, int I, int Is, int bits, int G, i
     s.cpg_d = s.ncb_d;
     s.gu_copy = align1k((uint32_t)s.cbw_gu * s.bh_gu * s.cpg_gu);
     s.d_copy = align1k((uint32_t)s.cbw_d * s.bh_d * s.cpg_d);
-    s.Rr = cdiv(E, G);
-    s.Rs = cdiv(Is, G);
-    s.Rsd = cdiv(H, G);
     return s;
+}
+
+// Staging bytes of a geometry: its gate/up slots and its down copies.
+MOE_HD uint32_t stage_bytes(const StageGeo& g)
+{
+    return (uint32_t)g.nslot_gu * 2 * g.nr_gu * g.gu_copy + (uint32_t)g.nr_d * g.d_copy;
 }
 
 // Shared-memory room for the scale or bias rows [r0, r0 + n) of a section whose rows hold row_b
@@ -188,7 +194,8 @@ struct StepParams {
     CUtensorMap tmap[3];
     int H, E, k, I, Is, bits, group, flags;
     BlobGeo geo, geo_s;           // routed / shared blob geometry
-    StageGeo sg;
+    StageGeo sg, sgs;             // staging of a routed / the shared expert's rows
+    const CUtensorMap* smaps;     // [L][3] the same maps over each layer's shared-expert blob (workspace)
     const uint8_t* arena;
     uint64_t stride;
     const int32_t* table;         // [L][E] slot of (layer, expert), -1 if absent
@@ -204,6 +211,7 @@ struct StepParams {
     unsigned long long* xlog;     // [E] (epoch << 32 | fp32 logit)
     unsigned long long* xh;       // [k + 1][max(I, Is)] (epoch << 32 | fp32 h); row k: shared expert
     long long* xacc;              // [2][H] counted fixed-point output words (step parity)
+    unsigned long long* xflag;    // [grid] epoch of the step whose output words the block has finished
     unsigned long long* bar;      // launch-start barrier counter (a multiple of the grid between launches)
     int* status;
     uint32_t epoch0;              // epoch of the launch's first step (>= 1)
@@ -219,33 +227,31 @@ struct StepParams {
 
 struct SmemPlan {
     uint32_t ctx, mbar, ctl, x, u, up, uc, lg, tk;
-    uint32_t rt, wsg, sgq, ssb, sdq, sdsb;
+    uint32_t rt, wsg, tab, bias;
     uint32_t ring, rsb, rdsb;
-    uint32_t hs, uhs, hj, uhj, hv, sp, spd, rp;
+    uint32_t hj, uhj, hv, sp, spd, rp;
     uint32_t total;
 };
 
 constexpr uint32_t kCtxBytes = 1024;   // room for the kernel's block context
 // mbarriers: gate/up copies [2 * kMaxGuSlots] (slot s: gate 2s, up 2s + 1), then down copies,
-// routed scales, dense rows, shared down rows
+// dense rows
 constexpr int kMaxGuSlots = 8;
-constexpr int kMbDown = 2 * kMaxGuSlots, kMbRsc = kMbDown + 1, kMbDense = kMbDown + 2, kMbSdown = kMbDown + 3;
-constexpr int kNumMbar = kMbDown + 4;
+constexpr int kMbDown = 2 * kMaxGuSlots, kMbDense = kMbDown + 1;
+constexpr int kNumMbar = kMbDown + 2;
 // control words: sel_idx[kMaxK], sel_w[kMaxK], sel_slot[kMaxK], red[64], misc[32], imisc[16]
 constexpr int kCtlWords = 3 * kMaxK + 64 + 32 + 16;
 
 MOE_HD uint32_t align_to(uint32_t v, uint32_t a) { return (v + a - 1) & ~(a - 1); }
 
-MOE_HD SmemPlan smem_plan(int H, int E, int k, int I, int Is, int bits, const StageGeo& sg)
+MOE_HD SmemPlan smem_plan(int H, int E, int I, int Is, int bits, int G, const StageGeo& sg, const StageGeo& sgs)
 {
     const int xp = (bits == 8) ? 2 : 1;           // int8 codes are read as two 4-bit fields
     const int KU = H * xp;                         // expanded length of u
     const int NCu = KU / kChunk;
-    const int KD = I * xp, KDs = Is * xp;
-    const int NCd = KD / kChunk, NCds = KDs / kChunk;
-    const int ngu = H / 64, ngd = I / 64, ngds = Is / 64;
-    const int rb_gu = H * bits / 8, rb_ds = Is * bits / 8;
-    const int ncb_ds = cdiv(rb_ds, kCb);
+    const int Im = imax(I, Is);
+    const int KD = Im * xp, NCd = KD / kChunk;
+    const int ngu = H / 64, ngd = Im / 64;
     SmemPlan s{};
     uint32_t o = 0;
     auto take = [&](uint32_t& field, uint32_t bytes, uint32_t a) {
@@ -261,24 +267,21 @@ MOE_HD SmemPlan smem_plan(int H, int E, int k, int I, int Is, int bits, const St
     take(s.up, 2u * KU, 16);
     take(s.uc, 8u * NCu, 16);
     take(s.lg, 4u * imax(E, 32), 16);
-    take(s.tk, 8u * (kMaxE + 2 * kWarps + 8), 16);
-    take(s.rt, 2u * sg.Rr * H, 128);
+    take(s.tk, 8u * kWarps + 4u * (kMaxE + kWarps) + 8u * kMaxE, 16);
+    take(s.rt, 2u * cdiv(E, G) * H, 128);
     take(s.wsg, 2u * H, 16);
-    take(s.sgq, 2u * sg.Rs * rb_gu, 128);
-    take(s.ssb, 4u * sb_span_max(sg.Rs, 2 * ngu), 16);
-    take(s.sdq, (uint32_t)sg.Rsd * rb_ds, 128);
-    take(s.sdsb, 2u * sb_span_max(sg.Rsd, 2 * ngds), 16);
-    take(s.ring, (uint32_t)sg.nslot_gu * 2 * sg.nr_gu * sg.gu_copy + (uint32_t)sg.nr_d * sg.d_copy, 1024);
-    take(s.rsb, 4u * sb_span_max(sg.SRgu, 2 * ngu), 16);
-    take(s.rdsb, 2u * sb_span_max(sg.SRd, 2 * ngd), 16);
-    take(s.hs, 2u * 2 * KDs, 16);
-    take(s.uhs, 8u * NCds, 16);
+    take(s.tab, 4u * E + 32, 16);
+    take(s.bias, 4u * E, 16);
+    take(s.ring, imax((int)stage_bytes(sg), (int)stage_bytes(sgs)), 1024);
+    const int srgu = imax(sg.SRgu, sgs.SRgu), srd = imax(sg.SRd, sgs.SRd);
+    take(s.rsb, 4u * sb_span_max(srgu, 2 * ngu), 16);
+    take(s.rdsb, 2u * sb_span_max(srd, 2 * ngd), 16);
     take(s.hj, 2u * 2 * KD, 16);
     take(s.uhj, 8u * NCd, 16);
-    take(s.hv, 4u * xh_stride(I, Is), 16);
-    take(s.sp, 4u * imax(sg.SRgu, sg.Rs) * 2 * sg.ncb_gu, 16);
-    take(s.spd, 4u * imax(sg.SRd, sg.Rsd) * imax(sg.ncb_d, ncb_ds), 16);
-    take(s.rp, 4u * imax(sg.Rr, 1) * kRouterParts, 16);
+    take(s.hv, 4u * Im, 16);
+    take(s.sp, 4u * srgu * 2 * imax(sg.ncb_gu, sgs.ncb_gu), 16);
+    take(s.spd, 4u * srd * imax(sg.ncb_d, sgs.ncb_d), 16);
+    take(s.rp, 4u * imax(cdiv(E, G), 1) * kRouterParts, 16);
     s.total = align_to(o, 16);
     return s;
 }

@@ -43,7 +43,7 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 namespace {
 
 struct StaticLayout {
-    size_t bar, status, table, layer, xlog, xh, xacc, total;
+    size_t bar, status, table, layer, smaps, xlog, xh, xflag, xacc, total;
 };
 
 size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -60,10 +60,14 @@ StaticLayout static_layout(const moe_shape& s)
     o = round256(o + sizeof(int32_t) * (size_t)s.n_experts);
     l.layer = o;
     o = round256(o + sizeof(LayerDesc));
+    l.smaps = o;
+    o = round256(o + 3 * sizeof(CUtensorMap));
     l.xlog = o;
     o = round256(o + sizeof(unsigned long long) * (size_t)s.n_experts);
     l.xh = o;
     o = round256(o + sizeof(unsigned long long) * (size_t)(s.top_k + 1) * xh_stride(s.inter, s.shared_inter));
+    l.xflag = o;
+    o = round256(o + sizeof(unsigned long long) * (size_t)kMaxGrid);
     l.xacc = o;
     o = round256(o + sizeof(long long) * 2 * (size_t)s.hidden);
     l.total = o;
@@ -92,8 +96,8 @@ struct DeviceSetup {
 
 bool same_layout(const StaticLayout& a, const StaticLayout& b)
 {
-    return a.bar == b.bar && a.status == b.status && a.table == b.table && a.layer == b.layer && a.xlog == b.xlog &&
-           a.xh == b.xh && a.xacc == b.xacc && a.total == b.total;
+    return a.bar == b.bar && a.status == b.status && a.table == b.table && a.layer == b.layer && a.smaps == b.smaps &&
+           a.xlog == b.xlog && a.xh == b.xh && a.xflag == b.xflag && a.xacc == b.xacc && a.total == b.total;
 }
 
 std::mutex g_setup_mu;
@@ -132,9 +136,14 @@ moe_status device_setup(int dev, DeviceSetup* out)
     return MOE_OK;
 }
 
+struct SharedMaps {
+    CUtensorMap m[3];
+};
+
 // Resets what must start at zero (barrier counter, status words) and writes the identity
-// expert table and the layer descriptor into the scratch array.
-__global__ void static_prepare(uint8_t* scratch, StaticLayout sl, int n_experts, LayerDesc desc, int* status_out)
+// expert table, the layer descriptor and the maps over the shared blob into the scratch array.
+__global__ void static_prepare(uint8_t* scratch, StaticLayout sl, int n_experts, LayerDesc desc,
+                               const __grid_constant__ SharedMaps maps, int* status_out)
 {
     if (threadIdx.x == 0) {
         *reinterpret_cast<unsigned long long*>(scratch + sl.bar) = 0ull;
@@ -143,6 +152,9 @@ __global__ void static_prepare(uint8_t* scratch, StaticLayout sl, int n_experts,
         if (status_out)
             *status_out = 0;
     }
+    if (threadIdx.x < 3 * sizeof(CUtensorMap) / 8)
+        reinterpret_cast<unsigned long long*>(scratch + sl.smaps)[threadIdx.x] =
+            reinterpret_cast<const unsigned long long*>(maps.m)[threadIdx.x];
     int32_t* table = reinterpret_cast<int32_t*>(scratch + sl.table);
     for (int e = threadIdx.x; e < n_experts; e += blockDim.x)
         table[e] = e;
@@ -203,9 +215,9 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
         return st;
     if (ds.sms > kMaxGrid)
         return fail_static(MOE_E_SHAPE, "%d SMs exceed the %d blocks a decode launch supports", ds.sms, kMaxGrid);
-    StageGeo sg{};
+    StageGeo sg{}, sgs{};
     const uint32_t smem = plan_decode(shape->hidden, shape->n_experts, shape->top_k, shape->inter,
-                                      shape->shared_inter, shape->bits, ds.sms, ds.smem_optin, &sg);
+                                      shape->shared_inter, shape->bits, ds.sms, ds.smem_optin, &sg, &sgs);
     if (smem == 0)
         return fail_static(MOE_E_SHAPE, "the fused decode kernel cannot stage this shape on this GPU");
 
@@ -221,6 +233,10 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     P.geo = blob_geo(P.H, P.I, P.bits, P.group);
     P.geo_s = blob_geo(P.H, P.Is, P.bits, P.group);
     P.sg = sg;
+    P.sgs = sgs;
+    SharedMaps smaps{};
+    if (encode_arena_maps(smaps.m, static_cast<const uint8_t*>(w->shared_blob), 1, P.geo_s, sgs) != 0)
+        return fail_static(MOE_E_CUDA, "cuTensorMapEncodeTiled over the shared blob failed");
     const int rc = encode_arena_maps(P.tmap, static_cast<const uint8_t*>(d_experts), P.E, P.geo, P.sg);
     if (rc != 0)
         return fail_static(MOE_E_CUDA, "cuTensorMapEncodeTiled over the expert blobs failed (%d)", rc);
@@ -232,6 +248,8 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
     P.xlog = reinterpret_cast<unsigned long long*>(s + sl.xlog);
     P.xh = reinterpret_cast<unsigned long long*>(s + sl.xh);
     P.xacc = reinterpret_cast<long long*>(s + sl.xacc);
+    P.xflag = reinterpret_cast<unsigned long long*>(s + sl.xflag);
+    P.smaps = reinterpret_cast<const CUtensorMap*>(s + sl.smaps);
     P.bar = reinterpret_cast<unsigned long long*>(s + sl.bar);
     P.status = reinterpret_cast<int*>(d_status);
     P.timeout_ns = kStaticTimeoutNs;
@@ -275,7 +293,7 @@ extern "C" moe_status moe_layer_forward_static(const moe_shape* shape, const voi
         if ((e = cudaMemsetAsync(s + sl.xlog, 0, sl.xacc - sl.xlog, cs)) != cudaSuccess)
             return fail_static(MOE_E_CUDA, "clearing the exchange buffers failed: %s", cudaGetErrorString(e));
     }
-    static_prepare<<<1, 256, 0, cs>>>(s, sl, P.E, desc, reinterpret_cast<int*>(d_status));
+    static_prepare<<<1, 256, 0, cs>>>(s, sl, P.E, desc, smaps, reinterpret_cast<int*>(d_status));
     if ((e = cudaGetLastError()) != cudaSuccess)
         return fail_static(MOE_E_CUDA, "scratch preparation launch failed: %s", cudaGetErrorString(e));
     void* args[] = {&P};
