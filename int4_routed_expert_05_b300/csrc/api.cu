@@ -82,8 +82,8 @@ WsLayout ws_layout(const moe_shape& s, int L)
     take(w.sel, sizeof(int32_t) * 3 * kMaxK);
     take(w.xlog, sizeof(unsigned long long) * (size_t)s.n_experts);
     take(w.xh, sizeof(unsigned long long) * (size_t)(s.top_k + 1) * xh_stride(s.inter, s.shared_inter));
-    take(w.xflag, sizeof(unsigned long long) * (size_t)kMaxGrid);
-    take(w.xacc, sizeof(long long) * 2 * (size_t)s.hidden);
+    take(w.xflag, sizeof(unsigned long long));  // the step counter
+    take(w.xacc, sizeof(long long) * 3 * (size_t)s.hidden);
     take(w.xbuf, sizeof(float) * 2 * (size_t)s.hidden);
     w.total = o;
     return w;

@@ -167,11 +167,6 @@ __device__ __forceinline__ void ld_s64x2(const long long* p, long long& a, long 
 
 __device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
-__device__ __forceinline__ void ld_acq_pair2(const unsigned long long* p, unsigned long long& a, unsigned long long& b)
-{
-    asm volatile("ld.acquire.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
-
 __device__ __forceinline__ uint2 lds64(uint32_t addr)
 {
     uint2 v;
@@ -188,6 +183,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* m, int n)
 __device__ __forceinline__ void mbar_expect(uint64_t* m, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(m)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_at(uint32_t m, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(m), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try(uint64_t* m, uint32_t parity)
@@ -219,6 +219,22 @@ __device__ __forceinline__ void tma4d(void* dst, const CUtensorMap* map, int x, 
         : "memory");
 }
 
+// The same two copies with the shared-memory addresses given as such.
+__device__ __forceinline__ void bulk_g2s_at(uint32_t dst, const void* src, uint32_t bytes, uint32_t m)
+{
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(m)
+                 : "memory");
+}
+__device__ __forceinline__ void tma4d_at(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w, uint32_t m)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(m)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
@@ -231,6 +247,25 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map)
 // Block-uniform constants of a launch: shape, the expert group this block serves, its rows, its
 // copies and the shared-memory carve-up. One copy per block in shared memory, written by thread 0
 // at start; the phases below copy what they need into registers at their start.
+// Division by a launch constant d (1 <= d < 2^16) of x (0 <= x < 2^16): with m = ceil(2^32 / d),
+// floor(x * m / 2^32) = floor(x / d) exactly (the error x (m - 2^32 / d) / 2^32 < x / 2^32 < 1 / d
+// cannot carry the quotient past the next integer). d = 1 (m = 2^32 does not fit) is m = 0.
+__host__ __device__ __forceinline__ uint32_t div_magic(int d)
+{
+    return d <= 1 ? 0u : (uint32_t)((0x100000000ull + (uint64_t)d - 1) / (uint64_t)d);
+}
+__device__ __forceinline__ int div_by(int x, uint32_t m) { return m ? (int)__umulhi((uint32_t)x, m) : x; }
+
+// One planned copy of a block's expert bytes: a tile of one of the expert's code maps (b < 0:
+// map index in bits 24..30, column-block coordinate in bits 0..23; a: row coordinate) or a span
+// of its scale rows (a: byte offset in the blob; b: bytes).
+struct CopyOp {
+    uint32_t dst;   // shared-memory address
+    uint32_t mbar;  // shared-memory address of the copy's mbarrier
+    int32_t a, b;
+};
+static_assert(sizeof(CopyOp) == 16, "one 16-byte load per planned copy");
+
 struct Ctx {
     int H, E, k, I, Is, xp, KU, NCu, ngu;
     int j;            // group rank: the routed expert of rank j (j < k) or the shared expert (j = k)
@@ -260,7 +295,8 @@ struct Ctx {
     uint16_t* swsg;   // [H] shared gate vector
     int32_t* stab;    // the layer's slot-table row (16-byte aligned superset of [E])
     float* sbias;     // the layer's logit bias [E] (when staged)
-    LayerDesc cur;    // the step's layer descriptor
+    LayerDesc* ld;    // [2] layer descriptors of the steps, by step parity
+    const LayerDesc* cur;  // the step's
     int tab_off;      // offset (entries) of the row inside stab
     int bias_staged;  // 1: sbias holds the bias, 0: read it from global memory
     uint8_t* ring;    // gate/up slots [nslot][2][nr_gu][gu_copy], then down [nr_d][d_copy]
@@ -273,6 +309,13 @@ struct Ctx {
     float* spd;       // down partials [rows][ncb_d]
     float* rp;        // router partials [Rr][kRouterParts]
     uint32_t span_gu, span_d;  // bytes per staged scale span
+    // work items of the gate/up and down loops (launch constants; divisors as div_by magics)
+    int nrc_gu, per_m;            // gate/up row boxes; items per matrix of a column group
+    int nrc_d, tpi_d, ntg_d, n_dn;  // down row boxes, tiles per item, tile groups, items
+    uint32_t mg_cpg_gu, mg_cpp_gu, mg_ntg_d, mg_cpg_d;
+    CopyOp* cops;     // [kMaxCopies] the copies of one step's expert bytes (planned at launch)
+    uint2* cexp;      // [kMaxExpects] their mbarriers {address, bytes expected}
+    int ncop, nexp;   // counts (ncop < 0: too many to plan; the copies are issued one by one)
 };
 
 static_assert(sizeof(Ctx) <= kCtxBytes, "the block context outgrew its shared-memory slot");
@@ -342,6 +385,7 @@ __device__ __noinline__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base
     C.srt = (uint16_t*)(base + s.rt);
     C.swsg = (uint16_t*)(base + s.wsg);
     C.stab = (int32_t*)(base + s.tab);
+    C.ld = (LayerDesc*)(base + s.ld);
     C.sbias = (float*)(base + s.bias);
     C.ring = base + s.ring;
     C.rsb = base + s.rsb;
@@ -355,6 +399,22 @@ __device__ __noinline__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base
     const int Im = imax(P.I, P.Is);
     C.span_gu = sb_span_max(imax(P.sg.SRgu, P.sgs.SRgu), 2 * C.ngu);
     C.span_d = sb_span_max(imax(P.sg.SRd, P.sgs.SRd), 2 * (Im / 64));
+    {
+        const StageGeo& g = C.g;
+        C.nrc_gu = cdiv(imax(C.r1 - C.r0, 0), g.bh_gu);
+        C.per_m = C.nrc_gu * g.cpg_gu;
+        C.nrc_d = cdiv(imax(C.d1 - C.d0, 0), g.bh_d);
+        const int tb = cdiv(g.bh_d, 16);
+        C.tpi_d = imax(1, cdiv(C.nrc_d * g.cpg_d * tb, kWarps));
+        C.ntg_d = cdiv(tb, C.tpi_d);
+        C.n_dn = C.nrc_d * g.cpg_d * C.ntg_d;
+        C.mg_cpg_gu = div_magic(g.cpg_gu);
+        C.mg_cpp_gu = div_magic(g.cpp_gu);
+        C.mg_ntg_d = div_magic(C.ntg_d);
+        C.mg_cpg_d = div_magic(g.cpg_d);
+    }
+    C.cops = (CopyOp*)(base + s.cp);
+    C.cexp = (uint2*)(base + s.cp + 16u * kMaxCopies);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -362,16 +422,18 @@ __device__ __noinline__ void make_ctx(const StepParams& P, Ctx& C, uint8_t* base
 // ------------------------------------------------------------------------------------------
 
 // One thread: what a step reads of layer l besides its experts: the router rows [e0, e1), the
-// layer's slot-table row and logit bias (rt), and the shared gate vector (wsg). Also records the
-// layer's descriptor for the step.
-__device__ __noinline__ void issue_dense(const StepParams& P, Ctx& C, int l, bool rt, bool wsg)
+// layer's slot-table row and logit bias (rt), the shared gate vector (wsg), and the descriptor of
+// the layer after (ln) into the other descriptor slot. Layer l's descriptor is in slot par: it
+// landed with the previous step's copies (or was written at launch).
+__device__ __noinline__ void issue_dense(const StepParams& P, Ctx& C, int l, int par, int ln, bool rt, bool wsg)
 {
     uint64_t* m = C.mbar + kMbDense;
-    const LayerDesc L = P.layers[l];
-    C.cur = L;
+    const LayerDesc& L = C.ld[par];
+    C.cur = &C.ld[par];
     const int H = C.H, E = C.E;
     const bool rr = rt && C.e1 > C.e0;
-    uint32_t bytes = (rr ? (uint32_t)(C.e1 - C.e0) * H * 2 : 0u) + (wsg ? (uint32_t)H * 2 : 0u);
+    uint32_t bytes = (rr ? (uint32_t)(C.e1 - C.e0) * H * 2 : 0u) + (wsg ? (uint32_t)H * 2 : 0u) +
+                     (uint32_t)sizeof(LayerDesc);
     // the slot-table row: its 16-byte aligned superset (inside the table's buffer)
     const int32_t* row = P.table + (size_t)l * E;
     const uintptr_t ta = reinterpret_cast<uintptr_t>(row) & ~(uintptr_t)15;
@@ -381,6 +443,7 @@ __device__ __noinline__ void issue_dense(const StepParams& P, Ctx& C, int l, boo
     if (rt)
         bytes += tb + (C.bias_staged ? (uint32_t)E * 4 : 0u);
     mbar_expect(m, bytes);
+    bulk_g2s(&C.ld[par ^ 1], P.layers + ln, (uint32_t)sizeof(LayerDesc), m);
     if (rr)
         bulk_g2s(C.srt, L.router + (size_t)C.e0 * H, (uint32_t)(C.e1 - C.e0) * H * 2, m);
     if (wsg)
@@ -402,25 +465,35 @@ __device__ __forceinline__ uint8_t* d_copy_at(const Ctx& C, int rc)
     return C.ring + (size_t)C.g.nslot_gu * 2 * C.g.nr_gu * C.g.gu_copy + (size_t)rc * C.g.d_copy;
 }
 
+// Mbarrier bit of gate/up piece p of matrix m in slot sl.
+__device__ __forceinline__ int gu_bar(const StageGeo& g, int sl, int m, int p) { return (2 * sl + m) * g.npc_gu + p; }
+// Mask of n low bits (n <= 32).
+__device__ __forceinline__ uint32_t low_bits(int n) { return n >= 32 ? 0xFFFFFFFFu : (1u << n) - 1u; }
+
 // One thread: the gate (m = 0) or up (m = 1) copy of column group cg of the block's gate/up rows,
-// into slot sl; with the matrix's scale and bias rows when `scales` (the first group).
-// maps: the expert's gate/up/down maps; w: the blob's coordinate in them; blob: the blob itself.
+// into slot sl, piece by piece; with the matrix's scale and bias rows (on piece 0) when `scales`
+// (the first group). maps: the expert's gate/up/down maps; w: the blob's coordinate in them;
+// blob: the blob itself.
 __device__ __noinline__ void issue_gu(const Ctx& C, const uint8_t* blob, const CUtensorMap* maps, int w, int cg, int sl,
                                       int m, bool scales)
 {
     const StageGeo& g = C.g;
     const int nrc = cdiv(C.r1 - C.r0, g.bh_gu);
-    uint64_t* mb = C.mbar + 2 * sl + m;
-    mbar_expect(mb, (uint32_t)nrc * g.cbw_gu * g.bh_gu * g.cpg_gu +
-                        (scales ? C.sc_bytes[2 * m] + C.sc_bytes[2 * m + 1] : 0u));
+    const uint32_t pbytes = (uint32_t)g.cbw_gu * g.bh_gu * g.cpp_gu;
 #pragma unroll 1
-    for (int rc = 0; rc < nrc; ++rc)
-        tma4d(gu_copy_at(C, sl, m, rc), maps + m, 0, C.r0 + rc * g.bh_gu, cg * g.cpg_gu, w, mb);
-    if (scales)
+    for (int p = 0; p < g.npc_gu; ++p) {
+        uint64_t* mb = C.mbar + gu_bar(g, sl, m, p);
+        mbar_expect(mb, (uint32_t)nrc * pbytes + ((scales && p == 0) ? C.sc_bytes[2 * m] + C.sc_bytes[2 * m + 1] : 0u));
 #pragma unroll 1
-        for (int i = 2 * m; i < 2 * m + 2; ++i)
-            if (C.sc_bytes[i])
-                bulk_g2s(C.rsb + i * C.span_gu, blob + C.sc_src[i], C.sc_bytes[i], mb);
+        for (int rc = 0; rc < nrc; ++rc)
+            tma4d(gu_copy_at(C, sl, m, rc) + p * pbytes, maps + m, 0, C.r0 + rc * g.bh_gu, cg * g.cpg_gu + p * g.cpp_gu,
+                  w, mb);
+        if (scales && p == 0)
+#pragma unroll 1
+            for (int i = 2 * m; i < 2 * m + 2; ++i)
+                if (C.sc_bytes[i])
+                    bulk_g2s(C.rsb + i * C.span_gu, blob + C.sc_src[i], C.sc_bytes[i], mb);
+    }
 }
 
 // One thread: every byte the block reads of its expert in a step, gate rows first, then up rows,
@@ -446,6 +519,88 @@ __device__ __noinline__ void issue_expert(const Ctx& C, const uint8_t* blob, con
         for (int i = 4; i < 6; ++i)
             if (C.sc_bytes[i])
                 bulk_g2s(C.rdsb + (i - 4) * C.span_d, blob + C.sc_src[i], C.sc_bytes[i], md);
+    }
+}
+
+// One thread, at launch: the copies issue_expert makes, as a table (the same for every step but
+// for the blob and its coordinate), so that a warp can issue them side by side.
+__device__ __noinline__ void plan_copies(Ctx& C)
+{
+    const StageGeo& g = C.g;
+    int nc = 0, ne = 0;
+    auto add = [&](uint32_t dst, uint32_t mb, int a, int b) {
+        if (nc < kMaxCopies)
+            C.cops[nc] = CopyOp{dst, mb, a, b};
+        ++nc;
+    };
+    if (C.r1 > C.r0) {
+        // piece by piece, gate and up side by side, so that both matrices land progressively
+        const int nrc = cdiv(C.r1 - C.r0, g.bh_gu);
+        const uint32_t pbytes = (uint32_t)g.cbw_gu * g.bh_gu * g.cpp_gu;
+#pragma unroll 1
+        for (int cg = 0; cg < g.nslot_gu; ++cg)
+#pragma unroll 1
+            for (int p = 0; p < g.npc_gu; ++p)
+#pragma unroll 1
+                for (int m = 0; m < 2; ++m) {
+                    const uint32_t mb = smem_u32(C.mbar + gu_bar(g, cg, m, p));
+                    const bool sc = cg == 0 && p == 0;
+                    if (ne < kMaxExpects)
+                        C.cexp[ne] = make_uint2(mb, (uint32_t)nrc * pbytes +
+                                                        (sc ? C.sc_bytes[2 * m] + C.sc_bytes[2 * m + 1] : 0u));
+                    ++ne;
+#pragma unroll 1
+                    for (int rc = 0; rc < nrc; ++rc)
+                        add(smem_u32(gu_copy_at(C, cg, m, rc)) + p * pbytes, mb, C.r0 + rc * g.bh_gu,
+                            (int)(0x80000000u | ((uint32_t)m << 24) | (uint32_t)(cg * g.cpg_gu + p * g.cpp_gu)));
+                    if (sc)
+#pragma unroll 1
+                        for (int i = 2 * m; i < 2 * m + 2; ++i)
+                            if (C.sc_bytes[i])
+                                add(smem_u32(C.rsb + i * C.span_gu), mb, (int)C.sc_src[i], (int)C.sc_bytes[i]);
+                }
+    }
+    if (C.d1 > C.d0) {
+        const int nrc = cdiv(C.d1 - C.d0, g.bh_d);
+        const uint32_t mb = smem_u32(C.mbar + kMbDown);
+        if (ne < kMaxExpects)
+            C.cexp[ne] = make_uint2(mb, (uint32_t)nrc * g.cbw_d * g.bh_d * g.cpg_d + C.sc_bytes[4] + C.sc_bytes[5]);
+        ++ne;
+#pragma unroll 1
+        for (int rc = 0; rc < nrc; ++rc)
+            add(smem_u32(d_copy_at(C, rc)), mb, C.d0 + rc * g.bh_d, (int)(0x80000000u | (2u << 24)));
+#pragma unroll 1
+        for (int i = 4; i < 6; ++i)
+            if (C.sc_bytes[i])
+                add(smem_u32(C.rdsb + (i - 4) * C.span_d), mb, (int)C.sc_src[i], (int)C.sc_bytes[i]);
+    }
+    C.ncop = (nc <= kMaxCopies && ne <= kMaxExpects) ? nc : -1;
+    C.nexp = ne;
+}
+
+// One warp: every byte the block reads of its expert in a step (blob: the expert's bytes; w: its
+// coordinate in maps), the planned copies issued by the lanes side by side; one by one by lane 0
+// when the plan did not fit.
+__device__ __forceinline__ void issue_expert_warp(const Ctx& C, const uint8_t* blob, const CUtensorMap* maps, int w)
+{
+    const int nc = C.ncop;
+    if (nc < 0) {
+        if (LANE == 0)
+            issue_expert(C, blob, maps, w);
+        return;
+    }
+#pragma unroll 1
+    for (int i = LANE; i < C.nexp; i += 32) {
+        const uint2 e = C.cexp[i];
+        mbar_expect_at(e.x, e.y);
+    }
+#pragma unroll 1
+    for (int i = LANE; i < nc; i += 32) {
+        const CopyOp op = C.cops[i];
+        if (op.b < 0)
+            tma4d_at(op.dst, maps + ((op.b >> 24) & 0x7F), 0, op.a, op.b & 0xFFFFFF, w, op.mbar);
+        else
+            bulk_g2s_at(op.dst, blob + (uint32_t)op.a, (uint32_t)op.b, op.mbar);
     }
 }
 
@@ -484,11 +639,10 @@ __device__ __forceinline__ bool wait_warp(uint64_t* m, uint32_t parity, long lon
 }
 
 // Poll n epoch-tagged pairs until each carries `epoch`; values -> dst (fp32). Each thread spins on
-// its own 16-byte pieces, so only stale pieces are read again. With `acquire`, the loads are
-// acquire loads: what a publisher stored before its pair is visible to this block afterwards.
-// Block-uniform.
+// its own 16-byte pieces, so only stale pieces are read again (a pair carries its own value: no
+// ordering beyond the pair is needed). Block-uniform.
 __device__ __forceinline__ bool poll_pairs(const unsigned long long* src, int n, uint32_t epoch, float* dst,
-                                        bool acquire, long long limit, int* status)
+                                        long long limit, int* status)
 {
     const long long t0 = cycles();
     bool ok = true;
@@ -496,10 +650,7 @@ __device__ __forceinline__ bool poll_pairs(const unsigned long long* src, int n,
     for (int e = 2 * TID; ok && e < n; e += 2 * kThreads) {
         unsigned long long a, b;
         while (true) {
-            if (acquire)
-                ld_acq_pair2(src + e, a, b);
-            else
-                ld_pair2(src + e, a, b);
+            ld_pair2(src + e, a, b);
             if ((uint32_t)(a >> 32) == epoch && (e + 1 >= n || (uint32_t)(b >> 32) == epoch))
                 break;
             if (cycles() - t0 > limit) {
@@ -519,25 +670,23 @@ __device__ __forceinline__ bool poll_pairs(const unsigned long long* src, int n,
     return true;
 }
 
-// Wait until the n completion flags carry `epoch` (one warp polls them with acquire loads; the
-// block then reads what the flagging blocks stored before their flags). Block-uniform.
-__device__ __forceinline__ bool wait_flags(const unsigned long long* flags, int n, uint32_t epoch, long long limit,
-                                           int* status)
+// Wait until the step counter (one release-add per block and step) reaches `target` (thread 0
+// polls it with acquire loads; the block then reads what every counted block stored before its
+// add). Block-uniform.
+__device__ __forceinline__ bool wait_steps(const unsigned long long* counter, unsigned long long target,
+                                           long long limit, int* status)
 {
     bool ok = true;
-    if (WARP == 0) {
+    if (TID == 0) {
         const long long t0 = cycles();
-#pragma unroll 1
-        for (int f = LANE; ok && f < n; f += 32) {
-            while (true) {
-                unsigned long long v;
-                asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(flags + f) : "memory");
-                if ((uint32_t)v == epoch)
-                    break;
-                if (cycles() - t0 > limit) {
-                    ok = false;
-                    break;
-                }
+        while (true) {
+            unsigned long long v;
+            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(counter) : "memory");
+            if (v >= target)
+                break;
+            if (cycles() - t0 > limit) {
+                ok = false;
+                break;
             }
         }
     }
@@ -549,21 +698,26 @@ __device__ __forceinline__ bool wait_flags(const unsigned long long* flags, int 
     return true;
 }
 
-// Output words of elements [4q, 4q + 4) once each holds `want` contributions; false after the
-// limit.
-__device__ __forceinline__ bool poll_out4(const long long* X, int q, int want, long long t0, long long limit, float4& y)
+// Output words of element pairs qa and qb (16 bytes each) once each holds `want` contributions
+// (the two loads go out together); false after the limit. A warp reading pairs q0 + lane reads
+// 512 contiguous bytes: one request per 128-byte line.
+__device__ __forceinline__ bool poll_out2x2(const long long* X, int qa, int qb, bool hb, int want, long long t0,
+                                            long long limit, float2& ya, float2& yb)
 {
-    long long a, b, c, d;
+    long long v[4] = {0, 0, 0, 0};
     while (true) {
-        ld_s64x2(X + 4 * q, a, b);
-        ld_s64x2(X + 4 * q + 2, c, d);
-        if ((int)(a & 0xFF) == want && (int)(b & 0xFF) == want && (int)(c & 0xFF) == want && (int)(d & 0xFF) == want)
+        ld_s64x2(X + 2 * qa, v[0], v[1]);
+        if (hb)
+            ld_s64x2(X + 2 * qb, v[2], v[3]);
+        const bool all = (int)(v[0] & 0xFF) == want && (int)(v[1] & 0xFF) == want &&
+                         (!hb || ((int)(v[2] & 0xFF) == want && (int)(v[3] & 0xFF) == want));
+        if (all)
             break;
         if (cycles() - t0 > limit)
             return false;
     }
-    y = make_float4(__ll2float_rn(a >> kCountBits) * kFixInv, __ll2float_rn(b >> kCountBits) * kFixInv,
-                    __ll2float_rn(c >> kCountBits) * kFixInv, __ll2float_rn(d >> kCountBits) * kFixInv);
+    ya = make_float2(__ll2float_rn(v[0] >> kCountBits) * kFixInv, __ll2float_rn(v[1] >> kCountBits) * kFixInv);
+    yb = make_float2(__ll2float_rn(v[2] >> kCountBits) * kFixInv, __ll2float_rn(v[3] >> kCountBits) * kFixInv);
     return true;
 }
 
@@ -788,14 +942,15 @@ __device__ __forceinline__ float2 chunk_reduce(float2 v, int lpc)
 // token's input x_in (fp32, or bf16 bits) when `fresh`. Block 0 writes xo to out_prev (the
 // previous token's output, when non-null) and to trace_prev, and x to trace_cur. Then u =
 // bf16(x / rms(x)) (norm), bf16(x) (from_x) or the bf16 input bits as given, its B operand and
-// chunk sums. Each thread takes 8 consecutive elements. Block-uniform; false (status set) after
-// the limit.
+// chunk sums. x is formed in element pairs (coalesced reads of the output words), u and its B
+// operand from 8 consecutive elements per thread. Block-uniform; false (status set) after the
+// limit.
 __device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev, int want, bool residual, bool fresh,
                                             const void* x_in, bool in_f32, bool from_x, bool norm, float* out_prev,
                                             float* trace_prev, float* trace_cur, long long limit, int* status)
 {
     const int H = C.H, xp = C.xp, n8 = H / 8;
-    float4* __restrict__ sx = reinterpret_cast<float4*>(C.sx);
+    const float4* sx = reinterpret_cast<const float4*>(C.sx);
     uint16_t* __restrict__ su = C.su;
     uint16_t* __restrict__ bop = C.sup;
     float2* __restrict__ scs = C.scs;
@@ -804,56 +959,60 @@ __device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev
     const long long t0 = cycles();
     bool ok = true;
     float ss = 0.f;
-    float4 k0 = make_float4(0.f, 0.f, 0.f, 0.f), k1 = k0;
+    // element pairs: thread TID takes pairs q0 + TID and q0 + kThreads + TID (coalesced)
+    float2* sx2 = reinterpret_cast<float2*>(C.sx);
+    const int n2 = H / 2;
 #pragma unroll 1
-    for (int o = TID; o < n8; o += kThreads) {
-        float4 x0 = sx[2 * o], x1 = sx[2 * o + 1];
+    for (int q0 = 0; q0 < n2; q0 += 2 * kThreads) {
+        const int qa = q0 + TID, qb = qa + kThreads;
+        if (qa >= n2)
+            break;
+        const bool hb = qb < n2;
+        float2 xa = sx2[qa], xb = hb ? sx2[qb] : make_float2(0.f, 0.f);
         if (Xprev) {
-            float4 y0, y1;
-            if (!poll_out4(Xprev, 2 * o, want, t0, limit, y0) || !poll_out4(Xprev, 2 * o + 1, want, t0, limit, y1)) {
+            float2 ya, yb;
+            if (!poll_out2x2(Xprev, qa, qb, hb, want, t0, limit, ya, yb)) {
                 ok = false;
                 break;
             }
-            if (residual) {
-                x0 = make_float4(x0.x + y0.x, x0.y + y0.y, x0.z + y0.z, x0.w + y0.w);
-                x1 = make_float4(x1.x + y1.x, x1.y + y1.y, x1.z + y1.z, x1.w + y1.w);
-            } else {
-                x0 = y0;
-                x1 = y1;
-            }
+            xa = residual ? make_float2(xa.x + ya.x, xa.y + ya.y) : ya;
+            xb = residual ? make_float2(xb.x + yb.x, xb.y + yb.y) : yb;
             if (w0 && out_prev) {
-                reinterpret_cast<float4*>(out_prev)[2 * o] = x0;
-                reinterpret_cast<float4*>(out_prev)[2 * o + 1] = x1;
+                reinterpret_cast<float2*>(out_prev)[qa] = xa;
+                if (hb)
+                    reinterpret_cast<float2*>(out_prev)[qb] = xb;
             }
             if (w0 && trace_prev) {
-                reinterpret_cast<float4*>(trace_prev)[2 * o] = x0;
-                reinterpret_cast<float4*>(trace_prev)[2 * o + 1] = x1;
+                reinterpret_cast<float2*>(trace_prev)[qa] = xa;
+                if (hb)
+                    reinterpret_cast<float2*>(trace_prev)[qb] = xb;
             }
         }
         if (fresh) {
             if (in_f32) {
-                x0 = reinterpret_cast<const float4*>(x_in)[2 * o];
-                x1 = reinterpret_cast<const float4*>(x_in)[2 * o + 1];
+                xa = reinterpret_cast<const float2*>(x_in)[qa];
+                if (hb)
+                    xb = reinterpret_cast<const float2*>(x_in)[qb];
             } else {
-                const uint4 bits = reinterpret_cast<const uint4*>(x_in)[o];
-                x0 = make_float4(bf16f((uint16_t)bits.x), bf16f((uint16_t)(bits.x >> 16)), bf16f((uint16_t)bits.y),
-                                 bf16f((uint16_t)(bits.y >> 16)));
-                x1 = make_float4(bf16f((uint16_t)bits.z), bf16f((uint16_t)(bits.z >> 16)), bf16f((uint16_t)bits.w),
-                                 bf16f((uint16_t)(bits.w >> 16)));
+                const uint32_t ba = reinterpret_cast<const uint32_t*>(x_in)[qa];
+                xa = make_float2(bf16f((uint16_t)ba), bf16f((uint16_t)(ba >> 16)));
+                if (hb) {
+                    const uint32_t bb = reinterpret_cast<const uint32_t*>(x_in)[qb];
+                    xb = make_float2(bf16f((uint16_t)bb), bf16f((uint16_t)(bb >> 16)));
+                }
             }
         }
-        sx[2 * o] = x0;
-        sx[2 * o + 1] = x1;
+        sx2[qa] = xa;
+        if (hb)
+            sx2[qb] = xb;
         if (w0 && trace_cur) {
-            reinterpret_cast<float4*>(trace_cur)[2 * o] = x0;
-            reinterpret_cast<float4*>(trace_cur)[2 * o + 1] = x1;
+            reinterpret_cast<float2*>(trace_cur)[qa] = xa;
+            if (hb)
+                reinterpret_cast<float2*>(trace_cur)[qb] = xb;
         }
-        ss = fmaf(x0.x, x0.x, fmaf(x0.y, x0.y, fmaf(x0.z, x0.z, fmaf(x0.w, x0.w, ss))));
-        ss = fmaf(x1.x, x1.x, fmaf(x1.y, x1.y, fmaf(x1.z, x1.z, fmaf(x1.w, x1.w, ss))));
-        if (o == TID) {
-            k0 = x0;
-            k1 = x1;
-        }
+        ss = fmaf(xa.x, xa.x, fmaf(xa.y, xa.y, ss));
+        if (hb)
+            ss = fmaf(xb.x, xb.x, fmaf(xb.y, xb.y, ss));
     }
     if (__syncthreads_or(!ok)) {
         if (TID == 0)
@@ -872,7 +1031,7 @@ __device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev
                           ((d.x + d.y) + (d.z + d.w));
         rinv = rsqrtf(tot * C.invH + 1e-6f);
     }
-    const int lpc = 8 / xp;  // lanes per chunk (a chunk is 64 fields)
+    const int lsh = 4 - xp, lpc = 1 << lsh;  // lanes per chunk (a chunk is 64 fields): 8 at int4, 4 at int8
     // every lane of a warp runs every iteration: the chunk sums are shuffled across lanes
 #pragma unroll 1
     for (int o0 = 0; o0 < n8; o0 += kThreads) {
@@ -880,11 +1039,7 @@ __device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev
         const bool on = o < n8;
         float2 part = make_float2(0.f, 0.f);
         if (on) {
-            float4 x0 = k0, x1 = k1;
-            if (o != TID) {
-                x0 = sx[2 * o];
-                x1 = sx[2 * o + 1];
-            }
+            const float4 x0 = sx[2 * o], x1 = sx[2 * o + 1];
             uint16_t ub[8];
             if (from_x) {
                 const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -910,8 +1065,8 @@ __device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev
             part = put_b8(bop, xp, o, v);
         }
         const float2 cs = chunk_reduce(part, lpc);
-        if (on && o % lpc == 0)
-            scs[o / lpc] = make_float2(cs.x, 1024.f * cs.y);
+        if (on && (o & (lpc - 1)) == 0)
+            scs[o >> lsh] = make_float2(cs.x, 1024.f * cs.y);
     }
     __syncthreads();
     return true;
@@ -922,7 +1077,7 @@ __device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev
 __device__ __forceinline__ void stage_h(int xp, const float* __restrict__ hv, int n, uint16_t* __restrict__ sh,
                                         float2* __restrict__ chs)
 {
-    const int n8 = n / 8, lpc = 8 / xp;
+    const int n8 = n >> 3, lsh = 4 - xp, lpc = 1 << lsh;
     uint16_t* __restrict__ hi = sh;
     uint16_t* __restrict__ lo = sh + n * xp;
     // every lane of a warp runs every iteration: the chunk sums are shuffled across lanes
@@ -949,8 +1104,8 @@ __device__ __forceinline__ void stage_h(int xp, const float* __restrict__ hv, in
             store_b8(lo, xp, o, lb);
         }
         const float2 cs = chunk_reduce(make_float2(hs, bs), lpc);
-        if (on && o % lpc == 0)
-            chs[o / lpc] = make_float2(cs.x, 1024.f * cs.y);
+        if (on && (o & (lpc - 1)) == 0)
+            chs[o >> lsh] = make_float2(cs.x, 1024.f * cs.y);
     }
     __syncthreads();
 }
@@ -987,107 +1142,124 @@ __device__ __forceinline__ void router_rows(const Ctx& C, unsigned long long* xl
     if (TID < nr) {
         const float4 p4 = reinterpret_cast<const float4*>(rp)[TID];
         float bias = 0.f;
-        if (C.cur.logit_bias)
-            bias = C.bias_staged ? C.sbias[e0 + TID] : __ldg(C.cur.logit_bias + e0 + TID);
+        if (C.cur->logit_bias)
+            bias = C.bias_staged ? C.sbias[e0 + TID] : __ldg(C.cur->logit_bias + e0 + TID);
         st_pair(xlog + e0 + TID, epoch, (((p4.x + p4.y) + p4.z) + p4.w) + bias);
     }
 }
 
-// slg (logits) -> sel_idx / sel_w / sel_slot (rank order: larger fp32 logit first, equal logits ->
-// lower index). Each warp takes its own top-k by k rounds of a warp max reduction (equal keys go to
-// the lower lane, i.e. the lower index). Two lower bounds of the overall k-th key follow: the
-// largest of the warps' k-th keys, and the k-th largest of the warps' maxima (k warps hold a key
-// at least that large). Only members of a warp's top-k at or above the larger bound can be
-// selected; they are compacted and each is ranked by counting the larger ones. slots: look the
-// selected experts' pool slots up in the staged slot-table row.
-__device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, bool slots)
+// Warp 0: the combine weights (softmax over the k selected logits with renorm, else over all E)
+// and pool slots of the ranked selection sel_idx.
+__device__ __forceinline__ void topk_weights(const Ctx& C, bool renorm, bool slots)
 {
     const int E = C.E, k = C.k;
     const float* __restrict__ slg = C.slg;
-    uint2* __restrict__ wk = reinterpret_cast<uint2*>(C.tk);                       // [kWarps] (k-th key, max key)
-    int* __restrict__ wcnt = reinterpret_cast<int*>(C.tk) + 2 * kWarps + kMaxE;    // [kWarps]
-    unsigned long long* __restrict__ skey = reinterpret_cast<unsigned long long*>(C.tk + 2 * kWarps + kMaxE + kWarps);
+    const int isel = LANE < k ? C.sel_idx[LANE] : 0;
+    const float lsel = LANE < k ? slg[isel] : 0.f;
+    const float lmax = __shfl_sync(0xffffffffu, lsel, 0);
+    const float pj = LANE < k ? __expf(lsel - lmax) : 0.f;
+    float denom;
+    if (renorm) {
+        denom = warp_sum(pj);
+    } else {
+        float sum = 0.f;
+#pragma unroll 1
+        for (int e2 = LANE; e2 < E; e2 += 32)
+            sum += __expf(slg[e2] - lmax);
+        denom = warp_sum(sum);
+    }
+    if (LANE < k) {
+        C.sel_w[LANE] = __fdividef(pj, denom);
+        C.sel_slot[LANE] = slots ? C.stab[C.tab_off + isel] : -1;
+    }
+}
+
+// slg (logits) -> sel_idx / sel_w / sel_slot (rank order: larger fp32 logit first, equal logits ->
+// lower index). Thread e holds expert e's order-preserving key. Bounds first: the k-th largest of
+// the warps' maximum keys is a lower bound lo with at least k keys >= lo (k warps hold one), and
+// one past the largest key an upper bound hi with none. While more than 32 keys are >= lo, a
+// bisection of [lo, hi) on the key value (one block-wide count per step) raises lo, ending at the
+// k-th largest key itself at worst. The keys >= lo hold the top k; they are gathered and each is
+// ranked by counting the larger ones (composite keys: the logit key above, the complement of the
+// index below, so that equal logits rank by index). slots: look the selected experts' pool slots up
+// in the staged slot-table row.
+__device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, bool slots)
+{
+    const int E = C.E, k = C.k;
+    int* __restrict__ scnt = reinterpret_cast<int*>(C.tk);                                     // [1]
+    unsigned long long* __restrict__ skey = reinterpret_cast<unsigned long long*>(C.tk + 4);  // [E]
+    uint32_t* __restrict__ wmax = C.tk + 4 + 2 * kMaxE;                                        // [kWarps]
     const int e = TID;
     const bool valid = e < E;
-    const uint32_t key = valid ? ord_key(slg[e]) : 0u;  // finite logits map to keys > 0
-    const int nl = (E + 31) / 32;
-    bool taken = false;
+    const uint32_t key = valid ? ord_key(C.slg[e]) : 0u;
+    const int nl = (E + 31) / 32;  // warps holding keys
     if (WARP < nl) {
-        uint32_t kv = 0, mx = 0;
-#pragma unroll 1
-        for (int j = 0; j < k; ++j) {
-            kv = __reduce_max_sync(0xffffffffu, taken ? 0u : key);
-            const unsigned eq = __ballot_sync(0xffffffffu, !taken && key == kv && kv != 0u);
-            taken |= eq != 0u && LANE == __ffs(eq) - 1;
-            if (j == 0)
-                mx = kv;
-        }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, key);
         if (LANE == 0)
-            wk[WARP] = make_uint2(kv, mx);  // kv is 0 when the warp holds fewer than k keys
+            wmax[WARP] = m;
     }
+    if (TID == 0)
+        *scnt = 0;
     __syncthreads();
-    uint32_t thr;
+    // every warp alike: the largest maximum, and the k-th largest (equal maxima ranked by warp)
+    unsigned long long hi;
+    uint32_t lo = 0;
     {
-        const uint2 v = LANE < nl ? wk[LANE] : make_uint2(0u, 0u);
-        const uint32_t t1 = __reduce_max_sync(0xffffffffu, v.x);
-        // rank of this lane's warp maximum among the maxima (equal ones by lane)
+        const uint32_t mine = LANE < nl ? wmax[LANE] : 0u;
         int rank = 0;
 #pragma unroll
-        for (int d = 1; d < kWarps; ++d) {
-            const int src = (LANE + d) & 31;
-            const uint32_t o = __shfl_sync(0xffffffffu, v.y, src);
-            rank += src < nl && ((o > v.y) || (o == v.y && src < LANE));
+        for (int i = 0; i < kWarps; ++i) {
+            const uint32_t o = wmax[i];
+            rank += i < nl && (o > mine || (o == mine && i < LANE));
         }
-        const unsigned hit = __ballot_sync(0xffffffffu, LANE < nl && rank == k - 1);
-        const uint32_t t2 = hit ? __shfl_sync(0xffffffffu, v.y, __ffs(hit) - 1) : 0u;
-        thr = max(t1, t2);
+        hi = (unsigned long long)__reduce_max_sync(0xffffffffu, mine) + 1ull;
+        const unsigned at = __ballot_sync(0xffffffffu, LANE < nl && rank == k - 1);
+        if (nl >= k && at)
+            lo = __shfl_sync(0xffffffffu, mine, __ffs(at) - 1);
     }
-    const bool surv = taken && key >= thr;
-    const unsigned bal = __ballot_sync(0xffffffffu, surv);
-    if (LANE == 0)
-        wcnt[WARP] = __popc(bal);
-    __syncthreads();
-    int pos = 0, ns = 0;
-#pragma unroll
-    for (int q = 0; q < kWarps; q += 4) {
-        const int4 c4 = *reinterpret_cast<const int4*>(wcnt + q);
-        pos += (q < WARP ? c4.x : 0) + (q + 1 < WARP ? c4.y : 0) + (q + 2 < WARP ? c4.z : 0) + (q + 3 < WARP ? c4.w : 0);
-        ns += c4.x + c4.y + c4.z + c4.w;
-    }
-    // composite keys: logit key above, the complement of the index below (equal logits -> the
-    // lower index ranks first); unique, so a survivor's rank is the number of larger keys
-    if (surv)
-        skey[pos + __popc(bal & ((1u << LANE) - 1u))] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)e);
-    __syncthreads();
-    if (TID < ns) {
-        const unsigned long long mine = skey[TID];
-        int rank = 0;
-#pragma unroll 4
-        for (int q = 0; q < ns; ++q)
-            rank += skey[q] > mine;
-        if (rank < k)
-            C.sel_idx[rank] = (int)(0xFFFFFFFFu - (uint32_t)mine);
-    }
-    __syncthreads();
-    if (WARP == 0) {
-        const int isel = LANE < k ? C.sel_idx[LANE] : 0;
-        const float lsel = LANE < k ? slg[isel] : 0.f;
-        const float lmax = __shfl_sync(0xffffffffu, lsel, 0);
-        const float pj = LANE < k ? __expf(lsel - lmax) : 0.f;
-        float denom;
-        if (renorm) {
-            denom = warp_sum(pj);
-        } else {
-            float sum = 0.f;
+    int ns = __syncthreads_count(valid && key >= lo);
 #pragma unroll 1
-            for (int e2 = LANE; e2 < E; e2 += 32)
-                sum += __expf(slg[e2] - lmax);
-            denom = warp_sum(sum);
+    while (ns > 32 && hi - lo > 1ull) {
+        const uint32_t mid = (uint32_t)(lo + (hi - lo) / 2);
+        const int c = __syncthreads_count(valid && key >= mid);
+        if (c >= k) {
+            lo = mid;
+            ns = c;
+        } else {
+            hi = mid;
         }
-        if (LANE < k) {
-            C.sel_w[LANE] = __fdividef(pj, denom);
-            C.sel_slot[LANE] = slots ? C.stab[C.tab_off + isel] : -1;
+    }
+    if (valid && key >= lo)
+        skey[atomicAdd(scnt, 1)] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)e);
+    __syncthreads();
+    if (ns <= 32) {
+        if (WARP == 0) {
+            if (LANE < ns) {
+                const unsigned long long mine = skey[LANE];
+                int rank = 0;
+#pragma unroll 4
+                for (int q = 0; q < ns; ++q)
+                    rank += skey[q] > mine;
+                if (rank < k)
+                    C.sel_idx[rank] = (int)(0xFFFFFFFFu - (uint32_t)mine);
+            }
+            __syncwarp();
+            topk_weights(C, renorm, slots);
         }
+    } else {
+        // many equal keys at the k-th: every survivor ranked by its own thread
+        if (TID < ns) {
+            const unsigned long long mine = skey[TID];
+            int rank = 0;
+#pragma unroll 4
+            for (int q = 0; q < ns; ++q)
+                rank += skey[q] > mine;
+            if (rank < k)
+                C.sel_idx[rank] = (int)(0xFFFFFFFFu - (uint32_t)mine);
+        }
+        __syncthreads();
+        if (WARP == 0)
+            topk_weights(C, renorm, slots);
     }
     __syncthreads();
 }
@@ -1129,10 +1301,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
 #pragma unroll 1
             for (int i = 0; i < 3; ++i)
                 prefetch_map(&P.tmap[i]);
-        issue_dense(P, C, P.layer0, route, shb);
-        if (shb)
-            issue_expert(C, C.cur.shared_blob, P.smaps + 3 * P.layer0, 0);
+        // the first step's descriptor: written here, then overwritten by bulk copies (ordered after
+        // this write by the proxy fence)
+        C.ld[0] = P.layers[P.layer0];
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_dense(P, C, P.layer0, 0, P.layer0 + (1 % P.n_layers), route, shb);
+        if (experts)
+            plan_copies(C);
     }
+    __syncwarp();
+    if (shb && WARP == 0)
+        issue_expert_warp(C, C.cur->shared_blob, P.smaps + 3 * P.layer0, 0);
     // this block's slice of the first step's output words starts at zero
     if (experts && WARP == kClearWarp) {
 #pragma unroll 1
@@ -1142,30 +1321,38 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     }
 
     // mbarrier phases (block-uniform)
-    uint32_t ph_dense = 0, ph_down = 0, ph_gu = 0;  // ph_gu: bit 2s + m
+    uint32_t ph_dense = 0, ph_down = 0, ph_gu = 0;  // ph_gu: bit gu_bar(slot, matrix, piece)
     bool dense_pending = true, down_pending = shb && C.d1 > C.d0;
-    uint32_t gu_pending = (shb && C.r1 > C.r0) ? (1u << (2 * g.nslot_gu)) - 1u : 0u;
+    uint32_t gu_pending = (shb && C.r1 > C.r0) ? low_bits(2 * g.nslot_gu * g.npc_gu) : 0u;
 
+    // the step counter before this launch's first add: no block adds before every block has
+    // passed the launch barrier, so every block reads the same value here
+    unsigned long long done0 = 0;
+    if (TID == 0)
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(done0) : "l"(P.xflag) : "memory");
     bool ok = grid_barrier(P, limit);
 
+    // token t, layer li of the step; the layers of the next two steps; the step's output buffer
+    int t = 0, li = 0, xb = 0;
 #pragma unroll 1
-    for (int step = 0; ok && step < n_steps; ++step) {
-        const int t = step / P.n_layers, li = step - t * P.n_layers;
+    for (int step = 0; ok && step < n_steps;
+         ++step, xb = (xb == 2) ? 0 : xb + 1, t += (li + 1 == P.n_layers), li = (li + 1 == P.n_layers) ? 0 : li + 1) {
         const int l = P.layer0 + li;
-        const int ln = P.layer0 + (step + 1) % P.n_layers;
+        const int li1 = (li + 1 == P.n_layers) ? 0 : li + 1, li2 = (li1 + 1 == P.n_layers) ? 0 : li1 + 1;
+        const int ln = P.layer0 + li1;
         const uint32_t epoch = P.epoch0 + (uint32_t)step;
-        long long* X = P.xacc + (size_t)(step & 1) * H;
+        long long* X = P.xacc + (size_t)xb * H;
 
         // ---------------- 1. layer input, u ----------------
         {
             const bool fresh = li == 0;
             const size_t trow = (size_t)P.n_layers + 1;
-            if (step > 0 && experts && !(ok = wait_flags(P.xflag, GRID, epoch - 1, limit, P.status)))
+            if (step > 0 && experts && !(ok = wait_steps(P.xflag, done0 + (unsigned long long)GRID * step, limit, P.status)))
                 break;
             float* tr_prev = (step > 0 && fresh && P.trace) ? P.trace + ((size_t)(t - 1) * trow + P.n_layers) * H : nullptr;
             float* tr_cur = P.trace ? P.trace + ((size_t)t * trow + li) * H : nullptr;
             const char* xin = (const char*)P.x_in + (size_t)t * H * (prenorm ? 4 : 2);
-            if (!(ok = layer_input(C, (step > 0 && experts) ? P.xacc + (size_t)((step - 1) & 1) * H : nullptr, K + 1,
+            if (!(ok = layer_input(C, (step > 0 && experts) ? P.xacc + (size_t)(xb == 0 ? 2 : xb - 1) * H : nullptr, K + 1,
                                    residual, fresh, xin, prenorm, prenorm || li > 0, prenorm,
                                    (step > 0 && fresh) ? P.y_out + (size_t)(t - 1) * H : nullptr, tr_prev, tr_cur,
                                    limit, P.status)))
@@ -1201,7 +1388,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             if (pass == 1) {
                 // ---------------- 4. top-k ----------------
                 if (route) {
-                    if (!(ok = poll_pairs(P.xlog, C.E, epoch, C.slg, true, limit, P.status)))
+                    if (!(ok = poll_pairs(P.xlog, C.E, epoch, C.slg, limit, P.status)))
                         break;
                     topk_select(C, (P.flags & kRenorm) != 0, P.mode == kModeFull);
                     if (CTA == 0 && TID < K) {
@@ -1223,16 +1410,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
                     }
                     __syncthreads();
                 }
-                // the router rows and gate vector are consumed: the next step's; every block has
-                // read the previous step's output words (it published its logits after): clear
-                // this block's slice of them for the next step, ordered before this warp's later
-                // stores
+                // the next step's output words (three buffers, by step): every block read them
+                // last in the step before the previous one, which the step counter says is done;
+                // clear this block's slice of them. This block's count of this step, which the
+                // next step's adders wait for, is ordered after the clear.
                 if (step + 1 < n_steps) {
                     if (WARP == kClearWarp) {
 #pragma unroll 1
                         for (int o = C.o0 + LANE; o < C.o1; o += 32)
-                            st_s64(P.xacc + (size_t)((step + 1) & 1) * H + o, 0);
-                        fence_gpu();
+                            st_s64(P.xacc + (size_t)(xb == 2 ? 0 : xb + 1) * H + o, 0);
                     }
                 }
                 if (shb)
@@ -1241,11 +1427,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
                 rslot = C.sel_slot[C.j];
                 blob = rslot >= 0;
                 maps = P.tmap;
-                if (blob && TID == 0)
-                    issue_expert(C, P.arena + (uint64_t)rslot * P.stride, maps, rslot);
+                if (blob && WARP == 0)
+                    issue_expert_warp(C, P.arena + (uint64_t)rslot * P.stride, maps, rslot);
                 down_pending = blob && C.d1 > C.d0;
                 if (blob && C.r1 > C.r0)
-                    gu_pending = (1u << (2 * g.nslot_gu)) - 1u;
+                    gu_pending = low_bits(2 * g.nslot_gu * g.npc_gu);
             } else {
                 if (!shb)
                     continue;
@@ -1254,21 +1440,25 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             }
             const bool have_gu = blob && C.r1 > C.r0;
             if (have_gu) {
-                const int nrc = cdiv(C.r1 - C.r0, g.bh_gu), cpb = g.cbw_gu / 32;
-                const int per_m = nrc * g.cpg_gu;  // items per matrix of a column group: (row box, column block)
+                const int cpb = g.cbw_gu >> 5;
+                const int per_m = C.per_m;  // items per matrix of a column group: (row box, column block)
                 bool wok = true;
+                int sl = 0;
 #pragma unroll 1
-                for (int cg = 0; cg < g.ncs_gu; ++cg) {
-                    const int sl = cg % g.nslot_gu;
+                for (int cg = 0; cg < g.ncs_gu; ++cg, sl = (sl + 1 == g.nslot_gu) ? 0 : sl + 1) {
 #pragma unroll 1
                     for (int it = WARP; wok && it < 2 * per_m; it += kWarps) {
                         const int m = it >= per_m, q = it - m * per_m;
-                        const int cbl = q % g.cpg_gu, rc = q / g.cpg_gu;
+                        const int rc = div_by(q, C.mg_cpg_gu), cbl = q - rc * g.cpg_gu;
                         const int cb = cg * g.cpg_gu + cbl;
                         const int nvalid = imin(g.bh_gu, C.r1 - C.r0 - rc * g.bh_gu);
                         if (cb >= g.ncb_gu)
                             continue;
-                        if (!(wok = wait_warp(C.mbar + 2 * sl + m, (ph_gu >> (2 * sl + m)) & 1, limit)))
+                        // the item's piece (and, for the first group, piece 0 with the scales)
+                        const int pb = gu_bar(g, sl, m, div_by(cbl, C.mg_cpp_gu)), p0 = gu_bar(g, sl, m, 0);
+                        if (!(wok = wait_warp(C.mbar + pb, (ph_gu >> pb) & 1, limit)))
+                            break;
+                        if (cg == 0 && pb != p0 && !(wok = wait_warp(C.mbar + p0, (ph_gu >> p0) & 1, limit)))
                             break;
                         const int c0 = cb * cpb;
                         box_mma(gu_copy_at(C, sl, m, rc) + (size_t)cbl * g.bh_gu * g.cbw_gu, g.swz_gu ? 7u : 0u, g.cbw_gu,
@@ -1284,16 +1474,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
                         ok = false;
                         break;
                     }
-                    ph_gu ^= 3u << (2 * sl);
-                    gu_pending &= ~(3u << (2 * sl));
+                    const uint32_t slot_bits = low_bits(2 * g.npc_gu) << (2 * sl * g.npc_gu);
+                    ph_gu ^= slot_bits;
+                    gu_pending &= ~slot_bits;
                     // slot sl is free again: its next column group (when the groups take turns)
                     if (cg + g.nslot_gu < g.ncs_gu) {
                         if (TID == 0)
 #pragma unroll 1
                             for (int m = 0; m < 2; ++m)
-                                issue_gu(C, shb ? C.cur.shared_blob : P.arena + (uint64_t)rslot * P.stride, maps,
+                                issue_gu(C, shb ? C.cur->shared_blob : P.arena + (uint64_t)rslot * P.stride, maps,
                                          shb ? 0 : rslot, cg + g.nslot_gu, sl, m, false);
-                        gu_pending |= 3u << (2 * sl);
+                        gu_pending |= slot_bits;
                     }
                 }
                 if (!ok)
@@ -1325,19 +1516,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         const bool have_d = blob && C.d1 > C.d0;
         if (C.d1 > C.d0) {
             unsigned long long* xh = P.xh + (size_t)C.j * hdim;
-            if (!(ok = poll_pairs(xh, C.Ie, epoch, C.hv, false, limit, P.status)))
+            if (!(ok = poll_pairs(xh, C.Ie, epoch, C.hv, limit, P.status)))
                 break;
             if (have_d) {
                 stage_h(C.xp, C.hv, C.Ie, C.shj, C.chj);
-                const int nrc = cdiv(C.d1 - C.d0, g.bh_d), tb = cdiv(g.bh_d, 16), cpd = g.cbw_d / 32;
+                const int cpd = g.cbw_d >> 5, tpi = C.tpi_d;
                 // items (row box, column block, group of tpi tiles), about one per warp
-                const int tpi = cdiv(nrc * g.cpg_d * tb, kWarps), ntg = cdiv(tb, tpi);
                 bool wok = true;
 #pragma unroll 1
-                for (int it = WARP; it < nrc * g.cpg_d * ntg; it += kWarps) {
-                    const int tg = it % ntg, q = it / ntg, cb = q % g.cpg_d, rc = q / g.cpg_d;
+                for (int it = WARP; it < C.n_dn; it += kWarps) {
+                    const int q = div_by(it, C.mg_ntg_d), tg = it - q * C.ntg_d;
+                    const int rc = div_by(q, C.mg_cpg_d), cb = q - rc * g.cpg_d;
                     const int nvalid = imin(g.bh_d, C.d1 - C.d0 - rc * g.bh_d);
-                    const int tt0 = tg * tpi, tt1 = imin(tt0 + tpi, cdiv(nvalid, 16));
+                    const int tt0 = tg * tpi, tt1 = imin(tt0 + tpi, (nvalid + 15) >> 4);
                     if (tt0 >= tt1)
                         continue;
                     if (!(wok = wait_warp(C.mbar + kMbDown, ph_down & 1, limit)))
@@ -1369,32 +1560,35 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             }
         }
         __syncthreads();
+        // this block's contributions to the step's output words are in: its count, first (the other
+        // blocks wait for it)
+        if (TID == 0)
+            asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(P.xflag) : "memory");
         // the next step's router rows, slot-table row, bias, gate vector and (the shared expert's
         // blocks) shared rows: the staging is free again
+        // (warp 1: thread 0 is held by its release)
         if (step + 1 < n_steps) {
-            if (TID == 0) {
-                issue_dense(P, C, ln, route, shb);
+            if (WARP == 1) {
+                if (LANE == 0)
+                    issue_dense(P, C, ln, (step + 1) & 1, P.layer0 + li2, route, shb);
+                __syncwarp();
                 if (shb)
-                    issue_expert(C, C.cur.shared_blob, P.smaps + 3 * ln, 0);
+                    issue_expert_warp(C, C.cur->shared_blob, P.smaps + 3 * ln, 0);
             }
             dense_pending = true;
         }
         if (shb && step + 1 < n_steps) {
             down_pending = C.d1 > C.d0;
             if (C.r1 > C.r0)
-                gu_pending = (1u << (2 * g.nslot_gu)) - 1u;
+                gu_pending = low_bits(2 * g.nslot_gu * g.npc_gu);
         }
-        // this block's contributions to the step's output words are in: its flag
-        if (TID == 0)
-            asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(P.xflag + CTA), "l"((unsigned long long)epoch)
-                         : "memory");
     }
 
     // the last step's output
     if (ok && experts) {
         const int s = n_steps - 1, t = s / P.n_layers;
-        ok = wait_flags(P.xflag, GRID, P.epoch0 + (uint32_t)s, limit, P.status) &&
-             layer_input(C, P.xacc + (size_t)(s & 1) * H, K + 1, residual, false, nullptr, false, true, false,
+        ok = wait_steps(P.xflag, done0 + (unsigned long long)GRID * n_steps, limit, P.status) &&
+             layer_input(C, P.xacc + (size_t)(s % 3) * H, K + 1, residual, false, nullptr, false, true, false,
                          P.y_out + (size_t)t * H,
                          P.trace ? P.trace + ((size_t)t * (P.n_layers + 1) + P.n_layers) * H : nullptr, nullptr, limit,
                          P.status);
@@ -1408,7 +1602,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             }
         };
 #pragma unroll 1
-        for (int i = 0; i < 2 * kMaxGuSlots; ++i)
+        for (int i = 0; i < kMaxGuBars; ++i)
             if (gu_pending & (1u << i))
                 drain(C.mbar + i, (ph_gu >> i) & 1);
         if (down_pending)

@@ -32,8 +32,8 @@ inline EncodeTiledFn encode_tiled_fn()
 
 // The three code sections (gate.q, up.q, down.q) of every blob of an arena of n_slots blobs as 4D
 // byte tensors: (byte in a column block, row, column block, slot) with strides (row bytes, column
-// block bytes, blob stride); a box is the decode kernel's copy of bh rows by cpg column blocks,
-// 128-byte swizzled when rows are at least 128 bytes wide. Returns 0 or a CUresult (-1: no driver
+// block bytes, blob stride); a box is the decode kernel's copy of bh rows by cpg (down) or cpp
+// (a gate/up piece) column blocks, 128-byte swizzled when rows are at least 128 bytes wide. Returns 0 or a CUresult (-1: no driver
 // entry point).
 inline int encode_arena_maps(CUtensorMap (&maps)[3], const uint8_t* arena, int n_slots, const BlobGeo& geo,
                              const StageGeo& sg)
@@ -47,7 +47,7 @@ inline int encode_arena_maps(CUtensorMap (&maps)[3], const uint8_t* arena, int n
         const cuuint64_t dims[4] = {(cuuint64_t)cbw, (cuuint64_t)geo.rows[m], (cuuint64_t)ncb, (cuuint64_t)n_slots};
         const cuuint64_t strides[3] = {(cuuint64_t)geo.row_bytes[m], (cuuint64_t)cbw, (cuuint64_t)geo.stride};
         const cuuint32_t box[4] = {(cuuint32_t)cbw, (cuuint32_t)(dn ? sg.bh_d : sg.bh_gu),
-                                   (cuuint32_t)(dn ? sg.cpg_d : sg.cpg_gu), 1};
+                                   (cuuint32_t)(dn ? sg.cpg_d : sg.cpp_gu), 1};
         const cuuint32_t es[4] = {1, 1, 1, 1};
         const CUtensorMapSwizzle swz = (dn ? sg.swz_d : sg.swz_gu) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
         const CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, (void*)(arena + geo.q_off[m]), dims, strides,

@@ -112,6 +112,15 @@ MOE_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
 MOE_HD int imin(int a, int b) { return a < b ? a : b; }
 MOE_HD int imax(int a, int b) { return a > b ? a : b; }
 
+constexpr int kMaxCopies = 64;         // planned copies of a block's expert bytes per step
+constexpr int kMaxExpects = 64;        // their mbarriers
+// mbarriers: gate/up copy pieces [kMaxGuBars] (slot s, matrix m (gate 0, up 1), piece p: bit
+// (2s + m) * npc + p), then down copies, then the dense copies.
+constexpr int kMaxGuSlots = 8;
+constexpr int kMaxGuBars = 32;
+constexpr int kMbDown = kMaxGuBars, kMbDense = kMbDown + 1;
+constexpr int kNumMbar = kMbDown + 2;
+
 // The k routed experts of a step and the shared expert are served by k + 1 groups of blocks:
 // group j < k serves the expert of rank j, group k the shared expert.
 // How one block's share of an expert is staged. Block i of a group owns gate/up rows
@@ -123,7 +132,8 @@ MOE_HD int imax(int a, int b) { return a > b ? a : b; }
 // are whole multiples of the box heights. Gate and up rows are fetched in ncs_gu column groups; a
 // slot holds the gate and the up copies of one group, and with fewer slots than groups
 // (nslot_gu < ncs_gu) the groups take turns (a slot is refilled once the block is done with it).
-// Down rows are fetched all at once. Routed and shared experts have one geometry each (their
+// A gate or up copy goes out as npc_gu pieces of cpp_gu column blocks, each on its own mbarrier,
+// so that the work on a piece starts as soon as it lands. Down rows are fetched all at once. Routed and shared experts have one geometry each (their
 // intermediate sizes may differ).
 struct StageGeo {
     int SRgu, SRd;         // gate/up rows and down rows per block of a group
@@ -135,6 +145,7 @@ struct StageGeo {
     int cpg_gu, cpg_d;     // column blocks per copy
     int ncs_gu, ncs_d;     // column groups
     int nslot_gu;          // gate/up column-group slots
+    int cpp_gu, npc_gu;    // a gate/up copy in npc_gu pieces of cpp_gu column blocks, each on its own mbarrier
     uint32_t gu_copy;      // shared-memory bytes of one gate (or up) copy, 1024-aligned
     uint32_t d_copy;       // shared-memory bytes of one down copy, 1024-aligned
 };
@@ -168,6 +179,17 @@ MOE_HD StageGeo stage_geo(int H, int Ie, int bits, int G, int ngroups, int ncs_g
     s.nslot_gu = imax(1, imin(nslot_gu, s.ncs_gu));
     s.ncs_d = 1;
     s.cpg_d = s.ncb_d;
+    // pieces: the most (up to 8) that divide the copy's column blocks evenly, fit the mbarriers,
+    // and start on the swizzle period (1024 bytes) when the rows are swizzled
+    s.npc_gu = 1;
+#pragma unroll 1
+    for (int n = imin(8, s.cpg_gu); n > 1; --n)
+        if (s.cpg_gu % n == 0 && 2 * s.nslot_gu * n <= kMaxGuBars &&
+            (!s.swz_gu || ((s.cpg_gu / n) * s.bh_gu * s.cbw_gu) % 1024 == 0)) {
+            s.npc_gu = n;
+            break;
+        }
+    s.cpp_gu = s.cpg_gu / s.npc_gu;
     s.gu_copy = align1k((uint32_t)s.cbw_gu * s.bh_gu * s.cpg_gu);
     s.d_copy = align1k((uint32_t)s.cbw_d * s.bh_d * s.cpg_d);
     return s;
@@ -210,8 +232,8 @@ struct StepParams {
     // exchange buffers (workspace)
     unsigned long long* xlog;     // [E] (epoch << 32 | fp32 logit)
     unsigned long long* xh;       // [k + 1][max(I, Is)] (epoch << 32 | fp32 h); row k: shared expert
-    long long* xacc;              // [2][H] counted fixed-point output words (step parity)
-    unsigned long long* xflag;    // [grid] epoch of the step whose output words the block has finished
+    long long* xacc;              // [3][H] counted fixed-point output words (step % 3)
+    unsigned long long* xflag;    // step counter: every block adds 1 once its contributions to a step's output words are in
     unsigned long long* bar;      // launch-start barrier counter (a multiple of the grid between launches)
     int* status;
     uint32_t epoch0;              // epoch of the launch's first step (>= 1)
@@ -227,18 +249,13 @@ struct StepParams {
 
 struct SmemPlan {
     uint32_t ctx, mbar, ctl, x, u, up, uc, lg, tk;
-    uint32_t rt, wsg, tab, bias;
+    uint32_t rt, wsg, tab, bias, ld, cp;
     uint32_t ring, rsb, rdsb;
     uint32_t hj, uhj, hv, sp, spd, rp;
     uint32_t total;
 };
 
 constexpr uint32_t kCtxBytes = 1024;   // room for the kernel's block context
-// mbarriers: gate/up copies [2 * kMaxGuSlots] (slot s: gate 2s, up 2s + 1), then down copies,
-// dense rows
-constexpr int kMaxGuSlots = 8;
-constexpr int kMbDown = 2 * kMaxGuSlots, kMbDense = kMbDown + 1;
-constexpr int kNumMbar = kMbDown + 2;
 // control words: sel_idx[kMaxK], sel_w[kMaxK], sel_slot[kMaxK], red[64], misc[32], imisc[16]
 constexpr int kCtlWords = 3 * kMaxK + 64 + 32 + 16;
 
@@ -267,10 +284,12 @@ MOE_HD SmemPlan smem_plan(int H, int E, int I, int Is, int bits, int G, const St
     take(s.up, 2u * KU, 16);
     take(s.uc, 8u * NCu, 16);
     take(s.lg, 4u * imax(E, 32), 16);
-    take(s.tk, 8u * kWarps + 4u * (kMaxE + kWarps) + 8u * kMaxE, 16);
+    take(s.tk, 16u + 8u * kMaxE + 4u * kWarps, 16);
     take(s.rt, 2u * cdiv(E, G) * H, 128);
     take(s.wsg, 2u * H, 16);
     take(s.tab, 4u * E + 32, 16);
+    take(s.ld, 2u * (uint32_t)sizeof(LayerDesc), 16);
+    take(s.cp, 16u * kMaxCopies + 8u * kMaxExpects, 16);
     take(s.bias, 4u * E, 16);
     take(s.ring, imax((int)stage_bytes(sg), (int)stage_bytes(sgs)), 1024);
     const int srgu = imax(sg.SRgu, sgs.SRgu), srd = imax(sg.SRd, sgs.SRd);

@@ -66,10 +66,10 @@ StaticLayout static_layout(const moe_shape& s)
     o = round256(o + sizeof(unsigned long long) * (size_t)s.n_experts);
     l.xh = o;
     o = round256(o + sizeof(unsigned long long) * (size_t)(s.top_k + 1) * xh_stride(s.inter, s.shared_inter));
-    l.xflag = o;
-    o = round256(o + sizeof(unsigned long long) * (size_t)kMaxGrid);
+    l.xflag = o;  // the step counter
+    o = round256(o + sizeof(unsigned long long));
     l.xacc = o;
-    o = round256(o + sizeof(long long) * 2 * (size_t)s.hidden);
+    o = round256(o + sizeof(long long) * 3 * (size_t)s.hidden);
     l.total = o;
     return l;
 }
