@@ -23,10 +23,13 @@ def moe_shape(sh: synth.Shape, flags: int | None = None) -> moe.Shape:
     return moe.make_shape(sh.hidden, sh.n_experts, sh.top_k, sh.inter, sh.shared_inter, sh.bits, sh.group, flags)
 
 
-def dense_layer(sh: synth.Shape, mshape: moe.Shape, seed: int, layer: int, device: str = "cuda"):
+def dense_layer(sh: synth.Shape, mshape: moe.Shape, seed: int, layer: int, device: str = "cuda", router_bits=None):
     """Layer ``layer``'s resident weights on the device: router bf16 [E][H], shared-expert blob,
-    shared gate bf16 [H] (all drawn by ``synth``; the blob packed by the library)."""
-    router = torch.from_numpy(synth.router_bits(sh, seed, layer).view(np.int16)).to(device)
+    shared gate bf16 [H] (all drawn by ``synth``, the router unless given; the blob packed by the
+    library)."""
+    if router_bits is None:
+        router_bits = synth.router_bits(sh, seed, layer)
+    router = torch.from_numpy(np.ascontiguousarray(router_bits).view(np.int16)).to(device)
     sb = moe.pack_expert(mshape, synth.expert_tensors(sh, seed, layer, synth.SHARED_EXPERT), shared=True)
     shared = torch.from_numpy(sb).to(device)
     gate = torch.from_numpy(synth.shared_gate_bits(sh, seed, layer).view(np.int16)).to(device)
@@ -38,7 +41,7 @@ class Resident:
 
     def __init__(self, sh: synth.Shape, n_layers: int, seed: int, *, n_unique: int | None = None,
                  flags: int | None = None, slot_perm_seed: int | None = None, bias: list | None = None,
-                 device: str = "cuda", verbose: bool = False):
+                 router: dict | None = None, device: str = "cuda", verbose: bool = False):
         t0 = time.time()
         self.sh, self.L, self.seed = sh, n_layers, seed
         E = sh.n_experts
@@ -69,7 +72,7 @@ class Resident:
         # resident dense weights of every layer
         self.router, self.shared, self.gate, self.bias = [], [], [], []
         for l in range(n_layers):
-            rt, sb, g = dense_layer(sh, self.mshape, seed, l, device)
+            rt, sb, g = dense_layer(sh, self.mshape, seed, l, device, None if router is None else router.get(l))
             self.router.append(rt)
             self.shared.append(sb)
             self.gate.append(g)

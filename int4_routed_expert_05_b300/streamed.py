@@ -164,6 +164,13 @@ class Streamed:
     def bias_host(self, layer: int):
         return None if not self.beta else zipf_bias(self.sh, self.seed, layer, self.beta)
 
+    def layer_step(self, layer: int, x: torch.Tensor, out: torch.Tensor, stream=None,
+                   topk_idx: np.ndarray | None = None):
+        """Layer ``layer`` alone through the bounded pool (the pool's state carries over between
+        calls): x, out fp32 device tensors [H]; topk_idx int32 [top_k] receives its selection."""
+        s = torch.cuda.current_stream() if stream is None else stream
+        self.pool.stack_forward_streamed(layer, 1, x, out, self.h_blobs, s, self.copy_stream, topk_idx)
+
     def step(self, x: torch.Tensor, out: torch.Tensor, stream=None, topk_idx: np.ndarray | None = None):
         """One token through all layers: x, out fp32 device tensors [H]."""
         s = torch.cuda.current_stream() if stream is None else stream

@@ -13,7 +13,7 @@ normals by the Box-Muller transform (Box and Muller, 1958). Stream keys are fold
 Value distributions follow the workload descriptions of the benchmark configurations:
 int4 codes uniform on 0..15 (int8: 0..255), group 64 along each matrix's input dimension,
 scale s ~ U(0.005, 0.02) rounded to bf16 and bias b = -8*s (int8: s ~ U(0.005, 0.02)/16 and
-b = -128*s, so dequantised magnitudes match), router rows ~ N(0, 0.02) in bf16, shared-expert
+b = -128*s, so dequantised magnitudes match; a test-only switch draws b independently), router rows ~ N(0, 0.02) in bf16, shared-expert
 gate vector ~ N(0, 0.02) in bf16, activations ~ N(0, 1) rounded to bf16.
 """
 from __future__ import annotations
@@ -28,7 +28,7 @@ _MIX1 = np.uint64(0xBF58476D1CE4E5B9)
 _MIX2 = np.uint64(0x94D049BB133111EB)
 
 # tensor ids that separate the streams of one layer
-T_ROUTER, T_SHARED_GATE, T_ACT, T_CODES, T_SCALE, T_PERM, T_SEEDSEARCH = 1, 2, 3, 4, 5, 6, 7
+T_ROUTER, T_SHARED_GATE, T_ACT, T_CODES, T_SCALE, T_PERM, T_SEEDSEARCH, T_BIAS = 1, 2, 3, 4, 5, 6, 7, 8
 SHARED_EXPERT = -1  # expert id used for the shared expert's stream
 
 
@@ -101,6 +101,9 @@ class Shape:
     bits: int = 4
     group: int = 64
     renorm: bool = True
+    # test-only: draw each bias from its own stream, U(-0.16, 0.04) (int8: / 16), independent of
+    # the scale, instead of the centring b = -8 s (int8: -128 s)
+    free_bias: bool = False
 
     def with_bits(self, bits: int) -> "Shape":
         return replace(self, bits=bits)
@@ -133,7 +136,12 @@ def expert_tensors(shape: Shape, seed: int, layer: int, expert: int) -> dict:
         ks = stream_key(seed, T_SCALE, layer, expert, m)
         s = (0.005 + 0.015 * uniform01(ks, rows * (cols // g))) / sdiv
         s_bits = bf16_bits(s.astype(np.float32)).reshape(rows, cols // g)
-        b_bits = bf16_bits(-qmax_mid * bf16_value(s_bits))  # exact: power-of-two multiple
+        if shape.free_bias:
+            kb = stream_key(seed, T_BIAS, layer, expert, m)
+            b = (-0.16 + 0.2 * uniform01(kb, rows * (cols // g))) / sdiv
+            b_bits = bf16_bits(b.astype(np.float32)).reshape(rows, cols // g)
+        else:
+            b_bits = bf16_bits(-qmax_mid * bf16_value(s_bits))  # exact: power-of-two multiple
         out[name + "_s"] = s_bits
         out[name + "_b"] = b_bits
     return out

@@ -79,6 +79,10 @@ def _load():
     lib.orc_shared_gate.argtypes = [P, P, I]
     lib.orc_moe_layer.restype = None
     lib.orc_moe_layer.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P]
+    lib.orc_moe_layer_sel.restype = None
+    lib.orc_moe_layer_sel.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, I, P, P, P, P, P, P]
+    lib.orc_route_weights.restype = None
+    lib.orc_route_weights.argtypes = [P, I, I, I, P, P]
     lib.orc_rmsnorm_bf16.restype = None
     lib.orc_rmsnorm_bf16.argtypes = [P, I, ctypes.c_double, P]
     _lib = lib
@@ -209,8 +213,10 @@ def shared_gate(w_sg_bits, u_bits) -> float:
     return float(_load().orc_shared_gate(_ptr(w), _ptr(u), w.shape[0]))
 
 
-def moe_layer(shape, u_bits, Wr_bits, w_sg_bits, expert_blobs, shared_blob, bias=None) -> dict:
-    """One layer for one token (see orc_moe_layer). ``expert_blobs``: sequence of E blob arrays."""
+def moe_layer(shape, u_bits, Wr_bits, w_sg_bits, expert_blobs, shared_blob, bias=None, force_idx=None) -> dict:
+    """One layer for one token (see orc_moe_layer). ``expert_blobs``: sequence of E blob arrays.
+    With ``force_idx`` (k indices in rank order) the layer is evaluated for that selection instead
+    of the top-k's (orc_moe_layer_sel): the routing weights and y of the given experts."""
     E, k = shape.n_experts, shape.top_k
     u = _c(u_bits, np.uint16)
     Wr = _c(Wr_bits, np.uint16)
@@ -220,17 +226,30 @@ def moe_layer(shape, u_bits, Wr_bits, w_sg_bits, expert_blobs, shared_blob, bias
     arr = (ctypes.c_void_p * E)(*[b.ctypes.data for b in blobs])
     sb = _c(shared_blob, np.uint8)
     bias_a = None if bias is None else _c(bias, np.float32)
-    idx = np.zeros(k, dtype=np.int32)
+    if force_idx is None:
+        idx = np.zeros(k, dtype=np.int32)
+    else:
+        idx = _c(force_idx, np.int32).copy()
+        assert idx.shape == (k,) and len(set(idx.tolist())) == k and idx.min() >= 0 and idx.max() < E
     w = np.zeros(k)
     y = np.zeros(shape.hidden)
     lg = np.zeros(E)
     bd = np.zeros(E)
     gam = np.zeros(1)
-    _load().orc_moe_layer(shape.hidden, E, k, shape.inter, shape.shared_inter, shape.bits, shape.group,
-                          int(shape.renorm), _ptr(u), _ptr(Wr), _ptr(bias_a), _ptr(w_sg),
-                          ctypes.cast(arr, ctypes.c_void_p), _ptr(sb), _ptr(idx), _ptr(w), _ptr(y),
-                          _ptr(lg), _ptr(bd), _ptr(gam))
+    _load().orc_moe_layer_sel(shape.hidden, E, k, shape.inter, shape.shared_inter, shape.bits, shape.group,
+                              int(shape.renorm), _ptr(u), _ptr(Wr), _ptr(bias_a), _ptr(w_sg),
+                              ctypes.cast(arr, ctypes.c_void_p), _ptr(sb), int(force_idx is not None), _ptr(idx),
+                              _ptr(w), _ptr(y), _ptr(lg), _ptr(bd), _ptr(gam))
     return {"idx": idx, "w": w, "y": y, "logits": lg, "bound": bd, "gamma": float(gam[0])}
+
+
+def route_weights(logits, idx, renorm: bool = True):
+    """Routing weights of a given selection (see orc_route_weights)."""
+    lg = _c(logits, np.float64)
+    ix = _c(idx, np.int32)
+    w = np.zeros(ix.shape[0])
+    _load().orc_route_weights(_ptr(lg), lg.shape[0], ix.shape[0], int(renorm), _ptr(ix), _ptr(w))
+    return w
 
 
 def rmsnorm_bf16(x, eps: float = RMS_EPS) -> np.ndarray:

@@ -236,6 +236,26 @@ void orc_router_logits(const uint16_t* Wr, const uint16_t* u, const float* bias,
     }
 }
 
+/* R4/R5: the routing weights of a selection idx[k] (rank order): the softmax of the logits over
+ * all E experts at the selected ones, renormalised over the k selected when renorm. */
+void orc_route_weights(const double* logits, int E, int k, int renorm, const int32_t* idx, double* w)
+{
+    double mx = logits[0];
+    for (int e = 1; e < E; ++e)
+        if (logits[e] > mx)
+            mx = logits[e];
+    double all = 0.0;
+    for (int e = 0; e < E; ++e)
+        all += exp(logits[e] - mx);
+    double sel = 0.0;
+    for (int j = 0; j < k; ++j)
+        sel += exp(logits[idx[j]] - mx);
+    for (int j = 0; j < k; ++j) {
+        double p = exp(logits[idx[j]] - mx) / all;
+        w[j] = renorm ? p / (sel / all) : p;
+    }
+}
+
 /*
  * Top-k selection and routing weights.
  * Selection (R4, R5): the decision is taken in the precision the GPU path takes it, binary32:
@@ -263,21 +283,7 @@ void orc_topk(const double* logits, int E, int k, int renorm, int32_t* idx, doub
         idx[j] = best;
     }
     free(taken);
-
-    double mx = logits[0];
-    for (int e = 1; e < E; ++e)
-        if (logits[e] > mx)
-            mx = logits[e];
-    double all = 0.0;
-    for (int e = 0; e < E; ++e)
-        all += exp(logits[e] - mx);
-    double sel = 0.0;
-    for (int j = 0; j < k; ++j)
-        sel += exp(logits[idx[j]] - mx);
-    for (int j = 0; j < k; ++j) {
-        double p = exp(logits[idx[j]] - mx) / all;
-        w[j] = renorm ? p / (sel / all) : p;
-    }
+    orc_route_weights(logits, E, k, renorm, idx, w);
 }
 
 /* ------------------------------------------------------------------------------------------ */
@@ -336,14 +342,37 @@ double orc_shared_gate(const uint16_t* w_sg, const uint16_t* u, int H)
  * intermediate Is). The sum runs over j in rank order, then the shared term.
  * Outputs: idx[k], w[k], y[H]; logits[E], bound[E] and gamma[1] when not NULL.
  */
+void orc_moe_layer_sel(int H, int E, int k, int I, int Is, int bits, int group, int renorm,
+                       const uint16_t* u, const uint16_t* Wr, const float* bias, const uint16_t* w_sg,
+                       const uint8_t* const* expert_blobs, const uint8_t* shared_blob, int forced,
+                       int32_t* idx, double* w, double* y, double* logits, double* bound, double* gamma);
+
 void orc_moe_layer(int H, int E, int k, int I, int Is, int bits, int group, int renorm,
                    const uint16_t* u, const uint16_t* Wr, const float* bias, const uint16_t* w_sg,
                    const uint8_t* const* expert_blobs, const uint8_t* shared_blob,
                    int32_t* idx, double* w, double* y, double* logits, double* bound, double* gamma)
 {
+    orc_moe_layer_sel(H, E, k, I, Is, bits, group, renorm, u, Wr, bias, w_sg, expert_blobs, shared_blob, 0, idx, w,
+                      y, logits, bound, gamma);
+}
+
+/*
+ * The same layer with the selection either chosen by the top-k (forced = 0: idx is an output) or
+ * given (forced = 1: idx[k] is an input, in rank order, and only the routing weights and y are
+ * computed for it). A caller that meets a near tie (two logits closer than their binary32 error
+ * bound) evaluates the layer for the other valid selection this way.
+ */
+void orc_moe_layer_sel(int H, int E, int k, int I, int Is, int bits, int group, int renorm,
+                       const uint16_t* u, const uint16_t* Wr, const float* bias, const uint16_t* w_sg,
+                       const uint8_t* const* expert_blobs, const uint8_t* shared_blob, int forced,
+                       int32_t* idx, double* w, double* y, double* logits, double* bound, double* gamma)
+{
     double* lg = logits ? logits : (double*)malloc(sizeof(double) * (size_t)E);
     orc_router_logits(Wr, u, bias, E, H, lg, bound);
-    orc_topk(lg, E, k, renorm, idx, w);
+    if (forced)
+        orc_route_weights(lg, E, k, renorm, idx, w);
+    else
+        orc_topk(lg, E, k, renorm, idx, w);
 
     double* ye = (double*)malloc(sizeof(double) * (size_t)H);
     for (int o = 0; o < H; ++o)

@@ -14,8 +14,9 @@ def rel_l2(a, b) -> float:
 class OracleLayers:
     """The oracle evaluated on the same generated inputs as a ``Resident`` (same seed, maps, bias)."""
 
-    def __init__(self, orc, sh, seed, n_layers, n_unique=None, bias=None):
+    def __init__(self, orc, sh, seed, n_layers, n_unique=None, bias=None, router=None):
         self.orc, self.sh, self.seed, self.L = orc, sh, seed, n_layers
+        self.router = router or {}
         self.n_unique = n_unique or sh.n_experts
         self.maps = [synth.expert_map(sh, seed, l, self.n_unique) for l in range(n_layers)]
         self.bias = bias
@@ -26,7 +27,8 @@ class OracleLayers:
     def dense(self, l):
         if l not in self._dense:
             sh = self.sh
-            self._dense[l] = (synth.router_bits(sh, self.seed, l), synth.shared_gate_bits(sh, self.seed, l),
+            rt = self.router[l] if l in self.router else synth.router_bits(sh, self.seed, l)
+            self._dense[l] = (rt, synth.shared_gate_bits(sh, self.seed, l),
                               self.orc.pack(sh, synth.expert_tensors(sh, self.seed, l, synth.SHARED_EXPERT), shared=True))
         return self._dense[l]
 
@@ -37,18 +39,20 @@ class OracleLayers:
         return self._blobs[u]
 
     def layer(self, l, u_bits, force_idx=None):
-        """One layer for bf16 input u_bits. ``force_idx`` only chooses which expert blobs are built
-        (an optimisation: unselected experts are never read by the oracle)."""
+        """One layer for bf16 input u_bits: the oracle's own selection, or (``force_idx``, k indices
+        in rank order) the layer evaluated for that selection."""
         orc, sh = self.orc, self.sh
         Wr, w_sg, shared = self.dense(l)
         bias = None if self.bias is None else self.bias[l]
-        lg, bd = orc.router_logits(Wr, u_bits, bias)
-        idx, _ = orc.topk(lg, sh.top_k, sh.renorm)
+        if force_idx is None:
+            lg, bd = orc.router_logits(Wr, u_bits, bias)
+            idx, _ = orc.topk(lg, sh.top_k, sh.renorm)
+        else:
+            idx = np.asarray(force_idx)
         blobs = [self._dummy] * sh.n_experts
         for e in idx:
-            blobs[e] = self.blob(l, e)
-        r = orc.moe_layer(sh, u_bits, Wr, w_sg, blobs, shared, bias)
-        return r
+            blobs[int(e)] = self.blob(l, int(e))
+        return orc.moe_layer(sh, u_bits, Wr, w_sg, blobs, shared, bias, force_idx=force_idx)
 
     def expert_y(self, l, e, u_bits):
         y, _ = self.orc.expert_ffn(self.sh, self.blob(l, e), u_bits)
@@ -56,16 +60,38 @@ class OracleLayers:
 
 
 def check_selection(orc, r, gpu_idx):
-    """Selection parity: exact where the oracle's decision margin is positive; otherwise (a near tie
-    within the binary32 error bound) the GPU's set must still be a valid top-k under the bound.
-    Returns True when the selections are identical."""
-    gpu_idx = np.asarray(gpu_idx)
-    margin = orc.selection_margin(r["logits"], r["bound"], r["idx"])
+    """Selection parity. The GPU's k indices must be distinct experts in rank order (fp32 logits
+    non-increasing, equal logits by increasing index). They must equal the oracle's where the
+    oracle's decision margin is positive; otherwise (a near tie within the binary32 error bound)
+    they must still be a valid top-k under the bound. Returns True when the selections are
+    identical (the caller then compares with the oracle's result, else with the oracle evaluated for
+    the GPU's selection: see layer_reference)."""
+    gpu_idx = np.asarray(gpu_idx).astype(np.int64)
+    lg, bd = np.asarray(r["logits"]), np.asarray(r["bound"])
+    k = len(r["idx"])
+    assert gpu_idx.shape == (k,), gpu_idx
+    assert np.all((gpu_idx >= 0) & (gpu_idx < lg.shape[0])), f"index out of range: {gpu_idx}"
+    assert len(set(gpu_idx.tolist())) == k, f"repeated expert in the GPU selection {gpu_idx}"
+    f = lg[gpu_idx].astype(np.float32)
+    for j in range(k - 1):
+        assert f[j] > f[j + 1] or (f[j] == f[j + 1] and gpu_idx[j] < gpu_idx[j + 1]), \
+            f"GPU selection not in rank order at {j}: {gpu_idx} logits {f}"
     if np.array_equal(gpu_idx, r["idx"]):
         return True
+    margin = orc.selection_margin(lg, bd, r["idx"])
     assert margin <= 0, f"selection differs with positive margin {margin}: gpu {gpu_idx} oracle {r['idx']}"
-    lg, bd = r["logits"], r["bound"]
-    kth = np.sort(lg)[::-1][len(gpu_idx) - 1]
+    kth = np.sort(lg)[::-1][k - 1]
     slack = np.spacing(np.float32(abs(kth))) * 2
     assert np.all(lg[gpu_idx] + bd[gpu_idx] + slack >= kth - bd.max()), "GPU selection is not a valid near-tie top-k"
     return False
+
+
+def layer_reference(orc, O, l, u_bits, gpu_idx):
+    """The oracle's result to compare one GPU layer output with: the oracle's own layer when the
+    selections agree, else the oracle evaluated for the GPU's (valid, near-tie) selection. Returns
+    (result, exact) with exact False in the second case."""
+    r = O.layer(l, u_bits)
+    if check_selection(orc, r, gpu_idx):
+        return r, True
+    rf = O.layer(l, u_bits, force_idx=np.asarray(gpu_idx))
+    return rf, False

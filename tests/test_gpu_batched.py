@@ -16,11 +16,14 @@ import torch
 from int4_routed_expert_05_b300 import moe, synth
 from int4_routed_expert_05_b300.resident import Resident
 
-from gpu_ref import OracleLayers, check_selection, rel_l2
+from gpu_ref import OracleLayers, check_selection, layer_reference, rel_l2
 
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-3
+# a token whose GPU selection differs from the oracle's within the binary32 error bound of the
+# logits: compared with the oracle evaluated for the GPU's selection, at the stated 2e-3
+NEAR_TIE_TOL = 2e-3
 DERIVED = 1e-3
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -47,10 +50,12 @@ def _case(orc, sh, seed, T, sample=None, bias=None, n_unique=None):
     toks = range(T) if sample is None else sample
     errs = []
     for t in toks:
-        r = O.layer(0, x[t])
-        if check_selection(orc, r, idx[t]):
-            np.testing.assert_allclose(w[t], r["w"], rtol=0, atol=2e-6)
+        r, exact = layer_reference(orc, O, 0, x[t], idx[t])
+        np.testing.assert_allclose(w[t], r["w"], rtol=0, atol=2e-6)
+        if exact:
             errs.append(rel_l2(y[t], r["y"]))
+        else:
+            assert rel_l2(y[t], r["y"]) <= NEAR_TIE_TOL
     assert errs, "no token had an exactly determined selection"
     assert np.isfinite(y).all()
     return R, x, max(errs)
@@ -131,3 +136,36 @@ def test_batched_workspace_and_errors(orc):
     y2, i2, w2 = R.layer_forward_batched(0, x)
     assert torch.equal(i1, i2) and torch.equal(w1, w2)
     assert rel_l2(y1.cpu().numpy(), y2.cpu().numpy()) < 1e-6
+
+
+@pytest.mark.parametrize("rows,k", [((11, 3), 2), ((14, 3, 7), 2), ((5, 9, 2, 12), 3)])
+def test_exact_ties_lower_index_wins_batched(orc, rows, k):
+    """Planted exact logit ties (duplicated router rows) through the batched path: every token's
+    selection breaks the tie by index as the oracle does (the tied rows align with token 0's signs,
+    so token 0 selects them; the other tokens are compared as usual)."""
+    sh = synth.Shape(256, 16, k, 64, 64)
+    seed = 21
+    x = synth.activation_bits(sh, seed, 0, 5)
+    Wr = synth.router_bits(sh, seed, 0).copy()
+    big = synth.bf16_bits(np.float32(0.3) * np.sign(synth.bf16_value(x[0])))
+    for r in rows:
+        Wr[r] = big
+    R = Resident(sh, 1, seed, router={0: Wr})
+    O = OracleLayers(orc, sh, seed, 1, router={0: Wr})
+    y, idx, w = R.layer_forward_batched(0, _bits(x))
+    torch.cuda.synchronize()
+    assert R.pool.device_status() == moe.OK
+    y, idx, w = y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+    assert list(idx[0]) == sorted(rows)[:k]
+    for t in range(x.shape[0]):
+        r, exact = layer_reference(orc, O, 0, x[t], idx[t])
+        np.testing.assert_allclose(w[t], r["w"], rtol=0, atol=2e-6)
+        assert rel_l2(y[t], r["y"]) <= (TOL if exact else NEAR_TIE_TOL)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_independent_bias_batched(orc, bits):
+    """Bias drawn independently of the scale through the batched path."""
+    sh = synth.Shape(512, 64, 6, 128, 192, bits=bits, free_bias=True)
+    _, _, err = _case(orc, sh, seed=23, T=9)
+    assert err <= TOL, err

@@ -41,3 +41,33 @@ def test_streamed_stack_equals_resident(sh, n_slots):
     hits, misses, nbytes = S.pool.stats()
     assert hits + misses == steps * L * sh.top_k
     assert misses > 0 and nbytes == misses * S.stride
+
+
+def test_streamed_layers_against_oracle(orc):
+    """The bounded pool against the oracle, teacher-forced on every layer: an 80B-shaped stack of 8
+    layers (Zipf-biased routing; 96 slots for 80 selections per token out of 4096 experts, so that
+    later tokens hit the experts earlier ones loaded and miss the others), three tokens; each
+    layer's selection and output against the oracle evaluated on that layer's own GPU input (a
+    near tie with the oracle evaluated for the GPU's selection)."""
+    import sys, os
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from gpu_ref import OracleLayers, layer_reference, rel_l2
+    sh = synth.S80
+    L, seed, beta, n_unique, n_slots = 8, 5, 0.7, 64, 96
+    S = Streamed(sh, L, seed, n_slots, n_unique=n_unique, beta=beta)
+    O = OracleLayers(orc, sh, seed, L, n_unique=n_unique, bias=[S.bias_host(l) for l in range(L)])
+    x = torch.empty(sh.hidden, dtype=torch.float32, device="cuda")
+    y = torch.empty_like(x)
+    sel = np.zeros(sh.top_k, dtype=np.int32)
+    for step in range(3):
+        x.copy_(torch.from_numpy(synth.activation_f32(sh, seed, step)[0]))
+        for l in range(L):
+            S.layer_step(l, x, y, topk_idx=sel)
+            torch.cuda.synchronize()
+            assert S.pool.device_status() == moe.OK
+            xin, xout = x.cpu().numpy().astype(np.float64), y.cpu().numpy().astype(np.float64)
+            r, _ = layer_reference(orc, O, l, orc.rmsnorm_bf16(xin), sel)
+            assert rel_l2(xout - xin, r["y"]) <= 2e-3, (step, l)
+            x.copy_(y)
+    hits, misses, _ = S.pool.stats()
+    assert hits > 0 and misses > 0, (hits, misses)

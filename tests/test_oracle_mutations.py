@@ -25,6 +25,7 @@ MUTANTS = {
     "shared_term_dropped": ("y[o] += gs * ye[o];", "y[o] += 0.0 * ye[o];"),
     "rmsnorm_eps_inside_wrong": ("double r = sqrt(ss / H + eps);", "double r = sqrt(ss + eps);"),
     "bf16_round_truncates": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))", "if (0)"),
+    "logit_bound_doubled": ("bound[e] = gam * mag;", "bound[e] = 2.0 * gam * mag;"),
     "section_order_swapped": ("sz[0] = q_bytes(I, H, bits);          /* gate.q */",
                               "sz[0] = q_bytes(I, H, bits) + 16;     /* gate.q */"),
 }
@@ -44,3 +45,58 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+# Planted mistakes in the Python parts of the oracle: the slot-policy simulator and the selection
+# margin. Each mutant is the module's source with the replacements applied, executed fresh; the
+# golden trace (or the margin's closed-form cases) must reject it.
+POOL_MUTANTS = {
+    "evicts_largest": [("s = min(cand)[2]", "s = max(cand)[2]")],
+    "recency_before_frequency": [("cand = [(self.uses[s], self.last[s], s)", "cand = [(self.last[s], self.uses[s], s)")],
+    "pins_ignored": [("if not self.pinned[s]]", "if True]")],
+    "highest_free_slot": [("s = min(free)", "s = max(free)")],
+    "slot_tie_to_higher_index": [("(self.uses[s], self.last[s], s)", "(self.uses[s], self.last[s], -s)"),
+                                 ("s = min(cand)[2]", "s = -min(cand)[2]")],
+    "hit_not_counted": [("self.uses[s] += 1", "self.uses[s] += 0")],
+    "tick_not_advanced": [("self.tick += 1", "self.tick += 0")],
+}
+
+
+@pytest.mark.parametrize("name", sorted(POOL_MUTANTS))
+def test_pool_trace_catches_planted_mistake(name):
+    import json
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from test_oracle_pins import run_pool_trace
+    text = open(os.path.join(ROOT, "oracle", "pool_sim.py")).read()
+    for old, new in POOL_MUTANTS[name]:
+        assert text.count(old) == 1, (name, old)
+        text = text.replace(old, new)
+    ns = {}
+    exec(compile(text, "pool_sim_mutant.py", "exec"), ns)
+    with open(os.path.join(ROOT, "tests", "golden", "pool_trace.json")) as f:
+        trace = json.load(f)
+    assert run_pool_trace(ns["PoolSim"], trace), f"mutant {name} survived the golden trace"
+
+
+MARGIN_MUTANTS = {
+    "bound_doubled": ("bd = np.asarray(bound, dtype=np.float64)", "bd = 2 * np.asarray(bound, dtype=np.float64)"),
+    "chosen_side_bound_dropped": ("np.where(chosen, lg - bd, np.inf)", "np.where(chosen, lg, np.inf)"),
+    "unchosen_bound_dropped": ("np.where(chosen, -np.inf, lg + bd)", "np.where(chosen, -np.inf, lg)"),
+    "slack_dropped": ("- slack)", ")"),
+    "bounds_added": ("(lg[lo] - bd[lo]) - (lg[hi] + bd[hi])", "(lg[lo] + bd[lo]) - (lg[hi] - bd[hi])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MARGIN_MUTANTS))
+def test_margin_pin_catches_planted_mistake(name):
+    import inspect
+    import oracle
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from test_oracle_pins import check_margin
+    old, new = MARGIN_MUTANTS[name]
+    src = inspect.getsource(oracle.selection_margin)
+    assert src.count(old) == 1, name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "margin_mutant.py", "exec"), ns)
+    with pytest.raises(AssertionError):
+        check_margin(ns["selection_margin"])

@@ -358,3 +358,96 @@ def test_stack_is_residual_of_layers(orc):
     x1 = x0 + orc.moe_layer(sh, orc.rmsnorm_bf16(x0), L0["Wr"], L0["w_sg"], L0["blobs"], L0["shared"])["y"]
     np.testing.assert_array_equal(tr[1]["x_in"], x1)
     np.testing.assert_array_equal(x2, x1 + tr[1]["y"])
+
+
+# ---------------------------------------------------------------------------------------------
+# decision bounds, forced selection, slot policy
+# ---------------------------------------------------------------------------------------------
+
+def test_router_bound_exact_value(orc):
+    """The logit error bound on a constructed row is the classical binary32 summation bound
+    gamma_{H+1} * (sum |w u| + |bias|), gamma_n = n 2^-24 / (1 - n 2^-24), to the last bit of its
+    double evaluation: a bound twice as wide (or half) fails."""
+    H = 3
+    Wr = synth.bf16_bits(np.array([[1.0, 2.0, -4.0]], np.float32))
+    u = synth.bf16_bits(np.array([0.5, 0.25, 1.0], np.float32))
+    bias = np.array([1.5], np.float32)
+    lg, bd = orc.router_logits(Wr, u, bias)
+    assert lg[0] == 0.5 + 0.5 - 4.0 + 1.5
+    n = H + 1
+    gam = n * 2.0 ** -24 / (1.0 - n * 2.0 ** -24)
+    assert bd[0] == pytest.approx(gam * 6.5, rel=1e-15, abs=0)
+
+
+def test_selection_margin_closed_form(orc):
+    """Margin of a constructed selection: the smallest chosen logit less its bound, minus the
+    largest unchosen one plus its bound, minus half an ulp of binary32 rounding on each (one ulp
+    in total per side, as spacing at the two magnitudes)."""
+    check_margin(orc.selection_margin)
+
+
+def check_margin(selection_margin):
+    """The closed-form margin cases (also run against planted mistakes in the mutation tests)."""
+    lg = np.array([3.0, 1.0, 2.0, 0.5])
+    bd = np.array([0.1, 0.2, 0.05, 0.0])
+    m = selection_margin(lg, bd, np.array([0, 2]))
+    slack = 2.0 ** -22 + 2.0 ** -23  # binary32 spacing at 2.0 and at 1.0
+    assert m == pytest.approx((2.0 - 0.05) - (1.0 + 0.2) - slack, rel=0, abs=1e-15)
+    # the sign flips where the gap meets the bounds: exactly there only the rounding slack is left
+    lg2 = np.array([1.0, 0.9])
+    sl2 = float(np.spacing(np.float32(1.0)) + np.spacing(np.float32(0.9)))
+    assert selection_margin(lg2, np.array([0.04, 0.05]), np.array([0])) == pytest.approx(0.01 - sl2, abs=1e-15)
+    assert selection_margin(lg2, np.array([0.05, 0.05]), np.array([0])) == pytest.approx(-sl2, abs=1e-15)
+    assert selection_margin(lg2, np.array([0.05, 0.06]), np.array([0])) < 0
+    assert selection_margin(lg, bd, np.arange(4)) == np.inf
+    # the bounds decide which chosen logit is the weakest (3.0 - 1.5 below 2.0) and which unchosen
+    # one the strongest (0.5 + 1.0 above 1.0)
+    bd3 = np.array([1.5, 0.0, 0.0, 1.0])
+    sl3 = 2.0 ** -22 + 2.0 ** -24  # binary32 spacing at 3.0 and at 0.5
+    assert selection_margin(lg, bd3, np.array([0, 2])) == pytest.approx((3.0 - 1.5) - (0.5 + 1.0) - sl3, abs=1e-15)
+
+
+def test_forced_selection_reproduces_own(orc):
+    """The layer evaluated for a given selection equals the layer's own when given its own
+    selection (bit for bit), and a selection given in another order permutes the weights and
+    leaves y equal up to summation order."""
+    sh = synth.TINY
+    t_blobs = [orc.pack(sh, synth.expert_tensors(sh, 3, 0, e)) for e in range(sh.n_experts)]
+    shared = orc.pack(sh, synth.expert_tensors(sh, 3, 0, synth.SHARED_EXPERT), shared=True)
+    Wr = synth.router_bits(sh, 3, 0)
+    w_sg = synth.shared_gate_bits(sh, 3, 0)
+    u = synth.activation_bits(sh, 3, 0)[0]
+    r = orc.moe_layer(sh, u, Wr, w_sg, t_blobs, shared)
+    rf = orc.moe_layer(sh, u, Wr, w_sg, t_blobs, shared, force_idx=r["idx"])
+    assert np.array_equal(rf["idx"], r["idx"]) and np.array_equal(rf["w"], r["w"]) and np.array_equal(rf["y"], r["y"])
+    rev = r["idx"][::-1].copy()
+    rr = orc.moe_layer(sh, u, Wr, w_sg, t_blobs, shared, force_idx=rev)
+    np.testing.assert_allclose(rr["w"], r["w"][::-1], rtol=1e-15, atol=0)
+    np.testing.assert_allclose(rr["y"], r["y"], rtol=1e-12, atol=1e-14)
+
+
+def run_pool_trace(sim_cls, trace):
+    """Replay a golden slot-policy trace on a PoolSim-like class; returns the mismatching steps."""
+    sim = sim_cls(trace["n_slots"])
+    bad = []
+    for i, op in enumerate(trace["ops"]):
+        if op["op"] == "release":
+            sim.release()
+            continue
+        if op["op"] == "lookup":
+            got = sim.lookup(op["layer"], op["experts"])
+        else:
+            got = sim.load(op["layer"], op["expert"])
+        if got != op["expect"]:
+            bad.append((i, op, got))
+    return bad
+
+
+def test_pool_sim_golden_trace():
+    """The slot-policy simulator against a hand-derived trace (tests/golden/pool_trace.json): fills
+    the lowest free slot, evicts the fewest uses, then the oldest tick, then the lowest slot, never
+    a pinned slot, and refuses when every slot is pinned."""
+    from oracle.pool_sim import PoolSim
+    with open(os.path.join(GOLDEN, "pool_trace.json")) as f:
+        trace = json.load(f)
+    assert run_pool_trace(PoolSim, trace) == []

@@ -55,6 +55,35 @@ def test_static_scratch_matches_workspace_path():
         assert err <= TIGHT, (call, err)
 
 
+def _static_vs_workspace(R, sh, x_np, T):
+    k, H = sh.top_k, sh.hidden
+    x = torch.from_numpy(x_np.view(np.int16)).cuda()
+    y_ref, idx_ref, w_ref = R.layer_forward(0, x)
+    y = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    idx = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+    w = torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    moe.layer_forward_static(R.mshape, R.arena, R.router[0], R.shared[0], R.gate[0], x, T, y, idx, w, status)
+    torch.cuda.synchronize()
+    assert R.pool.device_status() == moe.OK and int(status.item()) == moe.OK
+    assert torch.equal(idx, idx_ref), (idx, idx_ref)
+    assert torch.allclose(w, w_ref, rtol=0, atol=1e-6)
+    return rel_l2(y.cpu().numpy(), y_ref.cpu().numpy())
+
+
+def test_static_scratch_alternating_shapes():
+    """Calls with different shapes in turn (the scratch layout moves with the expert count, top-k
+    and intermediate sizes): each call must match the workspace path, so no exchange word of one
+    shape is taken for another's."""
+    shapes = [synth.Shape(2048, 512, 10, 512, 512), synth.Shape(512, 64, 2, 128, 128)]
+    Rs = [Resident(sh, 1, 31 + i, n_unique=64) for i, sh in enumerate(shapes)]
+    for call, i in enumerate([0, 1, 0, 1, 1, 0]):
+        sh, R = shapes[i], Rs[i]
+        assert np.array_equal(R.slots[0], np.arange(sh.n_experts))
+        err = _static_vs_workspace(R, sh, synth.activation_bits(sh, 40 + call, 0, 2), 2)
+        assert err <= TIGHT, (call, i, err)
+
+
 def test_static_scratch_rejects_oversized_shape():
     # (top_k + 1) x max(inter, shared_inter) fp32 activations alone exceed the fixed array
     big = moe.make_shape(2048, 64, 16, 4096, 4096)
