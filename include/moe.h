@@ -54,13 +54,22 @@ typedef enum {
     MOE_E_POOL_FULL = 4,     /* every slot is pinned by the step in flight */
     MOE_E_CUDA = 5,          /* a CUDA runtime call failed (message in moe_last_error) */
     MOE_E_TIMEOUT = 6,       /* a device-side wait ran past its limit */
-    MOE_E_NOMEM = 7          /* workspace or arena too small */
+    MOE_E_NOMEM = 7,         /* workspace or arena too small */
+    MOE_E_RANGE = 8          /* a value outside what the kernels' fp16 operands hold (device status):
+                              * an input, activation or h value above 65504 in magnitude; on the
+                              * batched path also a scale below fp16's normal range (2^-14) or a
+                              * weight s q + b or SwiGLU output that would overflow fp16 */
 } moe_status;
 
 /* flags of moe_shape.flags */
 #define MOE_RENORM   1  /* renormalise the top-k weights ([renorm]); off: full-softmax weights */
 #define MOE_PRENORM  2  /* stack layer: u = bf16(x / sqrt(mean(x^2) + 1e-6)) from an fp32 residual */
 #define MOE_RESIDUAL 4  /* stack layer: output x + y instead of y */
+#define MOE_DETERMINISTIC 8 /* batched path: each token's k + 1 contributions summed in rank order,
+                             * then the shared expert's, from a per-assignment buffer (bit for bit
+                             * reproducible; 4 T (k + 1) H more workspace bytes) instead of fp32
+                             * reductions in tile completion order. The decode kernels are always
+                             * deterministic and ignore it. */
 
 /* One MoE FFN layer. hidden H, n_experts E, top_k k, inter I (routed expert), shared_inter Is,
  * bits 4 or 8, group 64. Supported: H % 256 == 0, I % 64 == 0, Is % 64 == 0, 1 <= k <= 16,

@@ -19,13 +19,15 @@
 namespace moe {
 __global__ void moe_decode_kernel(const __grid_constant__ StepParams P);
 namespace bat {
-void launch_gather_rows(const uint16_t* x, const int32_t* list, int A, int H, int bits, __half* us, cudaStream_t st);
+void launch_gather_rows(const uint16_t* x, const int32_t* list, int A, int H, int bits, __half* us, int* status,
+                        cudaStream_t st);
 void launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm, const uint16_t* u,
                  const uint16_t* wsg, int H, int32_t* idx, float* w, float* gamma, int32_t* counts, cudaStream_t st);
 void launch_plan(const int32_t* counts, int E, int T, int I, int Is, int H, int32_t* offs, int32_t* cursor,
                  int4* tasks_gu, int4* tasks_dn, int32_t* n_tasks, cudaStream_t st);
 void launch_place(const int32_t* idx, const float* w, const float* gamma, int T, int E, int k, int32_t* cursor,
-                  int32_t* list, float* aw, cudaStream_t st);
+                  int32_t* list, float* aw, int32_t* apos, cudaStream_t st);
+void launch_combine(const float* ypart, const int32_t* apos, int T, int k, int H, float* y, cudaStream_t st);
 }  // namespace bat
 __global__ void scalar_router(const StepParams P);
 __global__ void scalar_topk(const StepParams P, int32_t* sel);
@@ -107,7 +109,7 @@ moe_status check_shape(const moe_shape* s)
         return fail(MOE_E_SHAPE, "top_k must be in [1, %d] (got %d)", kMaxK, s->top_k);
     if (s->n_experts < s->top_k || s->n_experts > kMaxE)
         return fail(MOE_E_SHAPE, "n_experts must be in [top_k, %d] (got %d)", kMaxE, s->n_experts);
-    if (s->flags & ~(MOE_RENORM | MOE_PRENORM | MOE_RESIDUAL))
+    if (s->flags & ~(MOE_RENORM | MOE_PRENORM | MOE_RESIDUAL | MOE_DETERMINISTIC))
         return fail(MOE_E_SHAPE, "unknown flag bits 0x%x", s->flags);
     return MOE_OK;
 }
@@ -825,7 +827,8 @@ moe_status moe_stack_forward_streamed(moe_pool* p, int32_t layer0, int32_t n_lay
 namespace {
 
 struct BatLayout {
-    size_t us, logits, idx, w, gamma, counts, offs, cursor, list, aw, hbuf, tasks_gu, tasks_dn, n_tasks, total;
+    size_t us, logits, idx, w, gamma, counts, offs, cursor, list, aw, apos, ypart, hbuf, tasks_gu, tasks_dn, n_tasks,
+        total;
     size_t max_gu, max_dn;
 };
 
@@ -850,6 +853,8 @@ BatLayout bat_layout(const moe_shape& s, int T)
     take(b.cursor, 4 * (E + 2));
     take(b.list, 4 * A);
     take(b.aw, 4 * A);
+    take(b.apos, 4 * A);
+    take(b.ypart, (s.flags & MOE_DETERMINISTIC) ? 4 * A * H : 0);
     take(b.hbuf, 2 * A * Imax);
     const size_t chunks = A / tc::kNT + E + 1;  // 128-token chunks over all experts (one partial each)
     b.max_gu = chunks * (Imax / 64);
@@ -984,6 +989,8 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     A.aw = reinterpret_cast<const float*>(w + bl.aw);
     A.hbuf = reinterpret_cast<__half*>(w + bl.hbuf);
     A.y = d_y;
+    const bool det = (sh.flags & MOE_DETERMINISTIC) != 0;
+    A.ypart = det ? reinterpret_cast<float*>(w + bl.ypart) : nullptr;
     A.logits = reinterpret_cast<float*>(w + bl.logits);
     A.status = reinterpret_cast<int*>(p->ws + p->wl.status);
     A.timeout_cycles = 2 * (long long)p->timeout_ns;
@@ -1000,21 +1007,25 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     const int grid = p->grid;
 
     CUDA_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * (E + 2), cs));
-    CUDA_TRY(cudaMemsetAsync(d_y, 0, sizeof(float) * (size_t)T * H, cs));
+    if (!det)
+        CUDA_TRY(cudaMemsetAsync(d_y, 0, sizeof(float) * (size_t)T * H, cs));
     const int r_tasks = ((E + 127) / 128) * ((T + tc::kNT - 1) / tc::kNT);
     tc::launch_router_gemm(A, r_tasks < grid ? r_tasks : grid, cs);
     bat::launch_topk(A.logits, L.logit_bias, T, E, k, (sh.flags & MOE_RENORM) ? 1 : 0,
                      static_cast<const uint16_t*>(d_x), L.shared_gate, H, idx, wts, gamma, counts, cs);
     bat::launch_plan(counts, E, T, I, Is, H, offs, cursor, tgu, tdn, ntasks, cs);
-    bat::launch_place(idx, wts, gamma, T, E, k, cursor, const_cast<int32_t*>(A.list), const_cast<float*>(A.aw), cs);
+    int32_t* apos = reinterpret_cast<int32_t*>(w + bl.apos);
+    bat::launch_place(idx, wts, gamma, T, E, k, cursor, const_cast<int32_t*>(A.list), const_cast<float*>(A.aw), apos, cs);
     bat::launch_gather_rows(static_cast<const uint16_t*>(d_x), A.list, nA, H, sh.bits, reinterpret_cast<__half*>(w + bl.us),
-                            cs);
+                            A.status, cs);
     const int nev = (int)p->gemm_ev.size() / 2;
     const int ei = nev ? p->gemm_next : -1;
     if (ei >= 0)
         CUDA_TRY(cudaEventRecord(p->gemm_ev[2 * ei], cs));
     tc::launch_expert_gemm(1, A, tgu, ntasks, grid, cs);
     tc::launch_expert_gemm(2, A, tdn, ntasks + 1, grid, cs);
+    if (det)
+        bat::launch_combine(A.ypart, apos, T, k, H, d_y, cs);
     if (ei >= 0) {
         CUDA_TRY(cudaEventRecord(p->gemm_ev[2 * ei + 1], cs));
         p->gemm_next = (p->gemm_next + 1) % nev;

@@ -9,8 +9,16 @@
 //   3. counting sort of the T*k assignments by expert (the shared expert takes all T tokens as
 //      "expert" E), so each expert's tokens are contiguous;
 //   4. grouped gate/up GEMM per expert with SwiGLU in the epilogue -> h[assignment][I] (fp16);
-//   5. grouped down GEMM per expert, scaled by the assignment's weight -> partial y rows (fp32);
-//   6. per token: y = sum of its partials in rank order, then the shared expert's (fixed order).
+//   5. grouped down GEMM per expert, scaled by the assignment's weight, added into y by fp32
+//      reductions in tile completion order (the sum of a token's k + 1 contributions is then not
+//      bit reproducible), or, with MOE_DETERMINISTIC, stored per assignment;
+//   6. (MOE_DETERMINISTIC) per token: y = its k routed contributions in rank order, then the
+//      shared expert's (a fixed order, bit reproducible).
+// Range: the expert GEMMs take fp16 operands. Input elements above 65504 in magnitude, scales
+// below fp16's normal range (their relative precision would be lost on every code of the group) or
+// above it, biases above it, and weights s q + b or SwiGLU outputs that would overflow fp16 set
+// MOE_E_RANGE in the status word. (Elements in fp16's subnormal range lose at most 2^-25 absolute,
+// which no output notices: they are not reported.)
 // This file holds everything around the GEMMs (grouped.cu): top-k, the device-side plan (offsets
 // per expert, GEMM task lists), the placement of assignments and the input rows in assignment order.
 #include <cuda_bf16.h>
@@ -32,8 +40,9 @@ __device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32
 // One warp per row, one 8-element block per lane and step. bf16 -> fp16 is exact for |x| in
 // [2^-14, 65504] (bf16's 8-bit significand fits in fp16's 11 bits).
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ list, int A, int H,
-                                   int bits, __half* __restrict__ us)
+                                   int bits, __half* __restrict__ us, int* status)
 {
+    bool inexact = false;  // an element fp16 cannot hold
     const int lane = threadIdx.x & 31;
     for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < A; p += (gridDim.x * blockDim.x) >> 5) {
         const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)list[p] * H);
@@ -43,8 +52,11 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             __half h[8], o[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                h[j] = __float2half_rn(bf((uint16_t)(w[j >> 1] >> (16 * (j & 1)))));
+            for (int j = 0; j < 8; ++j) {
+                const float f = bf((uint16_t)(w[j >> 1] >> (16 * (j & 1))));
+                h[j] = __float2half_rn(f);
+                inexact |= !(fabsf(f) <= 65504.f);  // beyond fp16's range
+            }
             if (bits == 4) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -57,6 +69,8 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t
             dst[c] = *reinterpret_cast<const uint4*>(o);
         }
     }
+    if (inexact)
+        atomicCAS(status, 0, kStatusRange);
 }
 
 __device__ __forceinline__ uint32_t ord_key(float f)
@@ -218,7 +232,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 // result: every column of the expert GEMMs is computed on its own.
 __global__ void place_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, const float* __restrict__ gamma,
                              int T, int E, int k, int32_t* __restrict__ cursor, int32_t* __restrict__ list,
-                             float* __restrict__ aw)
+                             float* __restrict__ aw, int32_t* __restrict__ apos)
 {
     const int n = T * (k + 1);
     for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < n; a += gridDim.x * blockDim.x) {
@@ -227,12 +241,38 @@ __global__ void place_kernel(const int32_t* __restrict__ idx, const float* __res
         const int p = atomicAdd(&cursor[e], 1);
         list[p] = t;
         aw[p] = j < k ? w[(size_t)t * k + j] : gamma[t];
+        apos[a] = p;
     }
 }
 
-void launch_gather_rows(const uint16_t* x, const int32_t* list, int A, int H, int bits, __half* us, cudaStream_t st)
+// Deterministic combine: y[t] = sum over j = 0..k (rank order, the shared expert last) of the
+// weighted down rows of assignment (t, j).
+__global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* __restrict__ apos, int T, int k, int H,
+                               float* __restrict__ y)
 {
-    gather_rows_kernel<<<(A + 7) / 8 < 2368 ? (A + 7) / 8 : 2368, 256, 0, st>>>(x, list, A, H, bits, us);
+    const int n4 = H / 4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)T * n4; i += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / n4), c = (int)(i - (size_t)t * n4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j <= k; ++j) {
+            const float4 v = reinterpret_cast<const float4*>(ypart + (size_t)apos[(size_t)t * (k + 1) + j] * H)[c];
+            acc = make_float4(acc.x + v.x, acc.y + v.y, acc.z + v.z, acc.w + v.w);
+        }
+        reinterpret_cast<float4*>(y + (size_t)t * H)[c] = acc;
+    }
+}
+
+void launch_gather_rows(const uint16_t* x, const int32_t* list, int A, int H, int bits, __half* us, int* status,
+                        cudaStream_t st)
+{
+    gather_rows_kernel<<<(A + 7) / 8 < 2368 ? (A + 7) / 8 : 2368, 256, 0, st>>>(x, list, A, H, bits, us, status);
+}
+
+void launch_combine(const float* ypart, const int32_t* apos, int T, int k, int H, float* y, cudaStream_t st)
+{
+    const size_t n = (size_t)T * (H / 4);
+    const size_t blocks = (n + 255) / 256;
+    combine_kernel<<<blocks < 2368 ? (int)blocks : 2368, 256, 0, st>>>(ypart, apos, T, k, H, y);
 }
 
 void launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm, const uint16_t* u,
@@ -248,10 +288,10 @@ void launch_plan(const int32_t* counts, int E, int T, int I, int Is, int H, int3
 }
 
 void launch_place(const int32_t* idx, const float* w, const float* gamma, int T, int E, int k, int32_t* cursor,
-                  int32_t* list, float* aw, cudaStream_t st)
+                  int32_t* list, float* aw, int32_t* apos, cudaStream_t st)
 {
     const int n = T * (k + 1);
-    place_kernel<<<(n + 255) / 256, 256, 0, st>>>(idx, w, gamma, T, E, k, cursor, list, aw);
+    place_kernel<<<(n + 255) / 256, 256, 0, st>>>(idx, w, gamma, T, E, k, cursor, list, aw, apos);
 }
 
 }  // namespace bat

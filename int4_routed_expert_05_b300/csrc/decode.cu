@@ -11,30 +11,36 @@
 //
 // Design: one cooperative launch covers every layer and token of a call, one 512-thread block per
 // SM. A layer at batch 1 moves about 20 MB, a few microseconds of HBM time, so the kernel is built
-// around the latency of the layer's three all-to-all dependencies (logits -> top-k, h_j -> down
-// rows, y -> next layer) and around what the copy engine charges per copy (each copy costs tens of
-// cycles to issue, so a block fetches its routed rows in three large copies). Per step (token,
-// layer) a block
-//   1. waits for the previous step's output words, forms x (every block the same) and u;
-//   2. computes its router rows (staged during the previous step) and publishes the logits as
-//      epoch-tagged (epoch, value) pairs;
-//   3. polls the logits and takes the top-k itself (every block, the same result);
-//   4. issues every byte it will read of its routed expert: its gate rows, its up rows and its
-//      down rows (one 4D tensor copy each, 128-byte swizzled) plus their scales, so the layer's
-//      whole routed stream is in flight at once;
-//   5. while those bytes travel: its rows of the shared expert's gate/up (staged during the
-//      previous step) -> h_shared, published; the next step's router and shared rows queued; the
-//      shared h polled and its down rows added as gamma * y_shared;
-//   6. turns its gate/up rows into h_j as the copies land, exchanges h_j within the expert's
-//      block group, and computes its down rows of y_j;
-//   7. adds w_j y_j into the output words: each word collects exactly k + 1 contributions as
-//      fixed-point integers with a contribution count in its low byte, so the sum is exact and
-//      order independent and the count tells every block when the layer output is complete: there
-//      is no grid barrier between layers.
+// around the latency of the layer's all-to-all dependencies (logits -> top-k, h -> down rows,
+// output -> next layer) and around what the copy engine charges per copy. The blocks form k + 1
+// groups: group j < k serves the routed expert of rank j, group k the shared expert; a block owns
+// a slice of its expert's gate/up rows and a slice of its down rows. Per step (token, layer) a block
+//   1. waits until the step counter says every block has added its share of the previous step's
+//      output (one release add per block and step, one acquire poll per block), reads the output
+//      words (coalesced) and forms x and u;
+//   2. computes its router rows (staged by bulk copy during the previous step with the layer's
+//      slot-table row, logit bias and descriptor) and publishes the logits as epoch-tagged
+//      (epoch, value) pairs;
+//   3. shared-expert blocks: their gate/up rows (fetched during the previous step) -> h, published;
+//      routed blocks: poll the logits and take the top-k (every block, the same result; bounds from
+//      the warps' maxima, then at most a short bisection), then issue every byte they read of their
+//      expert in one go from the lanes of one warp (launch-time copy plan: gate and up rows in
+//      column-block pieces, each on its own mbarrier, down rows, scale spans);
+//   4. turn their gate/up rows into h as the pieces land and publish h to their group;
+//   5. poll their group's h and compute their down rows;
+//   6. add w_j y_j (gamma y_shared for the shared group) into the step's output words: each word
+//      collects exactly k + 1 contributions as fixed-point integers with a contribution count in
+//      its low byte, so the sum is exact and order independent. The output words rotate over three
+//      buffers: a block clears its slice of the next step's buffer, which every block last read
+//      two steps before (the step counter orders the clear after those reads and before the next
+//      step's adds). Then the block counts the step done and queues the next step's dense copies
+//      (and, in the shared group, the next layer's shared rows).
 // int4 codes become fp16 values 1024 + q in registers (one lop3 per pair) and meet the activations
 // on the tensor cores (mma.m16n8k16, fp32 accumulate), one 64-field chunk at a time; the offset
 // and the affine dequantisation are applied per chunk as s * (sum q u) + b * (sum u). Every sum
 // runs in a fixed order, so the result depends neither on arrival order nor on pool placement.
+// Every wait has an iteration limit: on expiry the block records a timeout status and the launch
+// ends (nothing spins forever).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -1032,6 +1038,7 @@ __device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev
         rinv = rsqrtf(tot * C.invH + 1e-6f);
     }
     const int lsh = 4 - xp, lpc = 1 << lsh;  // lanes per chunk (a chunk is 64 fields): 8 at int4, 4 at int8
+    bool big = false;
     // every lane of a warp runs every iteration: the chunk sums are shuffled across lanes
 #pragma unroll 1
     for (int o0 = 0; o0 < n8; o0 += kThreads) {
@@ -1060,14 +1067,18 @@ __device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev
                            (uint32_t)ub[4] | ((uint32_t)ub[5] << 16), (uint32_t)ub[6] | ((uint32_t)ub[7] << 16));
             float v[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < 8; ++j) {
                 v[j] = bf16f(ub[j]);
+                big |= !(fabsf(v[j]) <= 65504.f);  // the fp16 B operand would overflow
+            }
             part = put_b8(bop, xp, o, v);
         }
         const float2 cs = chunk_reduce(part, lpc);
         if (on && (o & (lpc - 1)) == 0)
             scs[o >> lsh] = make_float2(cs.x, 1024.f * cs.y);
     }
+    if (big)
+        set_status(status, kStatusRange);
     __syncthreads();
     return true;
 }
@@ -1075,8 +1086,9 @@ __device__ __forceinline__ bool layer_input(const Ctx& C, const long long* Xprev
 // h values hv[0, n) -> B operand hi/lo parts (sh: [2][n * xp]) and per chunk {sum of h, 1024 *
 // sum of (hi + lo)}; hi + lo carries h to about 22 bits. Each thread takes 8 consecutive values.
 __device__ __forceinline__ void stage_h(int xp, const float* __restrict__ hv, int n, uint16_t* __restrict__ sh,
-                                        float2* __restrict__ chs)
+                                        float2* __restrict__ chs, int* status)
 {
+    bool big = false;
     const int n8 = n >> 3, lsh = 4 - xp, lpc = 1 << lsh;
     uint16_t* __restrict__ hi = sh;
     uint16_t* __restrict__ lo = sh + n * xp;
@@ -1093,6 +1105,7 @@ __device__ __forceinline__ void stage_h(int xp, const float* __restrict__ hv, in
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 hs += v[j];
+                big |= !(fabsf(v[j]) <= 65504.f);  // the fp16 hi part would overflow
                 const float e = (xp == 1 && (j & 1)) ? v[j] * 0.0625f : v[j];
                 hb[j] = f2h(e);
                 lb[j] = f2h(e - h2f((uint16_t)hb[j]));
@@ -1107,6 +1120,8 @@ __device__ __forceinline__ void stage_h(int xp, const float* __restrict__ hv, in
         if (on && (o & (lpc - 1)) == 0)
             chs[o >> lsh] = make_float2(cs.x, 1024.f * cs.y);
     }
+    if (big)
+        set_status(status, kStatusRange);
     __syncthreads();
 }
 
@@ -1519,7 +1534,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             if (!(ok = poll_pairs(xh, C.Ie, epoch, C.hv, limit, P.status)))
                 break;
             if (have_d) {
-                stage_h(C.xp, C.hv, C.Ie, C.shj, C.chj);
+                stage_h(C.xp, C.hv, C.Ie, C.shj, C.chj, P.status);
                 const int cpd = g.cbw_d >> 5, tpi = C.tpi_d;
                 // items (row box, column block, group of tpi tiles), about one per warp
                 bool wok = true;

@@ -12,12 +12,13 @@
 //     the 128-byte swizzle as K-major shared-memory tiles, so a slice goes global -> shared ->
 //     tensor core untouched;
 //   * expert GEMMs: TMA stages the packed codes (64 bytes per row and slice, 64-byte swizzled);
-//     eight dequantising warps turn them into fp16 weights w = s * q + b (one rounding, s and b
-//     exact in fp16 for the workloads' ranges) and write them straight into tensor memory
+//     eight dequantising warps turn them into fp16 weights w = s * q + b (one rounding; s is
+//     checked to be a normal fp16 value and w to stay finite, else MOE_E_RANGE) and write them straight into tensor memory
 //     (tcgen05.st; the MMA reads A from there); TMA brings the expert's token rows (input rows in
 //     assignment order, or h rows) into 128-byte swizzled B tiles in shared memory; four epilogue
 //     warps read the accumulators with tcgen05.ld and apply SwiGLU (gate/up: h to a per-assignment
-//     buffer) or the combine weight (down: fp32 reductions into y).
+//     buffer) or the combine weight (down: fp32 reductions into y, or per-assignment rows that a
+//     fixed-order combine sums).
 //   Operand tiles the MMA reads come from TMA or from tcgen05.st (rows written by cp.async and
 //   released after cp.async.wait_group + fence.proxy.async were measured to reach tcgen05.mma stale
 //   at times, and are not used).
@@ -539,8 +540,15 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                         b16 = brow[gg];
                     }
                 }
-                const __half2 s2 = __half2half2(__float2half_rn(bf2f(s16)));
-                const __half2 b2 = __half2half2(__float2half_rn(bf2f(b16)));
+                const float sf = bf2f(s16), bf = bf2f(b16);
+                const __half2 s2 = __half2half2(__float2half_rn(sf));
+                const __half2 b2 = __half2half2(__float2half_rn(bf));
+                // the fp16 dequantisation keeps s's relative precision and stays finite only when s
+                // is zero or a normal fp16 value and |s| qmax + |b| is within fp16's range (b in
+                // fp16's subnormal range is off by at most 2^-25, unnoticeable in a weight)
+                if (live && ((sf != 0.f && !(fabsf(sf) >= 6.103515625e-05f)) ||
+                             !(fabsf(sf) * (kBits == 4 ? 15.f : 255.f) + fabsf(bf) <= 65504.f)))
+                    atomicCAS(P.status, 0, kStatusRange);
                 const int st = it % kStages;
                 bar_wait(empty + st, ((it / kStages) & 1) ^ 1, ctl, P.status, lim);
                 // A row segment -> tensor memory (lane r): 32-bit columns of fp16 pairs in K order
@@ -619,6 +627,8 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
                                 if (n < t.nn) {
                                     const float gt = v[i], up = xch[r * 17 + c + i];
                                     const float h = __fdividef(gt, 1.f + __expf(-gt)) * up;
+                                    if (!(fabsf(h) <= 65504.f))
+                                        atomicCAS(P.status, 0, kStatusRange);
                                     P.hbuf[(size_t)(t.n0 + n) * P.Imax + pos] = __float2half_rn(h);
                                 }
                             }
@@ -636,8 +646,12 @@ __global__ void __launch_bounds__(kThreadsX, 1) expert_kernel(const __grid_const
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int a = t.n0 + c0 + i;
-                            if (c0 + i < t.nn)
-                                atomicAdd(P.y + (size_t)P.list[a] * P.H + o, P.aw[a] * v[i]);
+                            if (c0 + i < t.nn) {
+                                if (P.ypart)
+                                    P.ypart[(size_t)a * P.H + o] = P.aw[a] * v[i];
+                                else
+                                    atomicAdd(P.y + (size_t)P.list[a] * P.H + o, P.aw[a] * v[i]);
+                            }
                         }
                     }
                 }

@@ -43,6 +43,7 @@ struct GroupedArgs {
     const float* aw;          // [A] combine weight of each assignment
     __half* hbuf;             // [A][Imax] SwiGLU output, K-permuted (see kperm)
     float* y;                 // [T][H] output, zeroed before the down GEMM (fp32 reductions)
+    float* ypart;             // [A][H] weighted down rows per assignment (deterministic combine), or null
     float* logits;            // [T][E]
     const int4* tasks;        // {expert, m0, n0, n} per task
     const int32_t* n_tasks;   // device count of tasks

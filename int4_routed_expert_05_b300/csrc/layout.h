@@ -48,6 +48,7 @@ constexpr int kCountBits = 8;
 constexpr int kStatusInvalid = 1;
 constexpr int kStatusNotResident = 3;
 constexpr int kStatusTimeout = 6;
+constexpr int kStatusRange = 8;
 
 enum Mode : int { kModeFull = 0, kModeRoute = 1, kModeExperts = 2 };
 enum Flags : int { kRenorm = 1, kPrenorm = 2, kResidual = 4 };

@@ -169,3 +169,64 @@ def test_independent_bias_batched(orc, bits):
     sh = synth.Shape(512, 64, 6, 128, 192, bits=bits, free_bias=True)
     _, _, err = _case(orc, sh, seed=23, T=9)
     assert err <= TOL, err
+
+
+def test_deterministic_combine(orc):
+    """MOE_DETERMINISTIC: the batched layer is bit for bit the same on repeated calls (each token's
+    contributions summed in rank order, then the shared expert's), and matches the oracle."""
+    sh = synth.Shape(512, 64, 6, 128, 192)
+    seed, T = 29, 37
+    R = Resident(sh, 1, seed, flags=moe.RENORM | moe.DETERMINISTIC)
+    x = synth.activation_bits(sh, seed, 0, T)
+    outs = []
+    for _ in range(3):
+        y, idx, w = R.layer_forward_batched(0, _bits(x))
+        torch.cuda.synchronize()
+        assert R.pool.device_status() == moe.OK
+        outs.append((y.clone(), idx.clone()))
+    for y2, idx2 in outs[1:]:
+        assert torch.equal(outs[0][0], y2) and torch.equal(outs[0][1], idx2)
+    O = OracleLayers(orc, sh, seed, 1)
+    y, idx = outs[0][0].cpu().numpy(), outs[0][1].cpu().numpy()
+    for t in range(T):
+        r, exact = layer_reference(orc, O, 0, x[t], idx[t])
+        assert rel_l2(y[t], r["y"]) <= (TOL if exact else NEAR_TIE_TOL), t
+
+
+@pytest.mark.parametrize("path", ["decode", "batched"])
+def test_input_beyond_fp16_reports_range(path):
+    """An input element above fp16's range (the kernels' fp16 operands cannot hold it) is reported
+    as MOE_E_RANGE in the device status, not turned silently into inf."""
+    sh = synth.Shape(256, 16, 2, 64, 64)
+    R = Resident(sh, 1, 3)
+    x = synth.activation_bits(sh, 3, 0, 2).copy()
+    x[1, 5] = synth.bf16_bits(np.array([1.0e5], np.float32))[0]
+    if path == "decode":
+        R.layer_forward(0, _bits(x))
+    else:
+        R.layer_forward_batched(0, _bits(x))
+    torch.cuda.synchronize()
+    assert R.pool.device_status() == moe.E_RANGE
+    # in range again: the status word was cleared by the read
+    x[1, 5] = synth.bf16_bits(np.array([1.0], np.float32))[0]
+    R.layer_forward_batched(0, _bits(x)) if path == "batched" else R.layer_forward(0, _bits(x))
+    torch.cuda.synchronize()
+    assert R.pool.device_status() == moe.OK
+
+
+def test_scale_below_fp16_normal_reports_range():
+    """A group scale below fp16's normal range (2^-14) loses its relative precision in the batched
+    path's fp16 dequantisation: reported as MOE_E_RANGE."""
+    sh = synth.Shape(256, 16, 2, 64, 64)
+    R = Resident(sh, 1, 3)
+    # every expert's gate scales -> 1e-6 (bf16), written into the resident blobs
+    for e in range(sh.n_experts):
+        tt = synth.expert_tensors(sh, 3, 0, int(R.maps[0][e]))
+        tt["gate_s"] = np.full_like(tt["gate_s"], synth.bf16_bits(np.float32(1e-6)))
+        blob = moe.pack_expert(R.mshape, tt)
+        slot = int(R.slots[0][e])
+        R.arena[slot * R.stride: slot * R.stride + blob.size].copy_(torch.from_numpy(blob))
+    x = synth.activation_bits(sh, 3, 0, 3)
+    R.layer_forward_batched(0, _bits(x))
+    torch.cuda.synchronize()
+    assert R.pool.device_status() == moe.E_RANGE
