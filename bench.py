@@ -151,14 +151,15 @@ def _max_over_ranks(ws, v):
     return float(t.item())
 
 
-def cpu_oracle_sample(sh, n_layers_sample, n_layers_model, seed=SEED, budget_s=20.0):
-    """The oracle as it stands, single-threaded, on a bounded sample of the same workload:
-    n_layers_sample layers of the stack for as many tokens as fit the budget (at least one).
-    Returns tokens/s of the full n_layers_model stack (time scaled by the layer ratio)."""
+def cpu_oracle_sample(sh, n_layers_sample, n_layers_model, seed=SEED, budget_s=20.0, threads=1):
+    """The oracle as it stands on a bounded sample of the same workload: n_layers_sample layers of
+    the stack for as many tokens as fit the budget (at least one), its row loops on `threads` host
+    threads (1: serial). Returns tokens/s of the full n_layers_model stack (time scaled by the
+    layer ratio)."""
     import oracle
     from int4_routed_expert_05_b300 import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_ref import OracleLayers
+    from oracle.layers import OracleLayers
+    oracle.set_threads(threads)
     O = OracleLayers(oracle, sh, seed, n_layers_sample)
     for l in range(n_layers_sample):       # blobs of the layers are packed outside the timed region
         O.dense(l)
@@ -178,22 +179,25 @@ def cpu_oracle_sample(sh, n_layers_sample, n_layers_model, seed=SEED, budget_s=2
         tokens += 1
         if tokens >= 64:
             break
+    oracle.set_threads(1)
     per_token_full = t_total / tokens * (n_layers_model / n_layers_sample)
-    return 1.0 / per_token_full, {"layers": n_layers_sample, "tokens": tokens, "seconds": t_total}
+    return 1.0 / per_token_full, {"layers": n_layers_sample, "tokens": tokens, "seconds": t_total, "threads": threads}
 
 
 def run_reference(args):
-    """The oracle as it stands, on the host cores (single thread), on this arm's workload.
-    A step is a bounded sample: one full oracle layer for one token when K + W of them fit in
-    about two and a half minutes, else one expert FFN of a layer (the oracle's dominant cost), with
-    tokens/s of the whole stack derived from the sampled time."""
+    """The oracle as it stands, on every host core (its row loops threaded; the results equal the
+    serial ones bit for bit), on this arm's workload. A step is a bounded sample: one full oracle
+    layer for one token when K + W of them fit in about two and a half minutes, else one expert FFN
+    of a layer (the oracle's dominant cost), with tokens/s of the whole stack derived from the
+    sampled time."""
     ws, rank, _ = _dist()
     if rank != 0:
         return
     import oracle
     from int4_routed_expert_05_b300 import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_ref import OracleLayers
+    from oracle.layers import OracleLayers
+    ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    oracle.set_threads(ncores)
     name, L, bits, desc = CONFIGS[args.config]
     sh = _shape(name, bits)
     if args.config in BATCHED:
@@ -207,7 +211,7 @@ def run_reference(args):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times[args.warmup:] or times),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": args.config, "description": desc, "tokens": BATCHED[args.config]},
-                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": info},
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": ncores, "kind": "oracle", "sample": info},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -256,7 +260,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.config, "description": desc, "batch": 1, "layers": L},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": ncores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -435,9 +439,12 @@ def run_ours(args):
     tok_s = ws * args.steps / (ms / 1e3)
     peak, peak_kind = _peaks()
     achieved = per_launch_expert / (ms_step / 1e3) / 1e9
-    cpu_v, cpu_info = (None, None)
+    cpu_v, cpu_info, cpu1_v, cpu1_info = None, None, None, None
+    ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     if ws == 1 and not args.no_cpu_baseline:
-        cpu_v, cpu_info = cpu_oracle_sample(sh, args.ref_layers, L, budget_s=args.ref_budget)
+        # the oracle on every host core, and serially (half the budget each)
+        cpu_v, cpu_info = cpu_oracle_sample(sh, args.ref_layers, L, budget_s=args.ref_budget / 2, threads=ncores)
+        cpu1_v, cpu1_info = cpu_oracle_sample(sh, args.ref_layers, L, budget_s=args.ref_budget / 2, threads=1)
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
@@ -460,9 +467,12 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "moe_decode_kernel", "bytes_per_launch": per_launch_expert},
         "cpu_baseline": None if cpu_v is None else {
-            "value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "value": cpu_v, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
             "sample": f"{cpu_info['tokens']} token(s) through {cpu_info['layers']} of {L} layers in "
-                      f"{cpu_info['seconds']:.1f} s, time scaled to the full stack"},
+                      f"{cpu_info['seconds']:.1f} s on {ncores} threads (row loops), time scaled to the full stack",
+            "serial": {"value": cpu1_v, "unit": "tokens/s", "cores": 1,
+                       "sample": f"{cpu1_info['tokens']} token(s) through {cpu1_info['layers']} of {L} layers in "
+                                 f"{cpu1_info['seconds']:.1f} s, one thread"}},
         "e2e": {"value": ws * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * H, "d2h_bytes_per_step": 4 * H,
                 "steps": n_e2e},
         "gpu_launches": args.steps,
@@ -658,8 +668,7 @@ def cpu_oracle_batched(sh, T, seed=SEED, budget_s=15.0):
     budget is spent (at most T tokens); tokens/s of one layer."""
     import oracle
     from int4_routed_expert_05_b300 import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_ref import OracleLayers
+    from oracle.layers import OracleLayers
     O = OracleLayers(oracle, sh, seed, 1)
     xb = synth.activation_bits(sh, seed, 1000, min(T, 64))
     t_total, n = 0.0, 0

@@ -25,9 +25,10 @@ RMS_EPS = 1e-6
 
 
 def compile_c(src: str, out: str) -> str:
-    """gcc -O2, no fast-math, no floating-point contraction."""
+    """gcc -O2, no fast-math, no floating-point contraction; OpenMP for the optional threaded row
+    loops (serial unless set_threads asks for more)."""
     tmp = f"{out}.tmp{os.getpid()}"  # written aside and renamed: concurrent builders never see half a file
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-shared", "-fPIC",
            "-o", tmp, src, "-lm"]
     try:
         subprocess.run(cmd, check=True)
@@ -83,10 +84,23 @@ def _load():
     lib.orc_moe_layer_sel.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, I, P, P, P, P, P, P]
     lib.orc_route_weights.restype = None
     lib.orc_route_weights.argtypes = [P, I, I, I, P, P]
+    lib.orc_set_threads.restype = None
+    lib.orc_set_threads.argtypes = [I]
+    lib.orc_get_threads.restype = I
+    lib.orc_get_threads.argtypes = []
     lib.orc_rmsnorm_bf16.restype = None
     lib.orc_rmsnorm_bf16.argtypes = [P, I, ctypes.c_double, P]
     _lib = lib
     return lib
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's row loops (1: serial, the default). Results do not depend on it."""
+    _load().orc_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(_load().orc_get_threads())
 
 
 def _ptr(a: np.ndarray | None):

@@ -27,6 +27,12 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* Threads of the row loops (the oracle's timing on all host cores). Default 1: serial. Rows are
+ * independent and each row's sums keep their order, so the results do not depend on the count. */
+static int orc_threads = 1;
+void orc_set_threads(int n) { orc_threads = n < 1 ? 1 : n; }
+int orc_get_threads(void) { return orc_threads; }
+
 /* ------------------------------------------------------------------------------------------ */
 /* bf16 values                                                                                 */
 /* ------------------------------------------------------------------------------------------ */
@@ -196,6 +202,7 @@ void orc_dequant(const uint8_t* blob, int H, int I, int bits, int group, int whi
     const uint8_t* q = blob + off[which];
     const uint8_t* s = blob + off[3 + 2 * which];
     const uint8_t* b = blob + off[4 + 2 * which];
+#pragma omp parallel for num_threads(orc_threads) if (orc_threads > 1)
     for (int r = 0; r < rows; ++r)
         for (int c = 0; c < cols; ++c) {
             size_t gi = (size_t)r * ng + c / group;
@@ -219,6 +226,7 @@ void orc_router_logits(const uint16_t* Wr, const uint16_t* u, const float* bias,
 {
     double unit = ldexp(1.0, -24);
     double gam = (H + 1) * unit / (1.0 - (H + 1) * unit);
+#pragma omp parallel for num_threads(orc_threads) if (orc_threads > 1)
     for (int e = 0; e < E; ++e) {
         double acc = 0.0, mag = 0.0;
         for (int h = 0; h < H; ++h) {
@@ -302,6 +310,7 @@ void orc_expert_ffn(const uint8_t* blob, int H, int I, int bits, int group, cons
     orc_dequant(blob, H, I, bits, group, 0, Wg);
     orc_dequant(blob, H, I, bits, group, 1, Wu);
     orc_dequant(blob, H, I, bits, group, 2, Wd);
+#pragma omp parallel for num_threads(orc_threads) if (orc_threads > 1)
     for (int r = 0; r < I; ++r) {
         double g = 0.0, v = 0.0;
         for (int c = 0; c < H; ++c) {
@@ -313,6 +322,7 @@ void orc_expert_ffn(const uint8_t* blob, int H, int I, int bits, int group, cons
         if (h_out)
             h_out[r] = h[r];
     }
+#pragma omp parallel for num_threads(orc_threads) if (orc_threads > 1)
     for (int o = 0; o < H; ++o) {
         double acc = 0.0;
         for (int r = 0; r < I; ++r)

@@ -451,3 +451,21 @@ def test_pool_sim_golden_trace():
     with open(os.path.join(GOLDEN, "pool_trace.json")) as f:
         trace = json.load(f)
     assert run_pool_trace(PoolSim, trace) == []
+
+
+def test_threaded_oracle_is_bitwise_serial(orc):
+    """The oracle's optional threaded row loops give the serial results bit for bit (rows are
+    independent and keep their summation order)."""
+    sh = synth.Shape(512, 64, 6, 128, 192)
+    blobs = [orc.pack(sh, synth.expert_tensors(sh, 8, 0, e)) for e in range(sh.n_experts)]
+    shared = orc.pack(sh, synth.expert_tensors(sh, 8, 0, synth.SHARED_EXPERT), shared=True)
+    args = (sh, synth.activation_bits(sh, 8, 0)[0], synth.router_bits(sh, 8, 0), synth.shared_gate_bits(sh, 8, 0),
+            blobs, shared)
+    r1 = orc.moe_layer(*args)
+    orc.set_threads(4)
+    try:
+        r4 = orc.moe_layer(*args)
+    finally:
+        orc.set_threads(1)
+    for key in ("idx", "w", "y", "logits", "bound"):
+        assert np.array_equal(r1[key], r4[key]), key
