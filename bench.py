@@ -297,7 +297,9 @@ def run_streamed(args):
         L, desc = args.layers, desc + f" (first {args.layers} layers only)"
     sh = _shape(name, bits)
     n_slots = POOL_SLOTS[args.config]
-    S = Streamed(sh, L, SEED, n_slots, beta=0.0, verbose=(rank == 0))
+    if args.pool_gib:
+        n_slots = int(args.pool_gib * (1 << 30)) // 1769472
+    S = Streamed(sh, L, SEED, n_slots, beta=0.0, prefetch=0, verbose=(rank == 0))
     H = sh.hidden
     xs = torch.from_numpy(np.stack([synth.activation_f32(sh, SEED, s)[0] for s in range(64)])).cuda()
     # Zipf(1.1) popularity always on: beta is bisected on the device, over the timed run's own
@@ -305,7 +307,12 @@ def run_streamed(args):
     # (random-init routing alone already reuses experts).
     sched = dict(warm=args.warmup, tokens=args.steps)  # the timed run's own warm-up and length
     hr0 = S.measure_hit_rate(xs, **sched)
-    beta, hr_cal = (0.0, hr0) if hr0 >= 0.60 else S.calibrate_beta(xs, target=0.60, **sched)
+    if args.zipf_beta is not None:  # a fixed strength (a pool-size sweep keeps the routing fixed)
+        beta, hr_cal = args.zipf_beta, None
+    else:
+        beta, hr_cal = (0.0, hr0) if hr0 >= 0.60 else S.calibrate_beta(xs, target=0.60, **sched)
+    # the pool's own hit rate is calibrated without speculation; the timed run uses --prefetch
+    S.prefetch = args.prefetch
     if beta != S.beta:
         S.set_beta(beta)
     sim = simulated_hit_rate(sh, L, n_slots, beta, seed=SEED)
@@ -347,6 +354,7 @@ def run_streamed(args):
         "config": {"workload": args.config, "description": desc, "batch": 1, "layers": L, "pool_slots": n_slots,
                    "pool_bytes": n_slots * S.stride, "zipf_s": 1.1, "zipf_beta": beta,
                    "hit_rate_uniform_routing": hr0, "hit_rate_calibration": hr_cal, "simulated_hit_rate": sim,
+                   "prefetch": args.prefetch,
                    "host_store": f"{S.n_unique} unique blobs pinned, expert (l, e) -> blob maps[l][e]"},
         "pool": {"hit_rate": hits / max(1, hits + misses), "misses_per_token": misses / args.steps,
                  "miss_bytes_per_token": nbytes / args.steps, "miss_gbs": miss_gbs, "pinned_h2d_gbs": link,
@@ -694,6 +702,11 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graphs", action="store_true", help="batched workloads: time direct calls, not graph replays")
+    ap.add_argument("--pool-gib", type=float, default=0.0, help="bounded pool: size in GiB (default: the config's)")
+    ap.add_argument("--zipf-beta", type=float, default=None,
+                    help="bounded pool: fixed routing-popularity strength instead of the calibrated one")
+    ap.add_argument("--prefetch", type=int, default=6,
+                    help="bounded pool: copy ahead the next layer's N best predicted experts (0: off; default 6, the best of a 2 GiB sweep)")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the stack (small cases for profiling)")
     args = ap.parse_args()

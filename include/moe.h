@@ -175,6 +175,13 @@ moe_status moe_pool_wait_loads(moe_pool* pool, void* compute_stream);
  * slot, then unpin them all. */
 moe_status moe_pool_release(moe_pool* pool, void* compute_stream);
 
+/* Speculative copies in moe_stack_forward_streamed: the next layer's n best predicted experts (in
+ * rank order; n >= top_k: all of them) that are not resident are copied ahead; 0 (the default)
+ * turns it off. A guess costs link time when wrong and takes a slot, so it pays when the link has
+ * room (a pool smaller than a token's working set) and costs when the link is already the limit.
+ * Host-side setting, takes effect at the next call; MOE_E_INVALID for n < 0. */
+moe_status moe_pool_set_prefetch(moe_pool* pool, int32_t n);
+
 /* Counters since creation: lookups that hit, lookups that missed, bytes copied by load_slot. */
 moe_status moe_pool_stats(const moe_pool* pool, int64_t* hits, int64_t* misses, int64_t* bytes_loaded);
 
@@ -215,8 +222,14 @@ moe_status moe_experts(moe_pool* pool, int32_t layer, const void* d_x, const flo
 /* Bounded mode, a whole pre-norm residual stack for one token, driven on the host ([qpack],
  * [route]): per layer moe_route, a device-to-host read of the k selected experts (synchronous),
  * moe_pool_lookup, moe_pool_load_slot for every miss from h_blobs on copy_stream, moe_pool_wait_loads,
- * moe_experts and moe_pool_release. h_blobs: host array [n_layers][n_experts] (indexed from
- * layer0) of pinned host blob pointers (moe_expert_stride bytes each; entries may repeat).
+ * moe_experts and moe_pool_release. With prefetch set (moe_pool_set_prefetch, off by default) the
+ * next layer is also routed on this layer's input, in the same synchronous read, and its best
+ * predicted experts that are not resident are loaded behind this layer's misses while this layer
+ * runs;
+ * the next layer's real selection is looked up as usual, so the result does not depend on the
+ * guess (a wrong one costs link time and slots). h_blobs: host array of pinned host blob pointers
+ * indexed by absolute layer, entry [l * n_experts + e] for layer l (layers layer0 .. layer0 +
+ * n_layers - 1 must be filled; moe_expert_stride bytes each; entries may repeat).
  * d_x: fp32 [H] input residual; d_x_out: fp32 [H] final residual (the pool workspace holds the
  * residuals in between). h_topk_idx: host int32 [n_layers][k] receiving the selections, or NULL.
  * Returns when the last layer has been enqueued on compute_stream. */

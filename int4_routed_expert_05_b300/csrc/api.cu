@@ -81,7 +81,7 @@ WsLayout ws_layout(const moe_shape& s, int L)
     take(w.smaps, sizeof(CUtensorMap) * 3 * (size_t)L);
     take(w.logits, sizeof(float) * (size_t)s.n_experts);
     take(w.hbuf, sizeof(float) * (size_t)(s.top_k + 1) * Imax);
-    take(w.sel, sizeof(int32_t) * 3 * kMaxK);
+    take(w.sel, sizeof(int32_t) * 5 * kMaxK);
     take(w.xlog, sizeof(unsigned long long) * (size_t)s.n_experts);
     take(w.xh, sizeof(unsigned long long) * (size_t)(s.top_k + 1) * xh_stride(s.inter, s.shared_inter));
     take(w.xflag, sizeof(unsigned long long));  // the step counter
@@ -141,6 +141,7 @@ struct moe_pool {
     uint32_t smem = 0;
     int smem_optin = 0;
     uint64_t timeout_ns = 2000000000ull;
+    int prefetch = 0;  // bounded stacks: copy ahead the next layer's top `prefetch` predicted experts
     // bounded mode: events
     std::vector<cudaEvent_t> ring;   // last-use events, reused round robin
     size_t ring_next = 0;
@@ -376,6 +377,14 @@ moe_status moe_pool_set_timeout(moe_pool* p, uint64_t timeout_ns)
     if (!p || timeout_ns == 0)
         return fail(MOE_E_INVALID, "bad pool or zero timeout");
     p->timeout_ns = timeout_ns;
+    return MOE_OK;
+}
+
+moe_status moe_pool_set_prefetch(moe_pool* p, int32_t n)
+{
+    if (!p || n < 0)
+        return fail(MOE_E_INVALID, "bad pool or negative prefetch depth");
+    p->prefetch = n;
     return MOE_OK;
 }
 
@@ -783,15 +792,24 @@ moe_status moe_stack_forward_streamed(moe_pool* p, int32_t layer0, int32_t n_lay
     cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
     int32_t* d_idx = reinterpret_cast<int32_t*>(p->ws + p->wl.sel);
     float* d_w = reinterpret_cast<float*>(d_idx + kMaxK);
+    int32_t* d_spec = d_idx + 3 * kMaxK;  // the next layer routed on this layer's input
+    float* d_spec_w = reinterpret_cast<float*>(d_idx + 4 * kMaxK);
     float* bufs[2] = {reinterpret_cast<float*>(p->ws + p->wl.xbuf), reinterpret_cast<float*>(p->ws + p->wl.xbuf) + H};
     const float* cur = d_x;
-    int32_t idx[kMaxK], slots[kMaxK];
+    int32_t idx[kMaxK], slots[kMaxK], spec[kMaxK];
     for (int li = 0; li < n_layers; ++li) {
         const int l = layer0 + li;
         float* out = li == n_layers - 1 ? d_x_out : bufs[li & 1];
+        // speculation: the next layer's router on this layer's input (the residual changes by one
+        // layer's output in between), so that its likely misses can travel while this layer runs
+        const bool spec_on = p->prefetch > 0 && li + 1 < n_layers;
         if ((st = moe_route(p, l, cur, d_idx, d_w, cs)) != MOE_OK)
             return st;
+        if (spec_on && (st = moe_route(p, l + 1, cur, d_spec, d_spec_w, cs)) != MOE_OK)
+            return st;
         CUDA_TRY(cudaMemcpyAsync(idx, d_idx, sizeof(int32_t) * k, cudaMemcpyDeviceToHost, cs));
+        if (spec_on)
+            CUDA_TRY(cudaMemcpyAsync(spec, d_spec, sizeof(int32_t) * k, cudaMemcpyDeviceToHost, cs));
         CUDA_TRY(cudaStreamSynchronize(cs));
         for (int j = 0; j < k; ++j)
             if (idx[j] < 0 || idx[j] >= E)
@@ -810,6 +828,18 @@ moe_status moe_stack_forward_streamed(moe_pool* p, int32_t layer0, int32_t n_lay
         }
         if ((st = moe_pool_wait_loads(p, compute_stream)) != MOE_OK)
             return st;
+        // the next layer's top predicted experts that are not resident: copied behind this
+        // layer's misses on the copy stream (the next layer's own lookup decides what is used; a
+        // wrong guess only costs link time). A full pool skips the rest of the guesses.
+        if (spec_on)
+            for (int j = 0; j < k && j < p->prefetch; ++j) {
+                int32_t s_ = -1;
+                if (spec[j] < 0 || spec[j] >= E || moe_pool_slot_of(p, l + 1, spec[j], &s_) != MOE_OK || s_ >= 0)
+                    continue;
+                const void* blob = h_blobs[(size_t)(l + 1) * E + spec[j]];
+                if (!blob || moe_pool_load_slot(p, l + 1, spec[j], blob, copy_stream, &s_) != MOE_OK)
+                    break;
+            }
         if ((st = moe_experts(p, l, cur, d_w, slots, out, compute_stream)) != MOE_OK)
             return st;
         if ((st = moe_pool_release(p, compute_stream)) != MOE_OK)

@@ -26,6 +26,7 @@ ENTRY_POINTS = [
     "moe_pool_stats", "moe_layer_forward", "moe_stack_forward", "moe_route", "moe_experts",
     "moe_layer_forward_scalar", "moe_device_status", "moe_pool_set_timeout", "moe_pool_grid",
     "moe_last_error", "moe_pool_slot_of", "moe_pool_set_copy_hook", "moe_layer_forward_static",
+    "moe_pool_set_prefetch",
     "moe_stack_forward_streamed", "moe_batched_workspace_bytes", "moe_layer_forward_batched",
     "moe_pool_time_batched", "moe_pool_batched_gemm_ms",
 ]
@@ -84,6 +85,7 @@ def load() -> ctypes.CDLL:
         "moe_layer_forward_scalar": (ST, [P, I32, P, P, P, P, P]),
         "moe_device_status": (ST, [P, P, ctypes.POINTER(I32)]),
         "moe_pool_set_timeout": (ST, [P, ctypes.c_uint64]),
+        "moe_pool_set_prefetch": (ST, [P, I32]),
         "moe_pool_grid": (I32, [P]),
         "moe_last_error": (ctypes.c_char_p, []),
         "moe_pool_slot_of": (ST, [P, I32, I32, ctypes.POINTER(I32)]),
@@ -206,6 +208,11 @@ class Pool:
 
     def set_timeout(self, ns: int):
         _check(self.lib.moe_pool_set_timeout(self.h, ns))
+
+    def set_prefetch(self, n: int):
+        """Speculative copies of the next layer's n best predicted experts in stack_forward_streamed
+        (0: off)."""
+        _check(self.lib.moe_pool_set_prefetch(self.h, int(n)))
 
     def set_layer(self, layer: int, router, shared_blob, shared_gate, logit_bias=None):
         w = LayerWeights(_p(router), _p(shared_blob), _p(shared_gate), _p(logit_bias))

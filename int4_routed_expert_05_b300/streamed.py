@@ -76,7 +76,8 @@ class Streamed:
     """n_layers pre-norm residual MoE layers in bounded mode (n_slots expert slots in HBM)."""
 
     def __init__(self, sh: synth.Shape, n_layers: int, seed: int, n_slots: int, *, n_unique: int | None = None,
-                 beta: float = 0.0, device: str = "cuda", verbose: bool = False):
+                 beta: float = 0.0, prefetch: int = 0, device: str = "cuda", verbose: bool = False):
+        self.prefetch = prefetch
         t0 = time.time()
         self.sh, self.L, self.seed, self.n_slots = sh, n_layers, seed, n_slots
         E = sh.n_experts
@@ -126,6 +127,7 @@ class Streamed:
             self.pool.close()
         self.ws.zero_()
         self.pool = moe.Pool(self.mshape, self.L, self.n_slots, self.arena, self.arena.numel(), self.ws, self.ws.numel())
+        self.pool.set_prefetch(self.prefetch)
         for l in range(self.L):
             self.pool.set_layer(l, self.router[l], self.shared[l], self.gate[l], self.bias[l])
         self.pool.sync()

@@ -20,13 +20,14 @@ def _built():
     assert torch.cuda.is_available()
 
 
+@pytest.mark.parametrize("prefetch", [0, 4, 16])
 @pytest.mark.parametrize("sh,n_slots", [(synth.Shape(2048, 512, 10, 512, 512), 24), (synth.TINY, 5)])
-def test_streamed_stack_equals_resident(sh, n_slots):
+def test_streamed_stack_equals_resident(sh, n_slots, prefetch):
     L, seed, beta, n_unique = 4, 3, 0.7, 64
     flags = moe.RENORM | moe.PRENORM | moe.RESIDUAL
     bias = [zipf_bias(sh, seed, l, beta) for l in range(L)]
     R = Resident(sh, L, seed, n_unique=min(n_unique, sh.n_experts), flags=flags, bias=bias)
-    S = Streamed(sh, L, seed, n_slots, n_unique=min(n_unique, sh.n_experts), beta=beta)
+    S = Streamed(sh, L, seed, n_slots, n_unique=min(n_unique, sh.n_experts), beta=beta, prefetch=prefetch)
     out_s = torch.empty(sh.hidden, dtype=torch.float32, device="cuda")
     steps = 3
     for step in range(steps):
@@ -40,7 +41,11 @@ def test_streamed_stack_equals_resident(sh, n_slots):
         assert torch.equal(out_r, out_s), step
     hits, misses, nbytes = S.pool.stats()
     assert hits + misses == steps * L * sh.top_k
-    assert misses > 0 and nbytes == misses * S.stride
+    # speculative copies add bytes beyond the misses of the real selections
+    assert misses > 0 and (nbytes >= misses * S.stride if prefetch else nbytes == misses * S.stride)
+    if prefetch:
+        with pytest.raises(moe.MoeError):
+            S.pool.set_prefetch(-1)
 
 
 def test_streamed_layers_against_oracle(orc):
