@@ -1163,9 +1163,9 @@ __device__ __forceinline__ void router_rows(const Ctx& C, unsigned long long* xl
     }
 }
 
-// Warp 0: the combine weights (softmax over the k selected logits with renorm, else over all E)
-// and pool slots of the ranked selection sel_idx.
-__device__ __forceinline__ void topk_weights(const Ctx& C, bool renorm, bool slots)
+// One warp: the combine weights of the ranked selection sel_idx (softmax over the k selected
+// logits with renorm, else over all E).
+__device__ __forceinline__ void topk_weights(const Ctx& C, bool renorm)
 {
     const int E = C.E, k = C.k;
     const float* __restrict__ slg = C.slg;
@@ -1183,10 +1183,8 @@ __device__ __forceinline__ void topk_weights(const Ctx& C, bool renorm, bool slo
             sum += __expf(slg[e2] - lmax);
         denom = warp_sum(sum);
     }
-    if (LANE < k) {
+    if (LANE < k)
         C.sel_w[LANE] = __fdividef(pj, denom);
-        C.sel_slot[LANE] = slots ? C.stab[C.tab_off + isel] : -1;
-    }
 }
 
 // slg (logits) -> sel_idx / sel_w / sel_slot (rank order: larger fp32 logit first, equal logits ->
@@ -1197,8 +1195,9 @@ __device__ __forceinline__ void topk_weights(const Ctx& C, bool renorm, bool slo
 // k-th largest key itself at worst. The keys >= lo hold the top k; they are gathered and each is
 // ranked by counting the larger ones (composite keys: the logit key above, the complement of the
 // index below, so that equal logits rank by index). slots: look the selected experts' pool slots up
-// in the staged slot-table row.
-__device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, bool slots)
+// in the staged slot-table row. The combine weights are left to topk_weights (needed only when
+// the block adds its output, so they are computed off the path to the expert copies).
+__device__ __forceinline__ void topk_select(const Ctx& C, bool slots)
 {
     const int E = C.E, k = C.k;
     int* __restrict__ scnt = reinterpret_cast<int*>(C.tk);                                     // [1]
@@ -1259,7 +1258,8 @@ __device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, bool slot
                     C.sel_idx[rank] = (int)(0xFFFFFFFFu - (uint32_t)mine);
             }
             __syncwarp();
-            topk_weights(C, renorm, slots);
+            if (LANE < k)
+                C.sel_slot[LANE] = slots ? C.stab[C.tab_off + C.sel_idx[LANE]] : -1;
         }
     } else {
         // many equal keys at the k-th: every survivor ranked by its own thread
@@ -1273,8 +1273,8 @@ __device__ __forceinline__ void topk_select(const Ctx& C, bool renorm, bool slot
                 C.sel_idx[rank] = (int)(0xFFFFFFFFu - (uint32_t)mine);
         }
         __syncthreads();
-        if (WARP == 0)
-            topk_weights(C, renorm, slots);
+        if (WARP == 0 && LANE < k)
+            C.sel_slot[LANE] = slots ? C.stab[C.tab_off + C.sel_idx[LANE]] : -1;
     }
     __syncthreads();
 }
@@ -1405,13 +1405,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
                 if (route) {
                     if (!(ok = poll_pairs(P.xlog, C.E, epoch, C.slg, limit, P.status)))
                         break;
-                    topk_select(C, (P.flags & kRenorm) != 0, P.mode == kModeFull);
-                    if (CTA == 0 && TID < K) {
-                        const size_t o = ((size_t)t * P.n_layers + li) * K + TID;
-                        if (P.topk_idx)
-                            P.topk_idx[o] = C.sel_idx[TID];
-                        if (P.topk_w)
-                            P.topk_w[o] = C.sel_w[TID];
+                    topk_select(C, P.mode == kModeFull);
+                    // the combine weights (one warp, beside warp 0's expert copies below) and block
+                    // 0's selection outputs
+                    if (WARP == 1) {
+                        topk_weights(C, (P.flags & kRenorm) != 0);
+                        __syncwarp();
+                        if (CTA == 0 && LANE < K) {
+                            const size_t o = ((size_t)t * P.n_layers + li) * K + LANE;
+                            if (P.topk_idx)
+                                P.topk_idx[o] = C.sel_idx[LANE];
+                            if (P.topk_w)
+                                P.topk_w[o] = C.sel_w[LANE];
+                        }
                     }
                     if (!experts)
                         break;  // a route-only launch has one step

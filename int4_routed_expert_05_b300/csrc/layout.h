@@ -118,6 +118,11 @@ constexpr int kMaxExpects = 64;        // their mbarriers
 // mbarriers: gate/up copy pieces [kMaxGuBars] (slot s, matrix m (gate 0, up 1), piece p: bit
 // (2s + m) * npc + p), then down copies, then the dense copies.
 constexpr int kMaxGuSlots = 8;
+// Pieces per gate/up copy. Measured on the 80B-shaped stack: with every block's copies in flight at
+// once, a block's first 10 KB piece landed no earlier than its whole 43 KB gate copy did (the
+// memory system serves all blocks' requests interleaved), while 8 pieces per matrix raised the
+// copies per block from 9 to 23 and the issue time from 0.6 to 1.3 us. So one piece.
+constexpr int kMaxPieces = 1;
 constexpr int kMaxGuBars = 32;
 constexpr int kMbDown = kMaxGuBars, kMbDense = kMbDown + 1;
 constexpr int kNumMbar = kMbDown + 2;
@@ -180,11 +185,11 @@ MOE_HD StageGeo stage_geo(int H, int Ie, int bits, int G, int ngroups, int ncs_g
     s.nslot_gu = imax(1, imin(nslot_gu, s.ncs_gu));
     s.ncs_d = 1;
     s.cpg_d = s.ncb_d;
-    // pieces: the most (up to 8) that divide the copy's column blocks evenly, fit the mbarriers,
-    // and start on the swizzle period (1024 bytes) when the rows are swizzled
+    // pieces: the most (up to kMaxPieces) that divide the copy's column blocks evenly, fit the
+    // mbarriers, and start on the swizzle period (1024 bytes) when the rows are swizzled
     s.npc_gu = 1;
 #pragma unroll 1
-    for (int n = imin(8, s.cpg_gu); n > 1; --n)
+    for (int n = imin(kMaxPieces, s.cpg_gu); n > 1; --n)
         if (s.cpg_gu % n == 0 && 2 * s.nslot_gu * n <= kMaxGuBars &&
             (!s.swz_gu || ((s.cpg_gu / n) * s.bh_gu * s.cbw_gu) % 1024 == 0)) {
             s.npc_gu = n;
