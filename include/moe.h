@@ -33,8 +33,8 @@
  *    moe_pool_create.
  *  - Errors are returned as moe_status codes; moe_last_error() gives a message (per thread).
  *    Nothing throws across the ABI, exits, or traps on the device. Problems found by a kernel
- *    (an expert that is not resident, a grid barrier that timed out) are written to a device
- *    status word that moe_device_status() reads.
+ *    (an expert that is not resident, a device-side wait that timed out, a value the fp16
+ *    operands cannot hold) are written to a device status word that moe_device_status() reads.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -195,7 +195,10 @@ moe_status moe_pool_stats(const moe_pool* pool, int64_t* hits, int64_t* misses, 
  * d_topk_idx (int32 [T][k]) and d_topk_w (fp32 [T][k]): selected experts in rank order (largest
  * logit first, equal fp32 logits to the lower index) and their weights; either may be NULL.
  * Every selected expert must be placed (resident mode); one that is not sets the device status
- * MOE_E_NOT_RESIDENT and contributes nothing. One cooperative kernel launch. */
+ * MOE_E_NOT_RESIDENT and contributes nothing; an input or intermediate value above 65504 in
+ * magnitude (the kernel's fp16 operands) sets MOE_E_RANGE. The sum over the k + 1 experts is exact
+ * fixed-point integer arithmetic, so the output does not depend on pool placement or timing. One
+ * cooperative kernel launch. */
 moe_status moe_layer_forward(moe_pool* pool, int32_t layer, const void* d_x, int32_t n_tokens,
                              float* d_y, int32_t* d_topk_idx, float* d_topk_w, void* stream);
 
@@ -288,24 +291,28 @@ moe_status moe_layer_forward_scalar(moe_pool* pool, int32_t layer, const void* d
  *
  * moe_layer_forward_static computes the same layer as moe_layer_forward (same kernel, same
  * arguments d_x, n_tokens, d_y, d_topk_idx, d_topk_w, same results) without a pool. Its scratch
- * (barrier counter, status word, expert table, layer descriptor, logits, intermediate
- * activations) is a file-scope device array of MOE_STATIC_SCRATCH_BYTES that every GPU which
- * loads the library keeps until the process exits. It calls no cudaMalloc, cudaFree or other
- * allocating routine.
+ * (launch-barrier and step counters, status word, expert table, layer descriptor, the shared
+ * expert's tensor maps, exchanged logits and intermediate activations, output words) is a
+ * file-scope device array of MOE_STATIC_SCRATCH_BYTES that every GPU which loads the library
+ * keeps until the process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
  *  - d_experts: the n_experts routed blobs in the fixed-stride container layout, expert e at
  *    d_experts + e * moe_expert_stride(shape, 0) (256-byte aligned); w: the layer's resident
  *    weights as for moe_pool_set_layer. All caller-owned, device memory.
- *  - d_status: NULL, or a device int32 that receives the layer's device status (MOE_OK, or
- *    MOE_E_TIMEOUT if a device-side wait ran past 2 s); it is reset to MOE_OK by the call.
+ *  - d_status (required, 4-byte aligned): a device int32 that receives the layer's device status
+ *    (MOE_OK; MOE_E_TIMEOUT if a device-side wait ran past 2 s; MOE_E_RANGE as for
+ *    moe_layer_forward); it is reset to MOE_OK by the call. NULL returns MOE_E_INVALID.
  *  - A shape whose scratch does not fit returns MOE_E_NOMEM (message in moe_last_error); other
  *    argument errors return MOE_E_INVALID or MOE_E_SHAPE before anything is enqueued.
  *  - The first call on a device does a one-time set-up with that device current (the scratch
  *    array's device address via cudaGetSymbolAddress, the SM count). Make that first call before
  *    any stream capture.
  *  - Every call on a device shares the one scratch array, which keeps the previous call's
- *    contents; each call resets the parts that must start at zero. Calls that overlap on the GPU
- *    (issued on different streams without ordering) race on the array and give wrong results.
- * Enqueues two kernels on `stream` and returns. */
+ *    contents; each call resets the parts that must start at zero, and a call whose shape lays
+ *    the array out differently from the previous call's clears its exchange buffers first.
+ *    Calls that overlap on the GPU (issued on different streams without ordering) race on the
+ *    array and give wrong results.
+ * Enqueues a set-up kernel and the decode kernel (and a clear when the layout changed) on
+ * `stream` and returns. */
 #define MOE_STATIC_SCRATCH_BYTES (128 * 1024)
 moe_status moe_layer_forward_static(const moe_shape* shape, const void* d_experts, const moe_layer_weights* w,
                                     const void* d_x, int32_t n_tokens, float* d_y, int32_t* d_topk_idx,
@@ -316,8 +323,8 @@ moe_status moe_layer_forward_static(const moe_shape* shape, const void* d_expert
 /* ----------------------------------------------------------------------------------------- */
 
 /* Wait for `stream`, read and clear the pool's device status word into *h_status (a moe_status
- * value, MOE_OK if no kernel reported a problem). After MOE_E_TIMEOUT the grid-barrier counter is
- * reset too. Synchronous. */
+ * value, MOE_OK if no kernel reported a problem). After MOE_E_TIMEOUT the launch-barrier counter
+ * is reset too. Synchronous. */
 moe_status moe_device_status(moe_pool* pool, void* stream, int32_t* h_status);
 
 /* Limit, in nanoseconds, of every device-side wait of this pool's kernels (default 2 s). A wait
