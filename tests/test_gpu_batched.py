@@ -230,3 +230,23 @@ def test_scale_below_fp16_normal_reports_range():
     R.layer_forward_batched(0, _bits(x))
     torch.cuda.synchronize()
     assert R.pool.device_status() == moe.E_RANGE
+
+
+REPEAT_SHAPES = [(256, 40, 3, 64, 128), (768, 100, 7, 192, 320), (256, 512, 16, 64, 64)]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("dims", REPEAT_SHAPES)
+@pytest.mark.parametrize("T", [37, 129, 512])
+def test_batched_repeated_seeds(orc, bits, dims, T):
+    """The batched kernels against the oracle over ten seeds per shape, width and token count: an
+    ordering fault between the kernels' roles (mbarrier phases, proxy fences, tensor-memory waits)
+    would show as an intermittent wrong output. Eight tokens per call are compared (every selected
+    expert and the shared one run for all T tokens, so any tile of any expert can be wrong)."""
+    H, E, k, I, Is = dims
+    sh = synth.Shape(H, E, k, I, Is, bits=bits)
+    rng = np.random.default_rng(T * 1000 + bits)
+    for seed in range(100, 110):
+        sample = sorted(rng.choice(T, size=8, replace=False).tolist())
+        _, _, err = _case(orc, sh, seed=seed, T=T, sample=sample)
+        assert err <= DERIVED, (seed, err)
