@@ -291,6 +291,7 @@ def run_streamed(args):
     torch.cuda.set_device(local)
     from int4_routed_expert_05_b300 import _build, synth
     _build.build()
+    from int4_routed_expert_05_b300 import moe
     from int4_routed_expert_05_b300.streamed import Streamed, calibrate_beta, simulated_hit_rate
     name, L, bits, desc = CONFIGS[args.config]
     if args.layers:
@@ -319,8 +320,21 @@ def run_streamed(args):
     S.reset_pool()  # a fresh, empty pool for the timed run
     out = torch.empty(H, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    step = S.step
+    qinfo = None
+    if args.qpack:
+        # the misses come from an on-disk container instead of the pinned host store
+        t_w = time.perf_counter()
+        S.write_qpack(args.qpack)
+        t_w = time.perf_counter() - t_w
+        qp = S.qpack = moe.Qpack.open(args.qpack, direct=True, n_threads=8)
+        n_staging = 2 * sh.top_k
+        staging = torch.empty(n_staging * S.stride, dtype=torch.uint8, pin_memory=True)
+        step = lambda x, o, st: S.step_qpack(x, o, qp, staging, n_staging, st)  # noqa: E731
+        qinfo = {"path": args.qpack, "direct": qp.info()[3], "reader_threads": 8, "staging_slots": n_staging,
+                 "file_bytes": os.path.getsize(args.qpack), "write_s": t_w}
     for i in range(args.warmup):
-        S.step(xs[i % 64], out, stream)
+        step(xs[i % 64], out, stream)
     torch.cuda.synchronize()
     h0, m0, b0 = S.pool.stats()
     clocks = ClockSampler(local)
@@ -331,7 +345,7 @@ def run_streamed(args):
     t0 = time.perf_counter()
     e0.record(stream)
     for i in range(args.steps):
-        S.step(xs[(args.warmup + i) % 64], out, stream)
+        step(xs[(args.warmup + i) % 64], out, stream)
     e1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
@@ -356,6 +370,7 @@ def run_streamed(args):
                    "hit_rate_uniform_routing": hr0, "hit_rate_calibration": hr_cal, "simulated_hit_rate": sim,
                    "prefetch": args.prefetch,
                    "host_store": f"{S.n_unique} unique blobs pinned, expert (l, e) -> blob maps[l][e]"},
+        "qpack": None if qinfo is None else dict(qinfo, read_gbs=nbytes / wall / 1e9),
         "pool": {"hit_rate": hits / max(1, hits + misses), "misses_per_token": misses / args.steps,
                  "miss_bytes_per_token": nbytes / args.steps, "miss_gbs": miss_gbs, "pinned_h2d_gbs": link,
                  "wall_s": wall},
@@ -705,6 +720,9 @@ def main():
     ap.add_argument("--pool-gib", type=float, default=0.0, help="bounded pool: size in GiB (default: the config's)")
     ap.add_argument("--zipf-beta", type=float, default=None,
                     help="bounded pool: fixed routing-popularity strength instead of the calibrated one")
+    ap.add_argument("--qpack", default="",
+                    help="bounded pool: read the misses from an expert container written to this path "
+                         "(instead of the pinned host store)")
     ap.add_argument("--prefetch", type=int, default=6,
                     help="bounded pool: copy ahead the next layer's N best predicted experts (0: off; default 6, the best of a 2 GiB sweep)")
     ap.add_argument("--layers", type=int, default=0,

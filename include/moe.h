@@ -91,9 +91,10 @@ typedef struct {
  * rounded up to 4096. For hidden 2048, inter 512, int4 both are 1,769,472 bytes ([size]).
  */
 
-/* Bytes of one blob (shared = 1: the shared expert, whose inter is shape->shared_inter). */
+/* Bytes of one blob (shared = 1: the shared expert, whose inter is shape->shared_inter); 0 for a
+ * NULL shape or one without a blob (bits not 4 or 8, sizes not whole positive groups). */
 size_t moe_expert_bytes(const moe_shape* shape, int shared);
-/* Distance between consecutive blobs in a pool or host store. */
+/* Distance between consecutive blobs in a pool or host store (0 as for moe_expert_bytes). */
 size_t moe_expert_stride(const moe_shape* shape, int shared);
 
 /* Write one blob into h_blob (moe_expert_stride bytes, host; the padding is zeroed).
@@ -279,6 +280,53 @@ moe_status moe_layer_forward_batched(moe_pool* pool, int32_t layer, const void* 
  * the fused kernel. Same arguments as moe_layer_forward with n_tokens = 1. */
 moe_status moe_layer_forward_scalar(moe_pool* pool, int32_t layer, const void* d_x, float* d_y,
                                     int32_t* d_topk_idx, float* d_topk_w, void* stream);
+
+/* ----------------------------------------------------------------------------------------- */
+/* Expert container on disk ([qpack], [size])                                                  */
+/* ----------------------------------------------------------------------------------------- */
+/*
+ * One file holds every routed expert of a stack as a fixed-stride blob, so that a miss costs one
+ * positioned read and no index lookup: a 4096-byte header (magic "MOEQPCK1", version 1, the
+ * moe_shape, layers, experts, blob bytes, stride, data offset 4096, file bytes), then blob
+ * (layer l, expert e) at 4096 + (l * n_experts + e) * moe_expert_stride(shape, 0). Every blob
+ * starts on a 4096-byte boundary, so a reader can bypass the page cache (O_DIRECT). Host-only;
+ * no call needs a GPU. All calls are synchronous.
+ */
+typedef struct moe_qpack moe_qpack;
+#define MOE_QPACK_DIRECT 1 /* open flag: read with O_DIRECT when the file system allows it */
+
+/* Create (or truncate) the container at `path` for n_layers layers of `shape`'s routed experts,
+ * write its header and size the file (unwritten blobs read as zeros). MOE_E_INVALID if the file
+ * cannot be written; MOE_E_SHAPE for a shape without a blob size. */
+moe_status moe_qpack_create(const char* path, const moe_shape* shape, int32_t n_layers, moe_qpack** out);
+/* Open a container for reading. flags: MOE_QPACK_DIRECT or 0. n_threads: reader threads for the
+ * parallel reads of moe_stack_forward_qpack (0: reads run on the calling thread). MOE_E_INVALID if
+ * the file is missing, truncated or not of this format. */
+moe_status moe_qpack_open(const char* path, int32_t flags, int32_t n_threads, moe_qpack** out);
+/* The container's shape, layer count, blob stride, and whether it is read with O_DIRECT (1/0);
+ * any output may be NULL. */
+moe_status moe_qpack_info(const moe_qpack* q, moe_shape* shape, int32_t* n_layers, uint64_t* stride,
+                          int32_t* direct);
+/* Write one blob (moe_expert_stride bytes from h_blob, host memory) of a container opened by
+ * moe_qpack_create. MOE_E_INVALID for a layer or expert out of range. */
+moe_status moe_qpack_write(moe_qpack* q, int32_t layer, int32_t expert, const void* h_blob);
+/* Read one blob (moe_expert_stride bytes) into h_dst (host memory; 4096-byte aligned when the
+ * container reads with O_DIRECT). One positioned read. */
+moe_status moe_qpack_read(moe_qpack* q, int32_t layer, int32_t expert, void* h_dst);
+/* Close (a written container is flushed to the device first). NULL is a no-op. */
+moe_status moe_qpack_close(moe_qpack* q);
+
+/* Bounded mode as moe_stack_forward_streamed, with the misses read from the container `q` (which
+ * must hold the pool's shape and layers layer0 .. layer0 + n_layers - 1) instead of a pinned host
+ * store: per layer, the misses are read in parallel (one positioned read each, on the container's
+ * reader threads) into slots of h_staging, a caller-owned pinned host buffer of n_staging blobs
+ * (n_staging >= top_k, 4096-byte aligned), then copied to their pool slots on copy_stream. A
+ * staging slot is reused only after its previous copy has completed. The speculative copies of
+ * moe_pool_set_prefetch do not apply. MOE_E_INVALID for a container of another shape, too few
+ * staging slots or a failed read. */
+moe_status moe_stack_forward_qpack(moe_pool* pool, int32_t layer0, int32_t n_layers, const float* d_x, float* d_x_out,
+                                   moe_qpack* q, void* h_staging, int32_t n_staging, void* compute_stream,
+                                   void* copy_stream, int32_t* h_topk_idx);
 
 /* ----------------------------------------------------------------------------------------- */
 /* Forward pass that allocates nothing                                                         */

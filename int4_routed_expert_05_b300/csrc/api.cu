@@ -15,6 +15,7 @@
 #include <cuda_fp16.h>
 
 #include "grouped.h"
+#include "qpack.h"
 
 namespace moe {
 __global__ void moe_decode_kernel(const __grid_constant__ StepParams P);
@@ -149,6 +150,9 @@ struct moe_pool {
     cudaEvent_t loads_done = nullptr;
     cudaStream_t last_copy_stream = nullptr;
     bool loads_pending = false;
+    std::vector<cudaEvent_t> stage_ev;  // moe_stack_forward_qpack: last copy out of each staging slot
+    std::vector<char> stage_used;
+    int stage_next = 0;
     // test hook replacing the device copy of load_slot
     int (*copy_hook)(void*, int32_t, const void*, size_t) = nullptr;
     void* copy_user = nullptr;
@@ -171,16 +175,24 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_err.c_str(); }
 
+// A shape whose blob is defined: positive sizes that are whole groups and a code width of 4 or 8.
+static bool blob_defined(const moe_shape* s, int shared)
+{
+    const int I = shared ? s->shared_inter : s->inter;
+    return (s->bits == 4 || s->bits == 8) && s->group > 0 && s->hidden > 0 && I > 0 && s->hidden % s->group == 0 &&
+           I % s->group == 0;
+}
+
 size_t moe_expert_bytes(const moe_shape* s, int shared)
 {
-    if (!s)
+    if (!s || !blob_defined(s, shared))
         return 0;
     return blob_geo(s->hidden, shared ? s->shared_inter : s->inter, s->bits, s->group).bytes;
 }
 
 size_t moe_expert_stride(const moe_shape* s, int shared)
 {
-    if (!s)
+    if (!s || !blob_defined(s, shared))
         return 0;
     return blob_geo(s->hidden, shared ? s->shared_inter : s->inter, s->bits, s->group).stride;
 }
@@ -328,6 +340,8 @@ void moe_pool_destroy(moe_pool* p)
         cudaEventDestroy(ev);
     if (p->loads_done)
         cudaEventDestroy(p->loads_done);
+    for (cudaEvent_t ev : p->stage_ev)
+        cudaEventDestroy(ev);
     delete p;
 }
 
@@ -840,6 +854,100 @@ moe_status moe_stack_forward_streamed(moe_pool* p, int32_t layer0, int32_t n_lay
                 if (!blob || moe_pool_load_slot(p, l + 1, spec[j], blob, copy_stream, &s_) != MOE_OK)
                     break;
             }
+        if ((st = moe_experts(p, l, cur, d_w, slots, out, compute_stream)) != MOE_OK)
+            return st;
+        if ((st = moe_pool_release(p, compute_stream)) != MOE_OK)
+            return st;
+        if (h_topk_idx)
+            for (int j = 0; j < k; ++j)
+                h_topk_idx[(size_t)li * k + j] = idx[j];
+        cur = out;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_stack_forward_qpack(moe_pool* p, int32_t layer0, int32_t n_layers, const float* d_x, float* d_x_out,
+                                   moe_qpack* q, void* h_staging, int32_t n_staging, void* compute_stream,
+                                   void* copy_stream, int32_t* h_topk_idx)
+{
+    moe_status st = check_layers(p, layer0, n_layers);
+    if (st != MOE_OK)
+        return st;
+    if ((p->shape.flags & (MOE_PRENORM | MOE_RESIDUAL)) != (MOE_PRENORM | MOE_RESIDUAL))
+        return fail(MOE_E_SHAPE, "a stack needs MOE_PRENORM | MOE_RESIDUAL in the shape flags");
+    if ((st = check_ptr(d_x, 16, "d_x")) != MOE_OK || (st = check_ptr(d_x_out, 16, "d_x_out")) != MOE_OK)
+        return st;
+    const int E = p->shape.n_experts, k = p->shape.top_k, H = p->shape.hidden;
+    if (!q || !h_staging)
+        return fail(MOE_E_INVALID, "container or staging buffer is NULL");
+    const moe_shape& qs = moe::qp::shape(q);
+    if (qs.hidden != H || qs.n_experts != E || qs.inter != p->shape.inter || qs.bits != p->shape.bits ||
+        qs.group != p->shape.group || moe::qp::stride(q) != p->geo.stride || layer0 + n_layers > moe::qp::n_layers(q))
+        return fail(MOE_E_INVALID, "the container holds another shape or fewer layers than the pool's");
+    if (n_staging < k)
+        return fail(MOE_E_INVALID, "%d staging slots for top-%d", n_staging, k);
+    if (reinterpret_cast<uintptr_t>(h_staging) & 4095)
+        return fail(MOE_E_INVALID, "h_staging must be 4096-byte aligned");
+    if ((int)p->stage_ev.size() < n_staging) {
+        for (int i = (int)p->stage_ev.size(); i < n_staging; ++i) {
+            cudaEvent_t ev;
+            CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+            p->stage_ev.push_back(ev);
+            p->stage_used.push_back(0);
+        }
+    }
+    const uint64_t stride = p->geo.stride;
+    uint8_t* stage = static_cast<uint8_t*>(h_staging);
+    cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+    cudaStream_t ys = static_cast<cudaStream_t>(copy_stream);
+    int32_t* d_idx = reinterpret_cast<int32_t*>(p->ws + p->wl.sel);
+    float* d_w = reinterpret_cast<float*>(d_idx + kMaxK);
+    float* bufs[2] = {reinterpret_cast<float*>(p->ws + p->wl.xbuf), reinterpret_cast<float*>(p->ws + p->wl.xbuf) + H};
+    const float* cur = d_x;
+    int32_t idx[kMaxK], slots[kMaxK], mlayer[kMaxK], mexpert[kMaxK], mj[kMaxK], ms[kMaxK];
+    void* mdst[kMaxK];
+    for (int li = 0; li < n_layers; ++li) {
+        const int l = layer0 + li;
+        float* out = li == n_layers - 1 ? d_x_out : bufs[li & 1];
+        if ((st = moe_route(p, l, cur, d_idx, d_w, cs)) != MOE_OK)
+            return st;
+        CUDA_TRY(cudaMemcpyAsync(idx, d_idx, sizeof(int32_t) * k, cudaMemcpyDeviceToHost, cs));
+        CUDA_TRY(cudaStreamSynchronize(cs));
+        for (int j = 0; j < k; ++j)
+            if (idx[j] < 0 || idx[j] >= E)
+                return fail(MOE_E_CUDA, "routing returned expert %d at layer %d (device status %s)", idx[j], l,
+                            "unknown: read it with moe_device_status");
+        if ((st = moe_pool_lookup(p, l, idx, k, slots)) != MOE_OK)
+            return st;
+        // the misses: staging slots (each free once its previous copy is done), parallel reads
+        int nm = 0;
+        for (int j = 0; j < k; ++j) {
+            if (slots[j] >= 0)
+                continue;
+            const int s = p->stage_next;
+            p->stage_next = (p->stage_next + 1) % n_staging;
+            if (p->stage_used[s])
+                CUDA_TRY(cudaEventSynchronize(p->stage_ev[s]));
+            mlayer[nm] = l;
+            mexpert[nm] = idx[j];
+            mdst[nm] = stage + (size_t)s * stride;
+            mj[nm] = j;
+            ms[nm] = s;
+            ++nm;
+        }
+        if (nm) {
+            const int e = moe::qp::read_many(q, nm, mlayer, mexpert, mdst);
+            if (e)
+                return fail(MOE_E_INVALID, "reading layer %d's experts from the container failed (%s)", l, strerror(e));
+        }
+        for (int i = 0; i < nm; ++i) {
+            if ((st = moe_pool_load_slot(p, l, mexpert[i], mdst[i], copy_stream, &slots[mj[i]])) != MOE_OK)
+                return st;
+            CUDA_TRY(cudaEventRecord(p->stage_ev[ms[i]], ys));
+            p->stage_used[ms[i]] = 1;
+        }
+        if ((st = moe_pool_wait_loads(p, compute_stream)) != MOE_OK)
+            return st;
         if ((st = moe_experts(p, l, cur, d_w, slots, out, compute_stream)) != MOE_OK)
             return st;
         if ((st = moe_pool_release(p, compute_stream)) != MOE_OK)

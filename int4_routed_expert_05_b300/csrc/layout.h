@@ -188,7 +188,6 @@ MOE_HD StageGeo stage_geo(int H, int Ie, int bits, int G, int ngroups, int ncs_g
     // pieces: the most (up to kMaxPieces) that divide the copy's column blocks evenly, fit the
     // mbarriers, and start on the swizzle period (1024 bytes) when the rows are swizzled
     s.npc_gu = 1;
-#pragma unroll 1
     for (int n = imin(kMaxPieces, s.cpg_gu); n > 1; --n)
         if (s.cpg_gu % n == 0 && 2 * s.nslot_gu * n <= kMaxGuBars &&
             (!s.swz_gu || ((s.cpg_gu / n) * s.bh_gu * s.cbw_gu) % 1024 == 0)) {

@@ -29,7 +29,10 @@ ENTRY_POINTS = [
     "moe_pool_set_prefetch",
     "moe_stack_forward_streamed", "moe_batched_workspace_bytes", "moe_layer_forward_batched",
     "moe_pool_time_batched", "moe_pool_batched_gemm_ms",
+    "moe_qpack_create", "moe_qpack_open", "moe_qpack_info", "moe_qpack_write", "moe_qpack_read",
+    "moe_qpack_close", "moe_stack_forward_qpack",
 ]
+QPACK_DIRECT = 1
 
 
 class MoeError(RuntimeError):
@@ -92,6 +95,13 @@ def load() -> ctypes.CDLL:
         "moe_pool_set_copy_hook": (ST, [P, COPY_HOOK, P]),
         "moe_layer_forward_static": (ST, [PS, P, ctypes.POINTER(LayerWeights), P, I32, P, P, P, P, P]),
         "moe_stack_forward_streamed": (ST, [P, I32, I32, P, P, P, P, P, P]),
+        "moe_qpack_create": (ST, [ctypes.c_char_p, PS, I32, ctypes.POINTER(P)]),
+        "moe_qpack_open": (ST, [ctypes.c_char_p, I32, I32, ctypes.POINTER(P)]),
+        "moe_qpack_info": (ST, [P, PS, ctypes.POINTER(I32), ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(I32)]),
+        "moe_qpack_write": (ST, [P, I32, I32, P]),
+        "moe_qpack_read": (ST, [P, I32, I32, P]),
+        "moe_qpack_close": (ST, [P]),
+        "moe_stack_forward_qpack": (ST, [P, I32, I32, P, P, P, P, I32, P, P, P]),
         "moe_batched_workspace_bytes": (SZ, [PS, I32]),
         "moe_layer_forward_batched": (ST, [P, I32, P, I32, P, P, P, P, SZ, P]),
         "moe_pool_time_batched": (ST, [P, I32]),
@@ -173,6 +183,43 @@ def pack_expert(shape: Shape, t: dict, shared: bool = False, out: np.ndarray | N
                                   ctypes.cast(arr[1], ctypes.c_void_p), ctypes.cast(arr[2], ctypes.c_void_p),
                                   out.ctypes.data))
     return out
+
+
+class Qpack:
+    """The on-disk expert container (moe_qpack_*): create() to write one, open() to read one."""
+
+    def __init__(self, handle, lib):
+        self.h, self.lib = handle, lib
+
+    @classmethod
+    def create(cls, path: str, shape: Shape, n_layers: int) -> "Qpack":
+        lib, h = load(), ctypes.c_void_p()
+        _check(lib.moe_qpack_create(path.encode(), ctypes.byref(shape), n_layers, ctypes.byref(h)))
+        return cls(h, lib)
+
+    @classmethod
+    def open(cls, path: str, direct: bool = True, n_threads: int = 8) -> "Qpack":
+        lib, h = load(), ctypes.c_void_p()
+        _check(lib.moe_qpack_open(path.encode(), QPACK_DIRECT if direct else 0, n_threads, ctypes.byref(h)))
+        return cls(h, lib)
+
+    def info(self) -> tuple[Shape, int, int, bool]:
+        sh, nl, st, d = Shape(), ctypes.c_int32(), ctypes.c_uint64(), ctypes.c_int32()
+        _check(self.lib.moe_qpack_info(self.h, ctypes.byref(sh), ctypes.byref(nl), ctypes.byref(st), ctypes.byref(d)))
+        return sh, nl.value, st.value, bool(d.value)
+
+    def write(self, layer: int, expert: int, blob: np.ndarray):
+        _check(self.lib.moe_qpack_write(self.h, layer, expert, np.ascontiguousarray(blob, dtype=np.uint8).ctypes.data))
+
+    def read(self, layer: int, expert: int, dst):
+        """dst: host buffer of stride bytes (4096-byte aligned for direct reads): numpy array or
+        pointer."""
+        _check(self.lib.moe_qpack_read(self.h, layer, expert, dst.ctypes.data if hasattr(dst, "ctypes") else _p(dst)))
+
+    def close(self):
+        if self.h:
+            _check(self.lib.moe_qpack_close(self.h))
+            self.h = None
 
 
 class Pool:
@@ -266,6 +313,14 @@ class Pool:
     def stack_forward(self, layer0, n_layers, x, x_out, trace=None, topk_idx=None, topk_w=None, stream=None):
         _check(self.lib.moe_stack_forward(self.h, layer0, n_layers, _p(x), _p(x_out), _p(trace), _p(topk_idx),
                                           _p(topk_w), _s(stream)))
+
+    def stack_forward_qpack(self, layer0, n_layers, x, x_out, qpack: "Qpack", staging, n_staging: int,
+                            compute_stream=None, copy_stream=None, topk_idx: np.ndarray | None = None):
+        """Bounded-mode stack with the misses read from an on-disk container through `staging`
+        (pinned host buffer of n_staging blobs)."""
+        _check(self.lib.moe_stack_forward_qpack(self.h, layer0, n_layers, _p(x), _p(x_out), qpack.h, _p(staging),
+                                                n_staging, _s(compute_stream), _s(copy_stream),
+                                                None if topk_idx is None else topk_idx.ctypes.data))
 
     def stack_forward_streamed(self, layer0, n_layers, x, x_out, h_blobs: np.ndarray, compute_stream=None,
                                copy_stream=None, topk_idx: np.ndarray | None = None):

@@ -166,6 +166,23 @@ class Streamed:
     def bias_host(self, layer: int):
         return None if not self.beta else zipf_bias(self.sh, self.seed, layer, self.beta)
 
+    def write_qpack(self, path: str) -> None:
+        """Write every (layer, expert) blob of this stack into an on-disk container at `path`."""
+        q = moe.Qpack.create(path, self.mshape, self.L)
+        try:
+            for l in range(self.L):
+                for e in range(self.sh.n_experts):
+                    q.write(l, e, self.store[int(self.maps[l][e])].numpy())
+        finally:
+            q.close()
+
+    def step_qpack(self, x: torch.Tensor, out: torch.Tensor, qpack, staging: torch.Tensor, n_staging: int,
+                   stream=None, topk_idx: np.ndarray | None = None):
+        """One token through all layers, the misses read from the container `qpack` through the
+        pinned buffer `staging` (n_staging blobs)."""
+        s = torch.cuda.current_stream() if stream is None else stream
+        self.pool.stack_forward_qpack(0, self.L, x, out, qpack, staging, n_staging, s, self.copy_stream, topk_idx)
+
     def layer_step(self, layer: int, x: torch.Tensor, out: torch.Tensor, stream=None,
                    topk_idx: np.ndarray | None = None):
         """Layer ``layer`` alone through the bounded pool (the pool's state carries over between

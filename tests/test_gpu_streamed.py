@@ -76,3 +76,37 @@ def test_streamed_layers_against_oracle(orc):
             x.copy_(y)
     hits, misses, _ = S.pool.stats()
     assert hits > 0 and misses > 0, (hits, misses)
+
+
+@pytest.mark.parametrize("sh,n_slots,L", [(synth.TINY, 5, 4), (synth.S80, 24, 3)])
+def test_qpack_stack_equals_resident(tmp_path, sh, n_slots, L):
+    """Bounded pool fed from the on-disk expert container (parallel positioned reads into a pinned
+    staging ring, then copies to the pool): the output equals the resident stack's bit for bit,
+    and every miss moved exactly one blob."""
+    seed, beta, n_unique = 3, 0.7, 64
+    flags = moe.RENORM | moe.PRENORM | moe.RESIDUAL
+    bias = [zipf_bias(sh, seed, l, beta) for l in range(L)]
+    R = Resident(sh, L, seed, n_unique=min(n_unique, sh.n_experts), flags=flags, bias=bias)
+    S = Streamed(sh, L, seed, n_slots, n_unique=min(n_unique, sh.n_experts), beta=beta)
+    path = str(tmp_path / "experts.qpack")
+    S.write_qpack(path)
+    q = moe.Qpack.open(path, direct=True, n_threads=4)
+    n_staging = 2 * sh.top_k
+    staging = torch.empty(n_staging * S.stride, dtype=torch.uint8, pin_memory=True)
+    out_s = torch.empty(sh.hidden, dtype=torch.float32, device="cuda")
+    try:
+        for step in range(3):
+            x0 = torch.from_numpy(synth.activation_f32(sh, seed, step)[0]).cuda()
+            out_r, _, idx_r, _ = R.stack_forward(x0)
+            sel = np.zeros((L, sh.top_k), dtype=np.int32)
+            S.step_qpack(x0, out_s, q, staging, n_staging, topk_idx=sel)
+            torch.cuda.synchronize()
+            assert R.pool.device_status() == moe.OK and S.pool.device_status() == moe.OK
+            assert np.array_equal(sel, idx_r.cpu().numpy()), step
+            assert torch.equal(out_r, out_s), step
+        hits, misses, nbytes = S.pool.stats()
+        assert misses > 0 and nbytes == misses * S.stride
+        with pytest.raises(moe.MoeError):  # too few staging slots for a layer's misses
+            S.step_qpack(x0, out_s, q, staging, sh.top_k - 1)
+    finally:
+        q.close()
