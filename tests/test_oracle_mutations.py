@@ -100,3 +100,46 @@ def test_margin_pin_catches_planted_mistake(name):
     exec(compile(src.replace(old, new), "margin_mutant.py", "exec"), ns)
     with pytest.raises(AssertionError):
         check_margin(ns["selection_margin"])
+
+
+# Planted mistakes in the hybrid-step oracle (Gated DeltaNet step, gated GQA decode attention);
+# tests/test_hybrid_oracle_pins.py must reject each.
+HYBRID_SRC = os.path.join(ROOT, "oracle", "hybrid_oracle.c")
+HYBRID_MUTANTS = {
+    "gdn_alpha_dropped": ("M[(size_t)i * dk + j] = alpha[h] * (", "M[(size_t)i * dk + j] = 1.0 * ("),
+    "gdn_beta_sign": ("beta[h] = sigmoid(b[h]);", "beta[h] = sigmoid(-b[h]);"),
+    "gdn_decay_sign": ("alpha[h] = exp(-exp(A_log[h])", "alpha[h] = exp(exp(A_log[h])"),
+    "gdn_dt_bias_dropped": ("softplus(a[h] + dt_bias[h])", "softplus(a[h])"),
+    "gdn_outer_transposed": ("acc + beta[h] * vh[r] * kn[c];", "acc + beta[h] * vh[c % dv] * kn[r % dk];"),
+    "gdn_key_not_normalised": ("l2_normalise(k + (size_t)g * dk, dk, eps_l2, 1.0, kn);",
+                               "memcpy(kn, k + (size_t)g * dk, sizeof(double) * dk);"),
+    "gdn_head_map_modulo": ("const int g = h / rep;\n        l2_normalise", "const int g = h % Hk;\n        l2_normalise"),
+    "gdn_readout_with_key": ("acc += Sh[(size_t)r * dk + c] * qn[c];", "acc += Sh[(size_t)r * dk + c] * kn[c];"),
+    "gdn_scale_dropped": ("dk, eps_l2, scale, qn);", "dk, eps_l2, 1.0, qn);"),
+    "gdn_norm_sum_not_mean": ("sqrt(ss / dv + eps)", "sqrt(ss + eps)"),
+    "gdn_gate_sigmoid_not_silu": ("(zz * sigmoid(zz))", "sigmoid(zz)"),
+    "gdn_norm_weight_dropped": ("rinv * norm_w[r] *", "rinv *"),
+    "gqa_new_token_excluded": ("const int n = pos + 1;", "const int n = pos;"),
+    "gqa_scale_dropped": ("s[t] = scale * acc;", "s[t] = acc;"),
+    "gqa_head_map_modulo": ("const int g = h / rep;\n        const double* qh", "const int g = h % Hkv;\n        const double* qh"),
+    "gqa_gate_sign": ("acc * sigmoid(gate[", "acc * sigmoid(-gate["),
+    "gqa_max_not_subtracted": ("s[t] = exp(s[t] - m);", "s[t] = exp(s[t]);"),
+    "gqa_value_not_appended": ("memcpy(Vc + ((size_t)g * Lmax + pos) * D, v + (size_t)g * D, sizeof(double) * D);", ""),
+    "gqa_softmax_unnormalised": ("acc += s[t] / Z * Vc", "acc += s[t] * Vc"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(HYBRID_MUTANTS))
+def test_hybrid_pins_catch_planted_mistake(name, tmp_path):
+    import oracle
+    old, new = HYBRID_MUTANTS[name]
+    text = open(HYBRID_SRC).read()
+    assert text.count(old) == 1, name
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(old, new))
+    lib = oracle.compile_c(str(src), str(tmp_path / "libmutant.so"))
+    env = dict(os.environ, MOE_HYBRID_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_hybrid_oracle_pins.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
