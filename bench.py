@@ -39,6 +39,12 @@ for _t in (8, 64, 512, 4096):
     CONFIGS[f"prefill80_t{_t}"] = ("S80", 1, 4, f"80B-shaped single MoE layer, batched decode/prefill of {_t} tokens, "
                                    "int4, router top-10, tokens sorted per expert, grouped GEMMs on the tensor cores")
 BATCHED = {f"prefill80_t{_t}": _t for _t in (8, 64, 512, 4096)}
+# the hybrid stack's other per-layer steps: (step kind, layers, context)
+CONFIGS["gdn80"] = ("GDN80", 36, 32, "80B-shaped Gated DeltaNet decode step through the 36 DeltaNet layers "
+                    "(16 key / 32 value heads, 128 x 128 fp32 state per value head: 72 MiB in all)")
+CONFIGS["gqa80_8k"] = ("GQA80", 12, 32, "80B-shaped gated GQA decode attention through the 12 attention layers "
+                       "at an 8K context (16 query / 2 K/V heads of 256, fp32 K/V cache: 384 MiB in all)")
+HYBRID = {"gdn80": ("gdn", 36, 0), "gqa80_8k": ("gqa", 12, 8192)}
 BATCHED_LAYERS = 8  # resident layers rotated step by step, so consecutive steps read disjoint weights
 POOL_SLOTS = {"stack80_pool2g": (2 << 30) // 1769472}  # 1213 slots of 1,769,472 bytes
 METRIC = "MoE decode tokens/s (1 B300) and expert-byte HBM GB/s vs ~8 TB/s roofline"
@@ -192,6 +198,24 @@ def run_reference(args):
     sampled time."""
     ws, rank, _ = _dist()
     if rank != 0:
+        return
+    if args.config in HYBRID:
+        kind, L, ctx = HYBRID[args.config]
+        times, vals = [], []
+        for i in range(args.warmup + args.steps):
+            v, info = cpu_oracle_hybrid(kind, L, ctx, budget_s=min(2.0, args.ref_budget))
+            if i >= args.warmup:
+                vals.append(v)
+        value = statistics.median(vals)
+        line = {"impl": "reference", "metric": f"{'Gated DeltaNet' if kind == 'gdn' else 'gated GQA'} decode "
+                f"tokens/s through {L} layers (1 B300) and HBM GB/s vs the measured copy roofline",
+                "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 / value, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic (seeded generator)",
+                "config": {"workload": args.config, "description": CONFIGS[args.config][3], "batch": 1, "layers": L},
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": info},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
         return
     import oracle
     from int4_routed_expert_05_b300 import synth
@@ -686,6 +710,245 @@ def run_batched(args):
     print(json.dumps(line), flush=True)
 
 
+def _hybrid_setup(kind, L, batch, ctx, n_steps):
+    """Device state of a hybrid-step workload: per-layer parameters and state (or caches) and
+    per-step inputs, all from the seeded generator."""
+    import torch
+    from int4_routed_expert_05_b300 import moe
+    from int4_routed_expert_05_b300 import synth_hybrid as SH
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    W = {"kind": kind, "L": L, "batch": batch}
+    n_in = min(n_steps, 8)  # distinct input sets, cycled
+    if kind == "gdn":
+        sh = SH.GDN80
+        W["shape"] = moe.GdnShape(sh.n_key_heads, sh.n_value_heads, sh.key_dim, sh.value_dim)
+        W["state"] = [dev(SH.gdn_state(sh, SEED, l, batch)) for l in range(L)]
+        W["par"] = [{k: dev(v) for k, v in SH.gdn_params(sh, SEED, l).items()} for l in range(L)]
+        W["inp"] = [[{k: dev(v) for k, v in SH.gdn_inputs(sh, SEED, l, s, batch).items()} for l in range(L)]
+                    for s in range(n_in)]
+        W["y"] = torch.empty(batch, sh.n_value_heads, sh.value_dim, device="cuda")
+        # algorithmic bytes of one layer launch: state read + written, inputs, parameters, y
+        W["bytes_per_launch"] = batch * (2 * 4 * sh.state_floats() + 2 * 2 * sh.n_key_heads * sh.key_dim +
+                                         2 * 2 * sh.n_value_heads * sh.value_dim + 2 * 4 * sh.n_value_heads +
+                                         4 * sh.n_value_heads * sh.value_dim) + 4 * (2 * sh.n_value_heads + sh.value_dim)
+        W["h2d_per_layer"] = sum(v.numel() * v.element_size() for v in W["inp"][0][0].values())
+    else:
+        sh = SH.GQA80
+        W["shape"] = moe.GqaShape(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, ctx)
+        start = ctx - n_steps
+        W["kc"] = [dev(SH.gqa_cache(sh, SEED, l, ctx, start, batch)) for l in range(L)]
+        W["vc"] = [dev(SH.gqa_cache(sh, SEED + 1, l, ctx, start, batch)) for l in range(L)]
+        W["pos"] = torch.full((batch,), start, dtype=torch.int32, device="cuda")
+        W["start"] = start
+        W["inp"] = [[{k: dev(v) for k, v in SH.gqa_inputs(sh, SEED, l, s, batch).items()} for l in range(L)]
+                    for s in range(n_in)]
+        W["y"] = torch.empty(batch, sh.n_q_heads, sh.head_dim, device="cuda")
+        W["wb"] = moe.gqa_workspace_bytes(W["shape"], batch, ctx)
+        W["work"] = torch.empty(W["wb"] // 4 + 4, dtype=torch.float32, device="cuda")
+        W["status"] = torch.zeros(4, dtype=torch.int32, device="cuda")
+        # algorithmic bytes of one layer at position p: K and V rows 0..p read (the new row
+        # written), inputs, y
+        W["kv_row_bytes"] = 2 * 4 * sh.n_kv_heads * sh.head_dim * batch
+        W["io_bytes"] = batch * (2 * 2 * sh.n_q_heads * sh.head_dim + 2 * 2 * sh.n_kv_heads * sh.head_dim +
+                                 4 * sh.n_q_heads * sh.head_dim)
+        W["h2d_per_layer"] = sum(v.numel() * v.element_size() for v in W["inp"][0][0].values())
+    W["sh"] = sh
+    return W
+
+
+def _hybrid_step(W, s, stream_ptr):
+    """One decode token through the workload's L layers (one launch, or two for GQA, per layer)."""
+    from int4_routed_expert_05_b300 import moe
+    inp = W["inp"][s % len(W["inp"])]
+    for l in range(W["L"]):
+        d = inp[l]
+        if W["kind"] == "gdn":
+            p = W["par"][l]
+            moe.gdn_step(W["shape"], W["batch"], W["state"][l], d["q"], d["k"], d["v"], d["z"], d["a"], d["b"],
+                         p["A_log"], p["dt_bias"], p["norm_w"], W["sh"].key_dim ** -0.5, W["y"], stream=stream_ptr)
+        else:
+            moe.gqa_decode(W["shape"], W["batch"], W["shape"].max_len, W["kc"][l], W["vc"][l], W["pos"], d["q"],
+                           d["k"], d["v"], d["gate"], W["sh"].head_dim ** -0.5, W["work"], W["wb"], W["y"],
+                           W["status"], stream=stream_ptr)
+
+
+def cpu_oracle_hybrid(kind, L, ctx, budget_s=15.0):
+    """The hybrid-step oracle as it stands, on host data from the seeded generator: layer steps of
+    one sequence (cycling over the first layers' data) for as long as the budget allows (at least
+    one). Returns (tokens/s for L layers, description of the sample)."""
+    from oracle import hybrid as OH
+    from int4_routed_expert_05_b300 import synth_hybrid as SH
+    from int4_routed_expert_05_b300.synth import bf16_value
+    f = lambda a: bf16_value(a[0]).astype(np.float64)
+    n, t_total = 0, 0.0
+    while n == 0 or t_total < budget_s:
+        l = n % 2
+        if kind == "gdn":
+            sh = SH.GDN80
+            S = SH.gdn_state(sh, SEED, l, 1)[0].astype(np.float64)
+            p = SH.gdn_params(sh, SEED, l)
+            d = SH.gdn_inputs(sh, SEED, l, 0, 1)
+            t0 = time.perf_counter()
+            OH.gdn_step(S, f(d["q"]), f(d["k"]), f(d["v"]), f(d["z"]), d["a"][0], d["b"][0], p["A_log"], p["dt_bias"],
+                        p["norm_w"], sh.key_dim ** -0.5)
+        else:
+            sh = SH.GQA80
+            if n < 2:
+                caches = (SH.gqa_cache(sh, SEED, l, ctx, ctx - 1, 1)[0].astype(np.float64),
+                          SH.gqa_cache(sh, SEED + 1, l, ctx, ctx - 1, 1)[0].astype(np.float64))
+                cache_l = {l: caches}
+            Kc, Vc = cache_l.get(l, caches)
+            d = SH.gqa_inputs(sh, SEED, l, 0, 1)
+            t0 = time.perf_counter()
+            OH.gqa_step(Kc, Vc, ctx - 1, f(d["q"]), f(d["k"]), f(d["v"]), f(d["gate"]), sh.head_dim ** -0.5)
+        t_total += time.perf_counter() - t0
+        n += 1
+    what = "state update" if kind == "gdn" else f"attention step at position {ctx - 1}"
+    return (n / L) / t_total, (f"{n} single-sequence layer {what}(s) through the oracle in {t_total:.1f} s on one "
+                               f"thread, time scaled to {L} layers")
+
+
+def run_hybrid(args):
+    """A decode token through the hybrid stack's DeltaNet (gdn80) or attention (gqa80_8k) layers.
+    Each step is one CUDA-graph replay of the L layer launches; a 256 MiB buffer is written
+    between timed steps (outside the timed events) so no step finds the previous one's state or
+    cache in L2."""
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from int4_routed_expert_05_b300 import _build
+    _build.build()
+    kind, L, ctx = HYBRID[args.config]
+    _, _, _, desc = CONFIGS[args.config]
+    batch = args.batch
+    n_e2e = max(1, min(args.steps, 200))
+    n_total = args.warmup + args.steps + 1 + n_e2e  # attention: one cache position per step
+    if kind == "gqa" and n_total >= ctx:
+        raise SystemExit(f"warmup + steps must stay below the {ctx}-position context")
+    W = _hybrid_setup(kind, L, batch, ctx, n_total)
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB > 126 MB L2
+
+    # one graph per distinct input set (the graph holds the pointers of its inputs)
+    graphs = []
+    with torch.cuda.stream(stream):
+        _hybrid_step(W, 0, sp)  # first launch outside capture (sets kernel attributes)
+        if kind == "gqa":
+            W["pos"] += 1
+    torch.cuda.synchronize()
+    for s in range(len(W["inp"])):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            _hybrid_step(W, s, torch.cuda.current_stream().cuda_stream)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def replay(i):
+        graphs[i % len(graphs)].replay()
+        if kind == "gqa":
+            W["pos"] += 1  # on the same stream, after the step
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            replay(i)
+    torch.cuda.synchronize()
+    if kind == "gqa" and int(W["status"][0].item()) != 0:
+        raise RuntimeError(f"device status {int(W['status'][0].item())} after warm-up")
+
+    clocks = ClockSampler(local)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    pos_sum = 0
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            replay(args.warmup + i)
+            ev[i][1].record(stream)
+            pos_sum += (W["start"] + 1 + args.warmup + i) if kind == "gqa" else 0
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    ms = _max_over_ranks(ws, ms)
+    if kind == "gqa" and int(W["status"][0].item()) != 0:
+        raise RuntimeError(f"device status {int(W['status'][0].item())} after the timed region")
+
+    # end to end: every step's inputs from pinned host memory, the last layer's y back
+    h_in = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in d.items()} for d in W["inp"][0]]
+    for hl, dl in zip(h_in, W["inp"][0]):
+        for k in hl:
+            hl[k].copy_(dl[k])
+    h_y = torch.empty_like(W["y"], device="cpu").pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            for hl, dl in zip(h_in, W["inp"][0]):
+                for k in hl:
+                    dl[k].copy_(hl[k], non_blocking=True)
+            replay(0)
+            h_y.copy_(W["y"], non_blocking=True)
+            stream.synchronize()
+    e2e_s = _max_over_ranks(ws, time.perf_counter() - t0)
+
+    if rank != 0:
+        return
+    ms_step = ms / args.steps
+    launches_per_step = L * (1 if kind == "gdn" else 2)
+    if kind == "gdn":
+        bytes_step = W["bytes_per_launch"] * L
+        dom, per_launch = "gdn_step_kernel", W["bytes_per_launch"]
+    else:
+        # mean position over the timed steps: rows 0..p read per layer
+        mean_rows = pos_sum / args.steps
+        per_launch = W["kv_row_bytes"] * mean_rows + W["io_bytes"]
+        bytes_step = per_launch * L
+        dom = "gqa_split_kernel"
+    peak, peak_kind = _peaks()
+    achieved = bytes_step / (ms_step / 1e3) / 1e9
+    ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    cpu_v, cpu_info = (None, None)
+    if ws == 1 and not args.no_cpu_baseline:
+        cpu_v, cpu_info = cpu_oracle_hybrid(kind, L, ctx, budget_s=args.ref_budget)
+    line = {
+        "metric": f"{'Gated DeltaNet' if kind == 'gdn' else 'gated GQA'} decode tokens/s through {L} layers "
+                  "(1 B300) and HBM GB/s vs the measured copy roofline",
+        "value": ws * batch * args.steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (bf16 inputs)",
+        "data": "synthetic (seeded generator, random-init parameters of the stated shapes)",
+        "config": {"workload": args.config, "description": desc, "batch": batch, "layers": L,
+                   "context": ctx if kind == "gqa" else None,
+                   "l2": "256 MiB written between timed steps, outside the timed events",
+                   "graphs": "each step is one CUDA-graph replay of the layers' launches",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "layer_latency_us": ms_step * 1e3 / L,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_kind": peak_kind, "kernel": dom, "bytes_per_launch": per_launch,
+                     "note": "launch duration = step time / layers (graph replay, gaps included)"},
+        "cpu_baseline": None if cpu_v is None else {"value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                                    "sample": cpu_info},
+        "e2e": {"value": ws * batch * n_e2e / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": W["h2d_per_layer"] * L, "d2h_bytes_per_step": W["y"].numel() * 4,
+                "steps": n_e2e},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def cpu_oracle_batched(sh, T, seed=SEED, budget_s=15.0):
     """The oracle, single-threaded, on a sample of the batch: whole layers token by token until the
     budget is spent (at most T tokens); tokens/s of one layer."""
@@ -725,6 +988,7 @@ def main():
                          "(instead of the pinned host store)")
     ap.add_argument("--prefetch", type=int, default=6,
                     help="bounded pool: copy ahead the next layer's N best predicted experts (0: off; default 6, the best of a 2 GiB sweep)")
+    ap.add_argument("--batch", type=int, default=1, help="hybrid workloads: independent sequences per step")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the stack (small cases for profiling)")
     args = ap.parse_args()
@@ -734,6 +998,8 @@ def main():
         run_streamed(args)
     elif args.config in BATCHED:
         run_batched(args)
+    elif args.config in HYBRID:
+        run_hybrid(args)
     else:
         run_ours(args)
 

@@ -8,7 +8,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ["api.cu", "decode.cu", "scalar.cu", "noalloc.cu", "batched.cu", "grouped.cu", "qpack.cpp"]
+SOURCES = ["api.cu", "decode.cu", "scalar.cu", "noalloc.cu", "batched.cu", "grouped.cu", "hybrid.cu", "qpack.cpp"]
 HEADERS = ["layout.h", "policy.h", "host.h", "grouped.h", "qpack.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -23,7 +23,8 @@ def stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(ROOT, "include", "moe.h")]
+    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [
+        os.path.join(ROOT, "include", h) for h in ("moe.h", "hybrid.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 

@@ -32,6 +32,8 @@ ENTRY_POINTS = [
     "moe_qpack_create", "moe_qpack_open", "moe_qpack_info", "moe_qpack_write", "moe_qpack_read",
     "moe_qpack_close", "moe_stack_forward_qpack",
 ]
+# include/hybrid.h
+HYBRID_ENTRY_POINTS = ["moe_gdn_step", "moe_gqa_workspace_bytes", "moe_gqa_decode"]
 QPACK_DIRECT = 1
 
 
@@ -49,6 +51,14 @@ class Shape(ctypes.Structure):
 class LayerWeights(ctypes.Structure):
     _fields_ = [("router", ctypes.c_void_p), ("shared_blob", ctypes.c_void_p),
                 ("shared_gate", ctypes.c_void_p), ("logit_bias", ctypes.c_void_p)]
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n_key_heads", "n_value_heads", "key_dim", "value_dim")]
+
+
+class GqaShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n_q_heads", "n_kv_heads", "head_dim", "max_len")]
 
 
 COPY_HOOK = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t)
@@ -106,6 +116,9 @@ def load() -> ctypes.CDLL:
         "moe_layer_forward_batched": (ST, [P, I32, P, I32, P, P, P, P, SZ, P]),
         "moe_pool_time_batched": (ST, [P, I32]),
         "moe_pool_batched_gemm_ms": (ST, [P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I32)]),
+        "moe_gdn_step": (ST, [ctypes.POINTER(GdnShape), I32] + [P] * 10 + [ctypes.c_float, P, P, P]),
+        "moe_gqa_workspace_bytes": (SZ, [ctypes.POINTER(GqaShape), I32, I32]),
+        "moe_gqa_decode": (ST, [ctypes.POINTER(GqaShape), I32, I32] + [P] * 7 + [ctypes.c_float, P, SZ, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -149,6 +162,27 @@ def layer_forward_static(shape: Shape, experts, router, shared_blob, shared_gate
     w = LayerWeights(_p(router), _p(shared_blob), _p(shared_gate), _p(logit_bias))
     _check(load().moe_layer_forward_static(ctypes.byref(shape), _p(experts), ctypes.byref(w), _p(x), n_tokens, _p(y),
                                            _p(topk_idx), _p(topk_w), _p(status), _s(stream)))
+
+
+def gdn_step(shape: GdnShape, batch: int, state, q, k, v, z, a, b, A_log, dt_bias, norm_w, scale: float, y,
+             o=None, stream=None):
+    """moe_gdn_step: one Gated DeltaNet decode step of ``batch`` sequences; the state is updated in
+    place (layouts in include/hybrid.h)."""
+    _check(load().moe_gdn_step(ctypes.byref(shape), batch, _p(state), _p(q), _p(k), _p(v), _p(z), _p(a), _p(b),
+                               _p(A_log), _p(dt_bias), _p(norm_w), float(scale), _p(o), _p(y), _s(stream)))
+
+
+def gqa_workspace_bytes(shape: GqaShape, batch: int, max_pos: int) -> int:
+    return int(load().moe_gqa_workspace_bytes(ctypes.byref(shape), batch, max_pos))
+
+
+def gqa_decode(shape: GqaShape, batch: int, max_pos: int, k_cache, v_cache, pos, q, k, v, gate, scale: float,
+               work, work_bytes: int, y, status, o=None, stream=None):
+    """moe_gqa_decode: one gated GQA decode step of ``batch`` sequences; row pos[b] of each cache is
+    written in place, pos itself is left for the caller to advance."""
+    _check(load().moe_gqa_decode(ctypes.byref(shape), batch, max_pos, _p(k_cache), _p(v_cache), _p(pos), _p(q),
+                                 _p(k), _p(v), _p(gate), float(scale), _p(work), work_bytes, _p(o), _p(y),
+                                 _p(status), _s(stream)))
 
 
 def batched_workspace_bytes(shape: Shape, n_tokens: int) -> int:

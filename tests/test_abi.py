@@ -20,18 +20,47 @@ def lib():
     return moe.load()
 
 
-def _declared_functions():
-    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+def _declared_functions(header):
+    text = open(os.path.join(ROOT, "include", header)).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
-    names = _declared_functions()
+    names = _declared_functions("moe.h")
     assert len(names) >= 20
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(moe.ENTRY_POINTS)
+
+
+def test_exports_every_hybrid_symbol(lib):
+    headers = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    assert headers == ["hybrid.h", "moe.h"]
+    names = _declared_functions("hybrid.h")
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moe.HYBRID_ENTRY_POINTS)
+
+
+def test_hybrid_host_checks_without_a_gpu(lib):
+    # shape and argument checks run on the host before any CUDA call
+    bad = moe.GdnShape(16, 32, 64, 128)
+    with pytest.raises(moe.MoeError) as e:
+        moe.gdn_step(bad, 1, *([16] * 10), 1.0, 16)
+    assert e.value.status == moe.E_SHAPE
+    good = moe.GdnShape(16, 32, 128, 128)
+    with pytest.raises(moe.MoeError) as e:
+        moe.gdn_step(good, 1, *([16] * 9), 8, 1.0, 16)   # misaligned norm weight pointer
+    assert e.value.status == moe.E_INVALID
+    sh = moe.GqaShape(16, 2, 256, 8192)
+    assert moe.gqa_workspace_bytes(sh, 1, 8192) == 2 * 74 * 8 * (256 + 2) * 4
+    assert moe.gqa_workspace_bytes(sh, 1, 8193) == 0
+    assert moe.gqa_workspace_bytes(moe.GqaShape(16, 2, 96, 64), 1, 8) == 0
+    assert moe.gqa_workspace_bytes(moe.GqaShape(12, 2, 256, 64), 1, 8) == 0   # 6 query heads per K/V head
+    with pytest.raises(moe.MoeError) as e:
+        moe.gqa_decode(sh, 1, 8192, *([16] * 7), 1.0, 16, 100, 16, 16)
+    assert e.value.status == moe.E_NOMEM
 
 
 @pytest.mark.parametrize("sh", [synth.TINY, synth.TINY.with_bits(8), synth.S80, synth.S35.with_bits(8)])
