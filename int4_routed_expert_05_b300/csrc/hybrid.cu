@@ -12,13 +12,13 @@
 // update needs only the row, k^ and q^ (the gated delta rule is rank one along k):
 //     d = S_r . k^,  S_r <- alpha S_r + beta (v_r - alpha d) k^,  o_r = S_r . q^,
 // so each state element is loaded once, updated in registers and stored once. The head's RMS norm
-// needs the sum of o_r^2 over all dv rows: each CTA publishes its partial sum in shared memory and
-// every CTA of the cluster reads the eight partials through distributed shared memory (in rank
-// order, so all compute the same total), between two cluster barriers.
+// needs the sum of o_r^2 over all dv rows: each CTA writes its partial sum into slot `rank` of every
+// CTA's shared memory (distributed shared memory), one cluster barrier later every CTA adds its
+// eight slots in rank order (so all compute the same total).
 //
 // Gated GQA decode. Split-K ("flash decoding"): the positions of each (sequence, K/V head) are
 // cut into n_split ranges, about one CTA per SM in all. A CTA streams its range in chunks of 32
-// positions through a two-stage shared-memory ring filled by 1D bulk copies (K rows and V rows of a
+// positions through a three-stage shared-memory ring filled by 1D bulk copies (K rows and V rows of a
 // chunk are contiguous in the cache), computes the G heads' scores, keeps a running softmax
 // (maximum, sum) per head and accumulates the weighted V rows; it leaves (m, l, o) per head in the
 // workspace. A second kernel merges the ranges of each query head in range order and applies the
@@ -79,9 +79,52 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// Sums G per-lane values (one per head) over the warp's 32 lanes with one butterfly: at each of the
+// first log2(G) levels a lane keeps the half of its values its partner does not and adds the
+// partner's copy of it (G/2, G/4, ... shuffles), then the last levels sum the single remaining
+// value. Lane l ends with the full sum for head head_of<G>(l); 2^(5 - log2 G) lanes hold each head.
+// G + log2(32 / G) - 1 shuffles instead of 5 G.
+template <int G>
+__device__ __forceinline__ float reduce_scatter(float (&v)[G], int lane)
+{
+    int off = 16;
+#pragma unroll
+    for (int w = G / 2; w >= 1; w /= 2, off /= 2) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float send = upper ? v[i] : v[i + w];
+            const float keep = upper ? v[i + w] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    float r = v[0];
+    for (; off >= 1; off /= 2)
+        r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
+}
+
+template <int G>
+__device__ __forceinline__ int head_of(int lane)
+{
+    int h = 0, off = 16;
+#pragma unroll
+    for (int w = G / 2; w >= 1; w /= 2, off /= 2)
+        if (lane & off)
+            h += w;
+    return h;
+}
+
 __device__ __forceinline__ float dot4(float4 a, float4 b) { return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w; }
 
 __device__ __forceinline__ float sigmoidf(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// Programmatic dependent launch: the kernels are launched so that they may start while the
+// previous kernel in the stream finishes; each waits for that kernel's completion (and the
+// visibility of its writes) before its first global-memory access, and lets the next kernel start
+// once its own work is under way. Without the launch attribute both are no-ops.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------------------------------------------
 // Gated DeltaNet decode step
@@ -105,7 +148,7 @@ __global__ void __cluster_dims__(kGdnCluster, 1, 1) __launch_bounds__(kGdnThread
     gdn_step_kernel(const GdnArgs A)
 {
     __shared__ float warp_ss[kGdnThreads / 32];
-    __shared__ float cta_ss;
+    __shared__ float cta_ss[kGdnCluster];  // slot j: the partial sum of the cluster's CTA j
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int head = blockIdx.x / kGdnCluster;  // sequence * Hv + value head
@@ -114,6 +157,10 @@ __global__ void __cluster_dims__(kGdnCluster, 1, 1) __launch_bounds__(kGdnThread
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int dv = A.dv;
     const int row0 = rank * (4 * RPW) + warp * RPW;
+    // first half of a cluster barrier: no CTA writes into a peer's shared memory before every CTA
+    // of the cluster is running; the wait half comes after the loads, so it costs nothing
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    grid_dep_wait();
 
     // the state rows go out first: they are the step's bytes
     float* Sh = A.state + (size_t)head * dv * kGdnDk;
@@ -129,15 +176,19 @@ __global__ void __cluster_dims__(kGdnCluster, 1, 1) __launch_bounds__(kGdnThread
     }
     const size_t kq = ((size_t)seq * A.Hk + g) * kGdnDk + 4 * lane;
     float4 kk = bf4(A.k + kq), qq = bf4(A.q + kq);
+    // the per-head scalars and the norm weight of this lane's output row: all loads in one round trip
+    const float a_in = A.a[head], b_in = A.b[head], A_log = A.A_log[h], dt_bias = A.dt_bias[h];
+    const float nw = lane < RPW ? A.norm_w[row0 + lane] : 0.0f;
     const float kinv = 1.0f / sqrtf(warp_sum(dot4(kk, kk)) + MOE_GDN_L2_EPS);
     const float qmul = A.scale / sqrtf(warp_sum(dot4(qq, qq)) + MOE_GDN_L2_EPS);
     kk = make_float4(kk.x * kinv, kk.y * kinv, kk.z * kinv, kk.w * kinv);
     qq = make_float4(qq.x * qmul, qq.y * qmul, qq.z * qmul, qq.w * qmul);
 
-    const float x = A.a[head] + A.dt_bias[h];
+    grid_dep_launch();
+    const float x = a_in + dt_bias;
     const float sp = x > 0.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
-    const float alpha = expf(-expf(A.A_log[h]) * sp);
-    const float beta = sigmoidf(A.b[head]);
+    const float alpha = expf(-expf(A_log) * sp);
+    const float beta = sigmoidf(b_in);
 
     float o[RPW];
     float ss = 0.0f;
@@ -154,13 +205,15 @@ __global__ void __cluster_dims__(kGdnCluster, 1, 1) __launch_bounds__(kGdnThread
     if (lane == 0)
         warp_ss[warp] = ss;
     __syncthreads();
-    if (threadIdx.x == 0)
-        cta_ss = (warp_ss[0] + warp_ss[1]) + (warp_ss[2] + warp_ss[3]);
-    cluster.sync();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (threadIdx.x < kGdnCluster)  // this CTA's partial into slot `rank` of every CTA of the cluster
+        *cluster.map_shared_rank(&cta_ss[rank], threadIdx.x) = (warp_ss[0] + warp_ss[1]) + (warp_ss[2] + warp_ss[3]);
+    cluster.sync();  // release/acquire: every slot written before any is read (and no CTA exits
+                     // while a peer may still write into it)
     float tot = 0.0f;
 #pragma unroll
     for (int j = 0; j < kGdnCluster; ++j)
-        tot += *cluster.map_shared_rank(&cta_ss, j);
+        tot += cta_ss[j];
     const float rinv = 1.0f / sqrtf(tot / (float)dv + MOE_GDN_NORM_EPS);
     if (lane < RPW) {
         // lane i writes row i of the warp (o[] indexed by a lane-dependent value: pick by unrolled select)
@@ -174,9 +227,8 @@ __global__ void __cluster_dims__(kGdnCluster, 1, 1) __launch_bounds__(kGdnThread
         const int r = row0 + lane;
         if (A.o)
             A.o[(size_t)head * dv + r] = oi;
-        A.y[(size_t)head * dv + r] = oi * rinv * A.norm_w[r] * (zi * sigmoidf(zi));
+        A.y[(size_t)head * dv + r] = oi * rinv * nw * (zi * sigmoidf(zi));
     }
-    cluster.sync();  // the partial sums stay in place until every CTA of the cluster has read them
 }
 
 // ------------------------------------------------------------------------------------------
@@ -184,7 +236,7 @@ __global__ void __cluster_dims__(kGdnCluster, 1, 1) __launch_bounds__(kGdnThread
 // ------------------------------------------------------------------------------------------
 
 constexpr int kGqaChunk = 32;       // positions per bulk copy
-constexpr int kGqaStages = 2;       // shared-memory ring depth
+constexpr int kGqaStages = 3;       // shared-memory ring depth (3 x 64 KiB at D = 256)
 constexpr int kGqaThreads = 256;    // 8 warps
 constexpr int kGqaWarps = kGqaThreads / 32;
 constexpr int kGqaCtaTarget = 148;  // split CTAs per launch aimed at (one per SM of a B300)
@@ -261,9 +313,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity, long lon
     return true;
 }
 
+template <int G>
+constexpr int gqa_groups() { return G >= 4 ? 2 : 1; }  // warp groups, each with G / groups heads
+
 template <int D, int G>
-__global__ void __launch_bounds__(kGqaThreads, 1) gqa_split_kernel(const GqaArgs A)
+__global__ void __launch_bounds__(kGqaThreads * gqa_groups<G>(), 1) gqa_split_kernel(const GqaArgs A)
 {
+    constexpr int HG = gqa_groups<G>();
+    constexpr int GH = G / HG;  // heads of a warp group
+    constexpr int NT = kGqaThreads * HG;
     constexpr int NV = D / 128;  // float4 pieces of a row per lane: dims 128 j + 4 lane + 0..3
     constexpr int kStage = 2 * kGqaChunk * D;  // floats: K rows then V rows
     extern __shared__ __align__(128) float smem[];
@@ -275,17 +333,24 @@ __global__ void __launch_bounds__(kGqaThreads, 1) gqa_split_kernel(const GqaArgs
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // warps are (head group, position lane): group hg owns heads hg * GH ..; position lane pw takes
+    // positions pw, pw + 8, ... of each chunk, for its group's heads
+    const int hb = (warp / kGqaWarps) * GH, pw = warp % kGqaWarps;
+    grid_dep_wait();
     const int pos = A.pos[b];
     if (pos < 0 || pos >= A.max_pos) {
         if (tid == 0 && split == 0 && g == 0)
             atomicCAS(A.status, 0, (int)MOE_E_RANGE);
+        grid_dep_launch();
         return;
     }
     const int len = pos + 1;
     const int t0 = split * A.per_split;
     const int t1 = min(len, t0 + A.per_split);
-    if (t0 >= t1)
+    if (t0 >= t1) {
+        grid_dep_launch();
         return;  // past this sequence's end: the merge reads only ranges below len
+    }
     const size_t kvrow0 = (size_t)(b * A.Hkv + g) * A.L;  // row of position 0 in the caches
     const float* Kg = A.kc + kvrow0 * D;
     const float* Vg = A.vc + kvrow0 * D;
@@ -314,19 +379,20 @@ __global__ void __launch_bounds__(kGqaThreads, 1) gqa_split_kernel(const GqaArgs
     if (tid == 0)
         for (int c = 0; c < nchunk && c < kGqaStages; ++c)
             issue(c);
+    grid_dep_launch();
 
-    // the group's G query rows, pre-scaled, in registers
-    float4 qr[G][NV];
+    // this warp group's GH query rows, pre-scaled, in registers
+    float4 qr[GH][NV];
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < GH; ++h)
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            const float4 t = bf4(A.q + ((size_t)b * A.Hq + g * G + h) * D + 128 * j + 4 * lane);
+            const float4 t = bf4(A.q + ((size_t)b * A.Hq + g * G + hb + h) * D + 128 * j + 4 * lane);
             qr[h][j] = make_float4(t.x * A.scale, t.y * A.scale, t.z * A.scale, t.w * A.scale);
         }
-    float4 acc[G][NV];
+    float4 acc[GH][NV];
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < GH; ++h)
 #pragma unroll
         for (int j = 0; j < NV; ++j)
             acc[h][j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -349,7 +415,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1) gqa_split_kernel(const GqaArgs
             // the new token: its row comes from the inputs, into shared memory and the cache
             const int r = pos - a0;
             const size_t src = ((size_t)b * A.Hkv + g) * D;
-            for (int d = tid; d < D; d += kGqaThreads) {
+            for (int d = tid; d < D; d += NT) {
                 const float kv = bf(A.k[src + d]), vv = bf(A.v[src + d]);
                 Ks[r * D + d] = kv;
                 Vs[r * D + d] = vv;
@@ -360,26 +426,31 @@ __global__ void __launch_bounds__(kGqaThreads, 1) gqa_split_kernel(const GqaArgs
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncthreads();
         }
-        // scores: warp w takes positions w, w + 8, ...
-        for (int t = warp; t < n; t += kGqaWarps) {
-            float4 kr[NV];
+        // scores of the group's heads at positions pw, pw + 8, ... (unrolled: the chains interleave)
 #pragma unroll
-            for (int j = 0; j < NV; ++j)
-                kr[j] = *reinterpret_cast<const float4*>(Ks + t * D + 128 * j + 4 * lane);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float d = 0.0f;
+        for (int i = 0; i < kGqaChunk / kGqaWarps; ++i) {
+            const int t = pw + i * kGqaWarps;
+            if (t < n) {
+                float4 kr[NV];
 #pragma unroll
                 for (int j = 0; j < NV; ++j)
-                    d += dot4(qr[h][j], kr[j]);
-                d = warp_sum(d);
-                if (lane == 0)
-                    p_s[h * kGqaChunk + t] = d;
+                    kr[j] = *reinterpret_cast<const float4*>(Ks + t * D + 128 * j + 4 * lane);
+                float d[GH];
+#pragma unroll
+                for (int h = 0; h < GH; ++h) {
+                    d[h] = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < NV; ++j)
+                        d[h] += dot4(qr[h][j], kr[j]);
+                }
+                const float r = reduce_scatter<GH>(d, lane);
+                if ((lane & (32 / GH - 1)) == 0)
+                    p_s[(hb + head_of<GH>(lane)) * kGqaChunk + t] = r;
             }
         }
         __syncthreads();
         // running softmax per head (warp h): new maximum, weights exp(s - m), rescale of the old sum
-        for (int h = warp; h < G; h += kGqaWarps) {
+        for (int h = warp; h < G; h += NT / 32) {
             const float sc = lane < n ? p_s[h * kGqaChunk + lane] : -INFINITY;
             const float mo = m_s[h];
             const float mn = fmaxf(mo, warp_max(sc));
@@ -396,20 +467,24 @@ __global__ void __launch_bounds__(kGqaThreads, 1) gqa_split_kernel(const GqaArgs
         __syncthreads();
         // values: rescale this warp's sums, then add its positions' weighted V rows
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float cr = c_s[h];
+        for (int h = 0; h < GH; ++h) {
+            const float cr = c_s[hb + h];
 #pragma unroll
             for (int j = 0; j < NV; ++j)
                 acc[h][j] = make_float4(acc[h][j].x * cr, acc[h][j].y * cr, acc[h][j].z * cr, acc[h][j].w * cr);
         }
-        for (int t = warp; t < n; t += kGqaWarps) {
+#pragma unroll
+        for (int i = 0; i < kGqaChunk / kGqaWarps; ++i) {
+            const int t = pw + i * kGqaWarps;
+            if (t >= n)
+                break;
             float4 vr[NV];
 #pragma unroll
             for (int j = 0; j < NV; ++j)
                 vr[j] = *reinterpret_cast<const float4*>(Vs + t * D + 128 * j + 4 * lane);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float p = p_s[h * kGqaChunk + t];
+            for (int h = 0; h < GH; ++h) {
+                const float p = p_s[(hb + h) * kGqaChunk + t];
 #pragma unroll
                 for (int j = 0; j < NV; ++j) {
                     acc[h][j].x += p * vr[j].x;
@@ -432,17 +507,17 @@ __global__ void __launch_bounds__(kGqaThreads, 1) gqa_split_kernel(const GqaArgs
         }
         return;
     }
-    // the warps' sums into one, in warp order, through the (now idle) ring
+    // the position lanes' sums into one, in lane order, through the (now idle) ring
     float* red = smem;  // [kGqaWarps][G][D]: kGqaWarps * G <= 2 * kGqaStages * kGqaChunk
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < GH; ++h)
 #pragma unroll
         for (int j = 0; j < NV; ++j)
-            *reinterpret_cast<float4*>(red + ((size_t)warp * G + h) * D + 128 * j + 4 * lane) = acc[h][j];
+            *reinterpret_cast<float4*>(red + ((size_t)pw * G + hb + h) * D + 128 * j + 4 * lane) = acc[h][j];
     __syncthreads();
     const size_t part = ((size_t)(b * A.Hkv + g) * A.n_split + split) * G;
     float* po = A.part_o + part * D;
-    for (int e = 4 * tid; e < G * D; e += 4 * kGqaThreads) {
+    for (int e = 4 * tid; e < G * D; e += 4 * NT) {
         float4 t = *reinterpret_cast<const float4*>(red + e);
 #pragma unroll
         for (int w = 1; w < kGqaWarps; ++w) {
@@ -463,7 +538,9 @@ __global__ void __launch_bounds__(kGqaThreads, 1) gqa_split_kernel(const GqaArgs
 // Merge of the ranges of one query head (block = one (head, sequence), thread = one dimension):
 // M = max_s m_s, w_s = exp(m_s - M), o = sum_s w_s o_s / sum_s w_s l_s. Every reduction runs in a
 // fixed order for a given number of ranges, so the result does not depend on timing.
-template <int D>
+constexpr int kMergeThreads = 256;
+
+template <int NT>  // block size
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float* scratch)
 {
     v = is_max ? warp_max(v) : warp_sum(v);
@@ -474,43 +551,100 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* scrat
     __syncthreads();
     float r = scratch[0];
 #pragma unroll
-    for (int w = 1; w < D / 32; ++w)
+    for (int w = 1; w < NT / 32; ++w)
         r = is_max ? fmaxf(r, scratch[w]) : r + scratch[w];
     return r;
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(D) gqa_merge_kernel(const GqaArgs A)
+__global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const GqaArgs A)
 {
+    constexpr int kQuads = D / 4;                     // float4 columns of a head
+    constexpr int kGroups = kMergeThreads / kQuads;   // range groups summed separately, then in order
+    constexpr int kPer = (kGqaCtaTarget + kGroups - 1) / kGroups;  // ranges per group at most
     __shared__ float wgt[kGqaCtaTarget];
-    __shared__ float scratch[D / 32];
+    __shared__ float scratch[kMergeThreads / 32];
+    __shared__ float4 gsum[kGroups][kQuads];
     const int h = blockIdx.x, b = blockIdx.y;
     const int g = h / G, hh = h - g * G;
+    grid_dep_wait();
+    grid_dep_launch();
     const int pos = A.pos[b];
     if (pos < 0 || pos >= A.max_pos)
         return;
     const int nsp = (pos + 1 + A.per_split - 1) / A.per_split;
     const size_t part0 = (size_t)(b * A.Hkv + g) * A.n_split * G + hh;  // range s at part0 + s * G
     const int tid = threadIdx.x;
+    const int quad = tid % kQuads, grp = tid / kQuads;
+    // this thread's ranges s = grp + kGroups * i: their values first, all loads in flight together
+    float4 v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int s = grp + kGroups * i;
+        v[i] = s < nsp ? *reinterpret_cast<const float4*>(A.part_o + (part0 + (size_t)s * G) * D + 4 * quad)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float m = -INFINITY;
-    for (int s = tid; s < nsp; s += D)
+    for (int s = tid; s < nsp; s += kMergeThreads)
         m = fmaxf(m, A.part_ml[(part0 + (size_t)s * G) * 2]);
-    const float M = block_reduce<D>(m, true, scratch);
+    const float M = block_reduce<kMergeThreads>(m, true, scratch);
     float l = 0.0f;
-    for (int s = tid; s < nsp; s += D) {
+    for (int s = tid; s < nsp; s += kMergeThreads) {
         const float w = expf(A.part_ml[(part0 + (size_t)s * G) * 2] - M);
         wgt[s] = w;
         l += A.part_ml[(part0 + (size_t)s * G) * 2 + 1] * w;
     }
-    const float Lsum = block_reduce<D>(l, false, scratch);  // its barriers also publish wgt[]
-    float o = 0.0f;
-    for (int s = 0; s < nsp; ++s)
-        o += wgt[s] * A.part_o[(part0 + (size_t)s * G) * D + tid];
-    o /= Lsum;
-    const size_t i = ((size_t)b * A.Hq + h) * D + tid;
-    if (A.o)
-        A.o[i] = o;
-    A.y[i] = o * sigmoidf(bf(A.gate[i]));
+    const float Lsum = block_reduce<kMergeThreads>(l, false, scratch);  // its barriers also publish wgt[]
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int s = grp + kGroups * i;
+        if (s < nsp) {
+            const float w = wgt[s];
+            acc.x += w * v[i].x;
+            acc.y += w * v[i].y;
+            acc.z += w * v[i].z;
+            acc.w += w * v[i].w;
+        }
+    }
+    gsum[grp][quad] = acc;
+    __syncthreads();
+    if (grp == 0) {
+        float4 o = gsum[0][quad];
+#pragma unroll
+        for (int q = 1; q < kGroups; ++q) {
+            o.x += gsum[q][quad].x;
+            o.y += gsum[q][quad].y;
+            o.z += gsum[q][quad].z;
+            o.w += gsum[q][quad].w;
+        }
+        const float inv = 1.0f / Lsum;
+        o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        const size_t i = ((size_t)b * A.Hq + h) * D + 4 * quad;
+        if (A.o)
+            *reinterpret_cast<float4*>(A.o + i) = o;
+        const float4 gt = bf4(A.gate + i);
+        *reinterpret_cast<float4*>(A.y + i) =
+            make_float4(o.x * sigmoidf(gt.x), o.y * sigmoidf(gt.y), o.z * sigmoidf(gt.z), o.w * sigmoidf(gt.w));
+    }
+}
+
+// Launch with programmatic stream serialization (the kernel may start before the previous one in
+// the stream has finished; it waits for it with griddepcontrol.wait).
+template <typename Args>
+cudaError_t launch_pdl(void (*kernel)(Args), dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Args& a)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 template <int D, int G>
@@ -526,9 +660,12 @@ moe_status gqa_launch(const GqaArgs& A, int batch, cudaStream_t st)
             return hfail(MOE_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         attr = true;
     }
-    gqa_split_kernel<D, G><<<dim3(A.n_split, A.Hkv, batch), kGqaThreads, smem, st>>>(A);
-    gqa_merge_kernel<D, G><<<dim3(A.Hq, batch), D, 0, st>>>(A);
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(gqa_split_kernel<D, G>, dim3(A.n_split, A.Hkv, batch), dim3(kGqaThreads * gqa_groups<G>()),
+                               smem, st, A);
+    if (e == cudaSuccess)
+        e = launch_pdl(gqa_merge_kernel<D, G>, dim3(A.Hq, batch), dim3(kMergeThreads), 0, st, A);
+    if (e == cudaSuccess)
+        e = cudaGetLastError();
     return e == cudaSuccess ? MOE_OK : hfail(MOE_E_CUDA, "gqa launch: %s", cudaGetErrorString(e));
 }
 
@@ -555,13 +692,15 @@ extern "C" moe_status moe_gdn_step(const moe_gdn_shape* shape, int32_t batch, fl
     GdnArgs A{Hk, Hv, dv, Hv / Hk, d_state, d_q, d_k, d_v, d_z, d_a, d_b, d_A_log, d_dt_bias, d_norm_w, scale, d_o, d_y};
     const dim3 grid(batch * Hv * kGdnCluster);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
     switch (dv) {
-    case 32: gdn_step_kernel<1><<<grid, kGdnThreads, 0, st>>>(A); break;
-    case 64: gdn_step_kernel<2><<<grid, kGdnThreads, 0, st>>>(A); break;
-    case 128: gdn_step_kernel<4><<<grid, kGdnThreads, 0, st>>>(A); break;
-    default: gdn_step_kernel<8><<<grid, kGdnThreads, 0, st>>>(A); break;
+    case 32: e = launch_pdl(gdn_step_kernel<1>, grid, dim3(kGdnThreads), 0, st, A); break;
+    case 64: e = launch_pdl(gdn_step_kernel<2>, grid, dim3(kGdnThreads), 0, st, A); break;
+    case 128: e = launch_pdl(gdn_step_kernel<4>, grid, dim3(kGdnThreads), 0, st, A); break;
+    default: e = launch_pdl(gdn_step_kernel<8>, grid, dim3(kGdnThreads), 0, st, A); break;
     }
-    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = cudaGetLastError();
     return e == cudaSuccess ? MOE_OK : hfail(MOE_E_CUDA, "moe_gdn_step launch: %s", cudaGetErrorString(e));
 }
 
