@@ -353,7 +353,7 @@ def run_streamed(args):
         t_w = time.perf_counter() - t_w
         qp = S.qpack = moe.Qpack.open(args.qpack, direct=True, n_threads=8)
         n_staging = 2 * sh.top_k
-        staging = torch.empty(n_staging * S.stride, dtype=torch.uint8, pin_memory=True)
+        staging = S.pinned_staging(n_staging)
         step = lambda x, o, st: S.step_qpack(x, o, qp, staging, n_staging, st)  # noqa: E731
         qinfo = {"path": args.qpack, "direct": qp.info()[3], "reader_threads": 8, "staging_slots": n_staging,
                  "file_bytes": os.path.getsize(args.qpack), "write_s": t_w}
@@ -920,6 +920,11 @@ def run_hybrid(args):
         dom = "gqa_split_kernel"
     peak, peak_kind = _peaks()
     achieved = bytes_step / (ms_step / 1e3) / 1e9
+    traffic = None  # DRAM bytes of one launch of the dominant kernel, from an ncu capture (profiles/)
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp) and batch == 1:
+        t = json.load(open(tp)).get(args.config)
+        traffic = t.get("bytes_per_launch") if t else None
     ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     cpu_v, cpu_info = (None, None)
     if ws == 1 and not args.no_cpu_baseline:
@@ -940,7 +945,7 @@ def run_hybrid(args):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "layer_latency_us": ms_step * 1e3 / L,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_kind": peak_kind, "kernel": dom, "bytes_per_launch": per_launch,
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": dom, "bytes_per_launch": per_launch,
                      "note": "launch duration = step time / layers (graph replay, gaps included)"},
         "cpu_baseline": None if cpu_v is None else {"value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                                     "sample": cpu_info},

@@ -176,6 +176,13 @@ class Streamed:
         finally:
             q.close()
 
+    def pinned_staging(self, n: int) -> torch.Tensor:
+        """Pinned host buffer of n blobs at a 4096-byte aligned address (direct reads need it; the
+        caching pinned allocator does not promise that alignment), as a view of a larger buffer."""
+        raw = torch.empty(n * self.stride + 4096, dtype=torch.uint8, pin_memory=True)
+        off = (-raw.data_ptr()) % 4096
+        return raw[off:off + n * self.stride]
+
     def step_qpack(self, x: torch.Tensor, out: torch.Tensor, qpack, staging: torch.Tensor, n_staging: int,
                    stream=None, topk_idx: np.ndarray | None = None):
         """One token through all layers, the misses read from the container `qpack` through the

@@ -92,7 +92,7 @@ def test_qpack_stack_equals_resident(tmp_path, sh, n_slots, L):
     S.write_qpack(path)
     q = moe.Qpack.open(path, direct=True, n_threads=4)
     n_staging = 2 * sh.top_k
-    staging = torch.empty(n_staging * S.stride, dtype=torch.uint8, pin_memory=True)
+    staging = S.pinned_staging(n_staging)
     out_s = torch.empty(sh.hidden, dtype=torch.float32, device="cuda")
     try:
         for step in range(3):
