@@ -723,19 +723,43 @@ def _hybrid_setup(kind, L, batch, ctx, n_steps):
 
     W = {"kind": kind, "L": L, "batch": batch}
     n_in = min(n_steps, 8)  # distinct input sets, cycled
+
+    def packed(layers):
+        """Input set 0: every layer's inputs as views of one flat device buffer (16-byte aligned
+        pieces), so that the end-to-end run moves a step's inputs with one host-to-device copy."""
+        pieces, off = [], 0
+        for d in layers:
+            for k, a in d.items():
+                a = np.ascontiguousarray(a)
+                pieces.append((k, a, off))
+                off += (a.nbytes + 15) // 16 * 16
+        flat = np.zeros(off, np.uint8)
+        for _, a, o in pieces:
+            flat[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
+        W["flat"] = torch.from_numpy(flat).cuda()
+        out, i = [], 0
+        for d in layers:
+            e = {}
+            for k, a in d.items():
+                _, _, o = pieces[i]
+                i += 1
+                tdt = torch.int16 if a.dtype == np.uint16 else torch.float32
+                e[k] = W["flat"][o:o + a.nbytes].view(tdt).view(a.shape)
+            out.append(e)
+        return out
     if kind == "gdn":
         sh = SH.GDN80
         W["shape"] = moe.GdnShape(sh.n_key_heads, sh.n_value_heads, sh.key_dim, sh.value_dim)
         W["state"] = [dev(SH.gdn_state(sh, SEED, l, batch)) for l in range(L)]
         W["par"] = [{k: dev(v) for k, v in SH.gdn_params(sh, SEED, l).items()} for l in range(L)]
-        W["inp"] = [[{k: dev(v) for k, v in SH.gdn_inputs(sh, SEED, l, s, batch).items()} for l in range(L)]
-                    for s in range(n_in)]
+        W["inp"] = [packed([SH.gdn_inputs(sh, SEED, l, 0, batch) for l in range(L)])] + [
+            [{k: dev(v) for k, v in SH.gdn_inputs(sh, SEED, l, s, batch).items()} for l in range(L)]
+            for s in range(1, n_in)]
         W["y"] = torch.empty(batch, sh.n_value_heads, sh.value_dim, device="cuda")
         # algorithmic bytes of one layer launch: state read + written, inputs, parameters, y
         W["bytes_per_launch"] = batch * (2 * 4 * sh.state_floats() + 2 * 2 * sh.n_key_heads * sh.key_dim +
                                          2 * 2 * sh.n_value_heads * sh.value_dim + 2 * 4 * sh.n_value_heads +
                                          4 * sh.n_value_heads * sh.value_dim) + 4 * (2 * sh.n_value_heads + sh.value_dim)
-        W["h2d_per_layer"] = sum(v.numel() * v.element_size() for v in W["inp"][0][0].values())
     else:
         sh = SH.GQA80
         W["shape"] = moe.GqaShape(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, ctx)
@@ -744,8 +768,9 @@ def _hybrid_setup(kind, L, batch, ctx, n_steps):
         W["vc"] = [dev(SH.gqa_cache(sh, SEED + 1, l, ctx, start, batch)) for l in range(L)]
         W["pos"] = torch.full((batch,), start, dtype=torch.int32, device="cuda")
         W["start"] = start
-        W["inp"] = [[{k: dev(v) for k, v in SH.gqa_inputs(sh, SEED, l, s, batch).items()} for l in range(L)]
-                    for s in range(n_in)]
+        W["inp"] = [packed([SH.gqa_inputs(sh, SEED, l, 0, batch) for l in range(L)])] + [
+            [{k: dev(v) for k, v in SH.gqa_inputs(sh, SEED, l, s, batch).items()} for l in range(L)]
+            for s in range(1, n_in)]
         W["y"] = torch.empty(batch, sh.n_q_heads, sh.head_dim, device="cuda")
         W["wb"] = moe.gqa_workspace_bytes(W["shape"], batch, ctx)
         W["work"] = torch.empty(W["wb"] // 4 + 4, dtype=torch.float32, device="cuda")
@@ -755,7 +780,6 @@ def _hybrid_setup(kind, L, batch, ctx, n_steps):
         W["kv_row_bytes"] = 2 * 4 * sh.n_kv_heads * sh.head_dim * batch
         W["io_bytes"] = batch * (2 * 2 * sh.n_q_heads * sh.head_dim + 2 * 2 * sh.n_kv_heads * sh.head_dim +
                                  4 * sh.n_q_heads * sh.head_dim)
-        W["h2d_per_layer"] = sum(v.numel() * v.element_size() for v in W["inp"][0][0].values())
     W["sh"] = sh
     return W
 
@@ -887,19 +911,16 @@ def run_hybrid(args):
     if kind == "gqa" and int(W["status"][0].item()) != 0:
         raise RuntimeError(f"device status {int(W['status'][0].item())} after the timed region")
 
-    # end to end: every step's inputs from pinned host memory, the last layer's y back
-    h_in = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in d.items()} for d in W["inp"][0]]
-    for hl, dl in zip(h_in, W["inp"][0]):
-        for k in hl:
-            hl[k].copy_(dl[k])
+    # end to end: every step's inputs (all layers, one packed buffer) from pinned host memory, the
+    # last layer's y back
+    h_flat = torch.empty_like(W["flat"], device="cpu").pin_memory()
+    h_flat.copy_(W["flat"])
     h_y = torch.empty_like(W["y"], device="cpu").pin_memory()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(n_e2e):
-            for hl, dl in zip(h_in, W["inp"][0]):
-                for k in hl:
-                    dl[k].copy_(hl[k], non_blocking=True)
+            W["flat"].copy_(h_flat, non_blocking=True)
             replay(0)
             h_y.copy_(W["y"], non_blocking=True)
             stream.synchronize()
@@ -950,7 +971,7 @@ def run_hybrid(args):
         "cpu_baseline": None if cpu_v is None else {"value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                                     "sample": cpu_info},
         "e2e": {"value": ws * batch * n_e2e / e2e_s, "unit": "tokens/s",
-                "h2d_bytes_per_step": W["h2d_per_layer"] * L, "d2h_bytes_per_step": W["y"].numel() * 4,
+                "h2d_bytes_per_step": W["flat"].numel(), "d2h_bytes_per_step": W["y"].numel() * 4,
                 "steps": n_e2e},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

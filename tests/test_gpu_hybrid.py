@@ -6,8 +6,8 @@ in double. Gated DeltaNet: a state element takes a few roundings per step (2^-24
 about |A sp| 2^-24 (|A sp| < 50 here). Over 16 steps (alpha <= 1 does not amplify) that stays
 below 1e-5 relative; 2e-5 is asserted on the state, o and y. GQA decode: the scores are 256-term
 dot products (|s| error about 2^-24 |q||k| scale), the running softmax and the weighted sums of
-up to 8192 positions add random-sign roundings of about sqrt(n) 2^-24 = 5.4e-6; 2e-5 is asserted
-on o and y. The cache rows a step appends are bf16 values widened to fp32: bit-exact.
+up to 32768 positions add random-sign roundings of about sqrt(n) 2^-24 (5.4e-6 at 8K, 1.1e-5 at
+32K); 2e-5 is asserted on o and y. The cache rows a step appends are bf16 values widened to fp32: bit-exact.
 """
 import numpy as np
 import pytest
@@ -191,6 +191,12 @@ def test_gqa_matches_oracle(sh, filled):
 def test_gqa_80b_full_8k_context():
     # the pages' 8K context: 8190 cached positions, two steps fill the cache to its capacity
     _gqa_run(SH.GQA80, 1, 8192, [8190], steps=2)
+
+
+def test_gqa_80b_32k_context():
+    # the pages' 32K context (about 1.5 GiB of cache over the 12 layers; one layer here): one step
+    # at the last position, the ranges 886 positions long
+    _gqa_run(SH.GQA80, 1, 32768, [32767], steps=1)
 
 
 def test_gqa_split_count_changes_nothing_beyond_rounding():
