@@ -186,3 +186,55 @@ def test_batched_workspace_bytes(lib):
     for t, b in zip((1, 8, 64, 512, 4096), sizes):
         a = t * (k + 1)
         assert b >= 2 * a * H + 2 * a * Imax + 4 * t * E
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(16, 2, 256), (4, 4, 128), (16, 1, 128), (8, 2, 256)])
+@pytest.mark.parametrize("batch", [1, 3, 64])
+@pytest.mark.parametrize("max_pos", [1, 31, 32, 33, 1000, 8192, 32768])
+def test_gqa_split_policy_invariants(lib, Hq, Hkv, D, batch, max_pos):
+    # the ranges the workspace is sized for: at least one, at most one per SM of a 148-SM part over
+    # the (sequence, K/V head) pairs (or one), none empty, together covering every position
+    sh = moe.GqaShape(Hq, Hkv, D, 32768)
+    wb = moe.gqa_workspace_bytes(sh, batch, max_pos)
+    G = Hq // Hkv
+    per_range = batch * Hkv * G * (D + 2) * 4
+    assert wb > 0 and wb % per_range == 0
+    n_split = wb // per_range
+    assert 1 <= n_split <= max(1, 148 // (batch * Hkv))
+    assert n_split <= -(-max_pos // 32)                 # never more ranges than 32-position chunks
+    per = -(-max_pos // n_split)
+    assert (n_split - 1) * per < max_pos <= n_split * per  # no empty range, all positions covered
+
+
+def test_gqa_and_gdn_argument_checks(lib):
+    sh = moe.GqaShape(16, 2, 256, 128)
+    wb = moe.gqa_workspace_bytes(sh, 1, 64)
+    args = lambda **kw: dict(dict(k_cache=16, v_cache=16, pos=16, q=16, k=16, v=16, gate=16, work=16, y=16,
+                                  status=16), **kw)
+
+    def call(shape=sh, batch=1, max_pos=64, work_bytes=wb, **kw):
+        a = args(**kw)
+        moe.gqa_decode(shape, batch, max_pos, a["k_cache"], a["v_cache"], a["pos"], a["q"], a["k"], a["v"],
+                       a["gate"], 1.0, a["work"], work_bytes, a["y"], a["status"])
+
+    for kw, want in [(dict(max_pos=129), moe.E_INVALID), (dict(max_pos=0), moe.E_INVALID),
+                     (dict(batch=0), moe.E_INVALID), (dict(batch=70000), moe.E_INVALID),
+                     (dict(status=None), moe.E_INVALID), (dict(y=8), moe.E_INVALID),
+                     (dict(k_cache=None), moe.E_INVALID),
+                     (dict(shape=moe.GqaShape(12, 4, 256, 128)), moe.E_SHAPE),   # 3 query heads per K/V head
+                     (dict(shape=moe.GqaShape(32, 2, 256, 128)), moe.E_SHAPE),   # 16 per K/V head at D 256
+                     (dict(shape=moe.GqaShape(16, 2, 64, 128)), moe.E_SHAPE),
+                     (dict(work_bytes=wb - 1), moe.E_NOMEM)]:
+        with pytest.raises(moe.MoeError) as e:
+            call(**kw)
+        assert e.value.status == want, kw
+    gs = moe.GdnShape(16, 32, 128, 128)
+    ok = [16] * 10
+    for shape, batch, ptrs, want in [(moe.GdnShape(16, 24, 128, 128), 1, ok, moe.E_SHAPE),   # Hv % Hk
+                                     (moe.GdnShape(16, 32, 128, 96), 1, ok, moe.E_SHAPE),
+                                     (moe.GdnShape(0, 32, 128, 128), 1, ok, moe.E_SHAPE),
+                                     (gs, 0, ok, moe.E_INVALID),
+                                     (gs, 1, [None] + ok[1:], moe.E_INVALID)]:
+        with pytest.raises(moe.MoeError) as e:
+            moe.gdn_step(shape, batch, *ptrs, 1.0, 16)
+        assert e.value.status == want, (shape.n_key_heads, shape.n_value_heads, shape.value_dim, batch)
