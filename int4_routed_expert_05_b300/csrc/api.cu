@@ -1125,6 +1125,7 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     A.shared_blob = L.shared_blob;
     A.list = reinterpret_cast<const int32_t*>(w + bl.list);
     A.aw = reinterpret_cast<const float*>(w + bl.aw);
+    A.us = reinterpret_cast<const __half*>(w + bl.us);
     A.hbuf = reinterpret_cast<__half*>(w + bl.hbuf);
     A.y = d_y;
     const bool det = (sh.flags & MOE_DETERMINISTIC) != 0;
@@ -1160,8 +1161,15 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     const int ei = nev ? p->gemm_next : -1;
     if (ei >= 0)
         CUDA_TRY(cudaEventRecord(p->gemm_ev[2 * ei], cs));
-    tc::launch_expert_gemm(1, A, tgu, ntasks, grid, cs);
-    tc::launch_expert_gemm(2, A, tdn, ntasks + 1, grid, cs);
+    // few tokens: the experts' weights are streamed once through matrix-vector products; else GEMMs
+    if (T <= gv::kMaxTokens && gv::geometry_ok(p->geo) && gv::geometry_ok(p->geo_s) &&
+        gv::smem_bytes(H, Imax, sh.bits) <= (size_t)p->smem_optin) {
+        gv::launch(1, A, tgu, ntasks, 2 * grid, cs);
+        gv::launch(2, A, tdn, ntasks + 1, 2 * grid, cs);
+    } else {
+        tc::launch_expert_gemm(1, A, tgu, ntasks, grid, cs);
+        tc::launch_expert_gemm(2, A, tdn, ntasks + 1, grid, cs);
+    }
     if (det)
         bat::launch_combine(A.ypart, apos, T, k, H, d_y, cs);
     if (ei >= 0) {

@@ -41,6 +41,8 @@ struct GroupedArgs {
     const uint8_t* shared_blob;
     const int32_t* list;      // [A] token of each assignment, grouped by expert
     const float* aw;          // [A] combine weight of each assignment
+    const __half* us;         // [A][H] input rows in assignment order, K-permuted (the small-T path
+                              // reads them directly; the GEMMs through map_b[0])
     __half* hbuf;             // [A][Imax] SwiGLU output, K-permuted (see kperm)
     float* y;                 // [T][H] output, zeroed before the down GEMM (fp32 reductions)
     float* ypart;             // [A][H] weighted down rows per assignment (deterministic combine), or null
@@ -96,4 +98,13 @@ size_t router_smem_bytes();
 size_t expert_smem_bytes(int H, int Imax, int bits);
 
 }  // namespace tc
+namespace gv {
+// The small-token path (gemv.cu): the two expert products as matrix-vector products for token
+// counts up to kMaxTokens, on the same task lists and buffers as the GEMMs.
+constexpr int kMaxTokens = 64;
+size_t smem_bytes(int H, int Imax, int bits);
+bool geometry_ok(const BlobGeo& g);  // every section and row 16-byte aligned (row bulk copies)
+void launch(int kind, const tc::GroupedArgs& A, const int4* tasks, const int32_t* n_tasks, int grid, cudaStream_t st);
+}  // namespace gv
+
 }  // namespace moe
