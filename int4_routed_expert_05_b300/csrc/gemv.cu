@@ -12,9 +12,11 @@
 // task (128 rows) as 2 rounds of 64 rows. A round's rows arrive as one 1D bulk copy per row (plus
 // the rows' scale and bias spans) into shared-memory rows padded by 16 bytes, so that the 8 rows a
 // warp's fragment load touches fall in distinct banks; two rounds are in flight. The 8 warps split
-// K into 16-element slices (warp w takes slices w, w + 8, ...); per slice each warp dequantises its
+// K into 64-element groups of four 16-element slices; per slice each warp dequantises its
 // rows' codes straight into the A fragments of mma.sync m16n8k16 (rows = weight rows, K = 16, N = 8
-// assignments) with the activations as B, fp32 accumulation. The warps' partial sums are added in
+// assignments) with the activations as B, fp32 accumulation; a warp takes whole quantisation groups
+// (w, w + 8, ...), so each row's scale and bias are read once per group, and fetches the next
+// group's activation fragments while it works on the current one. The warps' partial sums are added in
 // warp order through shared memory, so the result does not depend on timing.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -113,7 +115,6 @@ struct Kind {
     static constexpr int kRows = KIND == 1 ? 16 : 64;   // rows per matrix per round
     static constexpr int kMats = KIND == 1 ? 2 : 1;     // matrices per round
     static constexpr int kUnits = kMats * kRows / 16;   // 16-row MMA tiles per round
-    static constexpr int kChunks = KIND == 1 ? 4 : 2;   // 8-assignment MMA columns per pass
 };
 
 struct Smem {
@@ -131,8 +132,8 @@ __host__ __device__ inline Smem smem_plan(int H, int Imax, int bits)
     s.code = 0;
     s.sc = s.row_stride * K::kMats * K::kRows;                      // [mat][s | b][row][G] bf16
     s.stage = (s.sc + (uint32_t)(K::kMats * 2 * K::kRows * G * 2) + 127) & ~127u;
-    s.red = kStages * s.stage;                                      // [warp][unit][16][8 chunks] fp32
-    s.bar = s.red + (uint32_t)(kWarps * K::kUnits * 16 * 8 * K::kChunks * 4);
+    s.red = kStages * s.stage;                                      // [warp][unit][16][8] fp32
+    s.bar = s.red + (uint32_t)(kWarps * K::kUnits * 16 * 8 * 4);
     s.total = s.bar + kStages * 8;
     return s;
 }
@@ -231,64 +232,47 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const tc::GroupedArgs P,
         if (blob) {
             const BlobGeo& geo = r.e < P.E ? P.geo : P.geo_s;
             const int kd = KIND == 1 ? P.H : geo.cols[2];
-            const int G = kd / 64, nsl = kd / 16;
+            const int G = kd / 64;
             const int ldb = KIND == 1 ? P.H : P.Imax;  // row length of the B operand rows
             const uint8_t* st = sm + (j % kStages) * pl.stage;
             const uint16_t* ssc = reinterpret_cast<const uint16_t*>(st + pl.sc);
-            // this thread's rows in each 16-row unit: g and g + 8
-            for (int cg0 = 0; cg0 < r.nn; cg0 += 8 * K::kChunks) {
-                float acc[K::kUnits][K::kChunks][4];
+            // passes of 8 assignments (the MMA's N); this thread feeds column g and holds rows g, g + 8
+            for (int cg0 = 0; cg0 < r.nn; cg0 += 8) {
+                float acc[K::kUnits][4];
 #pragma unroll
                 for (int u = 0; u < K::kUnits; ++u)
 #pragma unroll
-                    for (int ch = 0; ch < K::kChunks; ++ch)
+                    for (int i = 0; i < 4; ++i)
+                        acc[u][i] = 0.0f;
+                const bool colv = cg0 + g < r.nn;
+                const __half* brow = bop + (size_t)(r.n0 + (colv ? cg0 + g : 0)) * ldb + 2 * c;
+                // B fragments of one quantisation group (its 4 slices), fetched one group ahead so
+                // that their latency overlaps the current group's work
+                uint32_t bc[8], bn[8];
+                auto load_b = [&](int grp, uint32_t (&x)[8]) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            acc[u][ch][i] = 0.0f;
-                bool bad = false;
-                // B fragments of the pass's chunks (assignment column g of each chunk) for slice sl,
-                // loaded one slice ahead so that their latency overlaps the current slice's work
-                uint32_t b0[K::kChunks], b1[K::kChunks], n0f[K::kChunks], n1f[K::kChunks];
-                auto load_b = [&](int sl, uint32_t (&x0)[K::kChunks], uint32_t (&x1)[K::kChunks]) {
-#pragma unroll
-                    for (int ch = 0; ch < K::kChunks; ++ch) {
-                        const int col = cg0 + ch * 8 + g;
-                        if (sl < nsl && col < r.nn) {
-                            const __half* row = bop + (size_t)(r.n0 + col) * ldb + sl * 16 + 2 * c;
-                            x0[ch] = *reinterpret_cast<const uint32_t*>(row);
-                            x1[ch] = *reinterpret_cast<const uint32_t*>(row + 8);
-                        } else {
-                            x0[ch] = 0u;
-                            x1[ch] = 0u;
-                        }
+                    for (int i = 0; i < 4; ++i) {
+                        const bool v = colv && grp < G;
+                        const __half* q = brow + (4 * grp + i) * 16;
+                        x[2 * i] = v ? *reinterpret_cast<const uint32_t*>(q) : 0u;
+                        x[2 * i + 1] = v ? *reinterpret_cast<const uint32_t*>(q + 8) : 0u;
                     }
                 };
-                load_b(warp, n0f, n1f);
-                for (int sl = warp; sl < nsl; sl += kWarps) {
-                    const int grp = sl >> 2;
+                load_b(warp, bn);
+                bool bad = false;
+                // warp w takes the quantisation groups w, w + 8, ...: one scale and bias per row and
+                // group, four 16-element slices each
+                for (int grp = warp; grp < G; grp += kWarps) {
 #pragma unroll
-                    for (int ch = 0; ch < K::kChunks; ++ch) {
-                        b0[ch] = n0f[ch];
-                        b1[ch] = n1f[ch];
-                    }
-                    load_b(sl + kWarps, n0f, n1f);
+                    for (int i = 0; i < 8; ++i)
+                        bc[i] = bn[i];
+                    load_b(grp + kWarps, bn);
 #pragma unroll
                     for (int u = 0; u < K::kUnits; ++u) {
                         const int mat = u / (K::kRows / 16), rt = u % (K::kRows / 16);
-                        const int ra = rt * 16 + g, rb2 = ra + 8;          // rows within the matrix's round
+                        const int ra = rt * 16 + g, rb2 = ra + 8;  // rows within the matrix's round
                         const uint8_t* ca = st + pl.code + (uint32_t)(mat * K::kRows + ra) * pl.row_stride;
                         const uint8_t* cb = st + pl.code + (uint32_t)(mat * K::kRows + rb2) * pl.row_stride;
-                        uint32_t wa[4], wb[4];
-                        if (BITS == 4) {
-                            const uint2 va = *reinterpret_cast<const uint2*>(ca + sl * 8);
-                            const uint2 vb = *reinterpret_cast<const uint2*>(cb + sl * 8);
-                            wa[0] = va.x; wa[1] = va.y; wb[0] = vb.x; wb[1] = vb.y;
-                        } else {
-                            const uint4 va = *reinterpret_cast<const uint4*>(ca + sl * 16);
-                            const uint4 vb = *reinterpret_cast<const uint4*>(cb + sl * 16);
-                            wa[0] = va.x; wa[1] = va.y; wa[2] = va.z; wa[3] = va.w;
-                            wb[0] = vb.x; wb[1] = vb.y; wb[2] = vb.z; wb[3] = vb.w;
-                        }
                         const uint16_t* sp = ssc + (size_t)(mat * 2) * K::kRows * G;
                         const uint16_t* bp = sp + (size_t)K::kRows * G;
                         const float sa = bf2f(sp[ra * G + grp]), ba = bf2f(bp[ra * G + grp]);
@@ -299,43 +283,52 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const tc::GroupedArgs P,
                         bad |= (sb2 != 0.f && !(fabsf(sb2) >= 6.103515625e-05f)) || !(fabsf(sb2) * qmax + fabsf(bb) <= 65504.f);
                         const __half2 s2a = __half2half2(__float2half_rn(sa)), b2a = __half2half2(__float2half_rn(ba));
                         const __half2 s2b = __half2half2(__float2half_rn(sb2)), b2b = __half2half2(__float2half_rn(bb));
-                        // K block 0 of the slice = word(s) 0 (int4) / 0-1 (int8), block 1 the next
-                        const uint32_t a0 = deq(code_pair<BITS>(wa, c), s2a, b2a);
-                        const uint32_t a1 = deq(code_pair<BITS>(wb, c), s2b, b2b);
-                        const uint32_t a2 = deq(code_pair<BITS>(wa + (BITS == 4 ? 1 : 2), c), s2a, b2a);
-                        const uint32_t a3 = deq(code_pair<BITS>(wb + (BITS == 4 ? 1 : 2), c), s2b, b2b);
 #pragma unroll
-                        for (int ch = 0; ch < K::kChunks; ++ch)
-                            if (cg0 + ch * 8 < r.nn)
-                                mma16816(acc[u][ch], a0, a1, a2, a3, b0[ch], b1[ch]);
+                        for (int i = 0; i < 4; ++i) {
+                            const int sl = 4 * grp + i;
+                            uint32_t wa[4], wb[4];
+                            if (BITS == 4) {
+                                const uint2 va = *reinterpret_cast<const uint2*>(ca + sl * 8);
+                                const uint2 vb = *reinterpret_cast<const uint2*>(cb + sl * 8);
+                                wa[0] = va.x; wa[1] = va.y; wb[0] = vb.x; wb[1] = vb.y;
+                            } else {
+                                const uint4 va = *reinterpret_cast<const uint4*>(ca + sl * 16);
+                                const uint4 vb = *reinterpret_cast<const uint4*>(cb + sl * 16);
+                                wa[0] = va.x; wa[1] = va.y; wa[2] = va.z; wa[3] = va.w;
+                                wb[0] = vb.x; wb[1] = vb.y; wb[2] = vb.z; wb[3] = vb.w;
+                            }
+                            // K block 0 of the slice = word 0 (int4) / words 0-1 (int8), block 1 the next
+                            const uint32_t a0 = deq(code_pair<BITS>(wa, c), s2a, b2a);
+                            const uint32_t a1 = deq(code_pair<BITS>(wb, c), s2b, b2b);
+                            const uint32_t a2 = deq(code_pair<BITS>(wa + (BITS == 4 ? 1 : 2), c), s2a, b2a);
+                            const uint32_t a3 = deq(code_pair<BITS>(wb + (BITS == 4 ? 1 : 2), c), s2b, b2b);
+                            mma16816(acc[u], a0, a1, a2, a3, bc[2 * i], bc[2 * i + 1]);
+                        }
                     }
                 }
                 if (bad)
                     atomicCAS(P.status, 0, kStatusRange);
-                // the warps' partial sums -> shared memory [warp][unit][row 16][col 8 kChunks]
+                // the warps' partial sums -> shared memory [warp][unit][row 16][col 8]
 #pragma unroll
-                for (int u = 0; u < K::kUnits; ++u)
-#pragma unroll
-                    for (int ch = 0; ch < K::kChunks; ++ch) {
-                        float* rp = red + ((size_t)(warp * K::kUnits + u) * 16) * (8 * K::kChunks) + ch * 8 + 2 * c;
-                        rp[g * 8 * K::kChunks] = acc[u][ch][0];
-                        rp[g * 8 * K::kChunks + 1] = acc[u][ch][1];
-                        rp[(g + 8) * 8 * K::kChunks] = acc[u][ch][2];
-                        rp[(g + 8) * 8 * K::kChunks + 1] = acc[u][ch][3];
-                    }
+                for (int u = 0; u < K::kUnits; ++u) {
+                    float* rp = red + ((size_t)(warp * K::kUnits + u) * 16) * 8 + 2 * c;
+                    rp[g * 8] = acc[u][0];
+                    rp[g * 8 + 1] = acc[u][1];
+                    rp[(g + 8) * 8] = acc[u][2];
+                    rp[(g + 8) * 8 + 1] = acc[u][3];
+                }
                 __syncthreads();
-                constexpr int kCols = 8 * K::kChunks;
                 auto sum_warps = [&](int u, int row, int col) {
                     float v = 0.0f;
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w)
-                        v += red[((size_t)(w * K::kUnits + u) * 16 + row) * kCols + col];
+                        v += red[((size_t)(w * K::kUnits + u) * 16 + row) * 8 + col];
                     return v;
                 };
                 if (KIND == 1) {
                     // h = silu(gate) * up for the round's 16 rows and the pass's assignments
-                    for (int i = tid; i < 16 * kCols; i += kThreads) {
-                        const int row = i / kCols, col = i % kCols;
+                    for (int i = tid; i < 16 * 8; i += kThreads) {
+                        const int row = i / 8, col = i % 8;
                         if (cg0 + col < r.nn) {
                             const float gt = sum_warps(0, row, col), up = sum_warps(1, row, col);
                             const float h = __fdividef(gt, 1.f + __expf(-gt)) * up;
@@ -347,8 +340,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const tc::GroupedArgs P,
                         }
                     }
                 } else {
-                    for (int i = tid; i < K::kRows * kCols; i += kThreads) {
-                        const int row = i / kCols, col = i % kCols;
+                    for (int i = tid; i < K::kRows * 8; i += kThreads) {
+                        const int row = i / 8, col = i % 8;
                         const int o = r.m0 + row;
                         if (cg0 + col < r.nn && o < P.H) {
                             const int a = r.n0 + cg0 + col;
