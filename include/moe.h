@@ -70,6 +70,11 @@ typedef enum {
                              * reproducible; 4 T (k + 1) H more workspace bytes) instead of fp32
                              * reductions in tile completion order. The decode kernels are always
                              * deterministic and ignore it. */
+#define MOE_GEMV 16 /* batched path, T <= 64: the two expert products as matrix-vector products
+                     * (each touched expert's rows streamed once into mma.sync fragments) instead
+                     * of the tensor-core GEMMs. Same results within rounding (the same fp16
+                     * dequantisation, another summation order). Measured slower on B300 at T = 8
+                     * and 64 than the GEMMs, so off by default. The decode kernels ignore it. */
 
 /* One MoE FFN layer. hidden H, n_experts E, top_k k, inter I (routed expert), shared_inter Is,
  * bits 4 or 8, group 64. Supported: H % 256 == 0, I % 64 == 0, Is % 64 == 0, 1 <= k <= 16,

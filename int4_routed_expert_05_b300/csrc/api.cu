@@ -110,7 +110,7 @@ moe_status check_shape(const moe_shape* s)
         return fail(MOE_E_SHAPE, "top_k must be in [1, %d] (got %d)", kMaxK, s->top_k);
     if (s->n_experts < s->top_k || s->n_experts > kMaxE)
         return fail(MOE_E_SHAPE, "n_experts must be in [top_k, %d] (got %d)", kMaxE, s->n_experts);
-    if (s->flags & ~(MOE_RENORM | MOE_PRENORM | MOE_RESIDUAL | MOE_DETERMINISTIC))
+    if (s->flags & ~(MOE_RENORM | MOE_PRENORM | MOE_RESIDUAL | MOE_DETERMINISTIC | MOE_GEMV))
         return fail(MOE_E_SHAPE, "unknown flag bits 0x%x", s->flags);
     return MOE_OK;
 }
@@ -1161,8 +1161,9 @@ moe_status moe_layer_forward_batched(moe_pool* p, int32_t layer, const void* d_x
     const int ei = nev ? p->gemm_next : -1;
     if (ei >= 0)
         CUDA_TRY(cudaEventRecord(p->gemm_ev[2 * ei], cs));
-    // few tokens: the experts' weights are streamed once through matrix-vector products; else GEMMs
-    if (T <= gv::kMaxTokens && gv::geometry_ok(p->geo) && gv::geometry_ok(p->geo_s) &&
+    // MOE_GEMV and few tokens: the experts' weights streamed once through matrix-vector products;
+    // else (the default) the tensor-core GEMMs
+    if ((sh.flags & MOE_GEMV) && T <= gv::kMaxTokens && gv::geometry_ok(p->geo) && gv::geometry_ok(p->geo_s) &&
         gv::smem_bytes(H, Imax, sh.bits) <= (size_t)p->smem_optin) {
         gv::launch(1, A, tgu, ntasks, 2 * grid, cs);
         gv::launch(2, A, tdn, ntasks + 1, 2 * grid, cs);

@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 OK, E_INVALID, E_SHAPE, E_NOT_RESIDENT, E_POOL_FULL, E_CUDA, E_TIMEOUT, E_NOMEM, E_RANGE = range(9)
-RENORM, PRENORM, RESIDUAL, DETERMINISTIC = 1, 2, 4, 8
+RENORM, PRENORM, RESIDUAL, DETERMINISTIC, GEMV = 1, 2, 4, 8, 16
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_SHAPE", 3: "MOE_E_NOT_RESIDENT",
                 4: "MOE_E_POOL_FULL", 5: "MOE_E_CUDA", 6: "MOE_E_TIMEOUT", 7: "MOE_E_NOMEM", 8: "MOE_E_RANGE"}
 

@@ -214,11 +214,12 @@ def test_input_beyond_fp16_reports_range(path):
     assert R.pool.device_status() == moe.OK
 
 
-def test_scale_below_fp16_normal_reports_range():
+@pytest.mark.parametrize("flags", [0, moe.GEMV])
+def test_scale_below_fp16_normal_reports_range(flags):
     """A group scale below fp16's normal range (2^-14) loses its relative precision in the batched
-    path's fp16 dequantisation: reported as MOE_E_RANGE."""
+    path's fp16 dequantisation (either expert path): reported as MOE_E_RANGE."""
     sh = synth.Shape(256, 16, 2, 64, 64)
-    R = Resident(sh, 1, 3)
+    R = Resident(sh, 1, 3, flags=moe.RENORM | flags)
     # every expert's gate scales -> 1e-6 (bf16), written into the resident blobs
     for e in range(sh.n_experts):
         tt = synth.expert_tensors(sh, 3, 0, int(R.maps[0][e]))
@@ -250,3 +251,35 @@ def test_batched_repeated_seeds(orc, bits, dims, T):
         sample = sorted(rng.choice(T, size=8, replace=False).tolist())
         _, _, err = _case(orc, sh, seed=seed, T=T, sample=sample)
         assert err <= DERIVED, (seed, err)
+
+
+GEMV_SHAPES = [(256, 16, 2, 64, 64, 4), (256, 16, 2, 64, 64, 8), (768, 100, 7, 192, 320, 8), (256, 512, 16, 64, 64, 4),
+               (2048, 512, 10, 512, 512, 4)]
+
+
+@pytest.mark.parametrize("dims", GEMV_SHAPES)
+@pytest.mark.parametrize("T", [1, 8, 37, 64])
+def test_gemv_small_token_path(orc, dims, T):
+    """MOE_GEMV (T <= 64: the expert products as matrix-vector products): against the oracle, and
+    against the tensor-core GEMM path on the same layer and tokens (the same fp16 dequantisation;
+    only the summation order differs), deterministic combine on."""
+    H, E, k, I, Is, bits = dims
+    sh = synth.Shape(H, E, k, I, Is, bits=bits)
+    seed, nu = 31, min(64, E)
+    Rg = Resident(sh, 1, seed, n_unique=nu, flags=moe.RENORM | moe.DETERMINISTIC | moe.GEMV)
+    Rt = Resident(sh, 1, seed, n_unique=nu, flags=moe.RENORM | moe.DETERMINISTIC)
+    x = synth.activation_bits(sh, seed, 0, T)
+    yg, idxg, _ = Rg.layer_forward_batched(0, _bits(x))
+    yt, idxt, _ = Rt.layer_forward_batched(0, _bits(x))
+    torch.cuda.synchronize()
+    assert Rg.pool.device_status() == moe.OK and Rt.pool.device_status() == moe.OK
+    assert torch.equal(idxg, idxt)
+    yg, yt, idx = yg.cpu().numpy(), yt.cpu().numpy(), idxg.cpu().numpy()
+    # both paths round h = silu(g) u to fp16; another summation order moves an h value across an
+    # fp16 rounding boundary with a probability of about 2^-24 / 2^-11 per element, and such an h
+    # then differs by one fp16 ulp (2^-11 relative): the outputs' rel-L2 stays near 1e-5
+    assert rel_l2(yg, yt) <= 5e-5, rel_l2(yg, yt)
+    O = OracleLayers(orc, sh, seed, 1, n_unique=nu)
+    for t in range(min(T, 8)):
+        r, exact = layer_reference(orc, O, 0, x[t], idx[t])
+        assert rel_l2(yg[t], r["y"]) <= (TOL if exact else NEAR_TIE_TOL), t
