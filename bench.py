@@ -547,7 +547,7 @@ def run_batched(args):
     name, _, bits, desc = CONFIGS[args.config]
     sh = _shape(name, bits)
     L = args.layers or BATCHED_LAYERS
-    R = Resident(sh, L, SEED, flags=moe.RENORM, verbose=(rank == 0))
+    R = Resident(sh, L, SEED, flags=moe.RENORM | (moe.GEMV if args.gemv else 0), verbose=(rank == 0))
     H, E, k = sh.hidden, sh.n_experts, sh.top_k
     n_x = 4
     xs = torch.from_numpy(np.ascontiguousarray(
@@ -690,6 +690,7 @@ def run_batched(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights, fp16 tensor-core operands, fp32 accumulate",
         "data": "synthetic (seeded generator, random-init weights of the stated shapes)",
         "config": {"workload": args.config, "description": desc, "tokens": T, "layers_rotated": L,
+                   "expert_path": "matrix-vector (MOE_GEMV)" if args.gemv else "tensor-core GEMMs",
                    "cuda_graphs": bool(graphs),
                    "hidden": H, "experts": E, "top_k": k, "inter": sh.inter, "shared_inter": sh.shared_inter,
                    "bits": bits, "group": sh.group,
@@ -1019,6 +1020,8 @@ def main():
     ap.add_argument("--prefetch", type=int, default=6,
                     help="bounded pool: copy ahead the next layer's N best predicted experts (0: off; default 6, the best of a 2 GiB sweep)")
     ap.add_argument("--batch", type=int, default=1, help="hybrid workloads: independent sequences per step")
+    ap.add_argument("--gemv", action="store_true",
+                    help="batched workloads with T <= 64: the matrix-vector expert path (MOE_GEMV)")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the stack (small cases for profiling)")
     args = ap.parse_args()
