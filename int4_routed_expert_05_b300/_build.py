@@ -9,7 +9,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libmoe.so")
 SOURCES = ["api.cu", "decode.cu", "scalar.cu", "noalloc.cu", "batched.cu", "grouped.cu", "gemv.cu", "hybrid.cu", "qpack.cpp"]
-HEADERS = ["layout.h", "policy.h", "host.h", "grouped.h", "qpack.h"]
+HEADERS = ["layout.h", "policy.h", "host.h", "grouped.h", "qpack.h", "attr.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -24,6 +24,7 @@
 
 #include <cstdint>
 
+#include "attr.h"
 #include "grouped.h"
 #include "layout.h"
 
@@ -366,11 +367,8 @@ template <int KIND, int BITS>
 void launch_one(const tc::GroupedArgs& A, const int4* tasks, const int32_t* n_tasks, int grid, cudaStream_t st)
 {
     const Smem pl = smem_plan<KIND>(A.H, A.Imax, BITS);
-    static int set_bytes = 0;
-    if ((int)pl.total > set_bytes) {
-        cudaFuncSetAttribute(gemv_kernel<KIND, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.total);
-        set_bytes = (int)pl.total;
-    }
+    static std::atomic<int> done[kMaxDevices];
+    raise_smem_limit(gemv_kernel<KIND, BITS>, (int)pl.total, done);
     const __half* bop = KIND == 1 ? A.us : A.hbuf;
     gemv_kernel<KIND, BITS><<<grid, kThreads, pl.total, st>>>(A, tasks, n_tasks, bop);
 }

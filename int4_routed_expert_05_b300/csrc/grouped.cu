@@ -31,6 +31,7 @@
 
 #include <cstdint>
 
+#include "attr.h"
 #include "grouped.h"
 #include "layout.h"
 
@@ -800,19 +801,16 @@ size_t expert_smem_bytes(int H, int Imax, int bits) { return xplan(H, Imax, bits
 
 void launch_router_gemm(const GroupedArgs& A, int grid, cudaStream_t st)
 {
-    static bool attr = false;
+    static std::atomic<int> done[kMaxDevices];
     const size_t smem = router_smem_bytes();
-    if (!attr) {
-        cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-    }
+    raise_smem_limit(router_kernel, (int)smem, done);
     router_kernel<<<grid, kThreadsR, smem, st>>>(A);
 }
 
 void launch_expert_gemm(int kind, const GroupedArgs& A, const int4* tasks, const int32_t* n_tasks, int grid,
                         cudaStream_t st)
 {
-    static bool attr[4] = {false, false, false, false};
+    static std::atomic<int> done[4][kMaxDevices];
     GroupedArgs P = A;
     P.tasks = tasks;
     P.n_tasks = n_tasks;
@@ -820,10 +818,7 @@ void launch_expert_gemm(int kind, const GroupedArgs& A, const int4* tasks, const
     void (*k)(const GroupedArgs) = kind == 1 ? (A.bits == 4 ? expert_kernel<1, 4> : expert_kernel<1, 8>)
                                              : (A.bits == 4 ? expert_kernel<2, 4> : expert_kernel<2, 8>);
     const int ki = (kind - 1) * 2 + (A.bits == 4 ? 0 : 1);
-    if (!attr[ki]) {
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        attr[ki] = true;
-    }
+    raise_smem_limit(k, 227 * 1024, done[ki]);
     k<<<grid, kThreadsX, smem, st>>>(P);
 }
 

@@ -31,6 +31,7 @@
 #include <cstdint>
 #include <cstdio>
 
+#include "attr.h"
 #include "hybrid.h"
 
 namespace cg = cooperative_groups;
@@ -652,15 +653,11 @@ moe_status gqa_launch(const GqaArgs& A, int batch, cudaStream_t st)
 {
     constexpr size_t smem = (size_t)kGqaStages * 2 * kGqaChunk * D * sizeof(float) +
                             ((size_t)G * kGqaChunk + 3 * G + 2) * sizeof(float) + kGqaStages * sizeof(uint64_t) + 16;
-    static bool attr = false;  // per instantiation; the attribute is per function and device-wide
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess)
-            return hfail(MOE_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-        attr = true;
-    }
-    cudaError_t e = launch_pdl(gqa_split_kernel<D, G>, dim3(A.n_split, A.Hkv, batch), dim3(kGqaThreads * gqa_groups<G>()),
+    static std::atomic<int> done[moe::kMaxDevices];  // per instantiation and device
+    cudaError_t e = moe::raise_smem_limit(gqa_split_kernel<D, G>, (int)smem, done);
+    if (e != cudaSuccess)
+        return hfail(MOE_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    e = launch_pdl(gqa_split_kernel<D, G>, dim3(A.n_split, A.Hkv, batch), dim3(kGqaThreads * gqa_groups<G>()),
                                smem, st, A);
     if (e == cudaSuccess)
         e = launch_pdl(gqa_merge_kernel<D, G>, dim3(A.Hq, batch), dim3(kMergeThreads), 0, st, A);
