@@ -26,6 +26,7 @@
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstdarg>
 #include <cstdint>
@@ -258,11 +259,13 @@ struct GqaSplit {
     int n_split, per_split;
 };
 
+// Ranges per (sequence, K/V head): about one CTA per SM over all of them, never more ranges than
+// chunks of positions; then the range length, and the count of ranges that length actually needs.
 GqaSplit gqa_split(int batch, int Hkv, int max_pos)
 {
     const int by_chunks = (max_pos + kGqaChunk - 1) / kGqaChunk;
-    const int by_sms = kGqaCtaTarget / (batch * Hkv);
-    int n = by_chunks < (by_sms > 1 ? by_sms : 1) ? by_chunks : (by_sms > 1 ? by_sms : 1);
+    const int by_sms = std::max(1, kGqaCtaTarget / (batch * Hkv));
+    const int n = std::min(by_chunks, by_sms);
     const int per = (max_pos + n - 1) / n;
     return {(max_pos + per - 1) / per, per};
 }
