@@ -72,9 +72,10 @@ typedef enum {
                              * deterministic and ignore it. */
 #define MOE_GEMV 16 /* batched path, T <= 64: the two expert products as matrix-vector products
                      * (each touched expert's rows streamed once into mma.sync fragments) instead
-                     * of the tensor-core GEMMs. Same results within rounding (the same fp16
-                     * dequantisation, another summation order). Measured slower on B300 at T = 8
-                     * and 64 than the GEMMs, so off by default. The decode kernels ignore it. */
+                     * of the tensor-core GEMMs. The weights enter exactly (codes as 1024 + q, the
+                     * affine dequantisation per group in fp32), so any bf16 scale is exact here;
+                     * results agree with the GEMMs within the path's tolerance. Off by default
+                     * (measured on B300 against the GEMMs). The decode kernels ignore it. */
 
 /* One MoE FFN layer. hidden H, n_experts E, top_k k, inter I (routed expert), shared_inter Is,
  * bits 4 or 8, group 64. Supported: H % 256 == 0, I % 64 == 0, Is % 64 == 0, 1 <= k <= 16,

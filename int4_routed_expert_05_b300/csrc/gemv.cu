@@ -5,15 +5,19 @@
 // of the weights, not by tensor-core rate. These kernels replace the two tcgen05 GEMM launches of
 // the batched path for such T and keep everything around them: the same task lists (from the plan
 // kernel), the same fp16 operand rows in assignment order (K-permuted within 8-element blocks in
-// the order the dequantiser emits code pairs), the same dequantisation (w = s q + b in fp16,
-// exactly as the GEMM path forms it), the same SwiGLU and down epilogues and range checks.
+// the order the dequantiser emits code pairs), the same SwiGLU and down epilogues. The weights
+// enter exactly: a code q goes into the MMA as the fp16 value 1024 + q (one lop3 per code pair),
+// a second MMA with A = 1 gives each column's sum of x over the 64-element group, and the affine
+// dequantisation is applied per group in fp32, s (sum (1024 + q) x - 1024 sum x) + b sum x (the
+// GEMM path instead rounds s q + b to fp16 and reports scales fp16 cannot hold; here any bf16 scale
+// is exact).
 //
 // Work: a gate/up task (64 rows of gate and of up) runs as 4 rounds of 16 gate + 16 up rows; a down
-// task (128 rows) as 2 rounds of 64 rows. A round's rows arrive as one 1D bulk copy per row (plus
+// task (128 rows) as one round. A round's rows arrive as one 1D bulk copy per row (plus
 // the rows' scale and bias spans) into shared-memory rows padded by 16 bytes, so that the 8 rows a
 // warp's fragment load touches fall in distinct banks; two rounds are in flight. The 8 warps split
-// K into 64-element groups of four 16-element slices; per slice each warp dequantises its
-// rows' codes straight into the A fragments of mma.sync m16n8k16 (rows = weight rows, K = 16, N = 8
+// K into 64-element groups of four 16-element slices; per slice each warp feeds its rows' codes
+// straight into the A fragments of mma.sync m16n8k16 (rows = weight rows, K = 16, N = 8
 // assignments) with the activations as B, fp32 accumulation; a warp takes whole quantisation groups
 // (w, w + 8, ...), so each row's scale and bias are read once per group, and fetches the next
 // group's activation fragments while it works on the current one. The warps' partial sums are added in
@@ -39,8 +43,6 @@ constexpr int kPad = 16;  // bytes added to every staged row
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
 
 __device__ __forceinline__ void mbar_init(uint64_t* m, int n)
 {
@@ -98,11 +100,6 @@ __device__ __forceinline__ uint32_t code_pair(const uint32_t* w, int p)
     return __byte_perm((p >> 1) ? w[1] : w[0], 0x64646464u, (p & 1) ? 0x4341u : 0x4240u);
 }
 
-__device__ __forceinline__ uint32_t deq(uint32_t x, __half2 s, __half2 b)
-{
-    return h2u(__hfma2(__hsub2(u2h(x), u2h(0x64006400u)), s, b));
-}
-
 struct Round {
     int task, rr;      // task index, round within the task
     int e, m0, n0, nn; // expert (E = the shared one), first row of the round, assignments
@@ -112,8 +109,8 @@ struct Round {
 // Geometry of one kind: KIND 1 = gate/up (16 rows of each, K = H), KIND 2 = down (64 rows, K = I).
 template <int KIND>
 struct Kind {
-    static constexpr int kRounds = KIND == 1 ? 4 : 2;   // rounds per task
-    static constexpr int kRows = KIND == 1 ? 16 : 64;   // rows per matrix per round
+    static constexpr int kRounds = KIND == 1 ? 4 : 1;   // rounds per task
+    static constexpr int kRows = KIND == 1 ? 16 : 128;  // rows per matrix per round
     static constexpr int kMats = KIND == 1 ? 2 : 1;     // matrices per round
     static constexpr int kUnits = kMats * kRows / 16;   // 16-row MMA tiles per round
 };
@@ -188,8 +185,13 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const tc::GroupedArgs P,
         const int kd = KIND == 1 ? P.H : geo.cols[2];
         const int G = kd / 64;
         const uint32_t rb = (uint32_t)(kd * BITS / 8);          // code bytes of a row
-        const uint32_t sb = (uint32_t)(K::kRows * G * 2);       // bytes of a round's scale (or bias) span
-        const uint32_t total = blob ? K::kMats * (K::kRows * rb + 2 * sb) : 0;
+        // rows of the round inside the matrix: a down round may pass its end (H a multiple of 64,
+        // rounds of 128); rows past it are neither copied nor used
+        const int rows_total = KIND == 1 ? (r.e < P.E ? P.I : P.Is) : P.H;
+        const int nr = r.live ? min(K::kRows, rows_total - r.m0) : 0;
+        const uint32_t sstride = (uint32_t)(K::kRows * G * 2);  // shared-memory span of scales (or biases)
+        const uint32_t sb = (uint32_t)(nr * G * 2);             // bytes of it copied
+        const uint32_t total = blob ? K::kMats * (nr * rb + 2 * sb) : 0;
         if (lane == 0)
             mbar_expect(b, total);
         __syncwarp();
@@ -198,12 +200,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const tc::GroupedArgs P,
         for (int i = lane; i < K::kMats * (K::kRows + 2); i += 32) {
             const int mat = i / (K::kRows + 2), q = i % (K::kRows + 2);
             const int m = KIND == 1 ? mat : 2;                   // gate, up / down
-            if (q < K::kRows) {
+            if (q < nr) {
                 bulk_g2s(st + pl.code + (uint32_t)(mat * K::kRows + q) * pl.row_stride,
                          blob + geo.q_off[m] + (uint64_t)(r.m0 + q) * rb, rb, b);
-            } else {
+            } else if (q >= K::kRows) {
                 const uint64_t off = (q == K::kRows ? geo.s_off[m] : geo.b_off[m]) + (uint64_t)r.m0 * G * 2;
-                bulk_g2s(st + pl.sc + (uint32_t)(mat * 2 + (q - K::kRows)) * sb, blob + off, sb, b);
+                bulk_g2s(st + pl.sc + (uint32_t)(mat * 2 + (q - K::kRows)) * sstride, blob + off, sb, b);
             }
         }
     };
@@ -260,7 +262,6 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const tc::GroupedArgs P,
                     }
                 };
                 load_b(warp, bn);
-                bool bad = false;
                 // warp w takes the quantisation groups w, w + 8, ...: one scale and bias per row and
                 // group, four 16-element slices each
                 for (int grp = warp; grp < G; grp += kWarps) {
@@ -268,6 +269,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const tc::GroupedArgs P,
                     for (int i = 0; i < 8; ++i)
                         bc[i] = bn[i];
                     load_b(grp + kWarps, bn);
+                    // sum of the group's activations per column (an MMA with A = 1), the same in
+                    // every row of the fragment: accx[i] belongs to column 2c + (i & 1)
+                    float accx[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        mma16816(accx, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, bc[2 * i], bc[2 * i + 1]);
 #pragma unroll
                     for (int u = 0; u < K::kUnits; ++u) {
                         const int mat = u / (K::kRows / 16), rt = u % (K::kRows / 16);
@@ -278,12 +285,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const tc::GroupedArgs P,
                         const uint16_t* bp = sp + (size_t)K::kRows * G;
                         const float sa = bf2f(sp[ra * G + grp]), ba = bf2f(bp[ra * G + grp]);
                         const float sb2 = bf2f(sp[rb2 * G + grp]), bb = bf2f(bp[rb2 * G + grp]);
-                        // the same fp16 range condition as the GEMM path's dequantiser
-                        const float qmax = BITS == 4 ? 15.f : 255.f;
-                        bad |= (sa != 0.f && !(fabsf(sa) >= 6.103515625e-05f)) || !(fabsf(sa) * qmax + fabsf(ba) <= 65504.f);
-                        bad |= (sb2 != 0.f && !(fabsf(sb2) >= 6.103515625e-05f)) || !(fabsf(sb2) * qmax + fabsf(bb) <= 65504.f);
-                        const __half2 s2a = __half2half2(__float2half_rn(sa)), b2a = __half2half2(__float2half_rn(ba));
-                        const __half2 s2b = __half2half2(__float2half_rn(sb2)), b2b = __half2half2(__float2half_rn(bb));
+                        float accq[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // sum of (1024 + q) x over the group
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int sl = 4 * grp + i;
@@ -298,17 +300,21 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const tc::GroupedArgs P,
                                 wa[0] = va.x; wa[1] = va.y; wa[2] = va.z; wa[3] = va.w;
                                 wb[0] = vb.x; wb[1] = vb.y; wb[2] = vb.z; wb[3] = vb.w;
                             }
-                            // K block 0 of the slice = word 0 (int4) / words 0-1 (int8), block 1 the next
-                            const uint32_t a0 = deq(code_pair<BITS>(wa, c), s2a, b2a);
-                            const uint32_t a1 = deq(code_pair<BITS>(wb, c), s2b, b2b);
-                            const uint32_t a2 = deq(code_pair<BITS>(wa + (BITS == 4 ? 1 : 2), c), s2a, b2a);
-                            const uint32_t a3 = deq(code_pair<BITS>(wb + (BITS == 4 ? 1 : 2), c), s2b, b2b);
-                            mma16816(acc[u], a0, a1, a2, a3, bc[2 * i], bc[2 * i + 1]);
+                            // K block 0 of the slice = word 0 (int4) / words 0-1 (int8), block 1 the next;
+                            // the codes enter as the exact fp16 values 1024 + q
+                            const uint32_t a0 = code_pair<BITS>(wa, c);
+                            const uint32_t a1 = code_pair<BITS>(wb, c);
+                            const uint32_t a2 = code_pair<BITS>(wa + (BITS == 4 ? 1 : 2), c);
+                            const uint32_t a3 = code_pair<BITS>(wb + (BITS == 4 ? 1 : 2), c);
+                            mma16816(accq, a0, a1, a2, a3, bc[2 * i], bc[2 * i + 1]);
                         }
+                        // w = s q + b over the group: s (sum (1024 + q) x - 1024 sum x) + b sum x
+                        acc[u][0] += sa * (accq[0] - 1024.0f * accx[0]) + ba * accx[0];
+                        acc[u][1] += sa * (accq[1] - 1024.0f * accx[1]) + ba * accx[1];
+                        acc[u][2] += sb2 * (accq[2] - 1024.0f * accx[2]) + bb * accx[2];
+                        acc[u][3] += sb2 * (accq[3] - 1024.0f * accx[3]) + bb * accx[3];
                     }
                 }
-                if (bad)
-                    atomicCAS(P.status, 0, kStatusRange);
                 // the warps' partial sums -> shared memory [warp][unit][row 16][col 8]
 #pragma unroll
                 for (int u = 0; u < K::kUnits; ++u) {
