@@ -57,8 +57,9 @@ typedef enum {
     MOE_E_NOMEM = 7,         /* workspace or arena too small */
     MOE_E_RANGE = 8          /* a value outside what the kernels' fp16 operands hold (device status):
                               * an input, activation or h value above 65504 in magnitude; on the
-                              * batched path also a scale below fp16's normal range (2^-14) or a
-                              * weight s q + b or SwiGLU output that would overflow fp16 */
+                              * batched path's GEMMs also a scale below fp16's normal range (2^-14)
+                              * or a weight s q + b that would overflow fp16 (the MOE_GEMV path
+                              * applies scales in fp32 and has no such limit) */
 } moe_status;
 
 /* flags of moe_shape.flags */
