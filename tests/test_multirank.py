@@ -47,12 +47,13 @@ def test_two_gloo_ranks_barrier_and_max():
     assert got == [(0, 11.0), (1, 11.0)]
 
 
-def test_reference_arm_prints_on_rank_zero_only(capsys, monkeypatch):
+@pytest.mark.parametrize("config", ["stack80", "prefill80_t8", "gdn80", "gqa80_8k"])
+def test_reference_arm_prints_on_rank_zero_only(capsys, monkeypatch, config):
     sys.path.insert(0, ROOT)
     import bench
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
-    args = bench.argparse.Namespace(config="stack80", steps=1, warmup=0, gpus=2, layers=0, ref_layers=1,
+    args = bench.argparse.Namespace(config=config, steps=1, warmup=0, gpus=2, layers=0, ref_layers=1,
                                     ref_budget=0.1, no_cpu_baseline=True, impl="reference")
     bench.run_reference(args)
     assert capsys.readouterr().out == ""
